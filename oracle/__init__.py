@@ -1,0 +1,180 @@
+"""CPU oracle for the LSA c4 indexer hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The product path (sparse_attention_kv_c4_gb300)
+never imports it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64 accumulation, one OpenMP
+split over independent outputs).  This module only compiles it, loads it with
+ctypes and marshals numpy arrays.  Every function cites, in ``oracle.c``, the
+passage it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "oracle.c")
+SO = os.path.join(HERE, "liborc.so")
+
+u16p = ctypes.POINTER(ctypes.c_uint16)
+u8p = ctypes.POINTER(ctypes.c_uint8)
+u32p = ctypes.POINTER(ctypes.c_uint32)
+f32p = ctypes.POINTER(ctypes.c_float)
+f64p = ctypes.POINTER(ctypes.c_double)
+i32p = ctypes.POINTER(ctypes.c_int32)
+i64p = ctypes.POINTER(ctypes.c_int64)
+I64, I32, D, F = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_float
+
+
+def compile_oracle(src: str = SRC, so: str = SO, extra=()) -> str:
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-ffp-contract=off", "-std=c11",
+           *extra, "-o", so, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return so
+
+
+def build() -> str:
+    return compile_oracle()
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t) if a is not None else None
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, so: str = SO):
+        lib = ctypes.CDLL(so)
+        lib.orc_bf16.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16.restype = D
+        lib.orc_e4m3.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3.restype = D
+        lib.orc_sigmoid.argtypes = [D]
+        lib.orc_sigmoid.restype = D
+        lib.orc_score_bf16.argtypes = [u16p, f32p, u16p, I32, I32]
+        lib.orc_score_bf16.restype = D
+        lib.orc_score_fp8.argtypes = [u16p, f32p, u8p, F, I32, I32]
+        lib.orc_score_fp8.restype = D
+        lib.orc_memindex_logits.argtypes = [u16p, f32p, u16p, I64, I64, I64, I64, I64, I32, I32, f64p]
+        lib.orc_memindex_select.argtypes = [f64p, I64, I64, I64, D, u32p, f64p]
+        lib.orc_topk.argtypes = [i64p, f64p, I64, I32, i32p, f64p]
+        lib.orc_topk.restype = ctypes.c_int
+        lib.orc_paged_topk.argtypes = [u16p, f32p, u8p, f32p, i32p, i32p, i32p, I64, I64, I32, I32, I32,
+                                       I32, i32p, f64p, f64p]
+        lib.orc_causal_limit.argtypes = [I64, I64, I32]
+        lib.orc_causal_limit.restype = I64
+        lib.orc_prefill_topk.argtypes = [u16p, f32p, i64p, u16p, I64, I64, I32, I32, I32, I32, i32p, f64p]
+        lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_set_num_threads.argtypes = [ctypes.c_int]
+        self.lib = lib
+        self.path = so
+
+    # -- element decoding ----------------------------------------------------
+    def bf16(self, bits) -> np.ndarray:
+        b = np.asarray(bits, dtype=np.uint16).reshape(-1)
+        return np.array([self.lib.orc_bf16(int(v)) for v in b])
+
+    def e4m3(self, codes) -> np.ndarray:
+        c = np.asarray(codes, dtype=np.uint8).reshape(-1)
+        return np.array([self.lib.orc_e4m3(int(v)) for v in c])
+
+    def sigmoid(self, x: float) -> float:
+        return self.lib.orc_sigmoid(float(x))
+
+    # -- scores --------------------------------------------------------------
+    def score_bf16(self, q, w, k) -> float:
+        q = _c(q, np.uint16); w = _c(w, np.float32); k = _c(k, np.uint16)
+        n_h, d = q.shape
+        return self.lib.orc_score_bf16(_p(q, u16p), _p(w, f32p), _p(k, u16p), n_h, d)
+
+    def score_fp8(self, q, w, k8, scale) -> float:
+        q = _c(q, np.uint16); w = _c(w, np.float32); k8 = _c(k8, np.uint8)
+        n_h, d = q.shape
+        return self.lib.orc_score_fp8(_p(q, u16p), _p(w, f32p), _p(k8, u8p), float(scale), n_h, d)
+
+    # -- Memory Indexer --------------------------------------------------------
+    def memindex_logits(self, q, w, K) -> np.ndarray:
+        """q [B,L,n_h,d] bf16 bits, w [B,L,n_h], K [B,L,S,d] bf16 bits -> x [B,L,S] fp64."""
+        q = _c(q, np.uint16); w = _c(w, np.float32); K = _c(K, np.uint16)
+        B, L, n_h, d = q.shape
+        S = K.shape[2]
+        x = np.empty((B, L, S), dtype=np.float64)
+        self.lib.orc_memindex_logits(_p(q, u16p), _p(w, f32p), _p(K, u16p), L * S * d, S * d, B, L, S,
+                                     n_h, d, _p(x, f64p))
+        return x
+
+    def memindex_select(self, x, thr: float = 0.5):
+        """x [B,L,S] -> mask [B, ceil(S/32)] uint32, maxsig [B,S] fp64."""
+        x = _c(x, np.float64)
+        B, L, S = x.shape
+        mask = np.empty((B, (S + 31) // 32), dtype=np.uint32)
+        maxsig = np.empty((B, S), dtype=np.float64)
+        self.lib.orc_memindex_select(_p(x, f64p), B, L, S, float(thr), _p(mask, u32p), _p(maxsig, f64p))
+        return mask, maxsig
+
+    # -- top-k -------------------------------------------------------------------
+    def topk(self, ids, x, k: int = 512):
+        ids = _c(ids, np.int64); x = _c(x, np.float64)
+        idx = np.empty(k, dtype=np.int32)
+        sc = np.empty(k, dtype=np.float64)
+        m = self.lib.orc_topk(_p(ids, i64p), _p(x, f64p), len(ids), k, _p(idx, i32p), _p(sc, f64p))
+        return idx, sc, m
+
+    def paged_topk(self, q, w, k8, scale, page_phys, page_logical, n_res=None, k: int = 512,
+                   want_logits: bool = False):
+        q = _c(q, np.uint16); w = _c(w, np.float32); k8 = _c(k8, np.uint8); scale = _c(scale, np.float32)
+        page_phys = _c(page_phys, np.int32); page_logical = _c(page_logical, np.int32)
+        Q, n_h, d = q.shape
+        R = page_phys.shape[1]
+        page = k8.shape[1]
+        nr = _c(n_res, np.int32) if n_res is not None else None
+        idx = np.empty((Q, k), dtype=np.int32)
+        sc = np.empty((Q, k), dtype=np.float64)
+        lg = np.empty((Q, R * page), dtype=np.float64) if want_logits else None
+        self.lib.orc_paged_topk(_p(q, u16p), _p(w, f32p), _p(k8, u8p), _p(scale, f32p), _p(page_phys, i32p),
+                                _p(page_logical, i32p), _p(nr, i32p), Q, R, n_h, d, page, k, _p(idx, i32p),
+                                _p(sc, f64p), _p(lg, f64p))
+        return (idx, sc, lg) if want_logits else (idx, sc)
+
+    def causal_limit(self, pos: int, S: int, ratio: int = 4) -> int:
+        return self.lib.orc_causal_limit(int(pos), int(S), int(ratio))
+
+    def prefill_topk(self, q, w, pos, K, ratio: int = 4, k: int = 512):
+        q = _c(q, np.uint16); w = _c(w, np.float32); pos = _c(pos, np.int64); K = _c(K, np.uint16)
+        T, n_h, d = q.shape
+        S = K.shape[0]
+        idx = np.empty((T, k), dtype=np.int32)
+        sc = np.empty((T, k), dtype=np.float64)
+        self.lib.orc_prefill_topk(_p(q, u16p), _p(w, f32p), _p(pos, i64p), _p(K, u16p), T, S, n_h, d, ratio,
+                                  k, _p(idx, i32p), _p(sc, f64p))
+        return idx, sc
+
+    def num_threads(self) -> int:
+        return self.lib.orc_num_threads()
+
+    def set_num_threads(self, n: int) -> None:
+        self.lib.orc_set_num_threads(int(n))
+
+
+_default = None
+
+
+def get() -> Oracle:
+    """The oracle compiled from oracle.c (rebuilt if the source is newer)."""
+    global _default
+    if _default is None:
+        if not os.path.exists(SO) or os.path.getmtime(SRC) > os.path.getmtime(SO):
+            build()
+        _default = Oracle(SO)
+    return _default

@@ -1,0 +1,292 @@
+/*
+ * oracle.c -- plain, slow CPU reference for the LSA c4 indexer hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code with
+ * the CUDA path (sparse_attention_kv_c4_gb300/csrc) and includes none of its
+ * headers.  Every result is the plain definition written out, accumulated in
+ * fp64, in the order the pages state it.  OpenMP only splits independent
+ * outputs across threads; it never changes a summation order.
+ *
+ * Sources (page titles as published):
+ *   [FM]  "FlashMemory-DeepSeek-V4: Lightning Index Ultra-Long Context via
+ *         Lookahead Sparse Attention" (paper summary), sec. 3 "Memory Indexer
+ *         scoring function" and sec. 6 "Implementation boundary".
+ *   [RM]  "FlashMemory-DeepSeek-V4" (repository README): "Retriever
+ *         architecture", "compressed_k format", "Two-level recall algorithm".
+ *   [V4]  "DeepSeek-V4 CSA + HCA explained" (yuyanqi.com): sec. 3 "C4Indexer"
+ *         (CSA-1 score, CSA-2 top-512), sec. 8 (c4 chunk = 4 tokens).
+ *
+ * Readings where the pages are silent:
+ *   - Ranking is by the pre-sigmoid logit; equal logits are ordered by the
+ *     lower chunk id first.  NaN logits rank as -inf.
+ *   - The threshold test is inclusive: sigma(x) >= thr.
+ *   - Fewer candidates than k: all are returned, padded with id -1.
+ *   - Prefill causal limit: chunk s is a candidate of a query at position pos
+ *     iff s < min(S, floor(pos / ratio)).
+ *   - Selected ids are emitted sorted by ascending chunk id.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_API __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------------- */
+/* Element decoding                                                           */
+/* ------------------------------------------------------------------------- */
+
+/* bfloat16: the upper half of an IEEE binary32; the value is exact in fp64. */
+ORC_API double orc_bf16(uint16_t bits) {
+  union { uint32_t u; float f; } v;
+  v.u = (uint32_t)bits << 16;
+  return (double)v.f;
+}
+
+/* OCP FP8 E4M3 ([RM] "compressed_k format": bytes [:128] are float8_e4m3):
+ * sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 is
+ * subnormal (m/8 * 2^-6); S.1111.111 is NaN; there are no infinities. */
+ORC_API double orc_e4m3(uint8_t bits) {
+  int sign = (bits >> 7) & 1;
+  int e = (bits >> 3) & 0xF;
+  int m = bits & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* [RM] "compressed_k format": dequant = fp8.float() * scale, an fp32 product. */
+static double orc_dequant(uint8_t code, float scale) {
+  float kv = (float)orc_e4m3(code) * scale;
+  return (double)kv;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Indexer score                                                              */
+/* ------------------------------------------------------------------------- */
+
+/* x = sum_h w_h * ReLU(q_h . k)  -- the argument of sigma in [FM] sec. 3
+ * (I_{t,s}) and the native C4Indexer score of [V4] sec. 3 (CSA-1).
+ * q is [n_h][d] bf16, w is [n_h] fp32 (already fused with any head scaling,
+ * [RM] "fused_w"), k is the dequantised key [d] in fp64. */
+static double orc_score_k(const uint16_t* q, const float* w, const double* k, int n_h, int d) {
+  double x = 0.0;
+  for (int h = 0; h < n_h; ++h) {
+    double dot = 0.0;
+    for (int j = 0; j < d; ++j) dot += orc_bf16(q[(size_t)h * d + j]) * k[j];
+    double relu = dot > 0.0 ? dot : 0.0;
+    x += (double)w[h] * relu;
+  }
+  return x;
+}
+
+ORC_API double orc_score_bf16(const uint16_t* q, const float* w, const uint16_t* k, int n_h, int d) {
+  double kd[1024];
+  if (d > 1024) return NAN;
+  for (int j = 0; j < d; ++j) kd[j] = orc_bf16(k[j]);
+  return orc_score_k(q, w, kd, n_h, d);
+}
+
+ORC_API double orc_score_fp8(const uint16_t* q, const float* w, const uint8_t* k8, float scale, int n_h,
+                             int d) {
+  double kd[1024];
+  if (d > 1024) return NAN;
+  for (int j = 0; j < d; ++j) kd[j] = orc_dequant(k8[j], scale);
+  return orc_score_k(q, w, kd, n_h, d);
+}
+
+/* sigma(x) = 1 / (1 + e^-x), [FM] sec. 3. */
+ORC_API double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* ------------------------------------------------------------------------- */
+/* Memory Indexer: per-layer logits, OR-union over layers, resident bitmask   */
+/* ------------------------------------------------------------------------- */
+
+/* x[b][l][s] for q [B][L][n_h][d] bf16, w [B][L][n_h], keys bf16 at
+ * K + b*stride_b + l*stride_l + s*d (element strides). */
+ORC_API void orc_memindex_logits(const uint16_t* q, const float* w, const uint16_t* K, int64_t stride_b,
+                                 int64_t stride_l, int64_t B, int64_t L, int64_t S, int n_h, int d,
+                                 double* x_out) {
+#pragma omp parallel for collapse(2) schedule(dynamic, 64)
+  for (int64_t bl = 0; bl < B * L; ++bl)
+    for (int64_t s = 0; s < S; ++s) {
+      int64_t b = bl / L, l = bl % L;
+      const uint16_t* qb = q + (size_t)bl * n_h * d;
+      const float* wb = w + (size_t)bl * n_h;
+      const uint16_t* ks = K + b * stride_b + l * stride_l + s * d;
+      x_out[(size_t)bl * S + s] = orc_score_bf16(qb, wb, ks, n_h, d);
+    }
+}
+
+/* [FM] sec. 3: R[s] = 1(max_l sigma(x_l[s]) >= thr), the OR-union of the
+ * per-layer sets {s | I^(l) >= thr}.  mask bit (s & 31) of word s >> 5;
+ * bits at s >= S stay zero.  maxsig[b][s] = max_l sigma(x_l[s]). */
+ORC_API void orc_memindex_select(const double* x, int64_t B, int64_t L, int64_t S, double thr,
+                                 uint32_t* mask, double* maxsig) {
+  int64_t words = (S + 31) / 32;
+  memset(mask, 0, sizeof(uint32_t) * (size_t)(B * words));
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t s = 0; s < S; ++s) {
+      double best = -1.0;
+      for (int64_t l = 0; l < L; ++l) {
+        double sig = orc_sigmoid(x[((size_t)b * L + l) * S + s]);
+        if (sig > best) best = sig;
+      }
+      if (best >= thr) mask[b * words + (s >> 5)] |= 1u << (s & 31);
+      if (maxsig) maxsig[b * S + s] = best;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Top-k select                                                               */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+  double x;
+  int64_t id;
+} orc_cand;
+
+static int orc_rank_cmp(const void* pa, const void* pb) {
+  const orc_cand* a = (const orc_cand*)pa;
+  const orc_cand* b = (const orc_cand*)pb;
+  double xa = isnan(a->x) ? -INFINITY : a->x;
+  double xb = isnan(b->x) ? -INFINITY : b->x;
+  if (xa > xb) return -1;
+  if (xa < xb) return 1;
+  if (a->id != b->id) return a->id < b->id ? -1 : 1; /* tie: lower chunk id first */
+  return 0;
+}
+
+static int orc_id_cmp(const void* pa, const void* pb) {
+  const orc_cand* a = (const orc_cand*)pa;
+  const orc_cand* b = (const orc_cand*)pb;
+  return (a->id > b->id) - (a->id < b->id);
+}
+
+/* [FM] sec. 3 (C^CoreComp = Top-k of the native score inside the resident
+ * set), [V4] sec. 3 (CSA-2, top-512; fewer than 512 chunks -> take all,
+ * sec. 8 worked layout): the min(k, n) best candidates by (x desc, id asc),
+ * emitted by ascending id, padded with id -1 / score -inf.  Returns the
+ * number selected. */
+static int orc_topk_cands(orc_cand* c, int64_t n, int k, int32_t* idx_out, double* score_out) {
+  qsort(c, (size_t)n, sizeof(orc_cand), orc_rank_cmp);
+  int64_t m = n < k ? n : k;
+  qsort(c, (size_t)m, sizeof(orc_cand), orc_id_cmp);
+  for (int64_t i = 0; i < k; ++i) {
+    idx_out[i] = i < m ? (int32_t)c[i].id : -1;
+    if (score_out) score_out[i] = i < m ? c[i].x : -INFINITY;
+  }
+  return (int)m;
+}
+
+ORC_API int orc_topk(const int64_t* ids, const double* x, int64_t n, int k, int32_t* idx_out,
+                     double* score_out) {
+  orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(n > 0 ? n : 1));
+  if (!c) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    c[i].x = x[i];
+    c[i].id = ids[i];
+  }
+  int m = orc_topk_cands(c, n, k, idx_out, score_out);
+  free(c);
+  return m;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Native paged top-k over the resident pages                                 */
+/* ------------------------------------------------------------------------- */
+
+/* [RM] "Two-level recall algorithm", Level 2: the native indexer scores only
+ * the resident chunks (read through the page table, [RM] "Page-recall",
+ * 64-chunk pages) and keeps the top-k.  Query qi has q [n_h][d] bf16 and w
+ * [n_h]; its j-th resident page (j < n_res[qi], or R when n_res is NULL) lives
+ * at pool page page_phys[qi][j] and holds logical chunks
+ * page_logical[qi][j]*page_size + o.  Pool keys: k8 [P][page_size][d] E4M3,
+ * scale [P][page_size] fp32.  logit_out (optional) is [Q][R*page_size] in
+ * page-table order, NaN for slots past n_res. */
+ORC_API void orc_paged_topk(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
+                            const int32_t* page_phys, const int32_t* page_logical, const int32_t* n_res,
+                            int64_t Q, int64_t R, int n_h, int d, int page_size, int k, int32_t* idx_out,
+                            double* score_out, double* logit_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t qi = 0; qi < Q; ++qi) {
+    int64_t nr = n_res ? n_res[qi] : R;
+    if (nr > R) nr = R;
+    if (nr < 0) nr = 0;
+    orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(nr * page_size > 0 ? nr * page_size : 1));
+    int64_t n = 0;
+    for (int64_t j = 0; j < nr; ++j) {
+      int64_t p = page_phys[qi * R + j];
+      int64_t lp = page_logical[qi * R + j];
+      for (int o = 0; o < page_size; ++o) {
+        int64_t row = p * page_size + o;
+        double x = orc_score_fp8(q + (size_t)qi * n_h * d, w + (size_t)qi * n_h, k8 + (size_t)row * d,
+                                 scale[row], n_h, d);
+        c[n].x = x;
+        c[n].id = lp * page_size + o;
+        ++n;
+        if (logit_out) logit_out[(size_t)qi * R * page_size + j * page_size + o] = x;
+      }
+    }
+    if (logit_out)
+      for (int64_t j = nr; j < R; ++j)
+        for (int o = 0; o < page_size; ++o) logit_out[(size_t)qi * R * page_size + j * page_size + o] = NAN;
+    orc_topk_cands(c, n, k, idx_out + (size_t)qi * k, score_out ? score_out + (size_t)qi * k : NULL);
+    free(c);
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Prefill: many queries against dense chunk keys under the causal limit      */
+/* ------------------------------------------------------------------------- */
+
+/* Chunk s covers tokens ratio*s .. ratio*s+ratio-1 ([V4] sec. 1/8: c4 = 4
+ * tokens per chunk); it is visible to the query at position pos only when all
+ * of its tokens precede pos: s < floor(pos / ratio), and s < S. */
+ORC_API int64_t orc_causal_limit(int64_t pos, int64_t S, int ratio) {
+  if (pos < 0) return 0;
+  int64_t lim = pos / ratio;
+  return lim < S ? lim : S;
+}
+
+/* q [T][n_h][d] bf16, w [T][n_h], pos [T], K [S][d] bf16. */
+ORC_API void orc_prefill_topk(const uint16_t* q, const float* w, const int64_t* pos, const uint16_t* K,
+                              int64_t T, int64_t S, int n_h, int d, int ratio, int k, int32_t* idx_out,
+                              double* score_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t n = orc_causal_limit(pos[t], S, ratio);
+    orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(n > 0 ? n : 1));
+    for (int64_t s = 0; s < n; ++s) {
+      c[s].x = orc_score_bf16(q + (size_t)t * n_h * d, w + (size_t)t * n_h, K + (size_t)s * d, n_h, d);
+      c[s].id = s;
+    }
+    orc_topk_cands(c, n, k, idx_out + (size_t)t * k, score_out ? score_out + (size_t)t * k : NULL);
+    free(c);
+  }
+}
+
+ORC_API int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+ORC_API void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

@@ -1,0 +1,378 @@
+"""Pins of the CPU oracle to facts outside the oracle itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with a value fixed by the pages, by a published format
+definition, by mathematics (closed forms, identities, invariants) or by brute
+force on tiny inputs.  ``test_oracle_pins.py`` runs them against the oracle;
+``test_oracle_mutants.py`` plants single mistakes into a copy of the oracle's
+source and checks that at least one pin catches each of them.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------------------
+# helpers (input construction only)
+# ---------------------------------------------------------------------------
+
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """Round-to-nearest-even fp32 -> bf16 bit patterns (inputs for pins)."""
+    u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f64(b) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rank_key_sorted(ids, x):
+    """Brute force: all candidates ordered by (x desc, id asc); NaN as -inf."""
+    xs = [(-math.inf if math.isnan(v) else v) for v in x]
+    return sorted(zip(ids, xs), key=lambda t: (-t[1], t[0]))
+
+
+def expected_topk(ids, x, k):
+    order = rank_key_sorted(list(ids), list(x))
+    chosen = sorted(i for i, _ in order[:k])
+    return chosen + [-1] * (k - len(chosen))
+
+
+# ---------------------------------------------------------------------------
+# element decoding
+# ---------------------------------------------------------------------------
+
+def pin_bf16_decode(orc):
+    """bf16 is the top half of binary32: all 65536 codes vs numpy's view."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.bf16(codes)
+    want = bf16_bits_to_f64(codes)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), f"bf16 decode differs at {np.nonzero(~same)[0][:5]}"
+
+
+def pin_e4m3_golden(orc):
+    """OCP OFP8 E4M3 table values (tests/golden/e4m3_ocp.txt)."""
+    with open(os.path.join(GOLDEN, "e4m3_ocp.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    for code, val in rows:
+        got = orc.e4m3([int(code, 16)])[0]
+        want = float(val)
+        if math.isnan(want):
+            assert math.isnan(got), f"{code}: {got} should be NaN"
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), f"{code}: {got} != {want}"
+
+
+def pin_e4m3_all_codes_vs_torch(orc):
+    """All 256 E4M3 codes vs PyTorch's float8_e4m3fn (an independent decoder)."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = orc.e4m3(codes)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), f"e4m3 decode differs at codes {np.nonzero(~same)[0][:5]}"
+
+
+def pin_fp8_dequant_is_fp32_product(orc):
+    """compressed_k dequant = fp8.float() * scale in fp32: with n_h = d = 1,
+    q = 1, w = 1 the score is exactly the fp32 product (when positive)."""
+    q = f32_to_bf16_bits(np.array([[1.0]], dtype=np.float32))
+    w = np.array([1.0], dtype=np.float32)
+    for code, scale in [(0x3F, 0.1), (0x01, 3.0), (0x7E, 1e-3), (0x26, 7.25)]:
+        val = {0x3F: 1.875, 0x01: 2.0 ** -9, 0x7E: 448.0, 0x26: 0.21875}[code]
+        want = float(np.float32(val) * np.float32(scale))
+        got = orc.score_fp8(q, w, np.array([code], dtype=np.uint8), scale)
+        assert got == want, f"code {code:#x} scale {scale}: {got} != {want}"
+
+
+# ---------------------------------------------------------------------------
+# score: closed forms and identities
+# ---------------------------------------------------------------------------
+
+def pin_score_scalar(orc):
+    """n_h = d = 1: x = w * max(0, q*k)."""
+    bf = lambda v: f32_to_bf16_bits(np.array(v, dtype=np.float32))
+    cases = [(2.0, 3.0, 0.5, 3.0), (2.0, -3.0, 0.5, 0.0), (-2.0, -3.0, 0.5, 3.0),
+             (2.0, 3.0, -0.5, -3.0), (0.0, 5.0, 1.0, 0.0), (1.5, 0.25, 4.0, 1.5)]
+    for qv, kv, wv, want in cases:
+        got = orc.score_bf16(bf([[qv]]), np.array([wv], np.float32), bf([kv]))
+        assert got == want, f"q={qv} k={kv} w={wv}: {got} != {want}"
+
+
+def pin_score_unit_vectors(orc):
+    """q_h = c_h e_{pi(h)}, k = e_j: x = w_h max(0, c_h) for the head with
+    pi(h) = j, else 0.  Catches head/dim transposes and w misalignment."""
+    n_h, d = 4, 8
+    pi = [5, 2, 7, 0]
+    c = [1.0, 2.0, -1.0, 4.0]
+    w = np.array([0.5, 0.25, 2.0, -1.0], dtype=np.float32)
+    qf = np.zeros((n_h, d), np.float32)
+    for h in range(n_h):
+        qf[h, pi[h]] = c[h]
+    q = f32_to_bf16_bits(qf)
+    for j in range(d):
+        k = f32_to_bf16_bits(np.eye(d, dtype=np.float32)[j])
+        want = 0.0
+        for h in range(n_h):
+            if pi[h] == j:
+                want = float(w[h]) * max(0.0, c[h])
+        got = orc.score_bf16(q, w, k)
+        assert got == want, f"e_{j}: {got} != {want}"
+
+
+def pin_score_antisymmetry(orc):
+    """ReLU(v) - ReLU(-v) = v, so x(q) - x(-q) = sum_h w_h (q_h . k) = k . (Q^T w),
+    evaluated here by a matrix product in a different association."""
+    rng = np.random.default_rng(7)
+    for n_h, d in [(64, 128), (3, 5), (1, 128)]:
+        for _ in range(3):
+            q = f32_to_bf16_bits(rng.standard_normal((n_h, d)).astype(np.float32))
+            k = f32_to_bf16_bits((rng.standard_normal(d) / 11).astype(np.float32))
+            w = rng.standard_normal(n_h).astype(np.float32)
+            qneg = q ^ np.uint16(0x8000)
+            lhs = orc.score_bf16(q, w, k) - orc.score_bf16(qneg, w, k)
+            rhs = float(bf16_bits_to_f64(k) @ (bf16_bits_to_f64(q).T @ w.astype(np.float64)))
+            assert abs(lhs - rhs) <= 1e-10 * (1 + abs(rhs)), f"{lhs} vs {rhs}"
+
+
+def pin_score_homogeneity(orc):
+    """Positive homogeneity: x(2q) = 2 x(q) and x(q; 2w) = 2 x(q; w) exactly."""
+    rng = np.random.default_rng(11)
+    q = f32_to_bf16_bits(rng.standard_normal((64, 128)).astype(np.float32))
+    k = f32_to_bf16_bits((rng.standard_normal(128) / 11).astype(np.float32))
+    w = rng.standard_normal(64).astype(np.float32)
+    x = orc.score_bf16(q, w, k)
+    q2 = f32_to_bf16_bits(bf16_bits_to_f64(q).astype(np.float32) * 2)
+    assert orc.score_bf16(q2, w, k) == 2 * x
+    assert orc.score_bf16(q, (w * 2).astype(np.float32), k) == 2 * x
+
+
+def pin_score_relu_negative(orc):
+    """All head dots negative -> x = 0 for any w; sigma(0) = 0.5 is resident."""
+    q = f32_to_bf16_bits(np.abs(np.random.default_rng(3).standard_normal((64, 128))).astype(np.float32) + 0.01)
+    k = f32_to_bf16_bits(-np.full(128, 0.05, np.float32))
+    w = np.random.default_rng(4).standard_normal(64).astype(np.float32)
+    x = orc.score_bf16(q, w, k)
+    assert x == 0.0, x
+    mask, maxsig = orc.memindex_select(np.array([[[x]]]), 0.5)
+    assert mask[0, 0] == 1 and maxsig[0, 0] == 0.5
+
+
+def pin_fp8_scale_invariance(orc):
+    """Doubling the chunk scale and halving w leaves every score unchanged."""
+    rng = np.random.default_rng(5)
+    q = f32_to_bf16_bits(rng.standard_normal((64, 128)).astype(np.float32))
+    w = rng.standard_normal(64).astype(np.float32)
+    k8 = rng.integers(0, 256, 128).astype(np.uint8)
+    k8[(k8 & 0x7F) == 0x7F] = 0x11
+    a = orc.score_fp8(q, w, k8, 0.0123)
+    b = orc.score_fp8(q, (w / 2).astype(np.float32), k8, np.float32(0.0123) * 2)
+    assert a == b, (a, b)
+
+
+# ---------------------------------------------------------------------------
+# sigmoid, threshold, union
+# ---------------------------------------------------------------------------
+
+def pin_sigmoid_closed_forms(orc):
+    assert orc.sigmoid(0.0) == 0.5
+    assert abs(orc.sigmoid(math.log(3.0)) - 0.75) < 1e-15
+    assert abs(orc.sigmoid(-math.log(3.0)) - 0.25) < 1e-15
+    assert abs(orc.sigmoid(-40.0) - math.exp(-40.0) / (1 + math.exp(-40.0))) < 1e-30
+
+
+def pin_threshold_boundary(orc):
+    """sigma(x) >= 0.5 <=> x >= 0 (inclusive); other thresholds via logit."""
+    x = np.array([[[-1.0, 0.0, 1.0, -1e-12, 3.0, -5.0, 1e-12]]])
+    mask, _ = orc.memindex_select(x, 0.5)
+    assert mask[0, 0] == 0b1010110, bin(mask[0, 0])
+    lg = math.log(3.0)
+    x = np.array([[[lg + 1e-9, lg - 1e-9, 0.0]]])
+    mask, _ = orc.memindex_select(x, 0.75)
+    assert mask[0, 0] == 0b001, bin(mask[0, 0])
+
+
+def pin_union_invariants(orc):
+    """Mask = OR of per-layer masks = 1(max_l x >= 0); permuting layers changes
+    nothing; maxsig = max_l sigma(x_l); bits past S are zero."""
+    rng = np.random.default_rng(9)
+    B, L, S = 2, 3, 101
+    x = rng.standard_normal((B, L, S)) * 2
+    x[0, 1, 7] = 0.0
+    mask, maxsig = orc.memindex_select(x, 0.5)
+    per = [orc.memindex_select(x[:, l:l + 1, :], 0.5)[0] for l in range(L)]
+    assert (mask == (per[0] | per[1] | per[2])).all()
+    perm, _ = orc.memindex_select(x[:, ::-1, :].copy(), 0.5)
+    assert (perm == mask).all()
+    words = (S + 31) // 32
+    want = np.zeros((B, words), np.uint32)
+    for b in range(B):
+        for s in range(S):
+            if x[b, :, s].max() >= 0:
+                want[b, s >> 5] |= np.uint32(1 << (s & 31))
+    assert (mask == want).all()
+    sig = 1 / (1 + np.exp(-x))
+    assert np.allclose(maxsig, sig.max(axis=1), rtol=0, atol=1e-15)
+
+
+def pin_memindex_logits_layout(orc):
+    """orc_memindex_logits places layer l / request b at x[b, l] (checked with
+    per-element single-chunk scores on distinct layers)."""
+    rng = np.random.default_rng(13)
+    B, L, S, n_h, d = 2, 3, 5, 4, 8
+    q = f32_to_bf16_bits(rng.standard_normal((B, L, n_h, d)).astype(np.float32))
+    w = rng.standard_normal((B, L, n_h)).astype(np.float32)
+    K = f32_to_bf16_bits(rng.standard_normal((B, L, S, d)).astype(np.float32))
+    x = orc.memindex_logits(q, w, K)
+    for b in range(B):
+        for l in range(L):
+            for s in range(S):
+                qd = bf16_bits_to_f64(q[b, l])
+                kd = bf16_bits_to_f64(K[b, l, s])
+                want = float(np.sum(w[b, l].astype(np.float64) * np.maximum(qd @ kd, 0)))
+                assert abs(x[b, l, s] - want) <= 1e-12 * (1 + abs(want))
+
+
+# ---------------------------------------------------------------------------
+# top-k
+# ---------------------------------------------------------------------------
+
+def pin_topk_bruteforce(orc):
+    """Top-k with heavy ties vs a brute-force ordering by (x desc, id asc);
+    output sorted by id, padded with -1; every chosen beats every other."""
+    rng = np.random.default_rng(17)
+    for n, k in [(0, 8), (1, 8), (5, 8), (8, 8), (17, 8), (40, 8), (300, 64)]:
+        ids = rng.permutation(1000)[:n].astype(np.int64)
+        x = rng.integers(-3, 4, n).astype(np.float64)
+        if n > 3:
+            x[2] = np.nan
+            x[3] = -np.inf
+        idx, sc, m = orc.topk(ids, x, k)
+        assert m == min(n, k)
+        assert list(idx) == expected_topk(ids, x, k), (n, k)
+        chosen = set(int(i) for i in idx if i >= 0)
+        xs = {int(i): (-math.inf if math.isnan(v) else v) for i, v in zip(ids, x)}
+        for a in chosen:
+            for b in set(xs) - chosen:
+                assert (xs[a], -a) > (xs[b], -b)
+
+
+def pin_topk_512_random(orc):
+    rng = np.random.default_rng(19)
+    n, k = 4096, 512
+    ids = np.arange(n, dtype=np.int64)
+    x = np.round(rng.standard_normal(n), 2)
+    idx, _, m = orc.topk(ids, x, k)
+    assert m == k
+    assert list(idx) == expected_topk(ids, x, k)
+
+
+# ---------------------------------------------------------------------------
+# paged (Level-2) top-k
+# ---------------------------------------------------------------------------
+
+def _paged_case(rng, Q=3, R=5, n_pages=9, page=4, n_h=3, d=8):
+    P = Q * R + 2
+    q = f32_to_bf16_bits(rng.standard_normal((Q, n_h, d)).astype(np.float32))
+    w = rng.standard_normal((Q, n_h)).astype(np.float32)
+    k8 = rng.integers(0, 256, (P, page, d)).astype(np.uint8)
+    k8[(k8 & 0x7F) == 0x7F] = 0x33
+    scale = (rng.random((P, page)) + 0.1).astype(np.float32)
+    phys = rng.permutation(P)[: Q * R].reshape(Q, R).astype(np.int32)
+    logical = np.stack([rng.permutation(n_pages)[:R] for _ in range(Q)]).astype(np.int32)
+    return q, w, k8, scale, phys, logical, n_pages, page
+
+
+def pin_paged_mode_a(orc):
+    """Mode A (non-resident logits at -inf over the full logical chunk range):
+    paged top-k = brute-force top-k over all n_pages*page logical chunks of a
+    dense, scattered copy of the resident keys."""
+    rng = np.random.default_rng(23)
+    for k in (6, 40):
+        q, w, k8, scale, phys, logical, n_pages, page = _paged_case(rng)
+        idx, _ = orc.paged_topk(q, w, k8, scale, phys, logical, k=k)
+        Q, R = phys.shape
+        for qi in range(Q):
+            dense = np.full(n_pages * page, -math.inf)
+            for j in range(R):
+                for o in range(page):
+                    dense[logical[qi, j] * page + o] = orc.score_fp8(q[qi], w[qi], k8[phys[qi, j], o],
+                                                                     scale[phys[qi, j], o])
+            resident = [lp * page + o for lp in sorted(set(logical[qi].tolist())) for o in range(page)]
+            want = expected_topk(resident, [dense[i] for i in resident], k)
+            assert list(idx[qi]) == want, qi
+
+
+def pin_paged_row_order_and_nres(orc):
+    """Page-table row order does not matter; n_res limits the pages used."""
+    rng = np.random.default_rng(29)
+    q, w, k8, scale, phys, logical, n_pages, page = _paged_case(rng, Q=2, R=6)
+    idx, sc = orc.paged_topk(q, w, k8, scale, phys, logical, k=10)
+    perm = rng.permutation(phys.shape[1])
+    idx2, sc2 = orc.paged_topk(q, w, k8, scale, phys[:, perm].copy(), logical[:, perm].copy(), k=10)
+    assert (idx == idx2).all() and np.array_equal(sc, sc2)
+    n_res = np.array([2, 0], np.int32)
+    idx3, _ = orc.paged_topk(q, w, k8, scale, phys, logical, n_res=n_res, k=10)
+    allowed = {int(logical[0, j]) * page + o for j in range(2) for o in range(page)}
+    got = [int(i) for i in idx3[0] if i >= 0]
+    assert len(got) == 2 * page and set(got) <= allowed
+    assert (idx3[1] == -1).all()
+
+
+# ---------------------------------------------------------------------------
+# prefill
+# ---------------------------------------------------------------------------
+
+def pin_prefill_causal(orc):
+    """Candidates of a query at position pos are chunks s < min(S, pos // 4)
+    (chunk s covers tokens 4s..4s+3): brute force over tiny inputs."""
+    rng = np.random.default_rng(31)
+    T, S, n_h, d, k = 9, 23, 2, 8, 5
+    q = f32_to_bf16_bits(rng.standard_normal((T, n_h, d)).astype(np.float32))
+    w = rng.standard_normal((T, n_h)).astype(np.float32)
+    K = f32_to_bf16_bits(rng.standard_normal((S, d)).astype(np.float32))
+    pos = np.array([0, 3, 4, 7, 8, 22, 40, 91, 1000], np.int64)
+    idx, _ = orc.prefill_topk(q, w, pos, K, ratio=4, k=k)
+    for t in range(T):
+        lim = min(S, int(pos[t]) // 4)
+        assert orc.causal_limit(int(pos[t]), S, 4) == lim
+        xs = [orc.score_bf16(q[t], w[t], K[s]) for s in range(lim)]
+        assert list(idx[t]) == expected_topk(list(range(lim)), xs, k), t
+    assert (idx[0] == -1).all() and (idx[1] == -1).all()
+    assert list(idx[2]) == [0, -1, -1, -1, -1]
+
+
+# ---------------------------------------------------------------------------
+# planted construction (the generator's promise, checked through the oracle)
+# ---------------------------------------------------------------------------
+
+def pin_planted_tiny(orc):
+    """Tiny workload (1 query, S=4096, 12% planted): planted chunks score far
+    above the cold ones (~+50 vs N(-1.3, 1.9^2)), so every planted chunk is
+    resident and, being fewer than 512, all are in the top-512."""
+    import gen
+    cfg = gen.TINY
+    q, w, hot = gen.memindex_qw(cfg)
+    K = gen.memindex_keys_host(cfg, hot)
+    x = orc.memindex_logits(q, w, K)
+    mask, _ = orc.memindex_select(x, 0.5)
+    pl = gen.planted(cfg, 0, 0)
+    n_pl = int(pl.sum())
+    assert 0.10 * cfg.S < n_pl < 0.14 * cfg.S, n_pl
+    bits = np.unpackbits(mask.view(np.uint8), bitorder="little")[: cfg.S].astype(bool)
+    assert bits[pl].all()
+    assert x[0, 0, pl].min() > 20 and x[0, 0, ~pl].max() < 20
+    cold = x[0, 0, ~pl]
+    assert -1.6 < cold.mean() < -1.0 and 1.6 < cold.std() < 2.2, (cold.mean(), cold.std())
+    idx, _, m = orc.topk(np.arange(cfg.S), x[0, 0], 512)
+    assert m == 512 and set(np.nonzero(pl)[0]) <= set(idx.tolist())
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,96 @@
+"""Plant single mistakes into a copy of the oracle and check the pins catch them.
+
+Each mutant is one textual edit of oracle.c of the kind a careless restatement
+of the pages could make (a dropped ReLU, a transposed operand, a strict
+threshold, a reversed tie-break, a wrong E4M3 bias, ...).  The mutated copy is
+compiled into a temporary directory and all pins run against it in a child
+process (a crash counts as caught).  The test fails if any mutant survives.
+"""
+import json
+import os
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+import oracle
+
+TESTS = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(TESTS)
+
+MUTANTS = {
+    "relu_dropped": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
+    "relu_after_weight": ("x += (double)w[h] * relu;",
+                          "x += ((double)w[h] * dot > 0.0 ? (double)w[h] * dot : 0.0) + 0.0 * relu;"),
+    "weight_dropped": ("x += (double)w[h] * relu;", "x += relu;"),
+    "q_transposed": ("orc_bf16(q[(size_t)h * d + j])", "orc_bf16(q[(size_t)j * n_h + h])"),
+    "k_shifted": ("* k[j];", "* k[(j + 1) % d];"),
+    "threshold_strict": ("if (best >= thr)", "if (best > thr)"),
+    "union_by_min": ("if (sig > best) best = sig;", "if (l == 0 || sig < best) best = sig;"),
+    "sigmoid_sign": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));"),
+    "mask_bit_reversed": ("|= 1u << (s & 31);", "|= 1u << (31 - (s & 31));"),
+    "tie_higher_id_first": ("return a->id < b->id ? -1 : 1;", "return a->id > b->id ? -1 : 1;"),
+    "rank_ascending": ("if (xa > xb) return -1;\n  if (xa < xb) return 1;",
+                       "if (xa < xb) return -1;\n  if (xa > xb) return 1;"),
+    "output_not_id_sorted": ("qsort(c, (size_t)m, sizeof(orc_cand), orc_id_cmp);", ""),
+    "k_minus_one": ("int64_t m = n < k ? n : k;", "int64_t m = n < k ? n : k - 1;"),
+    "pad_zero": ("idx_out[i] = i < m ? (int32_t)c[i].id : -1;", "idx_out[i] = i < m ? (int32_t)c[i].id : 0;"),
+    "e4m3_bias_8": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_scale": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3_no_nan": ("if (e == 0xF && m == 0x7) return NAN;", ""),
+    "fp8_scale_ignored": ("float kv = (float)orc_e4m3(code) * scale;", "float kv = (float)orc_e4m3(code);"),
+    "fp8_dequant_in_fp64": ("float kv = (float)orc_e4m3(code) * scale;",
+                            "double kv = orc_e4m3(code) * (double)scale;"),
+    "paged_id_from_physical": ("c[n].id = lp * page_size + o;", "c[n].id = p * page_size + o;"),
+    "paged_nres_ignored": ("int64_t nr = n_res ? n_res[qi] : R;", "int64_t nr = R;"),
+    "causal_inclusive": ("int64_t lim = pos / ratio;", "int64_t lim = pos / ratio + 1;"),
+    "causal_token_not_chunk": ("int64_t lim = pos / ratio;", "int64_t lim = pos;"),
+    "nan_ranks_high": ("double xa = isnan(a->x) ? -INFINITY : a->x;", "double xa = isnan(a->x) ? INFINITY : a->x;"),
+}
+
+RUNNER = r"""
+import json, sys
+sys.path[:0] = [{root!r}, {tests!r}]
+import oracle, pins
+o = oracle.Oracle({so!r})
+failed = []
+for p in pins.ALL_PINS:
+    try:
+        p(o)
+    except Exception as e:
+        failed.append(p.__name__)
+print(json.dumps(failed))
+"""
+
+
+def _run_mutant(name, old, new, tmp):
+    src = open(oracle.SRC).read()
+    assert src.count(old) == 1, f"mutant {name}: target occurs {src.count(old)} times"
+    path = os.path.join(tmp, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    so = os.path.join(tmp, f"lib{name}.so")
+    oracle.compile_oracle(path, so, extra=("-w",))
+    code = RUNNER.format(root=ROOT, tests=TESTS, so=so)
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600, env=env)
+    if r.returncode != 0:
+        return name, ["<crashed>"]
+    return name, json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def test_every_mutant_is_caught():
+    with tempfile.TemporaryDirectory() as tmp:
+        with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+            results = dict(ex.map(lambda kv: _run_mutant(kv[0], *kv[1], tmp), MUTANTS.items()))
+    survivors = [n for n, failed in results.items() if not failed]
+    assert not survivors, f"mutants not caught by any pin: {survivors}"
+
+
+def test_unmutated_copy_passes_all_pins():
+    with tempfile.TemporaryDirectory() as tmp:
+        name, failed = _run_mutant("identity", "ORC_API int orc_num_threads(void) {",
+                                   "ORC_API int orc_num_threads(void) {", tmp)
+    assert failed == [], failed
