@@ -1,0 +1,189 @@
+/*
+ * fm_index.h -- C ABI of the GB300 (sm_103a) Lookahead-Sparse-Attention c4
+ * indexer library (libfm_index.so).
+ *
+ * The library computes the data-parallel hot path of the LSA indexer that
+ * scores DeepSeek-V4 compressed c4 chunk keys:
+ *   - the Memory Indexer score I = sigmoid(sum_h w_h * ReLU(q_h . K_s)), its
+ *     OR-union over indexer layers and the resident-set bitmask;
+ *   - the native lightning-indexer score sum_h w_h * ReLU(q_h . k_s) over the
+ *     resident 64-chunk pages, followed by the top-k (k <= 1024, normally 512);
+ *   - the same score for many prefill queries against dense chunk keys under
+ *     the causal chunk limit, followed by the top-k;
+ *   - the top-k select itself over caller-provided scores.
+ *
+ * Sources (page titles as published):
+ *   [FM] "FlashMemory-DeepSeek-V4: Lightning Index Ultra-Long Context via
+ *        Lookahead Sparse Attention" (paper summary), sec. 3 "Memory Indexer
+ *        scoring function" (I_{t,s}, the 0.5 threshold, the union over layers
+ *        10/12/20, R_t[s] = 1(max_l I^(l) >= 0.5)), sec. 6 (Mode A/B, Level 2
+ *        top-512 inside the resident set).
+ *   [RM] "FlashMemory-DeepSeek-V4" (repository README): "Retriever
+ *        architecture" (score formula, fused_w), "compressed_k format" (E4M3
+ *        key bytes + fp32 per-chunk scale, dequant = fp8.float() * scale),
+ *        "Two-level recall algorithm" (Level 1 / Level 2), key-optimisations
+ *        table ("Two-level recall", "Page-recall": 64-chunk pages).
+ *   [V4] "DeepSeek-V4 CSA + HCA explained": sec. 3 "C4Indexer" (n_heads = 64,
+ *        head_dim = 128, index_topk = 512; CSA-1 score, CSA-2 top-512), sec. 8
+ *        (4 tokens per c4 chunk; fewer than 512 chunks -> take them all).
+ *
+ * Conventions for every entry point
+ *   - Array pointers are caller-owned DEVICE memory unless stated otherwise;
+ *     the library never frees or retains them.  Layouts are dense row-major in
+ *     the order of the bracketed shape, except where a stride is passed.
+ *   - bf16 tensors are passed as uint16_t bit patterns; E4M3 keys as uint8_t
+ *     codes (OCP FP8 E4M3: bias 7, max 448, S.1111.111 = NaN).
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  The
+ *     host validates every argument before the first launch; on a non-OK
+ *     return nothing was enqueued (FM_ERR_CUDA: a launch failed; earlier
+ *     launches of the same call may have been enqueued).
+ *   - n_h must be 64 and d must be 128 (the C4Indexer's sizes).
+ *   - Ties in a top-k are broken by the lower chunk id.  Selected ids are
+ *     written in ascending id order and padded with -1 (scores with -inf).
+ *   - Kernels never trap and never spin without a bound.  A device-detected
+ *     problem (an out-of-range page id, a bounded wait that ran out) sets a
+ *     bit in the library's device status word and the affected work is
+ *     skipped; read it with fm_device_status().
+ *   - Thread-safety: calls may be issued from several host threads; the last
+ *     error message is thread-local.
+ */
+#ifndef FM_INDEX_H
+#define FM_INDEX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fm_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  FM_OK = 0,
+  FM_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, unsupported n_h/d/k   */
+  FM_ERR_UNSUPPORTED = 2, /* current device is not an sm_103 GPU                       */
+  FM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (see fm_last_error)     */
+  FM_ERR_WORKSPACE = 4    /* workspace pointer null/misaligned or smaller than needed  */
+} fm_status;
+
+/* Bits of the device status word (fm_device_status). */
+#define FM_DEVERR_PAGE_RANGE 0x1u  /* page_phys outside [0, P): that page was skipped     */
+#define FM_DEVERR_TIMEOUT 0x2u     /* a bounded on-chip wait ran out: the launch gave up  */
+#define FM_DEVERR_DUP_PAGE 0x4u    /* repeated logical page in one query's page table     */
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+int fm_version(void);
+
+/* Human-readable message for the last non-OK status returned on this thread. */
+const char* fm_last_error(void);
+
+/*
+ * Memory Indexer score, OR-union over layers and resident bitmask
+ * ([FM] sec. 3; [RM] "Retriever architecture", "Two-level recall", Level 1).
+ *
+ * For request b, layer l and chunk s:
+ *     x[b,l,s] = sum_{h<n_h} w[b,l,h] * ReLU( sum_{j<d} q[b,l,h,j] * K[b,l,s,j] )
+ * and the chunk is resident iff max_l sigmoid(x[b,l,s]) >= threshold, i.e. the
+ * OR of the per-layer sets { s | sigmoid(x[b,l,s]) >= threshold }.
+ *
+ *   q           [B, L, n_h, d] bf16             per-layer query heads
+ *   w           [B, L, n_h] fp32                fused head weights (the caller
+ *                                               has applied any head_dim^-1/2 *
+ *                                               n_h^-1/2 factor: [RM] fused_w)
+ *   keys        bf16, element (b,l,s,j) at keys[b*key_stride_b + l*key_stride_l
+ *               + s*d + j]; 16-byte aligned; strides multiples of 8 elements
+ *   B >= 0, 1 <= L <= 4, S >= 0 (S < 2^31), n_h = 64, d = 128
+ *   threshold   in (0, 1); 0.5 in the pages.  The device tests
+ *               max_l x >= log(threshold / (1 - threshold)).
+ *   mask_out    [B, ceil(S/32)] uint32: bit (s & 31) of word s >> 5 is chunk s;
+ *               bits at s >= S are written as zero.   (required)
+ *   maxsig_out  [B, S] fp32 max_l sigmoid(x), or NULL
+ *   logits_out  [B, L, S] fp32 x, or NULL
+ * Errors: FM_ERR_INVALID_ARG for any violated condition above.
+ */
+fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const uint16_t* keys,
+                                 int64_t key_stride_b, int64_t key_stride_l, int B, int L, int64_t S,
+                                 int n_h, int d, float threshold, uint32_t* mask_out, float* maxsig_out,
+                                 float* logits_out, fm_stream_t stream);
+
+/*
+ * Top-k select over caller-provided scores ([FM] sec. 3 "Top-k" of the native
+ * score; [V4] sec. 3 CSA-2 top-512).
+ *
+ *   scores      [rows, ld] fp32; row r has candidates 0 .. n_valid[r]-1
+ *               (n_valid == NULL: every row has n candidates), n <= ld
+ *   idx_out     [rows, k] int32: the min(k, n_r) best candidate indices by
+ *               (score desc, index asc), ascending, padded with -1
+ *   score_out   [rows, k] fp32 matching scores (-inf padding), or NULL
+ *   1 <= k <= 1024; n < 2^31.  NaN scores rank as -inf; -0 equals +0.
+ *   workspace   device scratch of at least fm_topk_workspace(rows, n) bytes,
+ *               256-byte aligned (may be NULL when that size is 0)
+ */
+size_t fm_topk_workspace(int rows, int64_t n);
+fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int64_t n,
+                         int k, int32_t* idx_out, float* score_out, void* workspace, size_t workspace_bytes,
+                         fm_stream_t stream);
+
+/*
+ * Native lightning-indexer score over the resident pages + top-k
+ * ([FM] sec. 3 C^CoreComp and sec. 6 Level 2; [RM] "Two-level recall" Level 2,
+ * "Page-recall" 64-chunk pages, "compressed_k format"; [V4] sec. 3 CSA-1/2).
+ *
+ * Query qi scores the chunks of its first n_res[qi] page-table entries:
+ *     y = sum_h w[qi,h] * ReLU( scale[p,o] * sum_j q[qi,h,j] * e4m3(k_pool[p,o,j]) )
+ * for pool page p = page_phys[qi,r] and offset o < 64; the chunk's id is
+ * page_logical[qi,r] * 64 + o.  Chunks outside the listed pages are not
+ * candidates (equivalent to Mode A's -inf).  The result does not depend on the
+ * order of a query's page-table entries.
+ *
+ *   q            [Q, n_h, d] bf16;  w [Q, n_h] fp32 (fused weights)
+ *   k_pool       [P, 64, d] E4M3 codes, 16-byte aligned
+ *   k_scale      [P, 64] fp32 per-chunk dequant scale
+ *   page_phys    [Q, R] int32 pool page; entries outside [0, P) are skipped and
+ *                flagged FM_DEVERR_PAGE_RANGE
+ *   page_logical [Q, R] int32 logical page id in [0, 2^25); distinct within
+ *                a query (a repeat is flagged FM_DEVERR_DUP_PAGE)
+ *   n_res        [Q] int32 entries used per query (clamped to [0, R]), or NULL = R
+ *   1 <= R <= 2048, 1 <= k <= 1024, Q >= 0
+ *   idx_out      [Q, k] int32 chunk ids; score_out [Q, k] fp32 or NULL
+ *   workspace    >= fm_native_topk_paged_workspace(Q, R) bytes, 256-byte aligned
+ */
+size_t fm_native_topk_paged_workspace(int Q, int R);
+fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
+                               int64_t P, const int32_t* page_phys, const int32_t* page_logical,
+                               const int32_t* n_res, int Q, int R, int n_h, int d, int k, int32_t* idx_out,
+                               float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
+
+/*
+ * Prefill: dense indexer scores of T query tokens against S chunk keys under
+ * the causal chunk limit, then top-k per query ([V4] sec. 3 CSA-1/2; chunk s
+ * covers tokens ratio*s .. ratio*s + ratio-1, [V4] sec. 1/8).
+ *
+ *     Y[t,s] = sum_h w[t,h] * ReLU( sum_j q[t,h,j] * keys[s,j] ),
+ * candidates of query t: s < min(S, floor(pos[t] / ratio)) (none if pos < 0).
+ *
+ *   q       [T, n_h, d] bf16, 16-byte aligned;  w [T, n_h] fp32
+ *   pos     [T] int64 token positions
+ *   keys    [S, d] bf16, 16-byte aligned
+ *   T >= 0, S >= 0 (S < 2^31), ratio >= 1 (4 for c4), 1 <= k <= 1024
+ *   idx_out [T, k] int32; score_out [T, k] fp32 or NULL
+ *   workspace >= fm_index_prefill_workspace(T, S) bytes, 256-byte aligned
+ */
+size_t fm_index_prefill_workspace(int T, int64_t S);
+fm_status fm_index_prefill_topk(const uint16_t* q, const float* w, const int64_t* pos, const uint16_t* keys,
+                                int T, int64_t S, int n_h, int d, int ratio, int k, int32_t* idx_out,
+                                float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
+
+/*
+ * Device status word of the current device: the OR of FM_DEVERR_* bits set by
+ * kernels since the last reset.  Synchronises `stream` before reading.  When
+ * reset != 0 the word is cleared after reading.  status_out is HOST memory.
+ */
+fm_status fm_device_status(uint32_t* status_out, int reset, fm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FM_INDEX_H */

@@ -1,0 +1,165 @@
+"""GB300-native Lookahead-Sparse-Attention c4 indexer.
+
+Thin Python binding of ``libfm_index.so`` (C ABI in ``include/fm_index.h``):
+the functions below carry the C names and only marshal torch tensors into
+pointers, sizes and the current CUDA stream.  Every step of the indexer runs
+in the library's sm_103a kernels; there is no Python or CPU fallback, and
+importing a function whose library is missing raises.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "FmError", "lib", "fm_version", "fm_last_error", "fm_device_status", "fm_memindex_score_mask",
+    "fm_topk_workspace", "fm_topk_select", "fm_native_topk_paged_workspace", "fm_native_topk_paged",
+    "fm_index_prefill_workspace", "fm_index_prefill_topk", "LIB_PATH",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfm_index.so")
+
+FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_CUDA, FM_ERR_WORKSPACE = 0, 1, 2, 3, 4
+FM_DEVERR_PAGE_RANGE, FM_DEVERR_TIMEOUT, FM_DEVERR_DUP_PAGE = 0x1, 0x2, 0x4
+
+_VP, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class FmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"fm status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfm_index.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        L.fm_version.restype = ctypes.c_int
+        L.fm_last_error.restype = ctypes.c_char_p
+        L.fm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), _I32, _VP]
+        L.fm_memindex_score_mask.argtypes = [_VP, _VP, _VP, _I64, _I64, _I32, _I32, _I64, _I32, _I32, _F, _VP,
+                                             _VP, _VP, _VP]
+        for name in ("fm_topk_workspace",):
+            if hasattr(L, name):
+                getattr(L, name).argtypes = [_I32, _I64]
+                getattr(L, name).restype = _SZ
+        if hasattr(L, "fm_topk_select"):
+            L.fm_topk_select.argtypes = [_VP, _I64, _VP, _I32, _I64, _I32, _VP, _VP, _VP, _SZ, _VP]
+        if hasattr(L, "fm_native_topk_paged_workspace"):
+            L.fm_native_topk_paged_workspace.argtypes = [_I32, _I32]
+            L.fm_native_topk_paged_workspace.restype = _SZ
+            L.fm_native_topk_paged.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
+                                               _I32, _VP, _VP, _VP, _SZ, _VP]
+        if hasattr(L, "fm_index_prefill_workspace"):
+            L.fm_index_prefill_workspace.argtypes = [_I32, _I64]
+            L.fm_index_prefill_workspace.restype = _SZ
+            L.fm_index_prefill_topk.argtypes = [_VP, _VP, _VP, _VP, _I32, _I64, _I32, _I32, _I32, _I32, _VP, _VP,
+                                                _VP, _SZ, _VP]
+        for name in ("fm_memindex_score_mask", "fm_topk_select", "fm_native_topk_paged", "fm_index_prefill_topk",
+                     "fm_device_status"):
+            if hasattr(L, name):
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != FM_OK:
+        raise FmError(status, fm_last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def fm_version() -> int:
+    return lib().fm_version()
+
+
+def fm_last_error() -> str:
+    return lib().fm_last_error().decode()
+
+
+def fm_device_status(reset: bool = True, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(lib().fm_device_status(ctypes.byref(v), int(reset), _stream(stream)))
+    return v.value
+
+
+def fm_memindex_score_mask(q, w, keys, mask_out, maxsig_out=None, logits_out=None, threshold: float = 0.5,
+                           stream=None) -> None:
+    """q [B,L,64,128] bf16, w [B,L,64] fp32, keys [B,L,S,128] bf16 (any b/l
+    strides, rows dense), mask_out [B, ceil(S/32)] int32/uint32,
+    maxsig_out [B,S] fp32 or None, logits_out [B,L,S] fp32 or None."""
+    B, L, n_h, d = q.shape
+    S = keys.shape[2]
+    if keys.stride(3) != 1 or keys.stride(2) != d:
+        raise ValueError("keys rows must be dense [.., S, d]")
+    _check(lib().fm_memindex_score_mask(_ptr(q), _ptr(w), _ptr(keys), keys.stride(0), keys.stride(1), B, L, S, n_h,
+                                        d, float(threshold), _ptr(mask_out), _ptr(maxsig_out), _ptr(logits_out),
+                                        _stream(stream)))
+
+
+def fm_topk_workspace(rows: int, n: int) -> int:
+    return lib().fm_topk_workspace(rows, n)
+
+
+def fm_topk_select(scores, k: int, idx_out, score_out=None, n_valid=None, n=None, workspace=None,
+                   stream=None) -> None:
+    """scores [rows, ld] fp32 (row stride ld, unit column stride); n_valid [rows]
+    int32 or None; idx_out [rows, k] int32; score_out [rows, k] fp32 or None."""
+    rows, ld = scores.shape[0], scores.stride(0)
+    n = scores.shape[1] if n is None else n
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_topk_select(_ptr(scores), ld, _ptr(n_valid), rows, n, k, _ptr(idx_out), _ptr(score_out),
+                                _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_native_topk_paged_workspace(Q: int, R: int) -> int:
+    return lib().fm_native_topk_paged_workspace(Q, R)
+
+
+def fm_native_topk_paged(q, w, k_pool, k_scale, page_phys, page_logical, k: int, idx_out, score_out=None,
+                         n_res=None, workspace=None, stream=None) -> None:
+    """q [Q,64,128] bf16, w [Q,64] fp32, k_pool [P,64,128] uint8 E4M3 codes,
+    k_scale [P,64] fp32, page_phys/page_logical [Q,R] int32, n_res [Q] int32
+    or None, idx_out [Q,k] int32, score_out [Q,k] fp32 or None."""
+    Q, n_h, d = q.shape
+    R = page_phys.shape[1]
+    P = k_pool.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_native_topk_paged(_ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), P, _ptr(page_phys),
+                                      _ptr(page_logical), _ptr(n_res), Q, R, n_h, d, k, _ptr(idx_out),
+                                      _ptr(score_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_index_prefill_workspace(T: int, S: int) -> int:
+    return lib().fm_index_prefill_workspace(T, S)
+
+
+def fm_index_prefill_topk(q, w, pos, keys, k: int, idx_out, score_out=None, ratio: int = 4, workspace=None,
+                          stream=None) -> None:
+    """q [T,64,128] bf16, w [T,64] fp32, pos [T] int64, keys [S,128] bf16,
+    idx_out [T,k] int32, score_out [T,k] fp32 or None."""
+    T, n_h, d = q.shape
+    S = keys.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_index_prefill_topk(_ptr(q), _ptr(w), _ptr(pos), _ptr(keys), T, S, n_h, d, ratio, k,
+                                       _ptr(idx_out), _ptr(score_out), _ptr(workspace), ws_bytes, _stream(stream)))

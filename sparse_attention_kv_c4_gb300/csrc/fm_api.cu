@@ -1,0 +1,141 @@
+// fm_api.cu -- the C ABI of libfm_index.so: argument validation, device
+// checks, tensor-map encoding, error reporting, dispatch to the launchers.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cudaTypedefs.h>
+
+#include "fm_common.cuh"
+#include "fm_internal.h"
+
+#define FM_API extern "C" __attribute__((visibility("default")))
+
+// Device status word: OR of FM_DEVERR_* bits raised by kernels.
+__device__ unsigned int g_fm_device_status;
+
+namespace fm {
+
+static thread_local char t_last_error[512] = "no error";
+
+fm_status set_error(fm_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fm_status check_device(int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  if (major != 10 || minor != 3)
+    return set_error(FM_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, major,
+                     minor);
+  if (num_sms) *num_sms = sms;
+  return FM_OK;
+}
+
+fm_status status_word(unsigned int** ptr) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_fm_device_status);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+  *ptr = static_cast<unsigned int*>(p);
+  return FM_OK;
+}
+
+fm_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return set_error(FM_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  uint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = encode(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), (const cuuint64_t*)dims,
+                      (const cuuint64_t*)strides_bytes, (const cuuint32_t*)box, (const cuuint32_t*)estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(FM_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return FM_OK;
+}
+
+}  // namespace fm
+
+using namespace fm;
+
+FM_API int fm_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+FM_API const char* fm_last_error(void) { return t_last_error; }
+
+FM_API fm_status fm_device_status(uint32_t* status_out, int reset, fm_stream_t stream) {
+  if (status_out == nullptr) return set_error(FM_ERR_INVALID_ARG, "fm_device_status: status_out is NULL");
+  unsigned int* dptr = nullptr;
+  fm_status st = status_word(&dptr);
+  if (st != FM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, dptr, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && reset) e = cudaMemsetAsync(dptr, 0, sizeof(unsigned int), s);
+  if (e == cudaSuccess && reset) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_device_status: %s", cudaGetErrorString(e));
+  *status_out = v;
+  return FM_OK;
+}
+
+FM_API fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const uint16_t* keys,
+                                        int64_t key_stride_b, int64_t key_stride_l, int B, int L, int64_t S,
+                                        int n_h, int d, float threshold, uint32_t* mask_out, float* maxsig_out,
+                                        float* logits_out, fm_stream_t stream) {
+  if (n_h != 64 || d != 128)
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask: n_h=%d d=%d (need 64, 128)", n_h, d);
+  if (B < 0 || L < 1 || L > 4 || S < 0 || S >= (int64_t(1) << 31))
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask: bad sizes B=%d L=%d S=%lld", B, L, (long long)S);
+  if (!(threshold > 0.0f && threshold < 1.0f))
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask: threshold %g not in (0, 1)", (double)threshold);
+  if (B == 0 || S == 0) return FM_OK;
+  if (!q || !w || !keys || !mask_out)
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask: q, w, keys and mask_out must be non-NULL");
+  if (!aligned(q, 16) || !aligned(keys, 16) || !aligned(w, 16) || !aligned(mask_out, 4) ||
+      (maxsig_out && !aligned(maxsig_out, 4)) || (logits_out && !aligned(logits_out, 4)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask: q/keys/w need 16-byte alignment");
+  if (key_stride_l < S * d || key_stride_b < (int64_t)(L - 1) * key_stride_l + S * d || key_stride_l % 8 != 0 ||
+      key_stride_b % 8 != 0)
+    return set_error(FM_ERR_INVALID_ARG,
+                     "fm_memindex_score_mask: key strides (b=%lld, l=%lld) must be multiples of 8 elements and "
+                     "lay the [L, S, d] blocks out without overlap",
+                     (long long)key_stride_b, (long long)key_stride_l);
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  unsigned int* status = nullptr;
+  st = status_word(&status);
+  if (st != FM_OK) return st;
+
+  MemindexArgs a;
+  a.q = q;
+  a.w = w;
+  a.keys = keys;
+  a.key_stride_b = key_stride_b;
+  a.key_stride_l = key_stride_l;
+  a.B = B;
+  a.L = L;
+  a.S = S;
+  a.thr_logit = (float)log((double)threshold / (1.0 - (double)threshold));
+  a.mask = mask_out;
+  a.maxsig = maxsig_out;
+  a.logits = logits_out;
+  return launch_memindex(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
+}

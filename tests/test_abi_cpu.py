@@ -1,0 +1,71 @@
+"""The C ABI library loads, exports every declared entry point and rejects bad
+arguments on the host before touching the GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fm_index.h")
+
+
+def declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fm_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import sparse_attention_kv_c4_gb300 as fm
+    if not os.path.exists(fm.LIB_PATH):
+        from sparse_attention_kv_c4_gb300 import _build
+        _build.build()
+    return fm.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for n in ("fm_memindex_score_mask", "fm_native_topk_paged", "fm_index_prefill_topk", "fm_topk_select",
+              "fm_native_topk_paged_workspace", "fm_index_prefill_workspace", "fm_topk_workspace",
+              "fm_last_error", "fm_device_status", "fm_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_version(lib):
+    assert lib.fm_version() >= 10000
+
+
+def test_memindex_rejects_bad_args_on_host(lib):
+    import sparse_attention_kv_c4_gb300 as fm
+    f = lib.fm_memindex_score_mask
+    fake = 4096  # never dereferenced: validation fails first
+    # n_h != 64
+    assert f(fake, fake, fake, 3 * 128 * 128, 128 * 128, 1, 3, 128, 32, 128, 0.5, fake, None, None, None) == 1
+    assert "n_h" in fm.fm_last_error()
+    # L > 4
+    assert f(fake, fake, fake, 5 * 128 * 128, 128 * 128, 1, 5, 128, 64, 128, 0.5, fake, None, None, None) == 1
+    # threshold outside (0, 1)
+    assert f(fake, fake, fake, 3 * 128 * 128, 128 * 128, 1, 3, 128, 64, 128, 1.0, fake, None, None, None) == 1
+    # NULL mask
+    assert f(fake, fake, fake, 3 * 128 * 128, 128 * 128, 1, 3, 128, 64, 128, 0.5, None, None, None, None) == 1
+    # misaligned keys
+    assert f(fake, fake, fake + 2, 3 * 128 * 128, 128 * 128, 1, 3, 128, 64, 128, 0.5, fake, None, None, None) == 1
+    # overlapping strides
+    assert f(fake, fake, fake, 128 * 128, 128 * 128, 2, 3, 128, 64, 128, 0.5, fake, None, None, None) == 1
+    # empty work is OK without a device
+    assert f(None, None, None, 0, 0, 0, 3, 128, 64, 128, 0.5, None, None, None, None) == 0
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import sparse_attention_kv_c4_gb300 as fm
+    monkeypatch.setattr(fm, "_lib", None)
+    monkeypatch.setattr(fm, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        fm.lib()
