@@ -139,3 +139,124 @@ FM_API fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const
   a.logits = logits_out;
   return launch_memindex(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
 }
+
+FM_API size_t fm_topk_workspace(int rows, int64_t n) {
+  (void)rows;
+  (void)n;
+  return 0;
+}
+
+FM_API fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int64_t n, int k,
+                                int32_t* idx_out, float* score_out, void* workspace, size_t workspace_bytes,
+                                fm_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (rows < 0 || n < 0 || n >= (int64_t(1) << 31) || k < 1 || k > 1024)
+    return set_error(FM_ERR_INVALID_ARG, "fm_topk_select: bad sizes rows=%d n=%lld k=%d (1 <= k <= 1024)", rows,
+                     (long long)n, k);
+  if (rows == 0) return FM_OK;
+  if (ld < n) return set_error(FM_ERR_INVALID_ARG, "fm_topk_select: ld=%lld < n=%lld", (long long)ld, (long long)n);
+  if (!idx_out || (n > 0 && !scores))
+    return set_error(FM_ERR_INVALID_ARG, "fm_topk_select: scores and idx_out must be non-NULL");
+  if (!aligned(scores, 4) || !aligned(idx_out, 4) || (score_out && !aligned(score_out, 4)) ||
+      (n_valid && !aligned(n_valid, 4)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_topk_select: pointers need 4-byte alignment");
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  return launch_topk_rows(scores, ld, n_valid, rows, (int)n, k, nullptr, 0, idx_out, score_out,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+FM_API size_t fm_native_topk_paged_workspace(int Q, int R) {
+  if (Q < 0 || R < 1 || R > 2048) return 0;
+  return paged_workspace_bytes(Q, R);
+}
+
+FM_API fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
+                                      int64_t P, const int32_t* page_phys, const int32_t* page_logical,
+                                      const int32_t* n_res, int Q, int R, int n_h, int d, int k, int32_t* idx_out,
+                                      float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream) {
+  if (n_h != 64 || d != 128)
+    return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: n_h=%d d=%d (need 64, 128)", n_h, d);
+  if (Q < 0 || R < 1 || R > 2048 || k < 1 || k > 1024 || P < 0 || P > (int64_t(1) << 26))
+    return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: bad sizes Q=%d R=%d k=%d P=%lld", Q, R, k,
+                     (long long)P);
+  if (Q == 0) return FM_OK;
+  if (!q || !w || !page_phys || !page_logical || !idx_out || (P > 0 && (!k_pool || !k_scale)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(w, 16) || (k_pool && !aligned(k_pool, 16)) || (k_scale && !aligned(k_scale, 16)) ||
+      !aligned(page_phys, 4) || !aligned(page_logical, 4) || (n_res && !aligned(n_res, 4)) ||
+      !aligned(idx_out, 4) || (score_out && !aligned(score_out, 4)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: q/w/k_pool/k_scale need 16-byte alignment");
+  const size_t need = paged_workspace_bytes(Q, R);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return set_error(FM_ERR_WORKSPACE, "fm_native_topk_paged: workspace needs %zu bytes, 256-byte aligned", need);
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  unsigned int* status = nullptr;
+  st = status_word(&status);
+  if (st != FM_OK) return st;
+  PagedArgs a;
+  a.q = q;
+  a.w = w;
+  a.k_pool = k_pool;
+  a.k_scale = k_scale;
+  a.P = P > 0 ? P : 1;
+  a.page_phys = page_phys;
+  a.page_logical = page_logical;
+  a.n_res = n_res;
+  a.Q = Q;
+  a.R = R;
+  a.k = k;
+  a.idx_out = idx_out;
+  a.score_out = score_out;
+  a.workspace = workspace;
+  if (P == 0) a.P = 0;
+  return launch_paged(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+FM_API size_t fm_index_prefill_workspace(int T, int64_t S) {
+  if (T < 0 || S < 0) return 0;
+  return prefill_workspace_bytes(T, S);
+}
+
+FM_API fm_status fm_index_prefill_topk(const uint16_t* q, const float* w, const int64_t* pos, const uint16_t* keys,
+                                       int T, int64_t S, int n_h, int d, int ratio, int k, int32_t* idx_out,
+                                       float* score_out, void* workspace, size_t workspace_bytes,
+                                       fm_stream_t stream) {
+  if (n_h != 64 || d != 128)
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_topk: n_h=%d d=%d (need 64, 128)", n_h, d);
+  if (T < 0 || S < 0 || S >= (int64_t(1) << 31) || ratio < 1 || k < 1 || k > 1024)
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_topk: bad sizes T=%d S=%lld ratio=%d k=%d", T,
+                     (long long)S, ratio, k);
+  if (T == 0) return FM_OK;
+  if (!q || !w || !pos || !idx_out || (S > 0 && !keys))
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_topk: required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(pos, 8) || (keys && !aligned(keys, 16)) ||
+      !aligned(idx_out, 4) || (score_out && !aligned(score_out, 4)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_topk: q/w/keys need 16-byte alignment");
+  const size_t need = prefill_workspace_bytes(T, S);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return set_error(FM_ERR_WORKSPACE, "fm_index_prefill_topk: workspace needs %zu bytes, 256-byte aligned", need);
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  unsigned int* status = nullptr;
+  st = status_word(&status);
+  if (st != FM_OK) return st;
+  PrefillArgs a;
+  a.q = q;
+  a.w = w;
+  a.pos = pos;
+  a.keys = keys;
+  a.T = T;
+  a.S = S;
+  a.ratio = ratio;
+  a.k = k;
+  a.idx_out = idx_out;
+  a.score_out = score_out;
+  a.workspace = workspace;
+  return launch_prefill(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
+}

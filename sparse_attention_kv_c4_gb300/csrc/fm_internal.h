@@ -42,4 +42,42 @@ struct MemindexArgs {
 };
 fm_status launch_memindex(const MemindexArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
 
+// One CTA per row; candidate i of row r has id page_ids[r*page_ld + i/64]*64 + i%64
+// when page_ids is non-null, else i.
+fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int n, int k,
+                           const int32_t* page_ids, int64_t page_ld, int32_t* idx_out, float* score_out,
+                           cudaStream_t stream);
+
+struct PagedArgs {
+  const uint16_t* q;
+  const float* w;
+  const uint8_t* k_pool;
+  const float* k_scale;
+  int64_t P;
+  const int32_t* page_phys;
+  const int32_t* page_logical;
+  const int32_t* n_res;
+  int Q, R, k;
+  int32_t* idx_out;
+  float* score_out;
+  void* workspace;
+};
+size_t paged_workspace_bytes(int Q, int R);
+
+struct PrefillArgs {
+  const uint16_t* q;
+  const float* w;
+  const int64_t* pos;
+  const uint16_t* keys;
+  int T;
+  int64_t S;
+  int ratio, k;
+  int32_t* idx_out;
+  float* score_out;
+  void* workspace;
+};
+size_t prefill_workspace_bytes(int T, int64_t S);
+fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
+fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
+
 }  // namespace fm

@@ -1,0 +1,509 @@
+// paged.cu -- native lightning-indexer scoring over the resident 64-chunk
+// pages, followed by the top-k select.
+//
+// Computes, for query qi and resident page-table entry r (the "FlashMemory-
+// DeepSeek-V4" README, "Two-level recall algorithm" Level 2 and the
+// "compressed_k format"; "DeepSeek-V4 CSA + HCA explained", sec. 3 CSA-1):
+//     y[qi, chunk] = sum_h w[qi,h] * ReLU( scale[p,o] * (q[qi,h,:] . e4m3(k[p,o,:])) )
+// with p = page_phys[qi,r], chunk id = page_logical[qi,r] * 64 + o, then the
+// top-k of y by (y desc, id asc) (CSA-2), ids ascending.
+//
+// GB300 mapping (three launches):
+//  1. paged_prep_kernel (one CTA per query): sorts the query's page-table
+//     entries by logical page id (so candidate order == chunk-id order and the
+//     result cannot depend on the table's row order), drops out-of-range and
+//     repeated entries (flagging the device status word), and splits the bf16
+//     query into two E4M3 terms per head: q_h = 2^e_h * (t1 + t2), with e_h a
+//     power of two putting max|q_h| in (224, 448].  t1 = RNE_e4m3(q_h 2^-e_h),
+//     t2 = RNE_e4m3(q_h 2^-e_h - t1); the pair reproduces every bf16 element
+//     whose residual stays inside E4M3's range.  2^e_h is folded into w.
+//  2. paged_score_kernel (persistent, one CTA per SM): TMA loads two E4M3 pages
+//     (2 x 8 KB, SWIZZLE_128B) per 128-chunk tile straight into the UMMA A
+//     operand -- no conversion pass; tcgen05.mma kind::f8f6f4 M=128 chunks x
+//     N=64 heads x K=32, issued once with t1 and once with t2 accumulating into
+//     the same TMEM columns; the epilogue (thread = chunk) reads its 64 head
+//     dots and the chunk's scale and writes y to the workspace.
+//  3. the block top-k (topk.cuh), mapping candidate i to its chunk id.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include "fm_common.cuh"
+#include "fm_internal.h"
+
+namespace fm {
+namespace {
+
+constexpr int kPage = 64;
+constexpr int kM = 128;                  // chunks per tile = 2 pages
+constexpr int kHeads = 64;
+constexpr int kDim = 128;                // bytes per E4M3 key row
+constexpr int kPageBytes = kPage * kDim; // 8 KB
+constexpr int kTileBytes = kM * kDim;    // 16 KB
+constexpr int kQBytes = 2 * kHeads * kDim;  // t1 rows 0..63, t2 rows 64..127
+constexpr int kMaxR = 2048;
+constexpr int kMaxStages = 12;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 128;
+constexpr int kPrepThreads = 256;
+
+// --------------------------------------------------------------------------
+// 1. prep: sort pages, validate, split q
+// --------------------------------------------------------------------------
+
+// fp32 -> E4M3 code, round to nearest even (|f| <= 448 here).
+FM_DEV uint32_t e4m3_rne(float f) {
+  return (uint32_t)__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
+}
+FM_DEV float e4m3_value(uint32_t code) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+__global__ void __launch_bounds__(kPrepThreads)
+    paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                      const int32_t* __restrict__ page_phys, const int32_t* __restrict__ page_logical,
+                      const int32_t* __restrict__ n_res, int R, int64_t P, int Rpow2,
+                      int32_t* __restrict__ s_logical, int32_t* __restrict__ s_phys,
+                      int32_t* __restrict__ nres_eff, int32_t* __restrict__ n_valid, uint8_t* __restrict__ qsplit,
+                      float* __restrict__ wq, unsigned int* __restrict__ status) {
+  __shared__ unsigned long long keys[kMaxR];
+  __shared__ uint32_t warp_tot[kPrepThreads / 32];
+  const int qi = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int nr = R;
+  if (n_res != nullptr) {
+    const int v = n_res[qi];
+    nr = v < 0 ? 0 : (v > R ? R : v);
+  }
+  for (int i = tid; i < Rpow2; i += kPrepThreads)
+    keys[i] = i < nr ? (((unsigned long long)(uint32_t)page_logical[(int64_t)qi * R + i] << 32) | (uint32_t)i)
+                     : ~0ull;
+  __syncthreads();
+  for (int k2 = 2; k2 <= Rpow2; k2 <<= 1)
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < Rpow2; i += kPrepThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = keys[i], b = keys[ixj];
+          if ((a > b) == ((i & k2) == 0)) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  uint32_t base = 0;
+  for (int i0 = 0; i0 < Rpow2; i0 += kPrepThreads) {
+    const int i = i0 + tid;
+    uint32_t valid = 0;
+    int32_t lg = 0, ph = 0;
+    if (i < nr) {
+      lg = (int32_t)(keys[i] >> 32);
+      ph = page_phys[(int64_t)qi * R + (uint32_t)keys[i]];
+      const bool dup = i > 0 && (keys[i - 1] >> 32) == (keys[i] >> 32);
+      const bool range_ok = ph >= 0 && ph < P && lg >= 0 && lg < (1 << 25);
+      if (dup) atomicOr(status, FM_DEV_DUP_PAGE);
+      if (!range_ok) atomicOr(status, FM_DEV_PAGE_RANGE);
+      valid = (!dup && range_ok) ? 1u : 0u;
+    }
+    // block exclusive scan of `valid`
+    uint32_t x = valid;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+    for (int wi = 0; wi < kPrepThreads / 32; ++wi) {
+      if (wi < warp) before += warp_tot[wi];
+      total += warp_tot[wi];
+    }
+    if (valid) {
+      s_logical[(int64_t)qi * R + base + before + x - 1] = lg;
+      s_phys[(int64_t)qi * R + base + before + x - 1] = ph;
+    }
+    base += total;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    nres_eff[qi] = (int32_t)base;
+    n_valid[qi] = (int32_t)base * kPage;
+  }
+  // q split: warp handles heads warp, warp+8, ...; lane handles d = 4*lane..4*lane+3
+  for (int h = warp; h < kHeads; h += kPrepThreads / 32) {
+    const uint16_t* qh = q + ((int64_t)qi * kHeads + h) * kDim;
+    float v[4], amax = 0.f;
+    for (int j = 0; j < 4; ++j) {
+      v[j] = __uint_as_float((uint32_t)qh[4 * lane + j] << 16);
+      amax = fmaxf(amax, fabsf(v[j]));
+    }
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // e: power of two putting amax * 2^-e in (224, 448] (E4M3's top binades)
+    int e = 0;
+    if (amax > 0.f && isfinite(amax)) {
+      e = ilogbf(amax) - 8;
+      if (ldexpf(amax, -e) > 448.f) e += 1;
+    }
+    uint8_t* t1 = qsplit + ((int64_t)qi * 2 * kHeads + h) * kDim;
+    uint8_t* t2 = t1 + (int64_t)kHeads * kDim;
+    for (int j = 0; j < 4; ++j) {
+      const float s = ldexpf(v[j], -e);
+      const uint32_t c1 = e4m3_rne(s);
+      const float r = s - e4m3_value(c1);
+      t1[4 * lane + j] = (uint8_t)c1;
+      t2[4 * lane + j] = (uint8_t)e4m3_rne(r);
+    }
+    if (lane == 0) wq[(int64_t)qi * kHeads + h] = ldexpf(w[(int64_t)qi * kHeads + h], e);
+  }
+}
+
+// --------------------------------------------------------------------------
+// 2. persistent tcgen05 scorer
+// --------------------------------------------------------------------------
+
+struct ScoreParams {
+  const int32_t* s_phys;
+  const int32_t* nres_eff;
+  const float* k_scale;
+  const float* wq;
+  float* scores;  // [Q, R*64]
+  unsigned int* status;
+  int64_t total_tiles;
+  int tiles_per_q;
+  int R;
+  int stages;
+};
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 A/B, fp32 accumulate, K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+FM_DEV void umma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_score_kernel(const __grid_constant__ CUtensorMap tmap_pool, const __grid_constant__ CUtensorMap tmap_q,
+                       const ScoreParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_smem = smem;                       // 16 KB
+  uint8_t* a_smem = smem + kQBytes;             // stages x 16 KB
+  int32_t* phys_s = reinterpret_cast<int32_t*>(a_smem + p.stages * kTileBytes);  // kMaxR
+
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_qfull, bar_qempty, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int stages = p.stages;
+  const int64_t t_begin = p.total_tiles * blockIdx.x / gridDim.x;
+  const int64_t t_end = p.total_tiles * (blockIdx.x + 1) / gridDim.x;
+  const int64_t ld = (int64_t)p.R * kPage;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 128);
+    }
+    mbar_init(&bar_qfull, 1);
+    mbar_init(&bar_qempty, 1);
+    mbar_init(&bar_drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmap_pool);
+    tma_prefetch(&tmap_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+
+  if (warp == 0) {
+    // -------------------------------- producer (whole warp) ------------------
+    uint32_t stage = 0, phase = 0, q_phase = 0;
+    int issued[kMaxStages];
+    for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
+    int q_issued = -1;
+    int64_t cur_q = -1;
+    int nres = 0;
+    bool ok = true;
+    for (int64_t t = t_begin; t < t_end && ok; ++t) {
+      const int64_t qi = t / p.tiles_per_q;
+      const int tile = (int)(t % p.tiles_per_q);
+      if (qi != cur_q) {
+        nres = p.nres_eff[qi];
+        __syncwarp();
+        for (int i = lane; i < nres; i += 32) phys_s[i] = p.s_phys[qi * p.R + i];
+        __syncwarp();
+        cur_q = qi;
+        if (nres > 0 && lane == 0) {
+          if (q_issued >= 0) {
+            if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) ok = false;
+            q_phase ^= 1;
+          }
+          if (ok) {
+            mbar_arrive_expect_tx(&bar_qfull, (uint32_t)kQBytes);
+            tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * 2 * kHeads));
+            q_issued = (q_issued + 1) & 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      if (2 * tile >= nres) continue;
+      if (lane == 0) {
+        if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) {
+          ok = false;
+        } else {
+          const int npg = nres - 2 * tile >= 2 ? 2 : 1;
+          mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)(npg * kPageBytes));
+          for (int h = 0; h < npg; ++h)
+            tma_load_2d(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0,
+                        phys_s[2 * tile + h] * kPage);
+          issued[stage] = (int)phase;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (++stage == (uint32_t)stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (lane == 0 && abort_flag) {
+      for (int s = 0; s < stages; ++s)
+        if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
+      if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------ UMMA issuer -----------------------------
+      const uint32_t idesc = idesc_e4m3_f32(kM, kHeads);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0;
+      int64_t cur_q = -1;
+      int nres = 0;
+      bool have_q = false, ok = true;
+      for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        const int64_t qi = t / p.tiles_per_q;
+        const int tile = (int)(t % p.tiles_per_q);
+        if (qi != cur_q) {
+          nres = p.nres_eff[qi];
+          cur_q = qi;
+          if (nres > 0) {
+            if (have_q) umma_commit(&bar_qempty);
+            if (!mbar_wait(&bar_qfull, q_phase, &abort_flag, p.status)) break;
+            q_phase ^= 1;
+            have_q = true;
+            tc_fence_after();
+          }
+        }
+        if (2 * tile >= nres) continue;
+        if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status)) break;
+        if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kHeads;
+        const uint32_t a_base = smem_u32(a_smem + stage * kTileBytes);
+        const uint32_t b_base = smem_u32(q_smem);
+#pragma unroll
+        for (int term = 0; term < 2; ++term)
+#pragma unroll
+          for (int k = 0; k < kDim / 32; ++k) {
+            const uint64_t ad = sdesc_sw128(a_base + k * 32);
+            const uint64_t bd = sdesc_sw128(b_base + term * (kHeads * kDim) + k * 32);
+            umma_e4m3_ss(d_tmem, ad, bd, idesc, (term | k) != 0 ? 1u : 0u);
+          }
+        umma_commit(&bar_empty[stage]);
+        umma_commit(&bar_tfull[acc]);
+        if (++stage == (uint32_t)stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit(&bar_drain);
+      mbar_wait_drain(&bar_drain, 0);
+    }
+  } else {
+    // -------------------------------- epilogue -------------------------------
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    int64_t cur_q = -1;
+    int nres = 0;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+      const int64_t qi = t / p.tiles_per_q;
+      const int tile = (int)(t % p.tiles_per_q);
+      if (qi != cur_q) {
+        nres = p.nres_eff[qi];
+        cur_q = qi;
+      }
+      if (2 * tile >= nres) continue;
+      const int j = 2 * tile + (row >> 6);
+      const bool valid = j < nres;
+      float sc = 0.f;
+      if (valid) sc = __ldg(p.k_scale + (int64_t)__ldg(p.s_phys + qi * p.R + j) * kPage + (row & 63));
+      if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kHeads;
+      tmem_ld32(taddr, r0);
+      tmem_ld32(taddr + 32, r1);
+      const float4* wl = reinterpret_cast<const float4*>(p.wq + qi * kHeads);
+      float wr[kHeads];
+#pragma unroll
+      for (int i = 0; i < kHeads / 4; ++i) {
+        const float4 v = __ldg(wl + i);
+        wr[4 * i] = v.x;
+        wr[4 * i + 1] = v.y;
+        wr[4 * i + 2] = v.z;
+        wr[4 * i + 3] = v.w;
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_tempty[acc]);
+      float y;
+      if (sc > 0.f) {
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 32; h += 2) {
+          x0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), x0);
+          x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), x1);
+          x2 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), x2);
+          x3 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), x3);
+        }
+        y = sc * ((x0 + x1) + (x2 + x3));
+      } else {
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          x0 = fmaf(wr[h], fmaxf(sc * __uint_as_float(r0[h]), 0.f), x0);
+          x1 = fmaf(wr[32 + h], fmaxf(sc * __uint_as_float(r1[h]), 0.f), x1);
+        }
+        y = x0 + x1;
+      }
+      if (valid) p.scores[qi * ld + (int64_t)tile * kM + row] = y;
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct PagedWs {
+  int32_t *s_logical, *s_phys, *nres_eff, *n_valid;
+  uint8_t* qsplit;
+  float *wq, *scores;
+  size_t bytes;
+};
+
+PagedWs paged_ws_layout(void* base, int Q, int R) {
+  PagedWs w;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    uint8_t* p = b ? b + off : nullptr;
+    off += align256(n);
+    return p;
+  };
+  w.s_logical = reinterpret_cast<int32_t*>(take((size_t)Q * R * 4));
+  w.s_phys = reinterpret_cast<int32_t*>(take((size_t)Q * R * 4));
+  w.nres_eff = reinterpret_cast<int32_t*>(take((size_t)Q * 4));
+  w.n_valid = reinterpret_cast<int32_t*>(take((size_t)Q * 4));
+  w.qsplit = take((size_t)Q * kQBytes);
+  w.wq = reinterpret_cast<float*>(take((size_t)Q * kHeads * 4));
+  w.scores = reinterpret_cast<float*>(take((size_t)Q * R * kPage * 4));
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace
+
+size_t paged_workspace_bytes(int Q, int R) { return paged_ws_layout(nullptr, Q, R).bytes; }
+
+fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
+  if (a.Q == 0) return FM_OK;
+  PagedWs ws = paged_ws_layout(a.workspace, a.Q, a.R);
+  int Rpow2 = 1;
+  while (Rpow2 < a.R) Rpow2 <<= 1;
+  paged_prep_kernel<<<a.Q, kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
+                                                      Rpow2, ws.s_logical, ws.s_phys, ws.nres_eff, ws.n_valid,
+                                                      ws.qsplit, ws.wq, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged prep: launch: %s", cudaGetErrorString(e));
+
+  CUtensorMap tmap_pool, tmap_q;
+  {
+    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.P * kPage};
+    const uint64_t strides[1] = {(uint64_t)kDim};
+    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)kPage};
+    fm_status st = make_tmap(&tmap_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.k_pool, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.Q * 2 * kHeads};
+    const uint64_t strides[1] = {(uint64_t)kDim};
+    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)(2 * kHeads)};
+    fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws.qsplit, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  }
+  const int tiles_per_q = (a.R + 1) / 2;
+  const int64_t total = (int64_t)a.Q * tiles_per_q;
+  const int smem_cap = 227 * 1024;
+  const int fixed = 1024 + kQBytes + kMaxR * 4;
+  int stages = (smem_cap - fixed) / kTileBytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  const int smem = fixed + stages * kTileBytes;
+
+  ScoreParams p;
+  p.s_phys = ws.s_phys;
+  p.nres_eff = ws.nres_eff;
+  p.k_scale = a.k_scale;
+  p.wq = ws.wq;
+  p.scores = ws.scores;
+  p.status = status;
+  p.total_tiles = total;
+  p.tiles_per_q = tiles_per_q;
+  p.R = a.R;
+  p.stages = stages;
+  e = cudaFuncSetAttribute(paged_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  const int grid = (int)(total < num_sms ? total : num_sms);
+  paged_score_kernel<<<grid, kThreads, smem, stream>>>(tmap_pool, tmap_q, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged score: launch: %s", cudaGetErrorString(e));
+
+  return launch_topk_rows(ws.scores, (int64_t)a.R * kPage, ws.n_valid, a.Q, a.R * kPage, a.k, ws.s_logical, a.R,
+                          a.idx_out, a.score_out, stream);
+}
+
+}  // namespace fm

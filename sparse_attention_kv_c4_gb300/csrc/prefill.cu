@@ -1,0 +1,340 @@
+// prefill.cu -- many-query indexer scoring against dense chunk keys under the
+// causal chunk limit, followed by the top-k select.
+//
+// Computes ("DeepSeek-V4 CSA + HCA explained", sec. 3 CSA-1 / CSA-2; c4 chunk
+// s covers tokens 4s..4s+3, sec. 1 and 8):
+//     Y[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . K[s,:]),
+//     candidates of query t: s < min(S, floor(pos[t] / ratio)),
+// then the top-k of each row by (Y desc, s asc), ids ascending.
+//
+// GB300 mapping.  This is the one real dense contraction of the indexer
+// (T x 64 heads against S chunks, K = 128), so it runs on the 5th-generation
+// tensor cores: a persistent CTA per SM owns a contiguous range of
+// (query block of 4 tokens, 128-chunk tile) work items, keeps the block's
+// q [256 rows = 4 tokens x 64 heads, 128] resident in shared memory (B
+// operand) and streams key tiles [128 chunks x 128] (A operand, L2-resident
+// after first touch) through a TMA ring; tcgen05.mma M=128 x N=256 x K=16
+// accumulates D [128 chunks x 256] in TMEM, double-buffered (512 columns).
+// Eight epilogue warps (two per TMEM lane quadrant, two tokens each) turn
+// each row of D into Y with fp32 max/FMA and store it to the workspace; tiles
+// wholly past a block's causal limit are skipped.  The block top-k then reads
+// each row up to its causal limit.
+#include <math.h>
+
+#include "fm_common.cuh"
+#include "fm_internal.h"
+
+namespace fm {
+namespace {
+
+constexpr int kM = 128;                   // chunks per tile
+constexpr int kHeads = 64;
+constexpr int kTok = 4;                   // query tokens per block
+constexpr int kN = kTok * kHeads;         // 256
+constexpr int kDim = 128;
+constexpr int kTileBytes = kM * kDim * 2;    // 32 KB
+constexpr int kAtomA = kM * 64 * 2;          // 16 KB
+constexpr int kQBytes = kN * kDim * 2;       // 64 KB
+constexpr int kAtomB = kN * 64 * 2;          // 32 KB
+constexpr int kMaxStages = 8;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr uint32_t kTmemCols = 512;
+
+struct Params {
+  const float* w;
+  const int64_t* pos;
+  float* logits;
+  unsigned int* status;
+  int64_t S;
+  int64_t total_items;
+  int T;
+  int tiles_per_qb;
+  int ratio;
+  int stages;
+};
+
+FM_DEV int64_t causal_limit(int64_t pos, int64_t S, int ratio) {
+  if (pos < 0) return 0;
+  const int64_t l = pos / ratio;
+  return l < S ? l : S;
+}
+
+// Largest causal limit among the tokens of query block qb.
+FM_DEV int64_t block_limit(const Params& p, int64_t qb) {
+  int64_t lim = 0;
+  for (int j = 0; j < kTok; ++j) {
+    const int64_t t = qb * kTok + j;
+    if (t < p.T) {
+      const int64_t l = causal_limit(__ldg(p.pos + t), p.S, p.ratio);
+      lim = l > lim ? l : lim;
+    }
+  }
+  return lim;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                         const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_smem = smem;
+  uint8_t* k_smem = smem + kQBytes;
+
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_qfull, bar_qempty, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int stages = p.stages;
+  const int64_t t_begin = p.total_items * blockIdx.x / gridDim.x;
+  const int64_t t_end = p.total_items * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], kEpiWarps * 32);
+    }
+    mbar_init(&bar_qfull, 1);
+    mbar_init(&bar_qempty, 1);
+    mbar_init(&bar_drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmap_k);
+    tma_prefetch(&tmap_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ TMA producer ------------------------------
+      uint32_t stage = 0, phase = 0, q_phase = 0;
+      int issued[kMaxStages];
+      for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
+      int q_issued = -1;
+      int64_t cur_qb = -1, lim = 0;
+      for (int64_t it = t_begin; it < t_end; ++it) {
+        const int64_t qb = it / p.tiles_per_qb;
+        const int ct = (int)(it % p.tiles_per_qb);
+        if (qb != cur_qb) {
+          cur_qb = qb;
+          lim = block_limit(p, qb);
+          if (lim > 0) {
+            if (q_issued >= 0) {
+              if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) break;
+              q_phase ^= 1;
+            }
+            mbar_arrive_expect_tx(&bar_qfull, (uint32_t)kQBytes);
+            for (int a = 0; a < 2; ++a)
+              tma_load_2d(q_smem + a * kAtomB, &tmap_q, &bar_qfull, a * 64, (int32_t)(qb * kN));
+            q_issued = (q_issued + 1) & 1;
+          }
+        }
+        if ((int64_t)ct * kM >= lim) continue;
+        if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)kTileBytes);
+        for (int a = 0; a < 2; ++a)
+          tma_load_2d(k_smem + stage * kTileBytes + a * kAtomA, &tmap_k, &bar_full[stage], a * 64, ct * kM);
+        issued[stage] = (int)phase;
+        if (++stage == (uint32_t)stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (abort_flag) {
+        for (int s = 0; s < stages; ++s)
+          if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
+        if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------ UMMA issuer -------------------------------
+      const uint32_t idesc = idesc_bf16_f32(kM, kN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0;
+      int64_t cur_qb = -1, lim = 0;
+      bool have_q = false;
+      for (int64_t it = t_begin; it < t_end; ++it) {
+        const int64_t qb = it / p.tiles_per_qb;
+        const int ct = (int)(it % p.tiles_per_qb);
+        if (qb != cur_qb) {
+          cur_qb = qb;
+          lim = block_limit(p, qb);
+          if (lim > 0) {
+            if (have_q) umma_commit(&bar_qempty);
+            if (!mbar_wait(&bar_qfull, q_phase, &abort_flag, p.status)) break;
+            q_phase ^= 1;
+            have_q = true;
+            tc_fence_after();
+          }
+        }
+        if ((int64_t)ct * kM >= lim) continue;
+        if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status)) break;
+        if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kN;
+        const uint32_t a_base = smem_u32(k_smem + stage * kTileBytes);
+        const uint32_t b_base = smem_u32(q_smem);
+#pragma unroll
+        for (int k = 0; k < kDim / 16; ++k) {
+          const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * kAtomA + (k & 3) * 32);
+          const uint64_t bd = sdesc_sw128(b_base + (k >> 2) * kAtomB + (k & 3) * 32);
+          umma_bf16_ss(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar_empty[stage]);
+        umma_commit(&bar_tfull[acc]);
+        if (++stage == (uint32_t)stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit(&bar_drain);
+      mbar_wait_drain(&bar_drain, 0);
+    }
+  } else {
+    // -------------------------------- epilogue ----------------------------------
+    const int quad = warp & 3;
+    const int group = (warp - 2) / 4;  // tokens 2*group, 2*group + 1 of the block
+    const int row = quad * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    int64_t cur_qb = -1, lim = 0;
+    for (int64_t it = t_begin; it < t_end; ++it) {
+      const int64_t qb = it / p.tiles_per_qb;
+      const int ct = (int)(it % p.tiles_per_qb);
+      if (qb != cur_qb) {
+        cur_qb = qb;
+        lim = block_limit(p, qb);
+      }
+      if ((int64_t)ct * kM >= lim) continue;
+      if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
+      tc_fence_after();
+      const int64_t s = (int64_t)ct * kM + row;
+#pragma unroll 1
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * group + jj;
+        const int64_t t = qb * kTok + j;
+        uint32_t r0[32], r1[32];
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHeads;
+        tmem_ld32(taddr, r0);
+        tmem_ld32(taddr + 32, r1);
+        float wr[kHeads];
+        const int64_t tw = t < p.T ? t : 0;
+        const float4* wl = reinterpret_cast<const float4*>(p.w + tw * kHeads);
+#pragma unroll
+        for (int i = 0; i < kHeads / 4; ++i) {
+          const float4 v = __ldg(wl + i);
+          wr[4 * i] = v.x;
+          wr[4 * i + 1] = v.y;
+          wr[4 * i + 2] = v.z;
+          wr[4 * i + 3] = v.w;
+        }
+        tmem_ld_wait();
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 32; h += 2) {
+          x0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), x0);
+          x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), x1);
+          x2 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), x2);
+          x3 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), x3);
+        }
+        if (t < p.T && s < p.S) p.logits[t * p.S + s] = (x0 + x1) + (x2 + x3);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+__global__ void causal_limits_kernel(const int64_t* __restrict__ pos, int T, int64_t S, int ratio,
+                                     int32_t* __restrict__ n_valid) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < T) n_valid[t] = (int32_t)causal_limit(pos[t], S, ratio);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int T, int64_t S) { return align256((size_t)T * S * 4) + align256((size_t)T * 4); }
+
+fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
+  if (a.T == 0) return FM_OK;
+  float* logits = static_cast<float*>(a.workspace);
+  int32_t* n_valid = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + align256((size_t)a.T * a.S * 4));
+  causal_limits_kernel<<<(a.T + 255) / 256, 256, 0, stream>>>(a.pos, a.T, a.S, a.ratio, n_valid);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill limits: launch: %s", cudaGetErrorString(e));
+
+  if (a.S > 0) {
+    CUtensorMap tmap_k, tmap_q;
+    {
+      const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.S};
+      const uint64_t strides[1] = {(uint64_t)kDim * 2};
+      const uint32_t box[2] = {64, (uint32_t)kM};
+      fm_status st = make_tmap(&tmap_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.keys, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != FM_OK) return st;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.T * kHeads};
+      const uint64_t strides[1] = {(uint64_t)kDim * 2};
+      const uint32_t box[2] = {64, (uint32_t)kN};
+      fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != FM_OK) return st;
+    }
+    const int tiles_per_qb = (int)((a.S + kM - 1) / kM);
+    const int64_t n_qb = (a.T + kTok - 1) / kTok;
+    const int64_t total = n_qb * tiles_per_qb;
+    const int smem_cap = 227 * 1024;
+    const int fixed = 1024 + kQBytes;
+    int stages = (smem_cap - fixed) / kTileBytes;
+    if (stages > kMaxStages) stages = kMaxStages;
+    const int smem = fixed + stages * kTileBytes;
+    Params p;
+    p.w = a.w;
+    p.pos = a.pos;
+    p.logits = logits;
+    p.status = status;
+    p.S = a.S;
+    p.total_items = total;
+    p.T = a.T;
+    p.tiles_per_qb = tiles_per_qb;
+    p.ratio = a.ratio;
+    p.stages = stages;
+    e = cudaFuncSetAttribute(prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    const int grid = (int)(total < num_sms ? total : num_sms);
+    prefill_score_kernel<<<grid, kThreads, smem, stream>>>(tmap_k, tmap_q, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill score: launch: %s", cudaGetErrorString(e));
+  }
+  return launch_topk_rows(logits, a.S, n_valid, a.T, (int)a.S, a.k, nullptr, 0, a.idx_out, a.score_out, stream);
+}
+
+}  // namespace fm
