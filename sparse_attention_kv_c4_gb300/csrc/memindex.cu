@@ -111,9 +111,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_issued = -1;
       int64_t cur_b = -1;
       bool ok = true;
+      int64_t b = t_begin / p.tiles_per_b;
+      int tile = (int)(t_begin % p.tiles_per_b) - 1;
       for (int64_t t = t_begin; t < t_end && ok; ++t) {
-        const int64_t b = t / p.tiles_per_b;
-        const int tile = (int)(t % p.tiles_per_b);
+        if (++tile == p.tiles_per_b) {
+          tile = 0;
+          ++b;
+        }
         if (b != cur_b) {
           if (cur_b >= 0) {
             if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) break;
@@ -156,8 +160,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0;
       int64_t cur_b = -1;
       bool ok = true;
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(k_smem));
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(q_smem));
+      int64_t b = t_begin / p.tiles_per_b;
+      int tile = (int)(t_begin % p.tiles_per_b) - 1;
       for (int64_t t = t_begin; t < t_end && ok; ++t) {
-        const int64_t b = t / p.tiles_per_b;
+        if (++tile == p.tiles_per_b) {
+          tile = 0;
+          ++b;
+        }
         if (b != cur_b) {
           if (cur_b >= 0) umma_commit(&bar_qempty);
           if (!mbar_wait(&bar_qfull, q_phase, &abort_flag, p.status)) break;
@@ -174,14 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * (kMaxL * kHeads) + l * kHeads;
-          const uint32_t a_base = smem_u32(k_smem + stage * kTileBytes);
-          const uint32_t b_base = smem_u32(q_smem + l * kQLayerBytes);
+          // descriptor start-address field counts 16-byte units
+          const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
+          const uint64_t b_desc = b_desc0 + (uint64_t)(l * (kQLayerBytes >> 4));
 #pragma unroll
-          for (int k = 0; k < kDim / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * kAtomA + (k & 3) * 32);
-            const uint64_t bd = sdesc_sw128(b_base + (k >> 2) * kAtomB + (k & 3) * 32);
-            umma_bf16_ss(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < kDim / 16; ++k)
+            umma_bf16_ss(d_tmem, a_desc + (k >> 2) * (kAtomA >> 4) + (k & 3) * 2,
+                         b_desc + (k >> 2) * (kAtomB >> 4) + (k & 3) * 2, idesc, k > 0 ? 1u : 0u);
           umma_commit(&bar_empty[stage]);
           if (++stage == (uint32_t)stages) {
             stage = 0;
@@ -202,9 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;
     const int64_t words = (p.S + 31) / 32;
     uint32_t acc = 0, acc_phase = 0;
+    int64_t b = t_begin / p.tiles_per_b;
+    int tile = (int)(t_begin % p.tiles_per_b) - 1;
     for (int64_t t = t_begin; t < t_end; ++t) {
-      const int64_t b = t / p.tiles_per_b;
-      const int tile = (int)(t % p.tiles_per_b);
+      if (++tile == p.tiles_per_b) {
+        tile = 0;
+        ++b;
+      }
       if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
       tc_fence_after();
       const int64_t s = (int64_t)tile * kM + row;

@@ -20,9 +20,10 @@
 //  2. paged_score_kernel (persistent, one CTA per SM): TMA loads two E4M3 pages
 //     (2 x 8 KB, SWIZZLE_128B) per 128-chunk tile straight into the UMMA A
 //     operand -- no conversion pass; tcgen05.mma kind::f8f6f4 M=128 chunks x
-//     N=64 heads x K=32, issued once with t1 and once with t2 accumulating into
-//     the same TMEM columns; the epilogue (thread = chunk) reads its 64 head
-//     dots and the chunk's scale and writes y to the workspace.
+//     N=128 ([t1; t2] for the 64 heads) x K=32, so the key tile is read from
+//     shared memory once; the epilogue (thread = chunk) adds the two halves of
+//     its 128 dots, applies the chunk's scale, ReLU and w, and writes y to the
+//     workspace.
 //  3. the block top-k (topk.cuh), mapping candidate i to its chunk id.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -43,8 +44,13 @@ constexpr int kTileBytes = kM * kDim;    // 16 KB
 constexpr int kQBytes = 2 * kHeads * kDim;  // t1 rows 0..63, t2 rows 64..127
 constexpr int kMaxR = 2048;
 constexpr int kMaxStages = 12;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 128;
+constexpr int kEpiGroups = 2;          // epilogue warp groups, alternating tiles
+constexpr int kMmaWarps = 2;           // UMMA issuers, alternating tiles
+constexpr int kFirstEpiWarp = 1 + kMmaWarps;
+constexpr int kThreads = kFirstEpiWarp * 32 + kEpiGroups * 128;
+constexpr int kAccBufs = 4;
+constexpr int kAccCols = 2 * kHeads;  // t1 dots in columns 0..63, t2 dots in 64..127
+constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
 constexpr int kPrepThreads = 256;
 
 // --------------------------------------------------------------------------
@@ -197,10 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_smem = smem;                       // 16 KB
   uint8_t* a_smem = smem + kQBytes;             // stages x 16 KB
-  int32_t* phys_s = reinterpret_cast<int32_t*>(a_smem + p.stages * kTileBytes);  // kMaxR
+  float* scale_smem = reinterpret_cast<float*>(a_smem + p.stages * kTileBytes);            // stages x 128
+  int32_t* phys_s = reinterpret_cast<int32_t*>(scale_smem + p.stages * kM);                 // kMaxR
 
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_qfull, bar_qempty, bar_drain;
+  __shared__ __align__(8) uint64_t bar_tfull[kAccBufs], bar_tempty[kAccBufs], bar_qfull, bar_qempty, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -213,15 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_empty[s], 128);  // the epilogue read the scales after the MMA finished
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&bar_tfull[i], 1);
       mbar_init(&bar_tempty[i], 128);
     }
     mbar_init(&bar_qfull, 1);
-    mbar_init(&bar_qempty, 1);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_qempty, kMmaWarps);
+    mbar_init(&bar_drain, kMmaWarps);  // each issuer arrives once its MMAs are done
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -247,9 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t cur_q = -1;
     int nres = 0;
     bool ok = true;
+    int64_t qi = t_begin / p.tiles_per_q;
+    int tile = (int)(t_begin % p.tiles_per_q) - 1;
     for (int64_t t = t_begin; t < t_end && ok; ++t) {
-      const int64_t qi = t / p.tiles_per_q;
-      const int tile = (int)(t % p.tiles_per_q);
+      if (++tile == p.tiles_per_q) {
+        tile = 0;
+        ++qi;
+      }
       if (qi != cur_q) {
         nres = p.nres_eff[qi];
         __syncwarp();
@@ -276,10 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         } else {
           const int npg = nres - 2 * tile >= 2 ? 2 : 1;
-          mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)(npg * kPageBytes));
-          for (int h = 0; h < npg; ++h)
-            tma_load_2d(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0,
-                        phys_s[2 * tile + h] * kPage);
+          mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)(npg * (kPageBytes + kPage * 4)));
+          for (int h = 0; h < npg; ++h) {
+            const int32_t ph = phys_s[2 * tile + h];
+            tma_load_2d(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0, ph * kPage);
+            bulk_load(scale_smem + stage * kM + h * kPage, p.k_scale + (int64_t)ph * kPage, kPage * 4,
+                      &bar_full[stage]);
+          }
           issued[stage] = (int)phase;
         }
       }
@@ -294,17 +308,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
       if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
     }
-  } else if (warp == 1) {
+  } else if (warp < kFirstEpiWarp) {
     if (lane == 0) {
-      // ------------------------------ UMMA issuer -----------------------------
-      const uint32_t idesc = idesc_e4m3_f32(kM, kHeads);
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0;
+      // ---------------------------- UMMA issuers ------------------------------
+      // Issuer m takes the tiles with sequence number = m (mod 2), so one
+      // issuer's barrier waits and commits overlap the other's MMAs.
+      const uint32_t me = (uint32_t)(warp - 1);
+      const uint32_t idesc = idesc_e4m3_f32(kM, kAccCols);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0, seq = 0;
       int64_t cur_q = -1;
       int nres = 0;
       bool have_q = false, ok = true;
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(a_smem));
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(q_smem));
+      int64_t qi = t_begin / p.tiles_per_q;
+      int tile = (int)(t_begin % p.tiles_per_q) - 1;
       for (int64_t t = t_begin; t < t_end && ok; ++t) {
-        const int64_t qi = t / p.tiles_per_q;
-        const int tile = (int)(t % p.tiles_per_q);
+        if (++tile == p.tiles_per_q) {
+          tile = 0;
+          ++qi;
+        }
         if (qi != cur_q) {
           nres = p.nres_eff[qi];
           cur_q = qi;
@@ -317,93 +340,113 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (2 * tile >= nres) continue;
-        if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status)) break;
-        if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kHeads;
-        const uint32_t a_base = smem_u32(a_smem + stage * kTileBytes);
-        const uint32_t b_base = smem_u32(q_smem);
+        if ((seq++ & 1u) == me) {
+          if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status)) break;
+          if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kAccCols;
+          // descriptor start-address field counts 16-byte units; B = [t1; t2]
+          // (128 rows), so one N=128 MMA per K step reads the key tile once
+          const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
 #pragma unroll
-        for (int term = 0; term < 2; ++term)
-#pragma unroll
-          for (int k = 0; k < kDim / 32; ++k) {
-            const uint64_t ad = sdesc_sw128(a_base + k * 32);
-            const uint64_t bd = sdesc_sw128(b_base + term * (kHeads * kDim) + k * 32);
-            umma_e4m3_ss(d_tmem, ad, bd, idesc, (term | k) != 0 ? 1u : 0u);
-          }
-        umma_commit(&bar_empty[stage]);
-        umma_commit(&bar_tfull[acc]);
+          for (int k = 0; k < kDim / 32; ++k)
+            umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc0 + 2 * k, idesc, k != 0 ? 1u : 0u);
+          umma_commit(&bar_tfull[acc]);  // also frees the stage: its epilogue releases it
+        }
         if (++stage == (uint32_t)stages) {
           stage = 0;
           phase ^= 1u;
         }
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == (uint32_t)kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       umma_commit(&bar_drain);
       mbar_wait_drain(&bar_drain, 0);
     }
   } else {
     // -------------------------------- epilogue -------------------------------
+    // Two groups of four warps (one per TMEM lane quadrant) take alternate
+    // tiles; every thread owns one chunk row of its group's tiles.
     const int quad = warp & 3;
+    const int group = (warp - kFirstEpiWarp) >> 2;
     const int row = quad * 32 + lane;
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0, stage = 0, phase = 0, seq = 0;
     int64_t cur_q = -1;
     int nres = 0;
+    int64_t qi = t_begin / p.tiles_per_q;
+    int tile = (int)(t_begin % p.tiles_per_q) - 1;
     for (int64_t t = t_begin; t < t_end; ++t) {
-      const int64_t qi = t / p.tiles_per_q;
-      const int tile = (int)(t % p.tiles_per_q);
+      if (++tile == p.tiles_per_q) {
+        tile = 0;
+        ++qi;
+      }
       if (qi != cur_q) {
         nres = p.nres_eff[qi];
         cur_q = qi;
       }
       if (2 * tile >= nres) continue;
-      const int j = 2 * tile + (row >> 6);
-      const bool valid = j < nres;
-      float sc = 0.f;
-      if (valid) sc = __ldg(p.k_scale + (int64_t)__ldg(p.s_phys + qi * p.R + j) * kPage + (row & 63));
-      if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kHeads;
-      tmem_ld32(taddr, r0);
-      tmem_ld32(taddr + 32, r1);
-      const float4* wl = reinterpret_cast<const float4*>(p.wq + qi * kHeads);
-      float wr[kHeads];
+      const bool mine = (seq++ % kEpiGroups) == (uint32_t)group;
+      if (mine) {
+        const int j = 2 * tile + (row >> 6);
+        const bool valid = j < nres;
+        if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
+        // the stage's scales landed with its full barrier (already complete)
+        if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
+        tc_fence_after();
+        const float sc = valid ? scale_smem[stage * kM + row] : 0.f;
+        mbar_arrive(&bar_empty[stage]);
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kAccCols;
+        const float4* wl = reinterpret_cast<const float4*>(p.wq + qi * kHeads);
+        float y = 0.f;
 #pragma unroll
-      for (int i = 0; i < kHeads / 4; ++i) {
-        const float4 v = __ldg(wl + i);
-        wr[4 * i] = v.x;
-        wr[4 * i + 1] = v.y;
-        wr[4 * i + 2] = v.z;
-        wr[4 * i + 3] = v.w;
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_tempty[acc]);
-      float y;
-      if (sc > 0.f) {
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32], u[32];
+          tmem_ld32(taddr + half * 32, r);
+          tmem_ld32(taddr + kHeads + half * 32, u);
+          float wr[32];
 #pragma unroll
-        for (int h = 0; h < 32; h += 2) {
-          x0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), x0);
-          x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), x1);
-          x2 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), x2);
-          x3 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), x3);
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = __ldg(wl + half * 8 + i);
+            wr[4 * i] = v.x;
+            wr[4 * i + 1] = v.y;
+            wr[4 * i + 2] = v.z;
+            wr[4 * i + 3] = v.w;
+          }
+          tmem_ld_wait();
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(&bar_tempty[acc]);
+          }
+          // q_h . k = 2^e_h (t1 . k + t2 . k); 2^e_h is folded into w
+          float x0 = 0.f, x1 = 0.f;
+          if (sc > 0.f) {
+#pragma unroll
+            for (int h = 0; h < 32; h += 2) {
+              x0 = fmaf(wr[h], fmaxf(__uint_as_float(r[h]) + __uint_as_float(u[h]), 0.f), x0);
+              x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1]), 0.f), x1);
+            }
+            y += sc * (x0 + x1);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 32; h += 2) {
+              x0 = fmaf(wr[h], fmaxf(sc * (__uint_as_float(r[h]) + __uint_as_float(u[h])), 0.f), x0);
+              x1 = fmaf(wr[h + 1], fmaxf(sc * (__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1])), 0.f), x1);
+            }
+            y += x0 + x1;
+          }
         }
-        y = sc * ((x0 + x1) + (x2 + x3));
-      } else {
-        float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          x0 = fmaf(wr[h], fmaxf(sc * __uint_as_float(r0[h]), 0.f), x0);
-          x1 = fmaf(wr[32 + h], fmaxf(sc * __uint_as_float(r1[h]), 0.f), x1);
-        }
-        y = x0 + x1;
+        if (valid) p.scores[qi * ld + (int64_t)tile * kM + row] = y;
       }
-      if (valid) p.scores[qi * ld + (int64_t)tile * kM + row] = y;
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == (uint32_t)kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+      if (++stage == (uint32_t)stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
   }
 
@@ -480,9 +523,10 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   const int64_t total = (int64_t)a.Q * tiles_per_q;
   const int smem_cap = 227 * 1024;
   const int fixed = 1024 + kQBytes + kMaxR * 4;
-  int stages = (smem_cap - fixed) / kTileBytes;
+  const int per_stage = kTileBytes + kM * 4;
+  int stages = (smem_cap - fixed) / per_stage;
   if (stages > kMaxStages) stages = kMaxStages;
-  const int smem = fixed + stages * kTileBytes;
+  const int smem = fixed + stages * per_stage;
 
   ScoreParams p;
   p.s_phys = ws.s_phys;

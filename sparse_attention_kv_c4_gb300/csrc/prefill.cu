@@ -14,8 +14,9 @@
 // q [256 rows = 4 tokens x 64 heads, 128] resident in shared memory (B
 // operand) and streams key tiles [128 chunks x 128] (A operand, L2-resident
 // after first touch) through a TMA ring; tcgen05.mma M=128 x N=256 x K=16
-// accumulates D [128 chunks x 256] in TMEM, double-buffered (512 columns).
-// Eight epilogue warps (two per TMEM lane quadrant, two tokens each) turn
+// accumulates D [128 chunks x 256] in TMEM, double-buffered (512 columns);
+// two issuing threads alternate tiles so barrier latency overlaps MMAs.
+// Sixteen epilogue warps (four per TMEM lane quadrant, one token each) turn
 // each row of D into Y with fp32 max/FMA and store it to the workspace; tiles
 // wholly past a block's causal limit are skipped.  The block top-k then reads
 // each row up to its causal limit.
@@ -37,8 +38,10 @@ constexpr int kAtomA = kM * 64 * 2;          // 16 KB
 constexpr int kQBytes = kN * kDim * 2;       // 64 KB
 constexpr int kAtomB = kN * 64 * 2;          // 32 KB
 constexpr int kMaxStages = 8;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kEpiWarps = 16;               // four per TMEM lane quadrant, one token each
+constexpr int kMmaWarps = 2;                // two UMMA issuers, alternating tiles
+constexpr int kFirstEpiWarp = 1 + kMmaWarps;
+constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -101,8 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_tempty[i], kEpiWarps * 32);
     }
     mbar_init(&bar_qfull, 1);
-    mbar_init(&bar_qempty, 1);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_qempty, kMmaWarps);
+    mbar_init(&bar_drain, kMmaWarps);  // each issuer arrives once its MMAs are done
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -127,9 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
       int q_issued = -1;
       int64_t cur_qb = -1, lim = 0;
+      int64_t qb = t_begin / p.tiles_per_qb;
+      int ct = (int)(t_begin % p.tiles_per_qb) - 1;
       for (int64_t it = t_begin; it < t_end; ++it) {
-        const int64_t qb = it / p.tiles_per_qb;
-        const int ct = (int)(it % p.tiles_per_qb);
+        if (++ct == p.tiles_per_qb) {
+          ct = 0;
+          ++qb;
+        }
         if (qb != cur_qb) {
           cur_qb = qb;
           lim = block_limit(p, qb);
@@ -161,16 +168,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp < kFirstEpiWarp) {
     if (lane == 0) {
-      // ------------------------------ UMMA issuer -------------------------------
+      // ---------------------------- UMMA issuers --------------------------------
+      // Issuer m takes the tiles with sequence number = m (mod 2) and always
+      // accumulates into TMEM buffer m, so one issuer's barrier waits and
+      // commits overlap the other's MMAs.
+      const uint32_t me = (uint32_t)(warp - 1);
       const uint32_t idesc = idesc_bf16_f32(kM, kN);
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0, seq = 0;
       int64_t cur_qb = -1, lim = 0;
       bool have_q = false;
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(k_smem));
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(q_smem));
+      int64_t qb = t_begin / p.tiles_per_qb;
+      int ct = (int)(t_begin % p.tiles_per_qb) - 1;
       for (int64_t it = t_begin; it < t_end; ++it) {
-        const int64_t qb = it / p.tiles_per_qb;
-        const int ct = (int)(it % p.tiles_per_qb);
+        if (++ct == p.tiles_per_qb) {
+          ct = 0;
+          ++qb;
+        }
         if (qb != cur_qb) {
           cur_qb = qb;
           lim = block_limit(p, qb);
@@ -183,20 +200,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if ((int64_t)ct * kM >= lim) continue;
-        if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status)) break;
-        if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kN;
-        const uint32_t a_base = smem_u32(k_smem + stage * kTileBytes);
-        const uint32_t b_base = smem_u32(q_smem);
+        if ((seq++ & 1u) == me) {
+          if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status)) break;
+          if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kN;
+          // descriptor start-address field counts 16-byte units
+          const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
 #pragma unroll
-        for (int k = 0; k < kDim / 16; ++k) {
-          const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * kAtomA + (k & 3) * 32);
-          const uint64_t bd = sdesc_sw128(b_base + (k >> 2) * kAtomB + (k & 3) * 32);
-          umma_bf16_ss(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+          for (int k = 0; k < kDim / 16; ++k)
+            umma_bf16_ss(d_tmem, a_desc + (k >> 2) * (kAtomA >> 4) + (k & 3) * 2,
+                         b_desc0 + (k >> 2) * (kAtomB >> 4) + (k & 3) * 2, idesc, k > 0 ? 1u : 0u);
+          umma_commit(&bar_empty[stage]);
+          umma_commit(&bar_tfull[acc]);
         }
-        umma_commit(&bar_empty[stage]);
-        umma_commit(&bar_tfull[acc]);
         if (++stage == (uint32_t)stages) {
           stage = 0;
           phase ^= 1u;
@@ -210,53 +227,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------- epilogue ----------------------------------
     const int quad = warp & 3;
-    const int group = (warp - 2) / 4;  // tokens 2*group, 2*group + 1 of the block
+    const int j = (warp - kFirstEpiWarp) >> 2;  // token of the block handled by this warp
     const int row = quad * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
     int64_t cur_qb = -1, lim = 0;
+    int64_t qb = t_begin / p.tiles_per_qb;
+    int ct = (int)(t_begin % p.tiles_per_qb) - 1;
     for (int64_t it = t_begin; it < t_end; ++it) {
-      const int64_t qb = it / p.tiles_per_qb;
-      const int ct = (int)(it % p.tiles_per_qb);
+      if (++ct == p.tiles_per_qb) {
+        ct = 0;
+        ++qb;
+      }
       if (qb != cur_qb) {
         cur_qb = qb;
         lim = block_limit(p, qb);
       }
       if ((int64_t)ct * kM >= lim) continue;
+      const int64_t t = qb * kTok + j;
+      const int64_t s = (int64_t)ct * kM + row;
+      const float4* wl = reinterpret_cast<const float4*>(p.w + (t < p.T ? t : 0) * kHeads);
       if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
       tc_fence_after();
-      const int64_t s = (int64_t)ct * kM + row;
-#pragma unroll 1
-      for (int jj = 0; jj < 2; ++jj) {
-        const int j = 2 * group + jj;
-        const int64_t t = qb * kTok + j;
-        uint32_t r0[32], r1[32];
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHeads;
-        tmem_ld32(taddr, r0);
-        tmem_ld32(taddr + 32, r1);
-        float wr[kHeads];
-        const int64_t tw = t < p.T ? t : 0;
-        const float4* wl = reinterpret_cast<const float4*>(p.w + tw * kHeads);
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHeads;
+      float y = 0.f;
 #pragma unroll
-        for (int i = 0; i < kHeads / 4; ++i) {
-          const float4 v = __ldg(wl + i);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32(taddr + half * 32, r);
+        float wr[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = __ldg(wl + half * 8 + i);
           wr[4 * i] = v.x;
           wr[4 * i + 1] = v.y;
           wr[4 * i + 2] = v.z;
           wr[4 * i + 3] = v.w;
         }
         tmem_ld_wait();
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bar_tempty[acc]);
+        }
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
-        for (int h = 0; h < 32; h += 2) {
-          x0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), x0);
-          x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), x1);
-          x2 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), x2);
-          x3 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), x3);
+        for (int h = 0; h < 32; h += 4) {
+          x0 = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.f), x0);
+          x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
+          x2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
+          x3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
         }
-        if (t < p.T && s < p.S) p.logits[t * p.S + s] = (x0 + x1) + (x2 + x3);
+        y += (x0 + x1) + (x2 + x3);
       }
-      tc_fence_before();
-      mbar_arrive(&bar_tempty[acc]);
+      if (t < p.T && s < p.S) p.logits[t * p.S + s] = y;
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }

@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(kTopkThreads)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid, int n, int k,
                      const int32_t* __restrict__ page_ids, int64_t page_ld, int32_t* __restrict__ idx_out,
                      float* __restrict__ score_out) {
-  __shared__ TopkSmem<kTopkThreads> sm;
+  extern __shared__ uint8_t topk_smem_raw[];
+  TopkFastSmem<kTopkThreads>& sm = *reinterpret_cast<TopkFastSmem<kTopkThreads>*>(topk_smem_raw);
   const int64_t r = blockIdx.x;
   int nr = n;
   if (n_valid != nullptr) {
@@ -43,7 +44,10 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
                            const int32_t* page_ids, int64_t page_ld, int32_t* idx_out, float* score_out,
                            cudaStream_t stream) {
   if (rows == 0) return FM_OK;
-  topk_rows_kernel<<<rows, kTopkThreads, 0, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, idx_out,
+  const int smem = (int)sizeof(TopkFastSmem<kTopkThreads>);
+  cudaError_t e0 = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e0 != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: cudaFuncSetAttribute: %s", cudaGetErrorString(e0));
+  topk_rows_kernel<<<rows, kTopkThreads, smem, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, idx_out,
                                                        score_out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: launch: %s", cudaGetErrorString(e));

@@ -54,11 +54,12 @@ FM_DEV uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total)
   return before + x - v;
 }
 
-// Select over row[0..n) (n >= 0).  idx_map(i) gives the id written for
-// candidate i.  Writes k entries of idx_out / score_out (score_out may be
+// Exact select over row[0..n) (n >= 0) straight from global memory (four
+// radix passes + one ordered output pass).  idx_map(i) gives the id written
+// for candidate i.  Writes k entries of idx_out / score_out (score_out may be
 // null).  All THREADS threads of the block must call this.
 template <int THREADS, typename IdxMap>
-FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
+FM_DEV void block_topk_radix(const float* __restrict__ row, int n, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
                        float* __restrict__ score_out, TopkSmem<THREADS>& sm) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int kk = n < k ? n : k;
@@ -151,6 +152,252 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   for (int p = kk + tid; p < k; p += THREADS) {
     idx_out[p] = -1;
     if (score_out) score_out[p] = -INFINITY;
+  }
+}
+
+}  // namespace fm
+
+namespace fm {
+
+// Fast path: a threshold from a sample, one filtering pass into shared memory,
+// an exact select among the candidates.
+//
+//  1. Sample 64 evenly spaced runs of 64 consecutive scores (coalesced) and
+//     take theta = the top 16 bits of the r-th largest sample key, r chosen so
+//     that about 2k scores of the row are expected at or above theta.
+//  2. One vectorised pass over the row appends every (key, index) with
+//     key >= theta to a shared-memory list (warp-aggregated slots), as the
+//     composite 64-bit key (key << 32 | ~index): composites are unique and
+//     order candidates by (score desc, index asc).
+//  3. If the list holds at least min(k, n) entries and did not overflow, the
+//     true top-k is inside it (the k-th largest key is >= theta): a radix
+//     select over the composites finds the min(k, n)-th largest, the selected
+//     entries are gathered, sorted by index and written.  Otherwise the exact
+//     global-memory radix path (block_topk_radix) runs instead.
+// Scores are reported from their keys: -0 reads as +0 and NaN as -inf.
+constexpr int kTopkCap = 6144;      // candidate slots (48 KB of shared memory)
+constexpr int kTopkSample = 4096;   // 64 runs x 64 scores
+
+template <int THREADS>
+struct TopkFastSmem {
+  unsigned long long cand[kTopkCap];
+  union {
+    uint32_t sample[kTopkSample];
+    unsigned long long sel[1024];
+  } u;
+  uint32_t count;
+  int overflow;
+  TopkSmem<THREADS> radix;
+};
+
+// Bitonic sort of s[0..P2) descending (P2 a power of two), all threads.
+template <int THREADS>
+FM_DEV void bitonic_desc(unsigned long long* s, int P2) {
+  for (int size = 2; size <= P2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P2 / 2; i += THREADS) {
+        const int lo = 2 * stride * (i / stride) + (i % stride);
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long a = s[lo], b = s[hi];
+        if ((a < b) == desc) {
+          s[lo] = b;
+          s[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+FM_DEV int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Radix select over a[0..n) in shared memory, most significant 8-bit digit
+// first, at most max_passes digits.  Returns T with count(a >= T) >= r
+// (1 <= r <= n); the count is exactly r when the values are distinct and the
+// select ran to completion or stopped early because the deciding digit held
+// exactly the remaining need.  All threads call it.
+template <int THREADS, typename V>
+FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, TopkSmem<THREADS>& sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  constexpr int kBits = 8 * (int)sizeof(V);
+  V prefix = 0, pmask = 0;
+  uint32_t need = (uint32_t)r;
+  for (int pass = 0; pass < max_passes && pass < kBits / 8; ++pass) {
+    const int shift = kBits - 8 * (pass + 1);
+    for (int i = tid; i < 256; i += THREADS) sm.hist[i] = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += THREADS) {
+      const int i = i0 + tid;
+      bool act = false;
+      uint32_t digit = 0x100u + (uint32_t)lane;
+      if (i < n) {
+        const V v = a[i];
+        act = (v & pmask) == prefix;
+        if (act) digit = (uint32_t)((v >> shift) & 0xFFu);
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (act && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (tid < 32) {
+      uint32_t c[8], s8 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sm.hist[255 - 8 * lane - j];
+        s8 += c[j];
+      }
+      uint32_t incl = s8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t above = incl - s8;
+      if (above < need && need <= incl) {
+        uint32_t acc = above;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (acc + c[j] >= need) {
+            sm.sel_prefix = 255u - 8u * (uint32_t)lane - (uint32_t)j;
+            sm.digit_above = acc;
+            sm.need = c[j];
+            break;
+          }
+          acc += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t d = sm.sel_prefix;
+    const uint32_t in_digit = sm.need;
+    need -= sm.digit_above;
+    prefix |= (V)d << shift;
+    pmask |= (V)0xFFu << shift;
+    __syncthreads();
+    if (in_digit == need) break;  // the whole digit is selected: lower bits do not matter
+  }
+  return prefix;
+}
+
+template <int THREADS, typename IdxMap>
+FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
+                       float* __restrict__ score_out, TopkFastSmem<THREADS>& sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int kk = n < k ? n : k;
+  if (kk == 0) {
+    for (int p = tid; p < k; p += THREADS) {
+      idx_out[p] = -1;
+      if (score_out) score_out[p] = -INFINITY;
+    }
+    return;
+  }
+  // ---- 1. threshold from a sample --------------------------------------------
+  uint32_t theta = 0;
+  if (n > kTopkCap) {
+    for (int i = tid; i < kTopkSample; i += THREADS) {
+      const int run = i >> 6, off = i & 63;
+      const int start = (int)(((long long)run * (n - 64)) / 63);
+      sm.u.sample[i] = float_key(__ldg(row + start + off));
+    }
+    __syncthreads();
+    int r = (int)(((long long)2 * kk * kTopkSample) / n);
+    r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
+    theta = smem_radix_select<THREADS, uint32_t>(sm.u.sample, kTopkSample, r, 2, sm.radix);
+  }
+  if (tid == 0) {
+    sm.count = 0;
+    sm.overflow = 0;
+  }
+  __syncthreads();
+  // ---- 2. filter pass ---------------------------------------------------------
+  auto push = [&](bool take, uint32_t key, int i) {
+    const uint32_t ballot = __ballot_sync(0xffffffffu, take);
+    if (ballot == 0) return;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&sm.count, (uint32_t)__popc(ballot));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (take) {
+      const uint32_t slot = base + __popc(ballot & ((1u << lane) - 1u));
+      if (slot < (uint32_t)kTopkCap)
+        sm.cand[slot] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)i);
+      else
+        sm.overflow = 1;
+    }
+  };
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  const int n4 = vec ? n / 4 : 0;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  for (int i40 = 0; i40 < n4; i40 += THREADS * 4) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i4 = i40 + u * THREADS + tid;
+      v[u] = i4 < n4 ? __ldg(row4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i4 = i40 + u * THREADS + tid;
+      const bool in = i4 < n4;
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t key = float_key(e[c]);
+        push(in && key >= theta, key, 4 * i4 + c);
+      }
+    }
+  }
+  for (int i0 = 4 * n4; i0 < n; i0 += THREADS) {
+    const int i = i0 + tid;
+    uint32_t key = 0;
+    if (i < n) key = float_key(__ldg(row + i));
+    push(i < n && key >= theta, key, i);
+  }
+  __syncthreads();
+  const int cnt = (int)sm.count;
+  if (sm.overflow || cnt < kk) {
+    __syncthreads();
+    block_topk_radix<THREADS>(row, n, k, idx_map, idx_out, score_out, sm.radix);
+    return;
+  }
+  // ---- 3. exact select among the candidates -------------------------------------
+  const unsigned long long T = smem_radix_select<THREADS, unsigned long long>(sm.cand, cnt, kk, 8, sm.radix);
+  if (tid == 0) sm.count = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < cnt; i0 += THREADS) {
+    const int i = i0 + tid;
+    const unsigned long long c = i < cnt ? sm.cand[i] : 0ull;
+    const bool take = i < cnt && c >= T;
+    const uint32_t ballot = __ballot_sync(0xffffffffu, take);
+    if (ballot != 0) {
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&sm.count, (uint32_t)__popc(ballot));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (take) {
+        // re-key by index: ascending index == descending ~index
+        sm.u.sel[base + __popc(ballot & ((1u << lane) - 1u))] = ((unsigned long long)(uint32_t)c << 32) | (c >> 32);
+      }
+    }
+  }
+  __syncthreads();
+  const int K2 = next_pow2(kk);
+  for (int i = kk + tid; i < K2; i += THREADS) sm.u.sel[i] = 0ull;
+  __syncthreads();
+  bitonic_desc<THREADS>(sm.u.sel, K2);
+  for (int p = tid; p < k; p += THREADS) {
+    if (p < kk) {
+      const unsigned long long c = sm.u.sel[p];
+      const int i = (int)(~(uint32_t)(c >> 32));
+      idx_out[p] = idx_map(i);
+      if (score_out) score_out[p] = key_float((uint32_t)c);
+    } else {
+      idx_out[p] = -1;
+      if (score_out) score_out[p] = -INFINITY;
+    }
   }
 }
 
