@@ -291,6 +291,17 @@ class OracleSample:
 # ---------------------------------------------------------------------------
 
 
+def reduce_max(value: float, device, world: int) -> float:
+    """MAX of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -381,10 +392,7 @@ def run_ours(args):
     status = fm.fm_device_status(reset=True)
     chk = sanity(torch, W, cfgs)
 
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(ms_total, dev, world)
     ms_step = ms_total / K
     figs = phase_figures(cfgs)
     cs_step = sum(f["chunk_scores"] for f in figs.values())
@@ -436,10 +444,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, dev, world)
     e2e_value = world * cs_step / (e2e_ms / 1e3)
 
     cpu = None
