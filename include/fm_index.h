@@ -156,6 +156,35 @@ fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t*
                                float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
 
 /*
+ * Native paged top-k without a caller workspace.
+ *
+ * The pages have no counterpart of this entry point: it exists for callers
+ * that cannot allocate device memory -- a serving engine that handed nearly
+ * all of HBM to its KV-cache pool at start-up (a further cudaMalloc would fail
+ * or fragment that pool), a decode loop that must not stall on the implicit
+ * device synchronisation cudaMalloc/cudaFree may perform, or a plugin host that
+ * gives its kernels no allocator.  It computes exactly what
+ * fm_native_topk_paged computes, with the same arguments minus the workspace,
+ * and calls no allocating routine.
+ *
+ * Its scratch is a fixed FM_NOALLOC_SCRATCH_BYTES array inside the library's
+ * device image: every GPU that loads the library holds it until the process
+ * exits.  Sizes whose workspace (fm_native_topk_paged_workspace(Q, R)) exceeds
+ * it are rejected with FM_ERR_INVALID_ARG before anything is enqueued (e.g.
+ * R = 384 allows about 140 queries per call).  The first call on a device
+ * resolves the array's device address with that device current; make that
+ * first call before any stream capture.  All calls share the array and it
+ * keeps the last call's contents (nothing in it needs to start at zero), so
+ * calls that overlap on the GPU -- different streams or host threads -- race
+ * on it: serialise them.
+ */
+#define FM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+fm_status fm_native_topk_paged_noalloc(const uint16_t* q, const float* w, const uint8_t* k_pool,
+                                       const float* k_scale, int64_t P, const int32_t* page_phys,
+                                       const int32_t* page_logical, const int32_t* n_res, int Q, int R, int n_h,
+                                       int d, int k, int32_t* idx_out, float* score_out, fm_stream_t stream);
+
+/*
  * Prefill: dense indexer scores of T query tokens against S chunk keys under
  * the causal chunk limit, then top-k per query ([V4] sec. 3 CSA-1/2; chunk s
  * covers tokens ratio*s .. ratio*s + ratio-1, [V4] sec. 1/8).

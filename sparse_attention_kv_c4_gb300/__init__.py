@@ -16,7 +16,7 @@ import os
 __all__ = [
     "FmError", "lib", "fm_version", "fm_last_error", "fm_device_status", "fm_memindex_score_mask",
     "fm_topk_workspace", "fm_topk_select", "fm_native_topk_paged_workspace", "fm_native_topk_paged",
-    "fm_index_prefill_workspace", "fm_index_prefill_topk", "LIB_PATH",
+    "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "LIB_PATH",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +60,10 @@ def lib() -> ctypes.CDLL:
             L.fm_native_topk_paged_workspace.restype = _SZ
             L.fm_native_topk_paged.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
                                                _I32, _VP, _VP, _VP, _SZ, _VP]
+        if hasattr(L, "fm_native_topk_paged_noalloc"):
+            L.fm_native_topk_paged_noalloc.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32,
+                                                       _I32, _I32, _VP, _VP, _VP]
+            L.fm_native_topk_paged_noalloc.restype = ctypes.c_int
         if hasattr(L, "fm_index_prefill_workspace"):
             L.fm_index_prefill_workspace.argtypes = [_I32, _I64]
             L.fm_index_prefill_workspace.restype = _SZ
@@ -148,6 +152,19 @@ def fm_native_topk_paged(q, w, k_pool, k_scale, page_phys, page_logical, k: int,
     _check(lib().fm_native_topk_paged(_ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), P, _ptr(page_phys),
                                       _ptr(page_logical), _ptr(n_res), Q, R, n_h, d, k, _ptr(idx_out),
                                       _ptr(score_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_native_topk_paged_noalloc(q, w, k_pool, k_scale, page_phys, page_logical, k: int, idx_out, score_out=None,
+                                 n_res=None, stream=None) -> None:
+    """fm_native_topk_paged without a workspace, for callers that cannot
+    allocate device memory: the scratch is a fixed 16 MiB array inside the
+    library (shared by all calls; serialise calls that could overlap)."""
+    Q, n_h, d = q.shape
+    R = page_phys.shape[1]
+    P = k_pool.shape[0]
+    _check(lib().fm_native_topk_paged_noalloc(_ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), P, _ptr(page_phys),
+                                              _ptr(page_logical), _ptr(n_res), Q, R, n_h, d, k, _ptr(idx_out),
+                                              _ptr(score_out), _stream(stream)))
 
 
 def fm_index_prefill_workspace(T: int, S: int) -> int:
