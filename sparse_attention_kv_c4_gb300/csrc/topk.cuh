@@ -162,28 +162,37 @@ namespace fm {
 // Fast path: a threshold from a sample, one filtering pass into shared memory,
 // an exact select among the candidates.
 //
-//  1. Sample 64 evenly spaced runs of 64 consecutive scores (coalesced) and
-//     take theta = the top 16 bits of the r-th largest sample key, r chosen so
-//     that about 2k scores of the row are expected at or above theta.
-//  2. One vectorised pass over the row appends every (key, index) with
-//     key >= theta to a shared-memory list (warp-aggregated slots), as the
-//     composite 64-bit key (key << 32 | ~index): composites are unique and
-//     order candidates by (score desc, index asc).
+//  Every candidate is ranked by its unique composite key (key << 32 | ~index),
+//  which orders (score desc, index asc).
+//  1. Sample 16 evenly spaced runs of 64 consecutive scores (coalesced) and
+//     take theta = about the r-th largest sample composite, r chosen so that
+//     about 2.5k candidates of the row are expected at or above it (equal
+//     scores are thresholded by index, so ties cannot flood the list).
+//  2. One vectorised pass compares each score with theta's score as a plain
+//     fp32 compare; only scores that reach it (a few percent) build their
+//     composite and are appended, when composite >= theta, to a shared-memory
+//     list (one shared-memory atomic per appended candidate).
 //  3. If the list holds at least min(k, n) entries and did not overflow, the
-//     true top-k is inside it (the k-th largest key is >= theta): a radix
-//     select over the composites finds the min(k, n)-th largest, the selected
-//     entries are gathered, sorted by index and written.  Otherwise the exact
-//     global-memory radix path (block_topk_radix) runs instead.
+//     true top-k is inside it (the k-th largest composite is >= theta): a radix
+//     select over the composites finds the min(k, n)-th largest; the selected
+//     indices are marked in a bitmap and emitted in index order by one
+//     block-wide prefix sum (longer rows gather and sort instead).  Otherwise
+//     the exact global-memory radix path (block_topk_radix) runs.
 // Scores are reported from their keys: -0 reads as +0 and NaN as -inf.
-constexpr int kTopkCap = 6144;      // candidate slots (48 KB of shared memory)
-constexpr int kTopkSample = 4096;   // 64 runs x 64 scores
+constexpr int kTopkCap = 4096;        // candidate slots (32 KB of shared memory)
+constexpr int kTopkRuns = 16;         // sample: 16 runs x 64 scores
+constexpr int kTopkSample = kTopkRuns * 64;
+constexpr int kTopkBitmapN = 131072;  // rows up to this length emit ids via a bitmap
 
 template <int THREADS>
 struct TopkFastSmem {
   unsigned long long cand[kTopkCap];
+  uint32_t whist[256];
+  unsigned long long wsel;
   union {
-    uint32_t sample[kTopkSample];
+    unsigned long long sample[kTopkSample];
     unsigned long long sel[1024];
+    uint32_t bitmap[kTopkBitmapN / 32];
   } u;
   uint32_t count;
   int overflow;
@@ -218,11 +227,11 @@ FM_DEV int next_pow2(int x) {
 
 // Radix select over a[0..n) in shared memory, most significant 8-bit digit
 // first, at most max_passes digits.  Returns T with count(a >= T) >= r
-// (1 <= r <= n); the count is exactly r when the values are distinct and the
-// select ran to completion or stopped early because the deciding digit held
-// exactly the remaining need.  All threads call it.
+// (1 <= r <= n).  It stops early when the deciding digit holds exactly the
+// remaining need (then count(a >= T) == r for distinct values) or at most
+// `loose` values (then count(a >= T) <= r + loose).  All threads call it.
 template <int THREADS, typename V>
-FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, TopkSmem<THREADS>& sm) {
+FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, uint32_t loose, TopkSmem<THREADS>& sm) {
   const int tid = threadIdx.x, lane = tid & 31;
   constexpr int kBits = 8 * (int)sizeof(V);
   V prefix = 0, pmask = 0;
@@ -279,7 +288,66 @@ FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, TopkSmem<TH
     prefix |= (V)d << shift;
     pmask |= (V)0xFFu << shift;
     __syncthreads();
-    if (in_digit == need) break;  // the whole digit is selected: lower bits do not matter
+    if (in_digit == need || in_digit <= loose) break;  // lower bits cannot matter (or need not)
+  }
+  return prefix;
+}
+
+// The same select run by one warp (no block barriers): for the short lists of
+// samples and candidates a single warp is faster than the whole block.
+template <typename V>
+FM_DEV V warp_radix_select(const V* a, int n, int r, int max_passes, uint32_t loose, uint32_t* hist) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kBits = 8 * (int)sizeof(V);
+  V prefix = 0, pmask = 0;
+  uint32_t need = (uint32_t)r;
+  for (int pass = 0; pass < max_passes && pass < kBits / 8; ++pass) {
+    const int shift = kBits - 8 * (pass + 1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hist[lane + 32 * j] = 0u;
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) {
+      const V v = a[i];
+      if ((v & pmask) == prefix) atomicAdd(&hist[(uint32_t)((v >> shift) & 0xFFu)], 1u);
+    }
+    __syncwarp();
+    uint32_t c[8], s8 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = hist[255 - 8 * lane - j];
+      s8 += c[j];
+    }
+    uint32_t incl = s8;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t above = incl - s8;
+    uint32_t d = 0, dabove = 0, din = 0;
+    const bool mine = above < need && need <= incl;
+    if (mine) {
+      uint32_t acc = above;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (acc + c[j] >= need) {
+          d = 255u - 8u * (uint32_t)lane - (uint32_t)j;
+          dabove = acc;
+          din = c[j];
+          break;
+        }
+        acc += c[j];
+      }
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    d = __shfl_sync(0xffffffffu, d, src);
+    dabove = __shfl_sync(0xffffffffu, dabove, src);
+    din = __shfl_sync(0xffffffffu, din, src);
+    need -= dabove;
+    prefix |= (V)d << shift;
+    pmask |= (V)0xFFu << shift;
+    __syncwarp();
+    if (din == need || din <= loose) break;
   }
   return prefix;
 }
@@ -287,7 +355,7 @@ FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, TopkSmem<TH
 template <int THREADS, typename IdxMap>
 FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
                        float* __restrict__ score_out, TopkFastSmem<THREADS>& sm) {
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int kk = n < k ? n : k;
   if (kk == 0) {
     for (int p = tid; p < k; p += THREADS) {
@@ -297,17 +365,22 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
     return;
   }
   // ---- 1. threshold from a sample --------------------------------------------
-  uint32_t theta = 0;
+  unsigned long long theta = 0ull;
   if (n > kTopkCap) {
     for (int i = tid; i < kTopkSample; i += THREADS) {
       const int run = i >> 6, off = i & 63;
-      const int start = (int)(((long long)run * (n - 64)) / 63);
-      sm.u.sample[i] = float_key(__ldg(row + start + off));
+      const int j = (int)(((long long)run * (n - 64)) / (kTopkRuns - 1)) + off;
+      sm.u.sample[i] = ((unsigned long long)float_key(__ldg(row + j)) << 32) | (uint32_t)(~(uint32_t)j);
     }
     __syncthreads();
-    int r = (int)(((long long)2 * kk * kTopkSample) / n);
+    int r = (int)(((long long)5 * kk * kTopkSample) / (2 * (long long)n));  // ~2.5 k candidates
     r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
-    theta = smem_radix_select<THREADS, uint32_t>(sm.u.sample, kTopkSample, r, 2, sm.radix);
+    if (tid < 32) {
+      const unsigned long long t = warp_radix_select<unsigned long long>(sm.u.sample, kTopkSample, r, 8, 8u, sm.whist);
+      if (tid == 0) sm.wsel = t;
+    }
+    __syncthreads();
+    theta = sm.wsel;
   }
   if (tid == 0) {
     sm.count = 0;
@@ -315,18 +388,23 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   }
   __syncthreads();
   // ---- 2. filter pass ---------------------------------------------------------
-  auto push = [&](bool take, uint32_t key, int i) {
-    const uint32_t ballot = __ballot_sync(0xffffffffu, take);
-    if (ballot == 0) return;
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&sm.count, (uint32_t)__popc(ballot));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (take) {
-      const uint32_t slot = base + __popc(ballot & ((1u << lane) - 1u));
-      if (slot < (uint32_t)kTopkCap)
-        sm.cand[slot] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)i);
-      else
-        sm.overflow = 1;
+  // A score can only pass if score >= theta's score (as floats: -0 compares
+  // equal to +0 like its key); the composite then decides ties by index.  A
+  // threshold at -inf (rows dominated by -inf/NaN) cannot be tested as a float
+  // because NaN ranks as -inf: then every score goes to the composite test.
+  const uint32_t theta_key = (uint32_t)(theta >> 32);
+  const bool take_all = theta == 0ull || theta_key <= 0x007FFFFFu;
+  const float theta_f = take_all ? -INFINITY : key_float(theta_key);
+  auto push = [&](bool maybe, float v, int i) {
+    if (maybe) {
+      const unsigned long long c = ((unsigned long long)float_key(v) << 32) | (uint32_t)(~(uint32_t)i);
+      if (c >= theta) {
+        const uint32_t slot = atomicAdd(&sm.count, 1u);
+        if (slot < (uint32_t)kTopkCap)
+          sm.cand[slot] = c;
+        else
+          sm.overflow = 1;
+      }
     }
   };
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
@@ -343,19 +421,15 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
     for (int u = 0; u < 4; ++u) {
       const int i4 = i40 + u * THREADS + tid;
       const bool in = i4 < n4;
-      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t key = float_key(e[c]);
-        push(in && key >= theta, key, 4 * i4 + c);
-      }
+      push(in && (take_all || v[u].x >= theta_f), v[u].x, 4 * i4);
+      push(in && (take_all || v[u].y >= theta_f), v[u].y, 4 * i4 + 1);
+      push(in && (take_all || v[u].z >= theta_f), v[u].z, 4 * i4 + 2);
+      push(in && (take_all || v[u].w >= theta_f), v[u].w, 4 * i4 + 3);
     }
   }
-  for (int i0 = 4 * n4; i0 < n; i0 += THREADS) {
-    const int i = i0 + tid;
-    uint32_t key = 0;
-    if (i < n) key = float_key(__ldg(row + i));
-    push(i < n && key >= theta, key, i);
+  for (int i = 4 * n4 + tid; i < n; i += THREADS) {
+    const float v = __ldg(row + i);
+    push(take_all || v >= theta_f, v, i);
   }
   __syncthreads();
   const int cnt = (int)sm.count;
@@ -365,39 +439,70 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
     return;
   }
   // ---- 3. exact select among the candidates -------------------------------------
-  const unsigned long long T = smem_radix_select<THREADS, unsigned long long>(sm.cand, cnt, kk, 8, sm.radix);
-  if (tid == 0) sm.count = 0;
-  __syncthreads();
-  for (int i0 = 0; i0 < cnt; i0 += THREADS) {
-    const int i = i0 + tid;
-    const unsigned long long c = i < cnt ? sm.cand[i] : 0ull;
-    const bool take = i < cnt && c >= T;
-    const uint32_t ballot = __ballot_sync(0xffffffffu, take);
-    if (ballot != 0) {
-      uint32_t base = 0;
-      if (lane == 0) base = atomicAdd(&sm.count, (uint32_t)__popc(ballot));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (take) {
-        // re-key by index: ascending index == descending ~index
-        sm.u.sel[base + __popc(ballot & ((1u << lane) - 1u))] = ((unsigned long long)(uint32_t)c << 32) | (c >> 32);
-      }
-    }
+  if (tid < 32) {
+    const unsigned long long t = warp_radix_select<unsigned long long>(sm.cand, cnt, kk, 8, 0u, sm.whist);
+    if (tid == 0) sm.wsel = t;
   }
   __syncthreads();
-  const int K2 = next_pow2(kk);
-  for (int i = kk + tid; i < K2; i += THREADS) sm.u.sel[i] = 0ull;
-  __syncthreads();
-  bitonic_desc<THREADS>(sm.u.sel, K2);
-  for (int p = tid; p < k; p += THREADS) {
-    if (p < kk) {
+  const unsigned long long T = sm.wsel;
+  if (n <= kTopkBitmapN) {
+    // mark the selected indices in a bitmap, then emit them in index order
+    // with one block-wide prefix sum over the bitmap words
+    const int words = (n + 31) >> 5;
+    for (int i = tid; i < words; i += THREADS) sm.u.bitmap[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < cnt; i += THREADS) {
+      const unsigned long long c = sm.cand[i];
+      if (c >= T) {
+        const uint32_t idx = ~(uint32_t)c;
+        atomicOr(&sm.u.bitmap[idx >> 5], 1u << (idx & 31));
+      }
+    }
+    __syncthreads();
+    const int per = (words + THREADS - 1) / THREADS;  // consecutive words per thread
+    const int w0 = tid * per;
+    uint32_t mine = 0;
+    for (int j = 0; j < per; ++j)
+      if (w0 + j < words) mine += (uint32_t)__popc(sm.u.bitmap[w0 + j]);
+    uint32_t tot;
+    uint32_t pos = block_excl_scan<THREADS>(mine, sm.radix.warp_tot, &tot);
+    for (int j = 0; j < per && w0 + j < words; ++j) {
+      uint32_t bits = sm.u.bitmap[w0 + j];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int i = ((w0 + j) << 5) + b;
+        idx_out[pos] = idx_map(i);
+        if (score_out) score_out[pos] = key_float(float_key(__ldg(row + i)));
+        ++pos;
+      }
+    }
+  } else {
+    if (tid == 0) sm.count = 0;
+    __syncthreads();
+    for (int i = tid; i < cnt; i += THREADS) {
+      const unsigned long long c = sm.cand[i];
+      if (c >= T) {
+        // re-key by index: ascending index == descending ~index
+        const uint32_t slot = atomicAdd(&sm.count, 1u);
+        sm.u.sel[slot] = ((unsigned long long)(uint32_t)c << 32) | (c >> 32);
+      }
+    }
+    __syncthreads();
+    const int K2 = next_pow2(kk);
+    for (int i = kk + tid; i < K2; i += THREADS) sm.u.sel[i] = 0ull;
+    __syncthreads();
+    bitonic_desc<THREADS>(sm.u.sel, K2);
+    for (int p = tid; p < kk; p += THREADS) {
       const unsigned long long c = sm.u.sel[p];
       const int i = (int)(~(uint32_t)(c >> 32));
       idx_out[p] = idx_map(i);
       if (score_out) score_out[p] = key_float((uint32_t)c);
-    } else {
-      idx_out[p] = -1;
-      if (score_out) score_out[p] = -INFINITY;
     }
+  }
+  for (int p = kk + tid; p < k; p += THREADS) {
+    idx_out[p] = -1;
+    if (score_out) score_out[p] = -INFINITY;
   }
 }
 
