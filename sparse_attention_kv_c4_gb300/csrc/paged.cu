@@ -21,9 +21,11 @@
 //     (2 x 8 KB, SWIZZLE_128B) per 128-chunk tile straight into the UMMA A
 //     operand -- no conversion pass; tcgen05.mma kind::f8f6f4 M=128 chunks x
 //     N=128 ([t1; t2] for the 64 heads) x K=32, so the key tile is read from
-//     shared memory once; the epilogue (thread = chunk) adds the two halves of
-//     its 128 dots, applies the chunk's scale, ReLU and w, and writes y to the
-//     workspace.
+//     shared memory once.  The producer warp issues a batch of tiles at once
+//     (lane i fills the stage of tile i), two issuing threads alternate tiles,
+//     and four epilogue warp groups take tiles in turn.  The epilogue (thread =
+//     chunk) adds the two halves of its 128 dots, applies the chunk's scale,
+//     ReLU and w, and writes y to the workspace.
 //  3. the block top-k (topk.cuh), mapping candidate i to its chunk id.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -44,7 +46,7 @@ constexpr int kTileBytes = kM * kDim;    // 16 KB
 constexpr int kQBytes = 2 * kHeads * kDim;  // t1 rows 0..63, t2 rows 64..127
 constexpr int kMaxR = 2048;
 constexpr int kMaxStages = 12;
-constexpr int kEpiGroups = 2;          // epilogue warp groups, alternating tiles
+constexpr int kEpiGroups = 4;          // epilogue warp groups, taking tiles in turn
 constexpr int kMmaWarps = 2;           // UMMA issuers, alternating tiles
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreads = kFirstEpiWarp * 32 + kEpiGroups * 128;
@@ -247,20 +249,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // -------------------------------- producer (whole warp) ------------------
-    uint32_t stage = 0, phase = 0, q_phase = 0;
-    int issued[kMaxStages];
-    for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
+    // Tiles are issued in batches of up to kBatch consecutive tiles of one
+    // query: lane i waits for the stage of the batch's i-th tile and issues its
+    // copies, so the per-copy issue latency is paid once per batch.
+    constexpr int kBatch = 8;
+    __shared__ int issued_ph[kMaxStages];
+    for (int s = lane; s < kMaxStages; s += 32) issued_ph[s] = -1;
+    uint32_t seq = 0, q_phase = 0;
     int q_issued = -1;
     int64_t cur_q = -1;
     int nres = 0;
     bool ok = true;
     int64_t qi = t_begin / p.tiles_per_q;
-    int tile = (int)(t_begin % p.tiles_per_q) - 1;
-    for (int64_t t = t_begin; t < t_end && ok; ++t) {
-      if (++tile == p.tiles_per_q) {
-        tile = 0;
-        ++qi;
-      }
+    int tile = (int)(t_begin % p.tiles_per_q);
+    int64_t t = t_begin;
+    __syncwarp();
+    while (t < t_end) {
       if (qi != cur_q) {
         nres = p.nres_eff[qi];
         __syncwarp();
@@ -278,34 +282,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             q_issued = (q_issued + 1) & 1;
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        if (__any_sync(0xffffffffu, !ok)) break;
       }
-      if (2 * tile >= nres) continue;
-      if (lane == 0) {
+      int nb = p.tiles_per_q - tile;
+      if ((int64_t)nb > t_end - t) nb = (int)(t_end - t);
+      if (nb > kBatch) nb = kBatch;
+      const int my_tile = tile + lane;
+      const bool valid = lane < nb && 2 * my_tile < nres;
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const uint32_t sq = seq + (uint32_t)__popc(vmask & ((1u << lane) - 1u));
+        const uint32_t stage = sq % (uint32_t)stages, phase = (sq / (uint32_t)stages) & 1u;
         if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) {
           ok = false;
         } else {
-          const int npg = nres - 2 * tile >= 2 ? 2 : 1;
+          const int npg = nres - 2 * my_tile >= 2 ? 2 : 1;
           mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)(npg * (kPageBytes + kPage * 4)));
           for (int h = 0; h < npg; ++h) {
-            const int32_t ph = phys_s[2 * tile + h];
+            const int32_t ph = phys_s[2 * my_tile + h];
             tma_load_2d(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0, ph * kPage);
             bulk_load(scale_smem + stage * kM + h * kPage, p.k_scale + (int64_t)ph * kPage, kPage * 4,
                       &bar_full[stage]);
           }
-          issued[stage] = (int)phase;
+          issued_ph[stage] = (int)phase;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (++stage == (uint32_t)stages) {
-        stage = 0;
-        phase ^= 1u;
+      seq += (uint32_t)__popc(vmask);
+      if (__any_sync(0xffffffffu, !ok)) break;
+      t += nb;
+      tile += nb;
+      if (tile == p.tiles_per_q) {
+        tile = 0;
+        ++qi;
       }
     }
-    if (lane == 0 && abort_flag) {
+    __syncwarp();
+    if (lane == 0 && abort_flag) {  // let copies already in flight land before the CTA exits
       for (int s = 0; s < stages; ++s)
-        if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
+        if (issued_ph[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued_ph[s]);
       if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
     }
   } else if (warp < kFirstEpiWarp) {
@@ -367,8 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------- epilogue -------------------------------
-    // Two groups of four warps (one per TMEM lane quadrant) take alternate
-    // tiles; every thread owns one chunk row of its group's tiles.
+    // Four groups of four warps (one per TMEM lane quadrant) take the tiles in
+    // turn, group g always reading accumulator g; every thread owns one chunk
+    // row of its group's tiles.
     const int quad = warp & 3;
     const int group = (warp - kFirstEpiWarp) >> 2;
     const int row = quad * 32 + lane;
@@ -401,21 +416,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* wl = reinterpret_cast<const float4*>(p.wq + qi * kHeads);
         float y = 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32], u[32];
-          tmem_ld32(taddr + half * 32, r);
-          tmem_ld32(taddr + kHeads + half * 32, u);
-          float wr[32];
+        for (int part = 0; part < 4; ++part) {  // 16 heads at a time
+          uint32_t r[16], u[16];
+          tmem_ld16(taddr + part * 16, r);
+          tmem_ld16(taddr + kHeads + part * 16, u);
+          float wr[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = __ldg(wl + half * 8 + i);
+          for (int i = 0; i < 4; ++i) {
+            const float4 v = __ldg(wl + part * 4 + i);
             wr[4 * i] = v.x;
             wr[4 * i + 1] = v.y;
             wr[4 * i + 2] = v.z;
             wr[4 * i + 3] = v.w;
           }
           tmem_ld_wait();
-          if (half == 1) {
+          if (part == 3) {
             tc_fence_before();
             mbar_arrive(&bar_tempty[acc]);
           }
@@ -423,14 +438,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x0 = 0.f, x1 = 0.f;
           if (sc > 0.f) {
 #pragma unroll
-            for (int h = 0; h < 32; h += 2) {
+            for (int h = 0; h < 16; h += 2) {
               x0 = fmaf(wr[h], fmaxf(__uint_as_float(r[h]) + __uint_as_float(u[h]), 0.f), x0);
               x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1]), 0.f), x1);
             }
             y += sc * (x0 + x1);
           } else {
 #pragma unroll
-            for (int h = 0; h < 32; h += 2) {
+            for (int h = 0; h < 16; h += 2) {
               x0 = fmaf(wr[h], fmaxf(sc * (__uint_as_float(r[h]) + __uint_as_float(u[h])), 0.f), x0);
               x1 = fmaf(wr[h + 1], fmaxf(sc * (__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1])), 0.f), x1);
             }
