@@ -22,8 +22,8 @@
 //     operand -- no conversion pass; tcgen05.mma kind::f8f6f4 M=128 chunks x
 //     N=128 ([t1; t2] for the 64 heads) x K=32, so the key tile is read from
 //     shared memory once.  The producer warp issues a batch of tiles at once
-//     (lane i fills the stage of tile i), two issuing threads alternate tiles,
-//     and four epilogue warp groups take tiles in turn.  The epilogue (thread =
+//     (lane i fills the stage of tile i), four issuing threads and four
+//     epilogue warp groups take tiles in turn.  The epilogue (thread =
 //     chunk) adds the two halves of its 128 dots, applies the chunk's scale,
 //     ReLU and w, and writes y to the workspace.
 //  3. the block top-k (topk.cuh), mapping candidate i to its chunk id.
@@ -47,7 +47,7 @@ constexpr int kQBytes = 2 * kHeads * kDim;  // t1 rows 0..63, t2 rows 64..127
 constexpr int kMaxR = 2048;
 constexpr int kMaxStages = 12;
 constexpr int kEpiGroups = 4;          // epilogue warp groups, taking tiles in turn
-constexpr int kMmaWarps = 2;           // UMMA issuers, alternating tiles
+constexpr int kMmaWarps = 4;           // UMMA issuers, taking tiles in turn (issuer m owns accumulator m)
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreads = kFirstEpiWarp * 32 + kEpiGroups * 128;
 constexpr int kAccBufs = 4;
@@ -325,8 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kFirstEpiWarp) {
     if (lane == 0) {
       // ---------------------------- UMMA issuers ------------------------------
-      // Issuer m takes the tiles with sequence number = m (mod 2), so one
-      // issuer's barrier waits and commits overlap the other's MMAs.
+      // Issuer m takes the tiles with sequence number = m (mod 4) and owns
+      // accumulator m, so the issuers' barrier waits and commits overlap each
+      // other's MMAs.
       const uint32_t me = (uint32_t)(warp - 1);
       const uint32_t idesc = idesc_e4m3_f32(kM, kAccCols);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0, seq = 0;
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (2 * tile >= nres) continue;
-        if ((seq++ & 1u) == me) {
+        if ((seq++ % kMmaWarps) == me) {
           if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status)) break;
           if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
           tc_fence_after();
