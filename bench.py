@@ -46,6 +46,41 @@ WORKLOAD = ("lsa_c4_indexer_1m: memindex 30x3x262144 bf16 (12% hot) + paged top-
             "E4M3 + prefill top-512 4096 tokens x 65536 chunks")
 
 
+PROFILE_CASES = {
+    # phase: [(profile summary, kernel source files, units in the summary's case, units in the bench step)]
+    "memindex": [("memindex_kernel_memindex_1m_b4_l3_s262144.md", ["memindex.cu", "fm_common.cuh"], 4, 30)],
+    "paged_topk": [("paged_score_kernel_paged_1m_q84_r384.md", ["paged.cu", "fm_common.cuh"], 84, 630)],
+    "prefill_topk": [("prefill_score_kernel_prefill_t512_s65536.md", ["prefill.cu", "fm_common.cuh"], 512, 4096),
+                     ("topk_rows_kernel_prefill_t512_s65536.md", ["topk.cu", "topk.cuh", "fm_common.cuh"], 512, 4096)],
+}
+
+
+def profiled_traffic(phase: str):
+    """DRAM traffic (read + write bytes) of a phase's kernels per step, from the
+    committed ncu summaries in profiles/, scaled from the captured case by the
+    units processed; None if a kernel's source changed since its capture."""
+    import hashlib
+    import re
+    total = 0.0
+    for name, files, units_case, units_step in PROFILE_CASES.get(phase, []):
+        path = os.path.join(ROOT, "profiles", name)
+        if not os.path.exists(path):
+            return None
+        text = open(path).read()
+        m_hash = re.search(r"first 16 hex\): `([0-9a-f]+)`", text)
+        m_traf = re.search(r"\| traffic \(read \+ write\) per launch \| ([0-9.]+) MB \|", text)
+        if not m_hash or not m_traf:
+            return None
+        h = hashlib.sha256()
+        for f in files:
+            with open(os.path.join(ROOT, "sparse_attention_kv_c4_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest()[:16] != m_hash.group(1):
+            return None
+        total += float(m_traf.group(1)) * 1e6 * units_step / units_case
+    return total or None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -415,9 +450,12 @@ def run_ours(args):
                         "frac": round(ach / peak, 4), "algorithmic_bytes": f["bytes"], "flops": f["flops"]}
     dom = max(phases, key=lambda n: phases[n]["ms"])
     d = phases[dom]
+    for name in phases:
+        phases[name]["traffic_bytes_est"] = profiled_traffic(name)
     roofline = {"bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"],
-                "frac": d["frac"], "traffic": None, "kernel": dom,
-                "peak_source": pk["source"] + (" sustained" if d["bound"] == "tensor" else "")}
+                "frac": d["frac"], "traffic": phases[dom]["traffic_bytes_est"], "kernel": dom,
+                "peak_source": pk["source"] + (" sustained" if d["bound"] == "tensor" else ""),
+                "scope": "the whole phase (score + top-k launches of one call), timed with CUDA events"}
 
     # ---- end to end through the same calls, inputs in pinned host memory ----
     host_in = {k: W[k].to("cpu").pin_memory() for k in INPUT_KEYS}
