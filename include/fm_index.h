@@ -118,7 +118,8 @@ fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const uint16
  *   score_out   [rows, k] fp32 matching scores (-inf padding), or NULL
  *   1 <= k <= 1024; n < 2^31.  NaN scores rank as -inf; -0 equals +0.
  *   workspace   device scratch of at least fm_topk_workspace(rows, n) bytes,
- *               256-byte aligned (may be NULL when that size is 0)
+ *               256-byte aligned (may be NULL when that size is 0; it is 0
+ *               for every size in this version)
  */
 size_t fm_topk_workspace(int rows, int64_t n);
 fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int64_t n,

@@ -141,16 +141,13 @@ FM_API fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const
 }
 
 FM_API size_t fm_topk_workspace(int rows, int64_t n) {
-  (void)rows;
-  (void)n;
-  return 0;
+  if (rows <= 0 || n <= 0 || n >= (int64_t(1) << 31)) return 0;
+  return topk_workspace_bytes(rows, (int)n);
 }
 
 FM_API fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int64_t n, int k,
                                 int32_t* idx_out, float* score_out, void* workspace, size_t workspace_bytes,
                                 fm_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (rows < 0 || n < 0 || n >= (int64_t(1) << 31) || k < 1 || k > 1024)
     return set_error(FM_ERR_INVALID_ARG, "fm_topk_select: bad sizes rows=%d n=%lld k=%d (1 <= k <= 1024)", rows,
                      (long long)n, k);
@@ -161,9 +158,12 @@ FM_API fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* 
   if (!aligned(scores, 4) || !aligned(idx_out, 4) || (score_out && !aligned(score_out, 4)) ||
       (n_valid && !aligned(n_valid, 4)))
     return set_error(FM_ERR_INVALID_ARG, "fm_topk_select: pointers need 4-byte alignment");
+  if (workspace != nullptr && !aligned(workspace, 256))
+    return set_error(FM_ERR_WORKSPACE, "fm_topk_select: workspace must be 256-byte aligned");
   int sms = 0;
   fm_status st = check_device(&sms);
   if (st != FM_OK) return st;
+  (void)workspace_bytes;  // the select needs no scratch (fm_topk_workspace is 0)
   return launch_topk_rows(scores, ld, n_valid, rows, (int)n, k, nullptr, 0, idx_out, score_out,
                           reinterpret_cast<cudaStream_t>(stream));
 }

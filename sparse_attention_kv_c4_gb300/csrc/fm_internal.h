@@ -42,8 +42,9 @@ struct MemindexArgs {
 };
 fm_status launch_memindex(const MemindexArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
 
-// One CTA per row; candidate i of row r has id page_ids[r*page_ld + i/64]*64 + i%64
-// when page_ids is non-null, else i.
+// Exact top-k of each row, one CTA per row; candidate i of row r has id
+// page_ids[r*page_ld + i/64]*64 + i%64 when page_ids is non-null, else i.
+size_t topk_workspace_bytes(int rows, int n);
 fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int n, int k,
                            const int32_t* page_ids, int64_t page_ld, int32_t* idx_out, float* score_out,
                            cudaStream_t stream);

@@ -160,42 +160,56 @@ FM_DEV void block_topk_radix(const float* __restrict__ row, int n, int k, IdxMap
 namespace fm {
 
 // Fast path: a threshold from a sample, one filtering pass into shared memory,
-// an exact select among the candidates.
+// an exact select among the candidates, output positions from a bitmap.
 //
 //  Every candidate is ranked by its unique composite key (key << 32 | ~index),
 //  which orders (score desc, index asc).
-//  1. Sample 16 evenly spaced runs of 64 consecutive scores (coalesced) and
+//  1. Sample 32 evenly spaced runs of 64 consecutive scores (coalesced) and
 //     take theta = about the r-th largest sample composite, r chosen so that
-//     about 2.5k candidates of the row are expected at or above it (equal
-//     scores are thresholded by index, so ties cannot flood the list).
+//     about 3 min(k, n) candidates (at most 2/3 of the list) are expected at or
+//     above it (equal scores are thresholded by index, so ties cannot flood
+//     the list).
 //  2. One vectorised pass compares each score with theta's score as a plain
 //     fp32 compare; only scores that reach it (a few percent) build their
 //     composite and are appended, when composite >= theta, to a shared-memory
-//     list (one shared-memory atomic per appended candidate).
+//     list (one shared-memory atomic per appended candidate); the largest
+//     appended composite is tracked too.
 //  3. If the list holds at least min(k, n) entries and did not overflow, the
-//     true top-k is inside it (the k-th largest composite is >= theta): a radix
-//     select over the composites finds the min(k, n)-th largest; the selected
-//     indices are marked in a bitmap and emitted in index order by one
-//     block-wide prefix sum (longer rows gather and sort instead).  Otherwise
-//     the exact global-memory radix path (block_topk_radix) runs.
+//     true top-k is inside it (the k-th largest composite is >= theta): a
+//     block-wide radix select over the composites, starting at the first bit
+//     where theta and the largest candidate differ, finds the min(k, n)-th
+//     largest T.  Otherwise the exact global-memory radix path
+//     (block_topk_radix) runs.
+//  4. The selected indices are marked in a bitmap; one block-wide prefix sum
+//     over the bitmap words gives each thread's word range its first output
+//     slot, and each selected candidate computes its own slot (rank by index)
+//     from it, so the output is in ascending index order with no sort and no
+//     second read of the row (longer rows sort the selection instead).
 // Scores are reported from their keys: -0 reads as +0 and NaN as -inf.
-constexpr int kTopkCap = 4096;        // candidate slots (32 KB of shared memory)
-constexpr int kTopkRuns = 16;         // sample: 16 runs x 64 scores
+constexpr int kTopkCap = 4096;       // candidate slots (32 KB of shared memory)
+constexpr int kTopkRuns = 32;        // sample: 32 runs x 64 scores
 constexpr int kTopkSample = kTopkRuns * 64;
 constexpr int kTopkBitmapN = 131072;  // rows up to this length emit ids via a bitmap
 
 template <int THREADS>
+struct SelectSmem {
+  uint32_t hist[2][256];
+  uint32_t digit[2], above[2], in_digit[2];
+};
+
+template <int THREADS>
 struct TopkFastSmem {
   unsigned long long cand[kTopkCap];
-  uint32_t whist[256];
-  unsigned long long wsel;
+  unsigned long long cmax;
   union {
     unsigned long long sample[kTopkSample];
     unsigned long long sel[1024];
     uint32_t bitmap[kTopkBitmapN / 32];
   } u;
+  uint32_t tpre[THREADS];
   uint32_t count;
   int overflow;
+  SelectSmem<THREADS> sel;
   TopkSmem<THREADS> radix;
 };
 
@@ -225,39 +239,43 @@ FM_DEV int next_pow2(int x) {
   return p;
 }
 
-// Radix select over a[0..n) in shared memory, most significant 8-bit digit
-// first, at most max_passes digits.  Returns T with count(a >= T) >= r
-// (1 <= r <= n).  It stops early when the deciding digit holds exactly the
-// remaining need (then count(a >= T) == r for distinct values) or at most
-// `loose` values (then count(a >= T) <= r + loose).  All threads call it.
-template <int THREADS, typename V>
-FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, uint32_t loose, TopkSmem<THREADS>& sm) {
+// Radix select of the r-th largest (1 <= r <= n) of the distinct values
+// a[0..n) in shared memory, all of which lie in [lo, hi]: 8-bit digits, most
+// significant first, starting at the highest bit where lo and hi differ (the
+// bits above it are common to every value, so they need no pass).  It stops
+// once the deciding digit holds exactly the remaining need (then the result T
+// has count(a >= T) == r) or at most `loose` values (then r <= count(a >= T)
+// <= r + loose); always count(a >= T) >= r.  Digit counts are plain
+// shared-memory atomics (cheaper here than aggregating them per warp with
+// __match_any_sync); the two histograms alternate so that each digit costs two
+// block barriers.  All threads call it.
+template <int THREADS>
+FM_DEV unsigned long long block_select_u64(const unsigned long long* a, int n, int r, unsigned long long lo,
+                                           unsigned long long hi, uint32_t loose, SelectSmem<THREADS>& sm) {
   const int tid = threadIdx.x, lane = tid & 31;
-  constexpr int kBits = 8 * (int)sizeof(V);
-  V prefix = 0, pmask = 0;
+  if (lo == hi) return lo;
+  const int hb = 63 - __clzll((long long)(lo ^ hi));
+  unsigned long long pmask = hb == 63 ? 0ull : (~0ull << (hb + 1));
+  unsigned long long prefix = lo & pmask;
   uint32_t need = (uint32_t)r;
-  for (int pass = 0; pass < max_passes && pass < kBits / 8; ++pass) {
-    const int shift = kBits - 8 * (pass + 1);
-    for (int i = tid; i < 256; i += THREADS) sm.hist[i] = 0;
-    __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += THREADS) {
-      const int i = i0 + tid;
-      bool act = false;
-      uint32_t digit = 0x100u + (uint32_t)lane;
-      if (i < n) {
-        const V v = a[i];
-        act = (v & pmask) == prefix;
-        if (act) digit = (uint32_t)((v >> shift) & 0xFFu);
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (act && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], (uint32_t)__popc(peers));
+  for (int i = tid; i < 256; i += THREADS) sm.hist[0][i] = 0u;
+  __syncthreads();
+  int b = 0;
+  for (int s = hb - 7;; s -= 8, b ^= 1) {
+    const int shift = s > 0 ? s : 0;
+    uint32_t* hist = sm.hist[b];
+    for (int i = tid; i < 256; i += THREADS) sm.hist[b ^ 1][i] = 0u;  // for the next digit
+    for (int i = tid; i < n; i += THREADS) {
+      const unsigned long long v = a[i];
+      if ((v & pmask) == prefix) atomicAdd(&hist[(uint32_t)(v >> shift) & 0xFFu], 1u);
     }
     __syncthreads();
     if (tid < 32) {
+      // lane l owns digits 255-8l .. 248-8l (descending)
       uint32_t c[8], s8 = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = sm.hist[255 - 8 * lane - j];
+        c[j] = hist[255 - 8 * lane - j];
         s8 += c[j];
       }
       uint32_t incl = s8;
@@ -272,9 +290,9 @@ FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, uint32_t lo
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (acc + c[j] >= need) {
-            sm.sel_prefix = 255u - 8u * (uint32_t)lane - (uint32_t)j;
-            sm.digit_above = acc;
-            sm.need = c[j];
+            sm.digit[b] = 255u - 8u * (uint32_t)lane - (uint32_t)j;
+            sm.above[b] = acc;
+            sm.in_digit[b] = c[j];
             break;
           }
           acc += c[j];
@@ -282,72 +300,11 @@ FM_DEV V smem_radix_select(const V* a, int n, int r, int max_passes, uint32_t lo
       }
     }
     __syncthreads();
-    const uint32_t d = sm.sel_prefix;
-    const uint32_t in_digit = sm.need;
-    need -= sm.digit_above;
-    prefix |= (V)d << shift;
-    pmask |= (V)0xFFu << shift;
-    __syncthreads();
-    if (in_digit == need || in_digit <= loose) break;  // lower bits cannot matter (or need not)
-  }
-  return prefix;
-}
-
-// The same select run by one warp (no block barriers): for the short lists of
-// samples and candidates a single warp is faster than the whole block.
-template <typename V>
-FM_DEV V warp_radix_select(const V* a, int n, int r, int max_passes, uint32_t loose, uint32_t* hist) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kBits = 8 * (int)sizeof(V);
-  V prefix = 0, pmask = 0;
-  uint32_t need = (uint32_t)r;
-  for (int pass = 0; pass < max_passes && pass < kBits / 8; ++pass) {
-    const int shift = kBits - 8 * (pass + 1);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) hist[lane + 32 * j] = 0u;
-    __syncwarp();
-    for (int i = lane; i < n; i += 32) {
-      const V v = a[i];
-      if ((v & pmask) == prefix) atomicAdd(&hist[(uint32_t)((v >> shift) & 0xFFu)], 1u);
-    }
-    __syncwarp();
-    uint32_t c[8], s8 = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      c[j] = hist[255 - 8 * lane - j];
-      s8 += c[j];
-    }
-    uint32_t incl = s8;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const uint32_t above = incl - s8;
-    uint32_t d = 0, dabove = 0, din = 0;
-    const bool mine = above < need && need <= incl;
-    if (mine) {
-      uint32_t acc = above;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (acc + c[j] >= need) {
-          d = 255u - 8u * (uint32_t)lane - (uint32_t)j;
-          dabove = acc;
-          din = c[j];
-          break;
-        }
-        acc += c[j];
-      }
-    }
-    const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-    d = __shfl_sync(0xffffffffu, d, src);
-    dabove = __shfl_sync(0xffffffffu, dabove, src);
-    din = __shfl_sync(0xffffffffu, din, src);
-    need -= dabove;
-    prefix |= (V)d << shift;
-    pmask |= (V)0xFFu << shift;
-    __syncwarp();
-    if (din == need || din <= loose) break;
+    const uint32_t d = sm.digit[b], in_digit = sm.in_digit[b];
+    need -= sm.above[b];
+    prefix |= (unsigned long long)d << shift;  // bits already decided agree with d
+    pmask |= 0xFFull << shift;
+    if (shift == 0 || in_digit == need || in_digit <= loose) break;
   }
   return prefix;
 }
@@ -373,18 +330,20 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
       sm.u.sample[i] = ((unsigned long long)float_key(__ldg(row + j)) << 32) | (uint32_t)(~(uint32_t)j);
     }
     __syncthreads();
-    int r = (int)(((long long)5 * kk * kTopkSample) / (2 * (long long)n));  // ~2.5 k candidates
+    const long long want = 3 * kk < 2 * kTopkCap / 3 ? 3 * kk : 2 * kTopkCap / 3;  // expected candidates
+    int r = (int)((want * kTopkSample) / (long long)n);
     r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
-    if (tid < 32) {
-      const unsigned long long t = warp_radix_select<unsigned long long>(sm.u.sample, kTopkSample, r, 8, 8u, sm.whist);
-      if (tid == 0) sm.wsel = t;
-    }
-    __syncthreads();
-    theta = sm.wsel;
+    theta = block_select_u64<THREADS>(sm.u.sample, kTopkSample, r, 0ull, ~0ull, 4u, sm.sel);
+  }
+  // the sample is dead from here: its space becomes the (cleared) bitmap
+  if (n <= kTopkBitmapN) {
+    const int words = (n + 31) >> 5;
+    for (int i = tid; i < words; i += THREADS) sm.u.bitmap[i] = 0u;
   }
   if (tid == 0) {
     sm.count = 0;
     sm.overflow = 0;
+    sm.cmax = 0ull;
   }
   __syncthreads();
   // ---- 2. filter pass ---------------------------------------------------------
@@ -395,42 +354,93 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   const uint32_t theta_key = (uint32_t)(theta >> 32);
   const bool take_all = theta == 0ull || theta_key <= 0x007FFFFFu;
   const float theta_f = take_all ? -INFINITY : key_float(theta_key);
-  auto push = [&](bool maybe, float v, int i) {
-    if (maybe) {
-      const unsigned long long c = ((unsigned long long)float_key(v) << 32) | (uint32_t)(~(uint32_t)i);
-      if (c >= theta) {
-        const uint32_t slot = atomicAdd(&sm.count, 1u);
-        if (slot < (uint32_t)kTopkCap)
-          sm.cand[slot] = c;
-        else
-          sm.overflow = 1;
-      }
+  // A score survives if its composite reaches theta: a score above theta's
+  // score always does; one equal to it only if the index breaks the tie (rare,
+  // so the composite is built only then).  Under take_all every score takes
+  // the composite test (NaN ranks as -inf).  Each warp counts its survivors,
+  // reserves their slots with one shared-memory atomic and then writes them.
+  const int lane = tid & 31;
+  auto composite_of = [](float v, int i) -> unsigned long long {
+    return ((unsigned long long)float_key(v) << 32) | (uint32_t)(~(uint32_t)i);
+  };
+  auto passes = [&](float v, int i) -> bool {
+    if (take_all || v == theta_f) return composite_of(v, i) >= theta;
+    return v > theta_f;
+  };
+  // 4-bit survivor mask of one float4 (the common case tests floats only)
+  auto mask4 = [&](const float4& v, int i) -> uint32_t {
+    const bool any_eq = v.x == theta_f || v.y == theta_f || v.z == theta_f || v.w == theta_f;
+    if (!take_all && !any_eq)
+      return (uint32_t)(v.x > theta_f) | ((uint32_t)(v.y > theta_f) << 1) | ((uint32_t)(v.z > theta_f) << 2) |
+             ((uint32_t)(v.w > theta_f) << 3);
+    return (uint32_t)passes(v.x, i) | ((uint32_t)passes(v.y, i + 1) << 1) | ((uint32_t)passes(v.z, i + 2) << 2) |
+           ((uint32_t)passes(v.w, i + 3) << 3);
+  };
+  auto reserve = [&](uint32_t mine) -> uint32_t {  // all lanes of the warp call it
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t base = 0;
+    if (lane == 31 && total > 0u) base = atomicAdd(&sm.count, total);
+    return __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+  };
+  unsigned long long tmax = 0ull;  // this thread's largest stored composite
+  auto store = [&](uint32_t slot, float v, int i) {
+    const unsigned long long c = composite_of(v, i);
+    if (slot < (uint32_t)kTopkCap) {
+      sm.cand[slot] = c;
+      tmax = c > tmax ? c : tmax;
+    } else {
+      sm.overflow = 1;
     }
   };
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
   const int n4 = vec ? n / 4 : 0;
   const float4* row4 = reinterpret_cast<const float4*>(row);
-  for (int i40 = 0; i40 < n4; i40 += THREADS * 4) {
-    float4 v[4];
+  constexpr int kVec = 8;  // float4 loads in flight per thread
+  for (int i40 = 0; i40 < n4; i40 += THREADS * kVec) {  // same trip count in every thread
+    float4 v[kVec];
+    uint32_t mask = 0;  // bit 4u + j: element j of v[u] survives
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kVec; ++u) {
       const int i4 = i40 + u * THREADS + tid;
       v[u] = i4 < n4 ? __ldg(row4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kVec; ++u) {
       const int i4 = i40 + u * THREADS + tid;
-      const bool in = i4 < n4;
-      push(in && (take_all || v[u].x >= theta_f), v[u].x, 4 * i4);
-      push(in && (take_all || v[u].y >= theta_f), v[u].y, 4 * i4 + 1);
-      push(in && (take_all || v[u].z >= theta_f), v[u].z, 4 * i4 + 2);
-      push(in && (take_all || v[u].w >= theta_f), v[u].w, 4 * i4 + 3);
+      if (i4 < n4) mask |= mask4(v[u], 4 * i4) << (4 * u);
+    }
+    uint32_t slot = reserve((uint32_t)__popc(mask));
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+      uint32_t sub = (mask >> (4 * u)) & 15u;
+      const int i = 4 * (i40 + u * THREADS + tid);
+      while (sub) {
+        const int j = __ffs(sub) - 1;
+        sub &= sub - 1u;
+        const float x = j == 0 ? v[u].x : (j == 1 ? v[u].y : (j == 2 ? v[u].z : v[u].w));
+        store(slot++, x, i + j);
+      }
     }
   }
-  for (int i = 4 * n4 + tid; i < n; i += THREADS) {
-    const float v = __ldg(row + i);
-    push(take_all || v >= theta_f, v, i);
+  for (int i0 = 4 * n4; i0 < n; i0 += THREADS) {  // scalar rest (all of an unaligned row)
+    const int i = i0 + tid;
+    const float v = i < n ? __ldg(row + i) : -INFINITY;
+    const bool p = i < n && passes(v, i);
+    const uint32_t slot = reserve((uint32_t)p);
+    if (p) store(slot, v, i);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, tmax, o);
+    tmax = y > tmax ? y : tmax;
+  }
+  if (lane == 0 && tmax != 0ull) atomicMax(&sm.cmax, tmax);
   __syncthreads();
   const int cnt = (int)sm.count;
   if (sm.overflow || cnt < kk) {
@@ -439,18 +449,11 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
     return;
   }
   // ---- 3. exact select among the candidates -------------------------------------
-  if (tid < 32) {
-    const unsigned long long t = warp_radix_select<unsigned long long>(sm.cand, cnt, kk, 8, 0u, sm.whist);
-    if (tid == 0) sm.wsel = t;
-  }
-  __syncthreads();
-  const unsigned long long T = sm.wsel;
+  // every candidate lies in [theta, cmax]
+  const unsigned long long T = block_select_u64<THREADS>(sm.cand, cnt, kk, theta, sm.cmax, 0u, sm.sel);
+  // ---- 4. emit in index order -------------------------------------------------
   if (n <= kTopkBitmapN) {
-    // mark the selected indices in a bitmap, then emit them in index order
-    // with one block-wide prefix sum over the bitmap words
     const int words = (n + 31) >> 5;
-    for (int i = tid; i < words; i += THREADS) sm.u.bitmap[i] = 0u;
-    __syncthreads();
     for (int i = tid; i < cnt; i += THREADS) {
       const unsigned long long c = sm.cand[i];
       if (c >= T) {
@@ -465,16 +468,17 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
     for (int j = 0; j < per; ++j)
       if (w0 + j < words) mine += (uint32_t)__popc(sm.u.bitmap[w0 + j]);
     uint32_t tot;
-    uint32_t pos = block_excl_scan<THREADS>(mine, sm.radix.warp_tot, &tot);
-    for (int j = 0; j < per && w0 + j < words; ++j) {
-      uint32_t bits = sm.u.bitmap[w0 + j];
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int i = ((w0 + j) << 5) + b;
-        idx_out[pos] = idx_map(i);
-        if (score_out) score_out[pos] = key_float(float_key(__ldg(row + i)));
-        ++pos;
+    sm.tpre[tid] = block_excl_scan<THREADS>(mine, sm.radix.warp_tot, &tot);
+    __syncthreads();
+    for (int i = tid; i < cnt; i += THREADS) {
+      const unsigned long long c = sm.cand[i];
+      if (c >= T) {
+        const uint32_t idx = ~(uint32_t)c;
+        const int w = (int)(idx >> 5), owner = w / per;
+        uint32_t pos = sm.tpre[owner] + (uint32_t)__popc(sm.u.bitmap[w] & ((1u << (idx & 31)) - 1u));
+        for (int w2 = owner * per; w2 < w; ++w2) pos += (uint32_t)__popc(sm.u.bitmap[w2]);
+        idx_out[pos] = idx_map((int)idx);
+        if (score_out) score_out[pos] = key_float((uint32_t)(c >> 32));
       }
     }
   } else {

@@ -69,3 +69,11 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fm, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         fm.lib()
+
+
+def test_topk_workspace_size_contract(lib):
+    """fm_topk_workspace is host-only arithmetic; the select needs no scratch."""
+    lib.fm_topk_workspace.argtypes = [ctypes.c_int, ctypes.c_int64]
+    lib.fm_topk_workspace.restype = ctypes.c_size_t
+    for rows, n in ((8, 4096), (8, 65536), (0, 65536), (4096, 131073)):
+        assert lib.fm_topk_workspace(rows, n) == 0
