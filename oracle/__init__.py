@@ -75,6 +75,7 @@ class Oracle:
         lib.orc_causal_limit.argtypes = [I64, I64, I32]
         lib.orc_causal_limit.restype = I64
         lib.orc_prefill_topk.argtypes = [u16p, f32p, i64p, u16p, I64, I64, I32, I32, I32, I32, i32p, f64p]
+        lib.orc_page_recall.argtypes = [u32p, I64, I64, I64, I64, I32, I32, i32p, i32p, i32p]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = lib
@@ -159,6 +160,18 @@ class Oracle:
         self.lib.orc_prefill_topk(_p(q, u16p), _p(w, f32p), _p(pos, i64p), _p(K, u16p), T, S, n_h, d, ratio,
                                   k, _p(idx, i32p), _p(sc, f64p))
         return idx, sc
+
+    def page_recall(self, mask, S: int, kmax: int, sink: int = 0, recent: int = 0, page_size: int = 64):
+        """mask [B, ceil(S/32)] uint32 -> (pages [B,kmax] int32 ascending, -1 padded;
+        density [B,kmax] int32, -1 padded; n [B] int32)."""
+        mask = _c(np.atleast_2d(mask), np.uint32)
+        B = mask.shape[0]
+        pages = np.empty((B, kmax), np.int32)
+        dens = np.empty((B, kmax), np.int32)
+        n = np.empty(B, np.int32)
+        self.lib.orc_page_recall(_p(mask, u32p), B, S, sink, recent, page_size, kmax,
+                                 _p(pages, i32p), _p(dens, i32p), _p(n, i32p))
+        return pages, dens, n
 
     def num_threads(self) -> int:
         return self.lib.orc_num_threads()

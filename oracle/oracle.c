@@ -275,6 +275,51 @@ ORC_API void orc_prefill_topk(const uint16_t* q, const float* w, const int64_t* 
   }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Page recall: the densest resident pages of each request                    */
+/* ------------------------------------------------------------------------- */
+
+/* [RM] "Two-level recall algorithm", Level 1: the resident set is the
+ * thresholded Memory-Indexer mask plus the recency tail and the attention
+ * sink; [RM] "Page-recall" (64-chunk pages) and the KMAX note under
+ * "Reference performance": each request recalls the KMAX pages that hold the
+ * most resident chunks (256K -> 96, 512K -> 192, 1M -> 384 pages).
+ * Readings where the pages are silent: the sink is chunks [0, sink), the
+ * recency tail chunks [S - recent, S); a page's density is its number of
+ * resident chunks (the last page may be partial); pages of density 0 are never
+ * recalled; equal densities go to the lower page id; the recalled pages are
+ * emitted by ascending id, padded with -1 (density -1).
+ * mask [B][ceil(S/32)]: bit s & 31 of word s >> 5 is chunk s.  pages_out and
+ * density_out are [B][kmax]; n_out[b] is the number of pages recalled. */
+ORC_API void orc_page_recall(const uint32_t* mask, int64_t B, int64_t S, int64_t sink, int64_t recent,
+                             int page_size, int kmax, int32_t* pages_out, int32_t* density_out, int32_t* n_out) {
+  const int64_t words = (S + 31) / 32;
+  const int64_t n_pages = (S + page_size - 1) / page_size;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t b = 0; b < B; ++b) {
+    orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(n_pages > 0 ? n_pages : 1));
+    double* dens = (double*)malloc(sizeof(double) * (size_t)(kmax > 0 ? kmax : 1));
+    int64_t n = 0;
+    for (int64_t p = 0; p < n_pages; ++p) {
+      int64_t density = 0;
+      for (int64_t s = p * page_size; s < (p + 1) * page_size && s < S; ++s) {
+        int resident = (mask[b * words + (s >> 5)] >> (s & 31)) & 1u;
+        if (s < sink || s >= S - recent) resident = 1;
+        density += resident;
+      }
+      if (density > 0) {
+        c[n].x = (double)density;
+        c[n].id = p;
+        ++n;
+      }
+    }
+    n_out[b] = orc_topk_cands(c, n, kmax, pages_out + b * kmax, dens);
+    for (int i = 0; i < kmax; ++i) density_out[b * kmax + i] = i < n_out[b] ? (int32_t)dens[i] : -1;
+    free(dens);
+    free(c);
+  }
+}
+
 ORC_API int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -375,4 +375,64 @@ def pin_planted_tiny(orc):
     assert m == 512 and set(np.nonzero(pl)[0]) <= set(idx.tolist())
 
 
+# ---------------------------------------------------------------------------
+# page recall (densest resident pages)
+# ---------------------------------------------------------------------------
+
+def _recall_bruteforce(mask_row, S, kmax, sink, recent, page=64):
+    """Resident set as a Python set, densities by counting, order by sorting."""
+    resident = {s for s in range(S) if (int(mask_row[s >> 5]) >> (s & 31)) & 1}
+    resident |= set(range(min(sink, S)))
+    resident |= set(range(max(S - recent, 0), S))
+    n_pages = (S + page - 1) // page
+    dens = [sum(1 for s in range(p * page, min((p + 1) * page, S)) if s in resident) for p in range(n_pages)]
+    order = sorted((p for p in range(n_pages) if dens[p] > 0), key=lambda p: (-dens[p], p))
+    chosen = sorted(order[:kmax])
+    return (chosen + [-1] * (kmax - len(chosen)), [dens[p] for p in chosen] + [-1] * (kmax - len(chosen)),
+            len(chosen))
+
+
+def pin_page_recall_bruteforce(orc):
+    """[RM] Level 1 resident set (threshold + recent + sink) and the KMAX
+    densest 64-chunk pages: brute force over small random masks, with partial
+    last pages, ties in density and forced sink / recency chunks."""
+    rng = np.random.default_rng(17)
+    for S in (1, 63, 64, 65, 200, 777, 1024):
+        words = (S + 31) // 32
+        for density_p in (0.02, 0.3, 0.9):
+            bits = rng.random((3, words * 32)) < density_p
+            bits[:, S:] = False  # bits past S are zero by contract
+            mask = np.packbits(bits.reshape(3, words, 32)[:, :, ::-1], axis=-1, bitorder="big")
+            mask = mask.reshape(3, words, 4)[:, :, ::-1].copy().view(np.uint32).reshape(3, words)
+            for kmax in (1, 3, 16):
+                sink, recent = int(rng.integers(0, 70)), int(rng.integers(0, 90))
+                pages, dens, n = orc.page_recall(mask, S, kmax, sink=sink, recent=recent)
+                for b in range(3):
+                    wp, wd, wn = _recall_bruteforce(mask[b], S, kmax, sink, recent)
+                    assert list(pages[b]) == wp and list(dens[b]) == wd and n[b] == wn, (S, kmax, b)
+
+
+def pin_page_recall_closed_forms(orc):
+    """Closed forms: an empty resident set recalls nothing; an all-resident
+    history of P full pages plus a partial page of r chunks has densities
+    64 ... 64, r; the recency tail alone recalls exactly the last pages."""
+    S = 64 * 5 + 17
+    words = (S + 31) // 32
+    zero = np.zeros((1, words), np.uint32)
+    pages, dens, n = orc.page_recall(zero, S, 8)
+    assert n[0] == 0 and (pages == -1).all() and (dens == -1).all()
+    ones = np.full((1, words), 0xFFFFFFFF, np.uint32)
+    ones[0, -1] = (1 << (S % 32)) - 1  # bits past S are zero
+    pages, dens, n = orc.page_recall(ones, S, 8)
+    assert n[0] == 6 and list(pages[0]) == [0, 1, 2, 3, 4, 5, -1, -1] and list(dens[0][:6]) == [64] * 5 + [17]
+    pages, dens, n = orc.page_recall(ones, S, 5)  # the partial page loses
+    assert list(pages[0]) == [0, 1, 2, 3, 4]
+    pages, dens, n = orc.page_recall(zero, S, 8, sink=S)  # the sink covers everything
+    assert n[0] == 6 and list(dens[0][:6]) == [64] * 5 + [17]
+    pages, dens, n = orc.page_recall(zero, S, 8, recent=17 + 64)  # the last page and a half
+    assert list(pages[0][:2]) == [4, 5] and list(dens[0][:2]) == [64, 17] and n[0] == 2
+    pages, dens, n = orc.page_recall(zero, S, 8, sink=1, recent=1)
+    assert list(pages[0][:2]) == [0, 5] and list(dens[0][:2]) == [1, 1] and n[0] == 2
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

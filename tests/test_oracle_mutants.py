@@ -48,6 +48,14 @@ MUTANTS = {
     "causal_inclusive": ("int64_t lim = pos / ratio;", "int64_t lim = pos / ratio + 1;"),
     "causal_token_not_chunk": ("int64_t lim = pos / ratio;", "int64_t lim = pos;"),
     "nan_ranks_high": ("double xa = isnan(a->x) ? -INFINITY : a->x;", "double xa = isnan(a->x) ? INFINITY : a->x;"),
+    "recall_keeps_empty_pages": ("if (density > 0) {", "if (density >= 0) {"),
+    "recall_recent_short": ("if (s < sink || s >= S - recent) resident = 1;",
+                            "if (s < sink || s > S - recent) resident = 1;"),
+    "recall_sink_long": ("if (s < sink || s >= S - recent) resident = 1;",
+                         "if (s <= sink || s >= S - recent) resident = 1;"),
+    "recall_partial_page_overrun": ("s < (p + 1) * page_size && s < S; ++s)", "s < (p + 1) * page_size; ++s)"),
+    "recall_bit_reversed": ("int resident = (mask[b * words + (s >> 5)] >> (s & 31)) & 1u;",
+                            "int resident = (mask[b * words + (s >> 5)] >> (31 - (s & 31))) & 1u;"),
 }
 
 RUNNER = r"""
