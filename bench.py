@@ -172,6 +172,8 @@ def build_inputs(torch, dev, cfgs, only=None):
     gen.memindex_keys_device(mi, hot_d.data_ptr(), W["mi_K"].data_ptr(), mi.L * mi.S * mi.d, mi.S * mi.d)
     W["mi_mask"] = torch.empty((mi.B, (mi.S + 31) // 32), dtype=torch.int32, device=dev)
     W["mi_maxsig"] = torch.empty((mi.B, mi.S), dtype=torch.float32, device=dev)
+    W["rc_pages"] = torch.empty((mi.B, KMAX), dtype=torch.int32, device=dev)
+    W["rc_n"] = torch.empty((mi.B,), dtype=torch.int32, device=dev)
     return _build_rest(torch, dev, W, cfgs, pg, pf)
 
 
@@ -212,7 +214,10 @@ def _build_prefill(torch, dev, W, cfgs, pf):
 
 INPUT_KEYS = ["mi_q", "mi_w", "mi_K", "pg_q", "pg_w", "pg_k8", "pg_scale", "pg_phys", "pg_logical", "pf_q", "pf_w",
               "pf_pos", "pf_K"]
-OUTPUT_KEYS = ["mi_mask", "mi_maxsig", "pg_idx", "pg_score", "pf_idx", "pf_score"]
+OUTPUT_KEYS = ["mi_mask", "mi_maxsig", "rc_pages", "rc_n", "pg_idx", "pg_score", "pf_idx", "pf_score"]
+# Pages recalled per request after the Memory Indexer: the KMAX of 1M context
+# (256K -> 96, 512K -> 192, 1M -> 384 densest 64-chunk pages).
+KMAX = 384
 
 
 def make_step(fm, W, cfgs, ws, events=None):
@@ -225,6 +230,10 @@ def make_step(fm, W, cfgs, ws, events=None):
             fm.fm_memindex_score_mask(W["mi_q"], W["mi_w"], W["mi_K"], W["mi_mask"], W["mi_maxsig"])
         if events is not None:
             events[1].record()
+        if "mi_K" in W:
+            fm.fm_page_recall(W["mi_mask"], mi.S, KMAX, W["rc_pages"], None, W["rc_n"])
+        if events is not None:
+            events[4].record()
         if "pg_k8" in W:
             fm.fm_native_topk_paged(W["pg_q"], W["pg_w"], W["pg_k8"], W["pg_scale"], W["pg_phys"],
                                     W["pg_logical"], pg.k, W["pg_idx"], W["pg_score"], workspace=ws["pg"])
@@ -238,7 +247,7 @@ def make_step(fm, W, cfgs, ws, events=None):
     return step
 
 
-KERNELS_PER_STEP = 1 + 3 + 3  # memindex; paged prep/score/top-k; prefill limits/score/top-k
+KERNELS_PER_STEP = 1 + 1 + 3 + 3  # memindex; page recall; paged prep/score/top-k; prefill limits/score/top-k
 
 
 def phase_figures(cfgs):
@@ -247,6 +256,9 @@ def phase_figures(cfgs):
         "memindex": {"chunk_scores": mi.chunk_scores, "queries": 0,
                      "bytes": mi.B * mi.L * mi.S * mi.d * 2 + mi.B * mi.S * 4 + mi.B * ((mi.S + 31) // 32) * 4,
                      "flops": mi.chunk_scores * mi.n_h * mi.d * 2, "bound": "hbm"},
+        "page_recall": {"chunk_scores": 0, "queries": 0,
+                        "bytes": mi.B * ((mi.S + 31) // 32) * 4 + mi.B * (KMAX + 1) * 4, "flops": 0,
+                        "bound": "hbm"},
         "paged_topk": {"chunk_scores": pg.chunk_scores, "queries": pg.Q,
                        "bytes": pg.P * pg.page * (pg.d + 4) + pg.Q * pg.R * 8 + pg.Q * pg.k * 8,
                        "flops": pg.chunk_scores * pg.n_h * pg.d * 2, "bound": "hbm"},
@@ -261,7 +273,8 @@ def sanity(torch, W, cfgs):
     frac = float(torch.bitwise_count(W["mi_mask"]).sum().item()) / (mi.B * mi.S) if hasattr(torch, "bitwise_count") \
         else None
     ok = bool((W["pg_idx"] >= 0).all().item()) and bool((W["pf_idx"] >= 0).all().item())
-    return {"resident_fraction": frac, "topk_full": ok}
+    recalled = float(W["rc_n"].float().mean().item())
+    return {"resident_fraction": frac, "topk_full": ok, "pages_recalled_mean": recalled}
 
 
 # ---------------------------------------------------------------------------
@@ -395,7 +408,7 @@ def run_ours(args):
         return run_profile_case(args, fm, torch, W, cfgs, ws)
     stream = torch.cuda.current_stream()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     warm = make_step(fm, W, cfgs, ws)
     for _ in range(args.warmup):
         warm()
@@ -419,10 +432,11 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     ms_total = start.elapsed_time(end)
-    phase_ms = {"memindex": [], "paged_topk": [], "prefill_topk": []}
+    phase_ms = {"memindex": [], "page_recall": [], "paged_topk": [], "prefill_topk": []}
     for e in ev:
         phase_ms["memindex"].append(e[0].elapsed_time(e[1]))
-        phase_ms["paged_topk"].append(e[1].elapsed_time(e[2]))
+        phase_ms["page_recall"].append(e[1].elapsed_time(e[4]))
+        phase_ms["paged_topk"].append(e[4].elapsed_time(e[2]))
         phase_ms["prefill_topk"].append(e[2].elapsed_time(e[3]))
     status = fm.fm_device_status(reset=True)
     chk = sanity(torch, W, cfgs)
@@ -497,7 +511,7 @@ def run_ours(args):
                 "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16/e4m3 in, fp32 accumulate", "data": "synthetic",
                 "config": {"workload": WORKLOAD, "global_batch": world * (mi.B + pg.Q + pf.T),
-                           "seq_len": 4 * mi.S, "parallelism": f"replicas x{world} (request sharding)",
+                           "seq_len": 4 * mi.S, "kmax": KMAX, "parallelism": f"replicas x{world} (request sharding)",
                            "l2": "inputs larger than L2 (8.1 GB of keys streamed per step); no flush"},
                 "queries_per_s": world * q_step * K / (ms_total / 1e3),
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

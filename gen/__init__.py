@@ -179,6 +179,22 @@ class PrefillCfg:
         return self.T * self.S
 
 
+@dataclass(frozen=True)
+class RecallCfg:
+    """Page recall: B requests' resident masks over S chunks, KMAX densest
+    pages recalled.  Mask recipe: hot runs of 64..256 consecutive chunks
+    covering about hot_frac of the history (the planted, query-relevant
+    regions) plus a fraction ``cold`` of the other chunks (cold chunks whose
+    logit still passes the threshold)."""
+    name: str
+    B: int
+    S: int
+    kmax: int
+    cold: float = 0.25
+    hot_frac: float = 0.12
+    seed: int = BASE_SEED + 6
+
+
 TINY = MemIndexCfg("tiny_s4096", B=1, L=1, S=4096, seed=BASE_SEED + 0)
 MEMINDEX_256K = MemIndexCfg("memindex_256k_b76_l3_s65536", B=76, L=3, S=65536, seed=BASE_SEED + 1)
 MEMINDEX_1M = MemIndexCfg("memindex_1m_b30_l3_s262144", B=30, L=3, S=262144, seed=BASE_SEED + 2)
@@ -187,6 +203,33 @@ PAGED_512K = PagedCfg("paged_512k_q1260_r192", requests=60, layers=21, n_pages=2
 PAGED_1M = PagedCfg("paged_1m_q630_r384", requests=30, layers=21, n_pages=4096, R=384,
                     seed=BASE_SEED + 4)
 PREFILL = PrefillCfg("prefill_t4096_s65536", T=4096, S=65536, pos0=262144, seed=BASE_SEED + 5)
+RECALL_256K = RecallCfg("recall_256k_b76_s65536_k96", B=76, S=65536, kmax=96)
+RECALL_512K = RecallCfg("recall_512k_b60_s131072_k192", B=60, S=131072, kmax=192, seed=BASE_SEED + 7)
+RECALL_1M = RecallCfg("recall_1m_b30_s262144_k384", B=30, S=262144, kmax=384, seed=BASE_SEED + 8)
+
+
+def pack_mask(bits: np.ndarray) -> np.ndarray:
+    """bool [B, S] -> uint32 [B, ceil(S/32)], bit s & 31 of word s >> 5 = chunk s."""
+    bits = np.atleast_2d(bits)
+    B, S = bits.shape
+    words = (S + 31) // 32
+    padded = np.zeros((B, words * 32), dtype=bool)
+    padded[:, :S] = bits
+    return np.packbits(padded, axis=-1, bitorder="little").view("<u4").reshape(B, words)
+
+
+def recall_mask(cfg: RecallCfg) -> np.ndarray:
+    """Seeded resident mask [B, ceil(S/32)] uint32 for a RecallCfg."""
+    rng = np.random.default_rng(cfg.seed)
+    bits = rng.random((cfg.B, cfg.S)) < cfg.cold
+    for b in range(cfg.B):
+        covered = 0
+        while covered < cfg.hot_frac * cfg.S:
+            run = int(rng.integers(64, 257))
+            start = int(rng.integers(0, max(cfg.S - run, 1)))
+            bits[b, start:start + run] = True
+            covered += run
+    return pack_mask(bits)
 
 
 # --------------------------------------------------------------------------

@@ -127,6 +127,30 @@ fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* n_valid
                          fm_stream_t stream);
 
 /*
+ * Page recall: the densest resident pages of each request ([RM] "Two-level
+ * recall algorithm", Level 1: resident_set = threshold + recent + sink;
+ * "Page-recall": 64-chunk pages; the KMAX note under "Reference performance":
+ * KMAX = 96 / 192 / 384 densest pages at 256K / 512K / 1M).
+ *
+ * For request b, chunk s < S is resident iff bit s & 31 of mask[b, s >> 5] is
+ * set, or s < sink, or s >= S - recent.  Page p holds chunks 64p .. 64p + 63;
+ * its density is its number of resident chunks.  The kmax pages of highest
+ * density are recalled (pages of density 0 never are; equal densities go to
+ * the lower page id).  This turns fm_memindex_score_mask's bitmask into the
+ * page table that fm_native_topk_paged reads (logical page ids).
+ *
+ *   mask        [B, ceil(S/32)] uint32 (bits at s >= S are ignored)
+ *   B >= 0, 0 <= S < 2^31, sink >= 0, recent >= 0 (each clamped to S),
+ *   1 <= kmax <= 65536
+ *   pages_out   [B, kmax] int32 recalled page ids, ascending, padded with -1
+ *   density_out [B, kmax] int32 their densities (-1 padding), or NULL
+ *   n_out       [B] int32 number of pages recalled, or NULL
+ * Errors: FM_ERR_INVALID_ARG for any violated condition above.
+ */
+fm_status fm_page_recall(const uint32_t* mask, int B, int64_t S, int64_t sink, int64_t recent, int kmax,
+                         int32_t* pages_out, int32_t* density_out, int32_t* n_out, fm_stream_t stream);
+
+/*
  * Native lightning-indexer score over the resident pages + top-k
  * ([FM] sec. 3 C^CoreComp and sec. 6 Level 2; [RM] "Two-level recall" Level 2,
  * "Page-recall" 64-chunk pages, "compressed_k format"; [V4] sec. 3 CSA-1/2).

@@ -16,7 +16,8 @@ import os
 __all__ = [
     "FmError", "lib", "fm_version", "fm_last_error", "fm_device_status", "fm_memindex_score_mask",
     "fm_topk_workspace", "fm_topk_select", "fm_native_topk_paged_workspace", "fm_native_topk_paged",
-    "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "LIB_PATH",
+    "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "fm_page_recall",
+    "LIB_PATH",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,8 +70,10 @@ def lib() -> ctypes.CDLL:
             L.fm_index_prefill_workspace.restype = _SZ
             L.fm_index_prefill_topk.argtypes = [_VP, _VP, _VP, _VP, _I32, _I64, _I32, _I32, _I32, _I32, _VP, _VP,
                                                 _VP, _SZ, _VP]
+        if hasattr(L, "fm_page_recall"):
+            L.fm_page_recall.argtypes = [_VP, _I32, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _VP]
         for name in ("fm_memindex_score_mask", "fm_topk_select", "fm_native_topk_paged", "fm_index_prefill_topk",
-                     "fm_device_status"):
+                     "fm_device_status", "fm_page_recall"):
             if hasattr(L, name):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -180,3 +183,13 @@ def fm_index_prefill_topk(q, w, pos, keys, k: int, idx_out, score_out=None, rati
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().fm_index_prefill_topk(_ptr(q), _ptr(w), _ptr(pos), _ptr(keys), T, S, n_h, d, ratio, k,
                                        _ptr(idx_out), _ptr(score_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_page_recall(mask, S: int, kmax: int, pages_out, density_out=None, n_out=None, sink: int = 0, recent: int = 0,
+                   stream=None) -> None:
+    """mask [B, ceil(S/32)] int32/uint32 (fm_memindex_score_mask's output),
+    pages_out [B, kmax] int32, density_out [B, kmax] int32 or None, n_out [B]
+    int32 or None."""
+    B = mask.shape[0]
+    _check(lib().fm_page_recall(_ptr(mask), B, S, sink, recent, kmax, _ptr(pages_out), _ptr(density_out),
+                                _ptr(n_out), _stream(stream)))

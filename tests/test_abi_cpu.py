@@ -63,6 +63,23 @@ def test_memindex_rejects_bad_args_on_host(lib):
     assert f(None, None, None, 0, 0, 0, 3, 128, 64, 128, 0.5, None, None, None, None) == 0
 
 
+def test_page_recall_rejects_bad_args_on_host(lib):
+    import sparse_attention_kv_c4_gb300 as fm
+    fm.lib()  # sets argtypes
+    f = lib.fm_page_recall
+    fake = 4096  # never dereferenced: validation fails first
+    assert f(fake, 2, 1024, 0, 0, 0, fake, None, None, None) == 1  # kmax < 1
+    assert "kmax" in fm.fm_last_error()
+    assert f(fake, 2, 1024, 0, 0, 65537, fake, None, None, None) == 1  # kmax too large
+    assert f(fake, 2, 1024, -1, 0, 8, fake, None, None, None) == 1  # negative sink
+    assert f(fake, 2, 1024, 0, -3, 8, fake, None, None, None) == 1  # negative recent
+    assert f(fake, 2, 1 << 31, 0, 0, 8, fake, None, None, None) == 1  # S too large
+    assert f(None, 2, 1024, 0, 0, 8, fake, None, None, None) == 1  # NULL mask
+    assert f(fake, 2, 1024, 0, 0, 8, None, None, None, None) == 1  # NULL pages_out
+    assert f(fake + 2, 2, 1024, 0, 0, 8, fake, None, None, None) == 1  # misaligned mask
+    assert f(None, 0, 1024, 0, 0, 8, None, None, None, None) == 0  # empty work is OK without a device
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import sparse_attention_kv_c4_gb300 as fm
     monkeypatch.setattr(fm, "_lib", None)
