@@ -16,9 +16,11 @@
 // after first touch) through a TMA ring; tcgen05.mma M=128 x N=256 x K=16
 // accumulates D [128 chunks x 256] in TMEM, double-buffered (512 columns);
 // two issuing threads alternate tiles so barrier latency overlaps MMAs.
-// Sixteen epilogue warps (four per TMEM lane quadrant, one token each) turn
-// each row of D into Y with fp32 max/FMA and store it to the workspace; tiles
-// wholly past a block's causal limit are skipped.  The block top-k then reads
+// Sixteen epilogue warps (four per TMEM lane quadrant, one token each) load
+// their row of D with both 32-column TMEM loads in flight, release the
+// accumulator, and turn it into Y with fp32 max/FMA against the token's head
+// weights (kept in shared memory per query block); tiles wholly past a
+// block's causal limit are skipped.  The block top-k then reads
 // each row up to its causal limit.
 #include <math.h>
 
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_qfull, bar_qempty, bar_drain;
   __shared__ uint32_t tmem_slot;
+  __shared__ __align__(16) float w_smem[kEpiWarps][kHeads];  // each epilogue warp's token weights
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -241,43 +244,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qb != cur_qb) {
         cur_qb = qb;
         lim = block_limit(p, qb);
+        // the warp's token weights stay in shared memory for the whole block
+        const int64_t tw = qb * kTok + j;
+        const float* wsrc = p.w + (tw < p.T ? tw : 0) * kHeads;
+        __syncwarp();
+        w_smem[warp - kFirstEpiWarp][lane] = __ldg(wsrc + lane);
+        w_smem[warp - kFirstEpiWarp][lane + 32] = __ldg(wsrc + lane + 32);
+        __syncwarp();
       }
       if ((int64_t)ct * kM >= lim) continue;
       const int64_t t = qb * kTok + j;
       const int64_t s = (int64_t)ct * kM + row;
-      const float4* wl = reinterpret_cast<const float4*>(p.w + (t < p.T ? t : 0) * kHeads);
       if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHeads;
-      float y = 0.f;
+      // both halves of the row in flight at once, one wait, then the
+      // accumulator is released before the arithmetic
+      uint32_t r0[32], r1[32];
+      tmem_ld32(taddr, r0);
+      tmem_ld32(taddr + 32, r1);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_tempty[acc]);
+      const float4* w4 = reinterpret_cast<const float4*>(w_smem[warp - kFirstEpiWarp]);
+      float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, x4 = 0.f, x5 = 0.f, x6 = 0.f, x7 = 0.f;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(taddr + half * 32, r);
-        float wr[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = __ldg(wl + half * 8 + i);
-          wr[4 * i] = v.x;
-          wr[4 * i + 1] = v.y;
-          wr[4 * i + 2] = v.z;
-          wr[4 * i + 3] = v.w;
-        }
-        tmem_ld_wait();
-        if (half == 1) {
-          tc_fence_before();
-          mbar_arrive(&bar_tempty[acc]);
-        }
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          x0 = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.f), x0);
-          x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
-          x2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
-          x3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
-        }
-        y += (x0 + x1) + (x2 + x3);
+      for (int h4 = 0; h4 < 8; ++h4) {
+        const float4 a = w4[h4];
+        const float4 c = w4[8 + h4];
+        x0 = fmaf(a.x, fmaxf(__uint_as_float(r0[4 * h4]), 0.f), x0);
+        x1 = fmaf(a.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), x1);
+        x2 = fmaf(a.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), x2);
+        x3 = fmaf(a.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), x3);
+        x4 = fmaf(c.x, fmaxf(__uint_as_float(r1[4 * h4]), 0.f), x4);
+        x5 = fmaf(c.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), x5);
+        x6 = fmaf(c.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), x6);
+        x7 = fmaf(c.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), x7);
       }
+      const float y = ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
       if (t < p.T && s < p.S) p.logits[t * p.S + s] = y;
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
@@ -333,7 +337,7 @@ fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status
     const int tiles_per_qb = (int)((a.S + kM - 1) / kM);
     const int64_t n_qb = (a.T + kTok - 1) / kTok;
     const int64_t total = n_qb * tiles_per_qb;
-    const int smem_cap = 227 * 1024;
+    const int smem_cap = 227 * 1024 - (int)sizeof(float) * kEpiWarps * kHeads;  // minus the static w_smem
     const int fixed = 1024 + kQBytes;
     int stages = (smem_cap - fixed) / kTileBytes;
     if (stages > kMaxStages) stages = kMaxStages;
