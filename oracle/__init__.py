@@ -72,6 +72,8 @@ class Oracle:
         lib.orc_topk.restype = ctypes.c_int
         lib.orc_paged_topk.argtypes = [u16p, f32p, u8p, f32p, i32p, i32p, i32p, I64, I64, I32, I32, I32,
                                        I32, i32p, f64p, f64p]
+        lib.orc_paged_topk_ex.argtypes = [u16p, f32p, u8p, f32p, i32p, i32p, i32p, I64, I64, I32, I32, I32, I32,
+                                          u32p, I64, I32, I32, i32p, f64p, f64p]
         lib.orc_causal_limit.argtypes = [I64, I64, I32]
         lib.orc_causal_limit.restype = I64
         lib.orc_prefill_topk.argtypes = [u16p, f32p, i64p, u16p, I64, I64, I32, I32, I32, I32, i32p, f64p]
@@ -133,7 +135,9 @@ class Oracle:
         return idx, sc, m
 
     def paged_topk(self, q, w, k8, scale, page_phys, page_logical, n_res=None, k: int = 512,
-                   want_logits: bool = False):
+                   want_logits: bool = False, res_mask=None, mask_group: int = 1, id_mode: int = 0):
+        """res_mask [rows, mask_ld] uint32 (row qi // mask_group per query) or
+        None; id_mode 0 = logical chunk ids, 1 = reserve cells phys*64 + o."""
         q = _c(q, np.uint16); w = _c(w, np.float32); k8 = _c(k8, np.uint8); scale = _c(scale, np.float32)
         page_phys = _c(page_phys, np.int32); page_logical = _c(page_logical, np.int32)
         Q, n_h, d = q.shape
@@ -143,9 +147,11 @@ class Oracle:
         idx = np.empty((Q, k), dtype=np.int32)
         sc = np.empty((Q, k), dtype=np.float64)
         lg = np.empty((Q, R * page), dtype=np.float64) if want_logits else None
-        self.lib.orc_paged_topk(_p(q, u16p), _p(w, f32p), _p(k8, u8p), _p(scale, f32p), _p(page_phys, i32p),
-                                _p(page_logical, i32p), _p(nr, i32p), Q, R, n_h, d, page, k, _p(idx, i32p),
-                                _p(sc, f64p), _p(lg, f64p))
+        m = _c(np.atleast_2d(res_mask), np.uint32) if res_mask is not None else None
+        mask_ld = m.shape[1] if m is not None else 0
+        self.lib.orc_paged_topk_ex(_p(q, u16p), _p(w, f32p), _p(k8, u8p), _p(scale, f32p), _p(page_phys, i32p),
+                                   _p(page_logical, i32p), _p(nr, i32p), Q, R, n_h, d, page, k, _p(m, u32p),
+                                   mask_ld, mask_group, id_mode, _p(idx, i32p), _p(sc, f64p), _p(lg, f64p))
         return (idx, sc, lg) if want_logits else (idx, sc)
 
     def causal_limit(self, pos: int, S: int, ratio: int = 4) -> int:

@@ -211,12 +211,23 @@ ORC_API int orc_topk(const int64_t* ids, const double* x, int64_t n, int k, int3
  * [n_h]; its j-th resident page (j < n_res[qi], or R when n_res is NULL) lives
  * at pool page page_phys[qi][j] and holds logical chunks
  * page_logical[qi][j]*page_size + o.  Pool keys: k8 [P][page_size][d] E4M3,
- * scale [P][page_size] fp32.  logit_out (optional) is [Q][R*page_size] in
- * page-table order, NaN for slots past n_res. */
-ORC_API void orc_paged_topk(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
-                            const int32_t* page_phys, const int32_t* page_logical, const int32_t* n_res,
-                            int64_t Q, int64_t R, int n_h, int d, int page_size, int k, int32_t* idx_out,
-                            double* score_out, double* logit_out) {
+ * scale [P][page_size] fp32.
+ * Level 2 confines the top-k to the resident set by giving non-resident
+ * chunks -inf ([RM] Level 2; [FM] sec. 6 Mode A): with res_mask, chunk c of
+ * query qi is a candidate only if bit c & 31 of word c >> 5 of mask row
+ * qi / mask_group (mask_ld words per row; words past the row read as 0) is
+ * set; without it every chunk of the listed pages is.  Reading: a chunk that
+ * is not a candidate is never selected (fewer candidates than k -> all of
+ * them, padded with -1).  id_mode 0 emits logical chunk ids; id_mode 1 emits
+ * reserve cells page_phys*page_size + o ([RM] "Fused remap": top-512 columns
+ * map directly to reserve cells), ordered and tie-broken the same way.
+ * logit_out (optional) is [Q][R*page_size] in page-table order: the score of
+ * every listed chunk, NaN for slots past n_res. */
+ORC_API void orc_paged_topk_ex(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
+                               const int32_t* page_phys, const int32_t* page_logical, const int32_t* n_res,
+                               int64_t Q, int64_t R, int n_h, int d, int page_size, int k, const uint32_t* res_mask,
+                               int64_t mask_ld, int mask_group, int id_mode, int32_t* idx_out, double* score_out,
+                               double* logit_out) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t qi = 0; qi < Q; ++qi) {
     int64_t nr = n_res ? n_res[qi] : R;
@@ -224,6 +235,7 @@ ORC_API void orc_paged_topk(const uint16_t* q, const float* w, const uint8_t* k8
     if (nr < 0) nr = 0;
     orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(nr * page_size > 0 ? nr * page_size : 1));
     int64_t n = 0;
+    const uint32_t* mrow = res_mask ? res_mask + (qi / mask_group) * mask_ld : NULL;
     for (int64_t j = 0; j < nr; ++j) {
       int64_t p = page_phys[qi * R + j];
       int64_t lp = page_logical[qi * R + j];
@@ -231,10 +243,16 @@ ORC_API void orc_paged_topk(const uint16_t* q, const float* w, const uint8_t* k8
         int64_t row = p * page_size + o;
         double x = orc_score_fp8(q + (size_t)qi * n_h * d, w + (size_t)qi * n_h, k8 + (size_t)row * d,
                                  scale[row], n_h, d);
-        c[n].x = x;
-        c[n].id = lp * page_size + o;
-        ++n;
         if (logit_out) logit_out[(size_t)qi * R * page_size + j * page_size + o] = x;
+        int64_t chunk = lp * page_size + o;
+        if (mrow) {
+          int64_t word = chunk >> 5;
+          uint32_t bits = word < mask_ld ? mrow[word] : 0u;
+          if (!((bits >> (chunk & 31)) & 1u)) continue; /* not resident: not a candidate */
+        }
+        c[n].x = x;
+        c[n].id = id_mode ? row : chunk;
+        ++n;
       }
     }
     if (logit_out)
@@ -243,6 +261,14 @@ ORC_API void orc_paged_topk(const uint16_t* q, const float* w, const uint8_t* k8
     orc_topk_cands(c, n, k, idx_out + (size_t)qi * k, score_out ? score_out + (size_t)qi * k : NULL);
     free(c);
   }
+}
+
+ORC_API void orc_paged_topk(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
+                            const int32_t* page_phys, const int32_t* page_logical, const int32_t* n_res,
+                            int64_t Q, int64_t R, int n_h, int d, int page_size, int k, int32_t* idx_out,
+                            double* score_out, double* logit_out) {
+  orc_paged_topk_ex(q, w, k8, scale, page_phys, page_logical, n_res, Q, R, n_h, d, page_size, k, NULL, 0, 1, 0,
+                    idx_out, score_out, logit_out);
 }
 
 /* ------------------------------------------------------------------------- */

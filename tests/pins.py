@@ -310,6 +310,41 @@ def pin_paged_mode_a(orc):
             assert list(idx[qi]) == want, qi
 
 
+def pin_paged_resident_mask_and_remap(orc):
+    """Level 2 inside the resident set ([RM] Level 2; [FM] sec. 6 Mode A):
+    with a chunk-level resident mask (shared by groups of queries, ragged mask
+    rows) only resident chunks are candidates; fewer than k -> all of them,
+    padded.  The fused remap emits reserve cells phys*page + o, ranked and
+    ordered by those ids.  Brute force over per-chunk scores."""
+    rng = np.random.default_rng(29)
+    q, w, k8, scale, phys, logical, n_pages, page = _paged_case(rng, Q=4)
+    Q, R = phys.shape
+    n_chunks = n_pages * page
+    for mask_ld in ((n_chunks + 31) // 32, 1):  # a short row: words past it read as 0
+        bits = rng.random((2, mask_ld * 32)) < 0.45
+        mask = np.packbits(bits, axis=-1, bitorder="little").view("<u4").reshape(2, mask_ld)
+        for k in (3, 40):
+            for id_mode in (0, 1):
+                idx, sc = orc.paged_topk(q, w, k8, scale, phys, logical, k=k, res_mask=mask, mask_group=2,
+                                         id_mode=id_mode)
+                for qi in range(Q):
+                    ids, xs = [], []
+                    for j in range(R):
+                        for o in range(page):
+                            c = int(logical[qi, j]) * page + o
+                            if c < mask_ld * 32 and bits[qi // 2, c]:
+                                ids.append(int(phys[qi, j]) * page + o if id_mode else c)
+                                xs.append(orc.score_fp8(q[qi], w[qi], k8[phys[qi, j], o], scale[phys[qi, j], o]))
+                    assert list(idx[qi]) == expected_topk(ids, xs, k), (mask_ld, k, id_mode, qi)
+    ones = np.full((Q, (n_chunks + 31) // 32), 0xFFFFFFFF, np.uint32)
+    a, _ = orc.paged_topk(q, w, k8, scale, phys, logical, k=10, res_mask=ones)
+    b, _ = orc.paged_topk(q, w, k8, scale, phys, logical, k=10)
+    assert (a == b).all(), "an all-resident mask must equal no mask"
+    zero = np.zeros((Q, 2), np.uint32)
+    a, sc = orc.paged_topk(q, w, k8, scale, phys, logical, k=10, res_mask=zero)
+    assert (a == -1).all() and np.isneginf(sc).all(), "an empty resident set selects nothing"
+
+
 def pin_paged_row_order_and_nres(orc):
     """Page-table row order does not matter; n_res limits the pages used."""
     rng = np.random.default_rng(29)

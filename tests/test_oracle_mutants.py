@@ -43,7 +43,14 @@ MUTANTS = {
     "fp8_scale_ignored": ("float kv = (float)orc_e4m3(code) * scale;", "float kv = (float)orc_e4m3(code);"),
     "fp8_dequant_in_fp64": ("float kv = (float)orc_e4m3(code) * scale;",
                             "double kv = orc_e4m3(code) * (double)scale;"),
-    "paged_id_from_physical": ("c[n].id = lp * page_size + o;", "c[n].id = p * page_size + o;"),
+    "paged_id_from_physical": ("int64_t chunk = lp * page_size + o;", "int64_t chunk = p * page_size + o;"),
+    "paged_mask_ignored": ("        if (mrow) {\n          int64_t word", "        if (0) {\n          int64_t word"),
+    "paged_mask_group_ignored": ("res_mask + (qi / mask_group) * mask_ld", "res_mask + qi * mask_ld"),
+    "paged_masked_kept_at_neg_inf": ("if (!((bits >> (chunk & 31)) & 1u)) continue;",
+                                     "if (!((bits >> (chunk & 31)) & 1u)) x = -INFINITY;"),
+    "paged_remap_ignored": ("c[n].id = id_mode ? row : chunk;", "c[n].id = chunk;"),
+    "paged_mask_past_row": ("uint32_t bits = word < mask_ld ? mrow[word] : 0u;",
+                            "uint32_t bits = word < mask_ld ? mrow[word] : ~0u;"),
     "paged_nres_ignored": ("int64_t nr = n_res ? n_res[qi] : R;", "int64_t nr = R;"),
     "causal_inclusive": ("int64_t lim = pos / ratio;", "int64_t lim = pos / ratio + 1;"),
     "causal_token_not_chunk": ("int64_t lim = pos / ratio;", "int64_t lim = pos;"),
