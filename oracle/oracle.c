@@ -220,7 +220,9 @@ ORC_API int orc_topk(const int64_t* ids, const double* x, int64_t n, int k, int3
  * is not a candidate is never selected (fewer candidates than k -> all of
  * them, padded with -1).  id_mode 0 emits logical chunk ids; id_mode 1 emits
  * reserve cells page_phys*page_size + o ([RM] "Fused remap": top-512 columns
- * map directly to reserve cells), ordered and tie-broken the same way.
+ * map directly to reserve cells).  Reading: the remap only translates the
+ * emitted ids -- the selection, its tie-break and its order stay those of
+ * the logical chunk ids.
  * logit_out (optional) is [Q][R*page_size] in page-table order: the score of
  * every listed chunk, NaN for slots past n_res. */
 ORC_API void orc_paged_topk_ex(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
@@ -251,14 +253,23 @@ ORC_API void orc_paged_topk_ex(const uint16_t* q, const float* w, const uint8_t*
           if (!((bits >> (chunk & 31)) & 1u)) continue; /* not resident: not a candidate */
         }
         c[n].x = x;
-        c[n].id = id_mode ? row : chunk;
+        c[n].id = chunk;
         ++n;
       }
     }
     if (logit_out)
       for (int64_t j = nr; j < R; ++j)
         for (int o = 0; o < page_size; ++o) logit_out[(size_t)qi * R * page_size + j * page_size + o] = NAN;
-    orc_topk_cands(c, n, k, idx_out + (size_t)qi * k, score_out ? score_out + (size_t)qi * k : NULL);
+    int m = orc_topk_cands(c, n, k, idx_out + (size_t)qi * k, score_out ? score_out + (size_t)qi * k : NULL);
+    if (id_mode) /* translate each selected logical chunk to its reserve cell */
+      for (int i = 0; i < m; ++i) {
+        int64_t chunk = idx_out[(size_t)qi * k + i];
+        for (int64_t j = 0; j < nr; ++j)
+          if (page_logical[qi * R + j] == chunk / page_size) {
+            idx_out[(size_t)qi * k + i] = (int32_t)(page_phys[qi * R + j] * page_size + chunk % page_size);
+            break;
+          }
+      }
     free(c);
   }
 }

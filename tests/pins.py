@@ -328,14 +328,18 @@ def pin_paged_resident_mask_and_remap(orc):
                 idx, sc = orc.paged_topk(q, w, k8, scale, phys, logical, k=k, res_mask=mask, mask_group=2,
                                          id_mode=id_mode)
                 for qi in range(Q):
-                    ids, xs = [], []
+                    ids, xs, cell = [], [], {}
                     for j in range(R):
                         for o in range(page):
                             c = int(logical[qi, j]) * page + o
+                            cell[c] = int(phys[qi, j]) * page + o
                             if c < mask_ld * 32 and bits[qi // 2, c]:
-                                ids.append(int(phys[qi, j]) * page + o if id_mode else c)
+                                ids.append(c)
                                 xs.append(orc.score_fp8(q[qi], w[qi], k8[phys[qi, j], o], scale[phys[qi, j], o]))
-                    assert list(idx[qi]) == expected_topk(ids, xs, k), (mask_ld, k, id_mode, qi)
+                    want = expected_topk(ids, xs, k)
+                    if id_mode:
+                        want = [cell[c] if c >= 0 else -1 for c in want]
+                    assert list(idx[qi]) == want, (mask_ld, k, id_mode, qi)
     ones = np.full((Q, (n_chunks + 31) // 32), 0xFFFFFFFF, np.uint32)
     a, _ = orc.paged_topk(q, w, k8, scale, phys, logical, k=10, res_mask=ones)
     b, _ = orc.paged_topk(q, w, k8, scale, phys, logical, k=10)

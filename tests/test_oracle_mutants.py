@@ -48,7 +48,9 @@ MUTANTS = {
     "paged_mask_group_ignored": ("res_mask + (qi / mask_group) * mask_ld", "res_mask + qi * mask_ld"),
     "paged_masked_kept_at_neg_inf": ("if (!((bits >> (chunk & 31)) & 1u)) continue;",
                                      "if (!((bits >> (chunk & 31)) & 1u)) x = -INFINITY;"),
-    "paged_remap_ignored": ("c[n].id = id_mode ? row : chunk;", "c[n].id = chunk;"),
+    "paged_remap_ignored": ("    if (id_mode) /* translate", "    if (0) /* translate"),
+    "paged_remap_to_logical_offset": ("(int32_t)(page_phys[qi * R + j] * page_size + chunk % page_size)",
+                                      "(int32_t)(page_phys[qi * R + j] * page_size)"),
     "paged_mask_past_row": ("uint32_t bits = word < mask_ld ? mrow[word] : 0u;",
                             "uint32_t bits = word < mask_ld ? mrow[word] : ~0u;"),
     "paged_nres_ignored": ("int64_t nr = n_res ? n_res[qi] : R;", "int64_t nr = R;"),
