@@ -181,6 +181,39 @@ fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t*
                                float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
 
 /*
+ * fm_native_topk_paged with the Level-2 resident mask and the fused remap
+ * ([RM] "Two-level recall algorithm" Level 2: the native top-512 is confined
+ * to the resident set by masking non-resident chunk logits to -inf; [FM]
+ * sec. 6 Mode A; [RM] "Fused remap": top-512 columns map directly to reserve
+ * cells).  fm_native_topk_paged is this call with res_mask = NULL, id_mode 0.
+ *
+ *   res_mask    NULL (every chunk of the listed pages is a candidate) or
+ *               [ceil(Q / mask_group), mask_ld] uint32: chunk c = logical
+ *               page * 64 + o of query qi is a candidate iff bit c & 31 of
+ *               word c >> 5 of row qi / mask_group is set (words at or past
+ *               mask_ld count as 0).  The Memory-Indexer bitmask
+ *               (fm_memindex_score_mask's mask_out, one row per request) is
+ *               this layout, with mask_group = layers per request.  A chunk
+ *               that is not a candidate is never selected: fewer than k
+ *               candidates -> all of them, padded with -1.
+ *   mask_ld     words per mask row (>= 1 when res_mask is given)
+ *   mask_group  consecutive queries sharing one mask row (>= 1)
+ *   id_mode     0: idx_out holds logical chunk ids; 1: reserve cells
+ *               page_phys * 64 + o (the pool row of the chunk).  The
+ *               selection, its tie-break and its order are the same in both
+ *               modes (by logical chunk id).
+ * Other arguments, outputs and errors as fm_native_topk_paged (the same
+ * workspace size); FM_ERR_INVALID_ARG also for a bad id_mode / mask_ld /
+ * mask_group.
+ */
+fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
+                                  int64_t P, const int32_t* page_phys, const int32_t* page_logical,
+                                  const int32_t* n_res, int Q, int R, int n_h, int d, int k,
+                                  const uint32_t* res_mask, int64_t mask_ld, int mask_group, int id_mode,
+                                  int32_t* idx_out, float* score_out, void* workspace, size_t workspace_bytes,
+                                  fm_stream_t stream);
+
+/*
  * Native paged top-k without a caller workspace.
  *
  * The pages have no counterpart of this entry point: it exists for callers

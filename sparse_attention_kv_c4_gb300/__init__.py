@@ -17,6 +17,7 @@ __all__ = [
     "FmError", "lib", "fm_version", "fm_last_error", "fm_device_status", "fm_memindex_score_mask",
     "fm_topk_workspace", "fm_topk_select", "fm_native_topk_paged_workspace", "fm_native_topk_paged",
     "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "fm_page_recall",
+    "fm_native_topk_paged_ex",
     "LIB_PATH",
 ]
 
@@ -61,6 +62,9 @@ def lib() -> ctypes.CDLL:
             L.fm_native_topk_paged_workspace.restype = _SZ
             L.fm_native_topk_paged.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
                                                _I32, _VP, _VP, _VP, _SZ, _VP]
+        if hasattr(L, "fm_native_topk_paged_ex"):
+            L.fm_native_topk_paged_ex.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
+                                                  _I32, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _SZ, _VP]
         if hasattr(L, "fm_native_topk_paged_noalloc"):
             L.fm_native_topk_paged_noalloc.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32,
                                                        _I32, _I32, _VP, _VP, _VP]
@@ -73,7 +77,7 @@ def lib() -> ctypes.CDLL:
         if hasattr(L, "fm_page_recall"):
             L.fm_page_recall.argtypes = [_VP, _I32, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _VP]
         for name in ("fm_memindex_score_mask", "fm_topk_select", "fm_native_topk_paged", "fm_index_prefill_topk",
-                     "fm_device_status", "fm_page_recall"):
+                     "fm_device_status", "fm_page_recall", "fm_native_topk_paged_ex"):
             if hasattr(L, name):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -155,6 +159,23 @@ def fm_native_topk_paged(q, w, k_pool, k_scale, page_phys, page_logical, k: int,
     _check(lib().fm_native_topk_paged(_ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), P, _ptr(page_phys),
                                       _ptr(page_logical), _ptr(n_res), Q, R, n_h, d, k, _ptr(idx_out),
                                       _ptr(score_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_native_topk_paged_ex(q, w, k_pool, k_scale, page_phys, page_logical, k: int, idx_out, score_out=None,
+                            n_res=None, res_mask=None, mask_group: int = 1, id_mode: int = 0, workspace=None,
+                            stream=None) -> None:
+    """fm_native_topk_paged plus the Level-2 resident mask res_mask
+    [rows, mask_ld] int32/uint32 (row qi // mask_group per query, or None) and
+    id_mode (0 = logical chunk ids, 1 = reserve cells phys * 64 + o)."""
+    Q, n_h, d = q.shape
+    R = page_phys.shape[1]
+    P = k_pool.shape[0]
+    mask_ld = 0 if res_mask is None else res_mask.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_native_topk_paged_ex(_ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), P, _ptr(page_phys),
+                                         _ptr(page_logical), _ptr(n_res), Q, R, n_h, d, k, _ptr(res_mask), mask_ld,
+                                         mask_group, id_mode, _ptr(idx_out), _ptr(score_out), _ptr(workspace),
+                                         ws_bytes, _stream(stream)))
 
 
 def fm_native_topk_paged_noalloc(q, w, k_pool, k_scale, page_phys, page_logical, k: int, idx_out, score_out=None,

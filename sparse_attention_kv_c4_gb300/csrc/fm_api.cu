@@ -164,7 +164,7 @@ FM_API fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* 
   fm_status st = check_device(&sms);
   if (st != FM_OK) return st;
   (void)workspace_bytes;  // the select needs no scratch (fm_topk_workspace is 0)
-  return launch_topk_rows(scores, ld, n_valid, rows, (int)n, k, nullptr, 0, idx_out, score_out,
+  return launch_topk_rows(scores, ld, n_valid, rows, (int)n, k, nullptr, 0, nullptr, nullptr, idx_out, score_out,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -173,15 +173,23 @@ FM_API size_t fm_native_topk_paged_workspace(int Q, int R) {
   return paged_workspace_bytes(Q, R);
 }
 
-FM_API fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
-                                      int64_t P, const int32_t* page_phys, const int32_t* page_logical,
-                                      const int32_t* n_res, int Q, int R, int n_h, int d, int k, int32_t* idx_out,
-                                      float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream) {
+FM_API fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const uint8_t* k_pool,
+                                         const float* k_scale, int64_t P, const int32_t* page_phys,
+                                         const int32_t* page_logical, const int32_t* n_res, int Q, int R, int n_h,
+                                         int d, int k, const uint32_t* res_mask, int64_t mask_ld, int mask_group,
+                                         int id_mode, int32_t* idx_out, float* score_out, void* workspace,
+                                         size_t workspace_bytes, fm_stream_t stream) {
   if (n_h != 64 || d != 128)
     return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: n_h=%d d=%d (need 64, 128)", n_h, d);
   if (Q < 0 || R < 1 || R > 2048 || k < 1 || k > 1024 || P < 0 || P > (int64_t(1) << 26))
     return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: bad sizes Q=%d R=%d k=%d P=%lld", Q, R, k,
                      (long long)P);
+  if (id_mode != 0 && id_mode != 1)
+    return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: id_mode=%d (0 = chunk ids, 1 = reserve cells)",
+                     id_mode);
+  if (res_mask != nullptr && (mask_ld < 1 || mask_group < 1 || !aligned(res_mask, 4)))
+    return set_error(FM_ERR_INVALID_ARG,
+                     "fm_native_topk_paged: resident mask needs mask_ld >= 1, mask_group >= 1, 4-byte alignment");
   if (Q == 0) return FM_OK;
   if (!q || !w || !page_phys || !page_logical || !idx_out || (P > 0 && (!k_pool || !k_scale)))
     return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: required pointer is NULL");
@@ -203,18 +211,29 @@ FM_API fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const u
   a.w = w;
   a.k_pool = k_pool;
   a.k_scale = k_scale;
-  a.P = P > 0 ? P : 1;
+  a.P = P;
   a.page_phys = page_phys;
   a.page_logical = page_logical;
   a.n_res = n_res;
   a.Q = Q;
   a.R = R;
   a.k = k;
+  a.res_mask = res_mask;
+  a.mask_ld = mask_ld;
+  a.mask_group = mask_group;
+  a.id_mode = id_mode;
   a.idx_out = idx_out;
   a.score_out = score_out;
   a.workspace = workspace;
-  if (P == 0) a.P = 0;
   return launch_paged(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+FM_API fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
+                                      int64_t P, const int32_t* page_phys, const int32_t* page_logical,
+                                      const int32_t* n_res, int Q, int R, int n_h, int d, int k, int32_t* idx_out,
+                                      float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream) {
+  return fm_native_topk_paged_ex(q, w, k_pool, k_scale, P, page_phys, page_logical, n_res, Q, R, n_h, d, k, nullptr,
+                                 0, 1, 0, idx_out, score_out, workspace, workspace_bytes, stream);
 }
 
 FM_API size_t fm_index_prefill_workspace(int T, int64_t S) {

@@ -42,11 +42,15 @@ struct MemindexArgs {
 };
 fm_status launch_memindex(const MemindexArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
 
-// Exact top-k of each row, one CTA per row; candidate i of row r has id
-// page_ids[r*page_ld + i/64]*64 + i%64 when page_ids is non-null, else i.
+// Exact top-k of each row, one CTA per row.  Candidate i of row r has id i;
+// with page_ids, page_ids[r*page_ld + i/64]*64 + i%64; with page_ids,
+// page_prefix [rows, page_ld+1] and page_mask [rows, page_ld] (a row compacted
+// to its resident chunks), page_ids[r*page_ld + j]*64 + o for the page j whose
+// prefix range holds i and the (i - prefix[j])-th set bit o of its mask.
 size_t topk_workspace_bytes(int rows, int n);
 fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int n, int k,
-                           const int32_t* page_ids, int64_t page_ld, int32_t* idx_out, float* score_out,
+                           const int32_t* page_ids, int64_t page_ld, const int32_t* page_prefix,
+                           const unsigned long long* page_mask, int32_t* idx_out, float* score_out,
                            cudaStream_t stream);
 
 struct PagedArgs {
@@ -59,6 +63,10 @@ struct PagedArgs {
   const int32_t* page_logical;
   const int32_t* n_res;
   int Q, R, k;
+  const uint32_t* res_mask;  // [ceil(Q/mask_group), mask_ld] resident chunks, or null (every listed chunk)
+  int64_t mask_ld;
+  int mask_group;
+  int id_mode;               // 0: logical chunk ids, 1: reserve cells phys*64 + o
   int32_t* idx_out;
   float* score_out;
   void* workspace;

@@ -103,6 +103,10 @@ FM_API fm_status fm_native_topk_paged_noalloc(const uint16_t* q, const float* w,
   a.Q = Q;
   a.R = R;
   a.k = k;
+  a.res_mask = nullptr;
+  a.mask_ld = 0;
+  a.mask_group = 1;
+  a.id_mode = 0;
   a.idx_out = idx_out;
   a.score_out = score_out;
   a.workspace = scratch;

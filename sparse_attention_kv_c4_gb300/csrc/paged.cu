@@ -72,9 +72,11 @@ __global__ void __launch_bounds__(kPrepThreads)
     paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                       const int32_t* __restrict__ page_phys, const int32_t* __restrict__ page_logical,
                       const int32_t* __restrict__ n_res, int R, int64_t P, int Rpow2,
+                      const uint32_t* __restrict__ res_mask, int64_t mask_ld, int mask_group,
                       int32_t* __restrict__ s_logical, int32_t* __restrict__ s_phys,
-                      int32_t* __restrict__ nres_eff, int32_t* __restrict__ n_valid, uint8_t* __restrict__ qsplit,
-                      float* __restrict__ wq, unsigned int* __restrict__ status) {
+                      int32_t* __restrict__ nres_eff, int32_t* __restrict__ n_valid,
+                      unsigned long long* __restrict__ pmask, int32_t* __restrict__ pprefix,
+                      uint8_t* __restrict__ qsplit, float* __restrict__ wq, unsigned int* __restrict__ status) {
   __shared__ unsigned long long keys[kMaxR];
   __shared__ uint32_t warp_tot[kPrepThreads / 32];
   const int qi = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -135,9 +137,52 @@ __global__ void __launch_bounds__(kPrepThreads)
     base += total;
     __syncthreads();
   }
-  if (tid == 0) {
-    nres_eff[qi] = (int32_t)base;
-    n_valid[qi] = (int32_t)base * kPage;
+  if (res_mask == nullptr) {
+    if (tid == 0) {
+      nres_eff[qi] = (int32_t)base;
+      n_valid[qi] = (int32_t)base * kPage;
+    }
+  } else {
+    // Level-2 resident set: page j's 64-bit mask of resident chunks (words
+    // past the mask row read as 0) and the prefix count of resident chunks
+    // before it; the scorer writes only resident chunks, compacted.  Pages
+    // past the listed ones get an empty mask and the final count.
+    const uint32_t* mrow = res_mask + (int64_t)(qi / mask_group) * mask_ld;
+    uint32_t run = 0;
+    for (int j0 = 0; j0 < R; j0 += kPrepThreads) {
+      const int j = j0 + tid;
+      unsigned long long m = 0ull;
+      if (j < (int)base) {
+        const int64_t wd = 2 * (int64_t)s_logical[(int64_t)qi * R + j];
+        const uint32_t lo = wd < mask_ld ? __ldg(mrow + wd) : 0u;
+        const uint32_t hi = wd + 1 < mask_ld ? __ldg(mrow + wd + 1) : 0u;
+        m = ((unsigned long long)hi << 32) | lo;
+      }
+      const uint32_t c = (uint32_t)__popcll(m);
+      uint32_t x = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) warp_tot[warp] = x;
+      __syncthreads();
+      uint32_t before = 0, total = 0;
+      for (int wi = 0; wi < kPrepThreads / 32; ++wi) {
+        if (wi < warp) before += warp_tot[wi];
+        total += warp_tot[wi];
+      }
+      if (j < R) {
+        pmask[(int64_t)qi * R + j] = m;
+        pprefix[(int64_t)qi * (R + 1) + j] = (int32_t)(run + before + x - c);
+      }
+      run += total;
+      __syncthreads();
+    }
+    if (tid == 0) {
+      pprefix[(int64_t)qi * (R + 1) + R] = (int32_t)run;
+      nres_eff[qi] = (int32_t)base;
+      n_valid[qi] = (int32_t)run;
+    }
   }
   // q split: warp handles heads warp, warp+8, ...; lane handles d = 4*lane..4*lane+3
   for (int h = warp; h < kHeads; h += kPrepThreads / 32) {
@@ -174,6 +219,8 @@ __global__ void __launch_bounds__(kPrepThreads)
 struct ScoreParams {
   const int32_t* s_phys;
   const int32_t* nres_eff;
+  const unsigned long long* pmask;  // resident-chunk masks per listed page, or null (every chunk)
+  const int32_t* pprefix;           // resident chunks before each page (compacted write positions)
   const float* k_scale;
   const float* wq;
   float* scores;  // [Q, R*64]
@@ -198,6 +245,10 @@ FM_DEV void umma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32
       : "memory");
 }
 
+// kMasked: write only the resident chunks of each page, compacted (the
+// Level-2 resident mask); a separate instantiation so that the unmasked
+// kernel's code is unchanged by it.
+template <bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_score_kernel(const __grid_constant__ CUtensorMap tmap_pool, const __grid_constant__ CUtensorMap tmap_q,
                        const ScoreParams p) {
@@ -453,7 +504,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             y += x0 + x1;
           }
         }
-        if (valid) p.scores[qi * ld + (int64_t)tile * kM + row] = y;
+        if constexpr (kMasked) {
+          if (valid) {
+            const unsigned long long m = __ldg(p.pmask + qi * p.R + j);
+            const int o = row & (kPage - 1);
+            if ((m >> o) & 1ull)
+              p.scores[qi * ld + __ldg(p.pprefix + qi * (p.R + 1) + j) + __popcll(m & ((1ull << o) - 1ull))] = y;
+          }
+        } else {
+          if (valid) p.scores[qi * ld + (int64_t)tile * kM + row] = y;
+        }
       }
       if (++acc == (uint32_t)kAccBufs) {
         acc = 0;
@@ -477,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct PagedWs {
-  int32_t *s_logical, *s_phys, *nres_eff, *n_valid;
+  int32_t *s_logical, *s_phys, *nres_eff, *n_valid, *pprefix;
+  unsigned long long* pmask;
   uint8_t* qsplit;
   float *wq, *scores;
   size_t bytes;
@@ -496,6 +557,8 @@ PagedWs paged_ws_layout(void* base, int Q, int R) {
   w.s_phys = reinterpret_cast<int32_t*>(take((size_t)Q * R * 4));
   w.nres_eff = reinterpret_cast<int32_t*>(take((size_t)Q * 4));
   w.n_valid = reinterpret_cast<int32_t*>(take((size_t)Q * 4));
+  w.pmask = reinterpret_cast<unsigned long long*>(take((size_t)Q * R * 8));
+  w.pprefix = reinterpret_cast<int32_t*>(take((size_t)Q * (R + 1) * 4));
   w.qsplit = take((size_t)Q * kQBytes);
   w.wq = reinterpret_cast<float*>(take((size_t)Q * kHeads * 4));
   w.scores = reinterpret_cast<float*>(take((size_t)Q * R * kPage * 4));
@@ -513,7 +576,8 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   int Rpow2 = 1;
   while (Rpow2 < a.R) Rpow2 <<= 1;
   paged_prep_kernel<<<a.Q, kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
-                                                      Rpow2, ws.s_logical, ws.s_phys, ws.nres_eff, ws.n_valid,
+                                                      Rpow2, a.res_mask, a.mask_ld, a.mask_group, ws.s_logical,
+                                                      ws.s_phys, ws.nres_eff, ws.n_valid, ws.pmask, ws.pprefix,
                                                       ws.qsplit, ws.wq, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged prep: launch: %s", cudaGetErrorString(e));
@@ -547,6 +611,8 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   ScoreParams p;
   p.s_phys = ws.s_phys;
   p.nres_eff = ws.nres_eff;
+  p.pmask = a.res_mask != nullptr ? ws.pmask : nullptr;
+  p.pprefix = ws.pprefix;
   p.k_scale = a.k_scale;
   p.wq = ws.wq;
   p.scores = ws.scores;
@@ -555,14 +621,18 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   p.tiles_per_q = tiles_per_q;
   p.R = a.R;
   p.stages = stages;
-  e = cudaFuncSetAttribute(paged_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* score_kernel = a.res_mask != nullptr ? paged_score_kernel<true> : paged_score_kernel<false>;
+  e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const int grid = (int)(total < num_sms ? total : num_sms);
-  paged_score_kernel<<<grid, kThreads, smem, stream>>>(tmap_pool, tmap_q, p);
+  score_kernel<<<grid, kThreads, smem, stream>>>(tmap_pool, tmap_q, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged score: launch: %s", cudaGetErrorString(e));
 
-  return launch_topk_rows(ws.scores, (int64_t)a.R * kPage, ws.n_valid, a.Q, a.R * kPage, a.k, ws.s_logical, a.R,
+  // ids: logical chunk ids, or reserve cells (the fused remap)
+  const int32_t* ids = a.id_mode == 1 ? ws.s_phys : ws.s_logical;
+  return launch_topk_rows(ws.scores, (int64_t)a.R * kPage, ws.n_valid, a.Q, a.R * kPage, a.k, ids, a.R,
+                          a.res_mask != nullptr ? ws.pprefix : nullptr, a.res_mask != nullptr ? ws.pmask : nullptr,
                           a.idx_out, a.score_out, stream);
 }
 

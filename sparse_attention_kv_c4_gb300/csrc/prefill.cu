@@ -360,7 +360,8 @@ fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill score: launch: %s", cudaGetErrorString(e));
   }
-  return launch_topk_rows(logits, a.S, n_valid, a.T, (int)a.S, a.k, nullptr, 0, a.idx_out, a.score_out, stream);
+  return launch_topk_rows(logits, a.S, n_valid, a.T, (int)a.S, a.k, nullptr, 0, nullptr, nullptr, a.idx_out,
+                          a.score_out, stream);
 }
 
 }  // namespace fm

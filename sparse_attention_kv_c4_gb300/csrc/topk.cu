@@ -20,15 +20,46 @@ struct PageMap {
   FM_DEV int32_t operator()(int i) const { return __ldg(ids + (i >> 6)) * 64 + (i & 63); }
 };
 
+// A paged row compacted to its resident chunks: page j holds candidates
+// prefix[j] .. prefix[j+1]-1, which are the set bits of mask[j] in increasing
+// order.  Candidate i is found by a binary search for the last page whose
+// prefix is <= i (an empty page shares its prefix with the next page, so the
+// last such page holds i) and the (i - prefix[j])-th set bit of its mask.
+struct MaskedPageMap {
+  const int32_t* ids;
+  const int32_t* prefix;
+  const unsigned long long* mask;
+  int n_pages;
+  FM_DEV int32_t operator()(int i) const {
+    int lo = 0, hi = n_pages - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(prefix + mid) <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    const unsigned long long m = __ldg(mask + lo);
+    int r = i - __ldg(prefix + lo);
+    const uint32_t m_lo = (uint32_t)m, m_hi = (uint32_t)(m >> 32);
+    const int c_lo = __popc(m_lo);
+    const int o = r < c_lo ? (int)__fns(m_lo, 0, r + 1) : 32 + (int)__fns(m_hi, 0, r - c_lo + 1);
+    return __ldg(ids + lo) * 64 + o;
+  }
+};
+
 FM_DEV int row_len(const int32_t* __restrict__ n_valid, int64_t r, int n) {
   if (n_valid == nullptr) return n;
   const int v = __ldg(n_valid + r);
   return v < 0 ? 0 : (v > n ? n : v);
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
+// kMap: 0 = candidate index, 1 = paged rows (PageMap), 2 = paged rows
+// compacted to resident chunks (MaskedPageMap); one instantiation each so the
+// id maps do not share a register allocation.
+template <int kMap>
+__global__ void __launch_bounds__(kTopkThreads, 4)  // four CTAs per SM (shared memory allows four)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid, int n, int k,
-                     const int32_t* __restrict__ page_ids, int64_t page_ld, int32_t* __restrict__ idx_out,
+                     const int32_t* __restrict__ page_ids, int64_t page_ld, const int32_t* __restrict__ page_prefix,
+                     const unsigned long long* __restrict__ page_mask, int32_t* __restrict__ idx_out,
                      float* __restrict__ score_out) {
   extern __shared__ uint8_t topk_smem_raw[];
   TopkFastSmem<kTopkThreads>& sm = *reinterpret_cast<TopkFastSmem<kTopkThreads>*>(topk_smem_raw);
@@ -37,10 +68,16 @@ __global__ void __launch_bounds__(kTopkThreads)
   const float* row = scores + r * ld;
   int32_t* io = idx_out + r * k;
   float* so = score_out != nullptr ? score_out + r * k : nullptr;
-  if (page_ids != nullptr)
+  if constexpr (kMap == 2) {
+    // all page_ld pages are searched: pages past the listed ones are empty
+    const MaskedPageMap map{page_ids + r * page_ld, page_prefix + r * (page_ld + 1), page_mask + r * page_ld,
+                            (int)page_ld};
+    block_topk<kTopkThreads>(row, nr, k, map, io, so, sm);
+  } else if constexpr (kMap == 1) {
     block_topk<kTopkThreads>(row, nr, k, PageMap{page_ids + r * page_ld}, io, so, sm);
-  else
+  } else {
     block_topk<kTopkThreads>(row, nr, k, IdentityMap{}, io, so, sm);
+  }
 }
 
 
@@ -53,14 +90,17 @@ size_t topk_workspace_bytes(int rows, int n) {
 }
 
 fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_valid, int rows, int n, int k,
-                           const int32_t* page_ids, int64_t page_ld, int32_t* idx_out, float* score_out,
+                           const int32_t* page_ids, int64_t page_ld, const int32_t* page_prefix,
+                           const unsigned long long* page_mask, int32_t* idx_out, float* score_out,
                            cudaStream_t stream) {
   if (rows == 0) return FM_OK;
   const int smem = (int)sizeof(TopkFastSmem<kTopkThreads>);
-  cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* kernel = page_mask != nullptr ? topk_rows_kernel<2> : (page_ids != nullptr ? topk_rows_kernel<1>
+                                                                                      : topk_rows_kernel<0>);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  topk_rows_kernel<<<rows, kTopkThreads, smem, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, idx_out,
-                                                       score_out);
+  kernel<<<rows, kTopkThreads, smem, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, page_prefix, page_mask,
+                                               idx_out, score_out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: launch: %s", cudaGetErrorString(e));
   return FM_OK;
