@@ -67,6 +67,8 @@ class Oracle:
         lib.orc_score_fp8.argtypes = [u16p, f32p, u8p, F, I32, I32]
         lib.orc_score_fp8.restype = D
         lib.orc_memindex_logits.argtypes = [u16p, f32p, u16p, I64, I64, I64, I64, I64, I32, I32, f64p]
+        lib.orc_memindex_logits_fp8.argtypes = [u16p, f32p, u8p, f32p, I64, I64, I64, I64, I64, I64, I64, I32, I32,
+                                                f64p]
         lib.orc_memindex_select.argtypes = [f64p, I64, I64, I64, D, u32p, f64p]
         lib.orc_topk.argtypes = [i64p, f64p, I64, I32, i32p, f64p]
         lib.orc_topk.restype = ctypes.c_int
@@ -115,6 +117,17 @@ class Oracle:
         x = np.empty((B, L, S), dtype=np.float64)
         self.lib.orc_memindex_logits(_p(q, u16p), _p(w, f32p), _p(K, u16p), L * S * d, S * d, B, L, S,
                                      n_h, d, _p(x, f64p))
+        return x
+
+    def memindex_logits_fp8(self, q, w, k8, scale) -> np.ndarray:
+        """q [B,L,n_h,d] bf16 bits, w [B,L,n_h], k8 [B,L,S,d] E4M3 codes,
+        scale [B,L,S] fp32 -> x [B,L,S] fp64."""
+        q = _c(q, np.uint16); w = _c(w, np.float32); k8 = _c(k8, np.uint8); scale = _c(scale, np.float32)
+        B, L, n_h, d = q.shape
+        S = k8.shape[2]
+        x = np.empty((B, L, S), dtype=np.float64)
+        self.lib.orc_memindex_logits_fp8(_p(q, u16p), _p(w, f32p), _p(k8, u8p), _p(scale, f32p), L * S * d, S * d,
+                                         L * S, S, B, L, S, n_h, d, _p(x, f64p))
         return x
 
     def memindex_select(self, x, thr: float = 0.5):

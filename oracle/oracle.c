@@ -127,6 +127,26 @@ ORC_API void orc_memindex_logits(const uint16_t* q, const float* w, const uint16
     }
 }
 
+/* The same logits over compressed keys ([FM] sec. 6 and [RM] "compressed_k
+ * format": the retriever reads each chunk as 128 E4M3 bytes plus an fp32
+ * scale, dequantised as fp8.float() * scale): keys k8 at
+ * k8 + b*stride_b + l*stride_l + s*d (byte strides), scales at
+ * scale + b*sstride_b + l*sstride_l + s (element strides). */
+ORC_API void orc_memindex_logits_fp8(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
+                                     int64_t stride_b, int64_t stride_l, int64_t sstride_b, int64_t sstride_l,
+                                     int64_t B, int64_t L, int64_t S, int n_h, int d, double* x_out) {
+#pragma omp parallel for collapse(2) schedule(dynamic, 64)
+  for (int64_t bl = 0; bl < B * L; ++bl)
+    for (int64_t s = 0; s < S; ++s) {
+      int64_t b = bl / L, l = bl % L;
+      const uint16_t* qb = q + (size_t)bl * n_h * d;
+      const float* wb = w + (size_t)bl * n_h;
+      const uint8_t* ks = k8 + b * stride_b + l * stride_l + s * d;
+      const float sc = scale[b * sstride_b + l * sstride_l + s];
+      x_out[(size_t)bl * S + s] = orc_score_fp8(qb, wb, ks, sc, n_h, d);
+    }
+}
+
 /* [FM] sec. 3: R[s] = 1(max_l sigma(x_l[s]) >= thr), the OR-union of the
  * per-layer sets {s | I^(l) >= thr}.  mask bit (s & 31) of word s >> 5;
  * bits at s >= S stay zero.  maxsig[b][s] = max_l sigma(x_l[s]). */

@@ -414,6 +414,36 @@ def pin_planted_tiny(orc):
     assert m == 512 and set(np.nonzero(pl)[0]) <= set(idx.tolist())
 
 
+def pin_memindex_fp8_equals_bf16_on_exact_keys(orc):
+    """Keys that E4M3 and bf16 both represent exactly, at scale 1, give the
+    same logits through the compressed-key path as through the bf16 path (an
+    identity between two decoders); doubling the scale equals doubling the
+    keys (x is positively homogeneous in k); layout: every (b, l, s) lands in
+    its own slot."""
+    rng = np.random.default_rng(31)
+    B, L, S, n_h, d = 2, 3, 7, 5, 16
+    q = f32_to_bf16_bits(rng.standard_normal((B, L, n_h, d)).astype(np.float32))
+    w = rng.standard_normal((B, L, n_h)).astype(np.float32)
+    codes = rng.integers(0, 256, (B, L, S, d)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x40  # no NaN codes
+    vals = orc.e4m3(codes.reshape(-1)).reshape(codes.shape)  # exact in bf16 too (3 mantissa bits)
+    kb = f32_to_bf16_bits(vals.astype(np.float32))
+    ones = np.ones((B, L, S), np.float32)
+    x8 = orc.memindex_logits_fp8(q, w, codes, ones)
+    xb = orc.memindex_logits(q, w, kb)
+    assert np.array_equal(x8, xb), np.abs(x8 - xb).max()
+    x2 = orc.memindex_logits_fp8(q, w, codes, 2 * ones)
+    assert np.array_equal(x2, 2 * x8)
+    # a distinct scale per (b, l, s) multiplies exactly that slot's keys
+    sc = (2.0 ** rng.integers(-3, 4, (B, L, S))).astype(np.float32)
+    xs = orc.memindex_logits_fp8(q, w, codes, sc)
+    for b in range(B):
+        for l in range(L):
+            for s in range(S):
+                kk = f32_to_bf16_bits((vals[b, l, s] * sc[b, l, s]).astype(np.float32))
+                assert xs[b, l, s] == orc.score_bf16(q[b, l], w[b, l], kk), (b, l, s)
+
+
 # ---------------------------------------------------------------------------
 # page recall (densest resident pages)
 # ---------------------------------------------------------------------------

@@ -57,6 +57,10 @@ MUTANTS = {
     "causal_inclusive": ("int64_t lim = pos / ratio;", "int64_t lim = pos / ratio + 1;"),
     "causal_token_not_chunk": ("int64_t lim = pos / ratio;", "int64_t lim = pos;"),
     "nan_ranks_high": ("double xa = isnan(a->x) ? -INFINITY : a->x;", "double xa = isnan(a->x) ? INFINITY : a->x;"),
+    "memindex_fp8_scale_from_wrong_layer": ("const float sc = scale[b * sstride_b + l * sstride_l + s];",
+                                            "const float sc = scale[b * sstride_b + s];"),
+    "memindex_fp8_key_stride_swapped": ("const uint8_t* ks = k8 + b * stride_b + l * stride_l + s * d;",
+                                        "const uint8_t* ks = k8 + l * stride_b + b * stride_l + s * d;"),
     "recall_keeps_empty_pages": ("if (density > 0) {", "if (density >= 0) {"),
     "recall_recent_short": ("if (s < sink || s >= S - recent) resident = 1;",
                             "if (s < sink || s > S - recent) resident = 1;"),
