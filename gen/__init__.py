@@ -282,6 +282,51 @@ def memindex_keys_device(cfg: MemIndexCfg, hot_dev_ptr: int, out_ptr: int, strid
         raise RuntimeError(f"gen_cuda_fill_k_bf16 failed: cuda error {rc}")
 
 
+def memindex_fp8_key_rows(cfg: MemIndexCfg, b: int, l: int, s_list, hot: np.ndarray):
+    """Compressed keys of (request b, layer l) for the listed chunk ids (host):
+    E4M3 codes [n, d] and fp32 scales [n] -- the same planted / cold keys as
+    the bf16 workload, quantised per chunk (scale = max|K_s| / 448)."""
+    s = np.ascontiguousarray(np.asarray(s_list, dtype=np.int64))
+    k8 = np.empty((len(s), cfg.d), dtype=np.uint8)
+    sc = np.empty(len(s), dtype=np.float32)
+    h = np.ascontiguousarray(hot[b, l], dtype=np.float32)
+    host_lib().gen_k_fp8_rows(cfg.seed, b, l, _p(s, i64p), len(s), cfg.d, thr32(cfg.hot_frac), _p(h, f32p),
+                              _p(k8, u8p), _p(sc, f32p))
+    return k8, sc
+
+
+def memindex_fp8_keys_host(cfg: MemIndexCfg, hot: np.ndarray):
+    """Dense k8 [B,L,S,d] E4M3 codes and scale [B,L,S] fp32 (small workloads)."""
+    k8 = np.empty((cfg.B, cfg.L, cfg.S, cfg.d), dtype=np.uint8)
+    sc = np.empty((cfg.B, cfg.L, cfg.S), dtype=np.float32)
+    for b in range(cfg.B):
+        for l in range(cfg.L):
+            k8[b, l], sc[b, l] = memindex_fp8_key_rows(cfg, b, l, np.arange(cfg.S), hot)
+    return k8, sc
+
+
+def memindex_fp8_keys_device(cfg: MemIndexCfg, hot_dev_ptr: int, owner_dev_ptr: int, k8_ptr: int, scale_ptr: int,
+                             stream: int = 0) -> None:
+    """Fill dense k8 [B,L,S,d] and scale [B,L,S] on the device with the values
+    of memindex_fp8_keys_host.  The dense layout is a pool of 64-chunk blocks:
+    block (b*L + l)*(S/64) + j holds chunks 64j.. of (b, l); owner_dev_ptr
+    points at memindex_fp8_owner(cfg) on the device.  Needs S % 64 == 0."""
+    if cfg.S % 64:
+        raise ValueError("memindex_fp8_keys_device needs S % 64 == 0")
+    P = cfg.B * cfg.L * (cfg.S // 64)
+    rc = cuda_lib().gen_cuda_fill_k_fp8_pool(cfg.seed, P, cfg.d, 64, thr32(cfg.hot_frac), owner_dev_ptr,
+                                             hot_dev_ptr, cfg.L * cfg.d, cfg.d, k8_ptr, scale_ptr, stream)
+    if rc != 0:
+        raise RuntimeError(f"gen_cuda_fill_k_fp8_pool failed: cuda error {rc}")
+
+
+def memindex_fp8_owner(cfg: MemIndexCfg) -> np.ndarray:
+    """owner [B*L*S/64, 3] int32: (request, layer, block) of each 64-chunk block."""
+    nb = cfg.S // 64
+    blk = np.arange(cfg.B * cfg.L * nb, dtype=np.int64)
+    return np.stack([blk // (cfg.L * nb), (blk // nb) % cfg.L, blk % nb], axis=1).astype(np.int32)
+
+
 # --------------------------------------------------------------------------
 # Paged inputs
 # --------------------------------------------------------------------------

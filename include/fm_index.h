@@ -108,6 +108,30 @@ fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const uint16
                                  float* logits_out, fm_stream_t stream);
 
 /*
+ * The same Memory Indexer over compressed keys ([FM] sec. 6 and [RM]
+ * "compressed_k format": the retriever reads each chunk as 128 E4M3 bytes plus
+ * an fp32 scale, dequantised as fp8.float() * scale):
+ *     x[b,l,s] = sum_h w[b,l,h] * ReLU( q[b,l,h,:] . (scale[b,l,s] * e4m3(k8[b,l,s,:])) )
+ * with the union, threshold and outputs of fm_memindex_score_mask.  The scale
+ * is applied to each head's dot (equal up to one fp32 rounding per element).
+ *
+ *   k8          E4M3 codes, element (b,l,s,j) at k8[b*key_stride_b +
+ *               l*key_stride_l + s*128 + j] (byte strides, multiples of 16;
+ *               16-byte aligned)
+ *   k_scale     fp32, (b,l,s) at k_scale[b*scale_stride_b + l*scale_stride_l + s]
+ *   workspace   >= fm_memindex_fp8_workspace(B, L) bytes, 256-byte aligned
+ *               (the split query: 16.25 KB per (request, layer))
+ * Other arguments, outputs and errors as fm_memindex_score_mask;
+ * FM_ERR_WORKSPACE for a missing or short workspace.
+ */
+size_t fm_memindex_fp8_workspace(int B, int L);
+fm_status fm_memindex_score_mask_fp8(const uint16_t* q, const float* w, const uint8_t* k8, const float* k_scale,
+                                     int64_t key_stride_b, int64_t key_stride_l, int64_t scale_stride_b,
+                                     int64_t scale_stride_l, int B, int L, int64_t S, int n_h, int d,
+                                     float threshold, uint32_t* mask_out, float* maxsig_out, float* logits_out,
+                                     void* workspace, size_t workspace_bytes, fm_stream_t stream);
+
+/*
  * Top-k select over caller-provided scores ([FM] sec. 3 "Top-k" of the native
  * score; [V4] sec. 3 CSA-2 top-512).
  *

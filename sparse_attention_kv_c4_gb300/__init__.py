@@ -17,7 +17,7 @@ __all__ = [
     "FmError", "lib", "fm_version", "fm_last_error", "fm_device_status", "fm_memindex_score_mask",
     "fm_topk_workspace", "fm_topk_select", "fm_native_topk_paged_workspace", "fm_native_topk_paged",
     "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "fm_page_recall",
-    "fm_native_topk_paged_ex",
+    "fm_native_topk_paged_ex", "fm_memindex_fp8_workspace", "fm_memindex_score_mask_fp8",
     "LIB_PATH",
 ]
 
@@ -74,10 +74,15 @@ def lib() -> ctypes.CDLL:
             L.fm_index_prefill_workspace.restype = _SZ
             L.fm_index_prefill_topk.argtypes = [_VP, _VP, _VP, _VP, _I32, _I64, _I32, _I32, _I32, _I32, _VP, _VP,
                                                 _VP, _SZ, _VP]
+        if hasattr(L, "fm_memindex_score_mask_fp8"):
+            L.fm_memindex_fp8_workspace.argtypes = [_I32, _I32]
+            L.fm_memindex_fp8_workspace.restype = _SZ
+            L.fm_memindex_score_mask_fp8.argtypes = [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I32, _I32, _I64,
+                                                     _I32, _I32, _F, _VP, _VP, _VP, _VP, _SZ, _VP]
         if hasattr(L, "fm_page_recall"):
             L.fm_page_recall.argtypes = [_VP, _I32, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _VP]
         for name in ("fm_memindex_score_mask", "fm_topk_select", "fm_native_topk_paged", "fm_index_prefill_topk",
-                     "fm_device_status", "fm_page_recall", "fm_native_topk_paged_ex"):
+                     "fm_device_status", "fm_page_recall", "fm_native_topk_paged_ex", "fm_memindex_score_mask_fp8"):
             if hasattr(L, name):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -126,6 +131,27 @@ def fm_memindex_score_mask(q, w, keys, mask_out, maxsig_out=None, logits_out=Non
     _check(lib().fm_memindex_score_mask(_ptr(q), _ptr(w), _ptr(keys), keys.stride(0), keys.stride(1), B, L, S, n_h,
                                         d, float(threshold), _ptr(mask_out), _ptr(maxsig_out), _ptr(logits_out),
                                         _stream(stream)))
+
+
+def fm_memindex_fp8_workspace(B: int, L: int) -> int:
+    return lib().fm_memindex_fp8_workspace(B, L)
+
+
+def fm_memindex_score_mask_fp8(q, w, k8, k_scale, mask_out, maxsig_out=None, logits_out=None, threshold: float = 0.5,
+                               workspace=None, stream=None) -> None:
+    """q [B,L,64,128] bf16, w [B,L,64] fp32, k8 [B,L,S,128] uint8 E4M3 codes
+    (any b/l strides, rows dense), k_scale [B,L,S] fp32 (any b/l strides,
+    unit s stride), mask_out [B, ceil(S/32)], maxsig_out [B,S] or None,
+    logits_out [B,L,S] or None, workspace >= fm_memindex_fp8_workspace(B, L)."""
+    B, L, n_h, d = q.shape
+    S = k8.shape[2]
+    if k8.stride(3) != 1 or k8.stride(2) != d or k_scale.stride(2) != 1:
+        raise ValueError("k8 rows must be dense [.., S, d] and k_scale rows dense [.., S]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_memindex_score_mask_fp8(_ptr(q), _ptr(w), _ptr(k8), _ptr(k_scale), k8.stride(0), k8.stride(1),
+                                            k_scale.stride(0), k_scale.stride(1), B, L, S, n_h, d, float(threshold),
+                                            _ptr(mask_out), _ptr(maxsig_out), _ptr(logits_out), _ptr(workspace),
+                                            ws_bytes, _stream(stream)))
 
 
 def fm_topk_workspace(rows: int, n: int) -> int:

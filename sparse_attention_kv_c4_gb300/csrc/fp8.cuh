@@ -1,0 +1,88 @@
+// fp8.cuh -- building blocks for scoring against E4M3 keys (the compressed_k
+// format of the "FlashMemory-DeepSeek-V4" README: 128 E4M3 bytes + an fp32
+// scale per chunk): E4M3 conversion, the query split below, the tcgen05
+// kind::f8f6f4 MMA and a 3-D TMA load.
+//
+// Query split.  For head h: q_h = 2^e_h * (t1 + t2) with e_h the power of two that puts
+// max|q_h| in (224, 448] (E4M3's top binades), t1 = RNE_e4m3(q_h 2^-e_h) and
+// t2 = RNE_e4m3(q_h 2^-e_h - t1).  The pair reproduces every bf16 element
+// whose residual stays inside E4M3's range; elements below max|q_h| 2^-13
+// lose low bits (at most 2^-10 of the head's scale).  2^e_h is folded into
+// the head weight, so the MMA's two dots (t1 . k, t2 . k) summed and scaled
+// by w_h 2^e_h give w_h (q_h . k).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include "fm_common.cuh"
+
+namespace fm {
+
+// fp32 -> E4M3 code, round to nearest even (|f| <= 448 here).
+FM_DEV uint32_t e4m3_rne(float f) {
+  return (uint32_t)__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
+}
+FM_DEV float e4m3_value(uint32_t code) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Split the n_heads x 128 bf16 query block q into t1 (rows 0..n_heads-1) and
+// t2 (rows n_heads..2 n_heads-1), 128 bytes per row, and write
+// wq[h] = w[h] * 2^e_h.  Called by every thread of a CTA of `nthreads`
+// threads; warp i takes heads i, i + nthreads/32, ...; lane l takes
+// elements 4l .. 4l+3.
+FM_DEV void split_query(const uint16_t* __restrict__ q, const float* __restrict__ w, int n_heads, int nthreads,
+                        uint8_t* __restrict__ t1, uint8_t* __restrict__ t2, float* __restrict__ wq) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int h = warp; h < n_heads; h += nthreads / 32) {
+    const uint16_t* qh = q + (int64_t)h * 128;
+    float v[4], amax = 0.f;
+    for (int j = 0; j < 4; ++j) {
+      v[j] = __uint_as_float((uint32_t)qh[4 * lane + j] << 16);
+      amax = fmaxf(amax, fabsf(v[j]));
+    }
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int e = 0;
+    if (amax > 0.f && isfinite(amax)) {
+      e = ilogbf(amax) - 8;
+      if (ldexpf(amax, -e) > 448.f) e += 1;
+    }
+    uint8_t* r1 = t1 + (int64_t)h * 128;
+    uint8_t* r2 = t2 + (int64_t)h * 128;
+    for (int j = 0; j < 4; ++j) {
+      const float s = ldexpf(v[j], -e);
+      const uint32_t c1 = e4m3_rne(s);
+      const float r = s - e4m3_value(c1);
+      r1[4 * lane + j] = (uint8_t)c1;
+      r2[4 * lane + j] = (uint8_t)e4m3_rne(r);
+    }
+    if (lane == 0) wq[h] = ldexpf(w[h], e);
+  }
+}
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 A/B, fp32 accumulate, K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+FM_DEV void umma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+FM_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+}  // namespace fm

@@ -1,0 +1,467 @@
+// memindex_fp8.cu -- the Memory Indexer over compressed E4M3 keys.
+//
+// Computes the same scores as memindex.cu ("FlashMemory-DeepSeek-V4: Lightning
+// Index Ultra-Long Context via Lookahead Sparse Attention", sec. 3 "Memory
+// Indexer scoring function"), with each chunk's key in the compressed_k
+// format the retriever reads (sec. 6; "FlashMemory-DeepSeek-V4" README,
+// "compressed_k format": 128 E4M3 bytes plus an fp32 scale, dequantised as
+// fp8.float() * scale):
+//     x[b,l,s] = sum_h w[b,l,h] * ReLU(q[b,l,h,:] . (scale[b,l,s] * e4m3(k8[b,l,s,:])))
+//     resident[b,s] = max_l x[b,l,s] >= logit(threshold)
+// The scale is applied to each head's dot instead of to each key element
+// (mathematically equal; the difference is one fp32 rounding per element).
+//
+// GB300 mapping.  At 132 B per chunk-layer the stream is half the bf16 path's,
+// so the dots run on the tensor cores in E4M3 (kind::f8f6f4) to stay
+// HBM-bound:
+//   prep    one CTA per (request, layer): q split into two E4M3 terms per head
+//           (fp8.cuh), 2^e_h folded into w.
+//   warp 0  TMA producer: the request's split q (L x 16 KB) once per request,
+//           then per layer a key tile [128 chunks x 128 B] (SWIZZLE_128B)
+//           into an N-stage ring.
+//   warp 1  UMMA issuer: per layer-tile 4 x tcgen05.mma M=128 (chunks) x
+//           N=128 (t1 and t2 rows of the 64 heads) x K=32 into one of four
+//           128-column TMEM accumulators taken in turn, so four layer-tiles
+//           can be in flight.
+//   warps 2-5  epilogue: thread = chunk row; loads its chunk's scale before
+//           waiting for the accumulator, reads the 64 (t1, t2) dot pairs,
+//           y = sum_h w_h 2^e_h ReLU(scale (t1.k + t2.k)), keeps the running
+//           max over the tile's layers, then ballots the mask word and
+//           writes max-sigmoid (and per-layer logits when asked).
+#include <math.h>
+
+#include "fm_common.cuh"
+#include "fm_internal.h"
+#include "fp8.cuh"
+
+#define FM_API extern "C" __attribute__((visibility("default")))
+
+namespace fm {
+namespace {
+
+constexpr int kM = 128;                      // chunks per tile (UMMA M)
+constexpr int kHeads = 64;
+constexpr int kN = 2 * kHeads;               // t1 and t2 rows of the split query (UMMA N)
+constexpr int kDim = 128;                    // E4M3 bytes per key (UMMA K, 4 steps of 32)
+constexpr int kMaxL = 4;
+constexpr int kTileBytes = kM * kDim;        // 16 KB of keys per layer-tile
+constexpr int kQLayerBytes = kN * kDim;      // 16 KB of split query per layer
+constexpr int kAccBufs = 4;                  // 128-column accumulators taken in turn
+constexpr int kMaxStages = 12;
+constexpr int kThreads = 192;
+constexpr int kPrepThreads = 256;
+constexpr uint32_t kTmemCols = kAccBufs * kN;  // 512
+
+struct Params {
+  const float* wq;            // [B*L, 64] head weights with 2^e_h folded in
+  const float* k_scale;
+  int64_t sstride_b, sstride_l;
+  uint32_t* mask;
+  float* maxsig;
+  float* logits;
+  unsigned int* status;
+  int64_t S;
+  int64_t total_tiles;
+  int tiles_per_b;
+  int L;
+  int stages;
+  float thr_logit;
+};
+
+__global__ void __launch_bounds__(kPrepThreads)
+    memindex_fp8_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                             uint8_t* __restrict__ qsplit, float* __restrict__ wq) {
+  const int64_t bl = blockIdx.x;
+  uint8_t* t1 = qsplit + bl * kQLayerBytes;
+  split_query(q + bl * kHeads * kDim, w + bl * kHeads, kHeads, kPrepThreads, t1, t1 + kHeads * kDim,
+              wq + bl * kHeads);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    memindex_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                        const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_smem = smem;
+  uint8_t* k_smem = smem + p.L * kQLayerBytes;
+
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_tfull[kAccBufs], bar_tempty[kAccBufs], bar_qfull, bar_qempty, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int L = p.L, stages = p.stages;
+  const int64_t t_begin = p.total_tiles * blockIdx.x / gridDim.x;
+  const int64_t t_end = p.total_tiles * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int i = 0; i < kAccBufs; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 128);
+    }
+    mbar_init(&bar_qfull, 1);
+    mbar_init(&bar_qempty, 1);
+    mbar_init(&bar_drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmap_k);
+    tma_prefetch(&tmap_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ TMA producer ------------------------------
+      uint32_t stage = 0, phase = 0, q_phase = 0;
+      int issued[kMaxStages];
+      for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
+      int q_issued = -1;
+      int64_t cur_b = -1;
+      bool ok = true;
+      int64_t b = t_begin / p.tiles_per_b;
+      int tile = (int)(t_begin % p.tiles_per_b) - 1;
+      for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        if (++tile == p.tiles_per_b) {
+          tile = 0;
+          ++b;
+        }
+        if (b != cur_b) {
+          if (cur_b >= 0) {
+            if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) break;
+            q_phase ^= 1;
+          }
+          mbar_arrive_expect_tx(&bar_qfull, (uint32_t)(L * kQLayerBytes));
+          for (int l = 0; l < L; ++l)
+            tma_load_2d(q_smem + l * kQLayerBytes, &tmap_q, &bar_qfull, 0, (int32_t)((b * L + l) * kN));
+          q_issued = (q_issued + 1) & 1;
+          cur_b = b;
+        }
+        for (int l = 0; l < L; ++l) {
+          if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)kTileBytes);
+          tma_load_4d(k_smem + stage * kTileBytes, &tmap_k, &bar_full[stage], 0, tile * kM, l, (int32_t)b);
+          issued[stage] = (int)phase;
+          if (++stage == (uint32_t)stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (abort_flag) {  // let copies already in flight land before the CTA exits
+        for (int s = 0; s < stages; ++s)
+          if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
+        if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------ UMMA issuer -------------------------------
+      const uint32_t idesc = idesc_e4m3_f32(kM, kN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0;
+      int64_t cur_b = -1;
+      bool ok = true;
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(k_smem));
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(q_smem));
+      int64_t b = t_begin / p.tiles_per_b;
+      int tile = (int)(t_begin % p.tiles_per_b) - 1;
+      for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        if (++tile == p.tiles_per_b) {
+          tile = 0;
+          ++b;
+        }
+        if (b != cur_b) {
+          if (cur_b >= 0) umma_commit(&bar_qempty);
+          if (!mbar_wait(&bar_qfull, q_phase, &abort_flag, p.status)) break;
+          q_phase ^= 1;
+          tc_fence_after();
+          cur_b = b;
+        }
+        for (int l = 0; l < L; ++l) {
+          if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status) ||
+              !mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kN;
+          // descriptor start-address field counts 16-byte units; K steps of
+          // 32 bytes advance it by 2 inside the 128-byte swizzle atom
+          const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
+          const uint64_t b_desc = b_desc0 + (uint64_t)(l * (kQLayerBytes >> 4));
+#pragma unroll
+          for (int k = 0; k < kDim / 32; ++k)
+            umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k != 0 ? 1u : 0u);
+          umma_commit(&bar_empty[stage]);
+          umma_commit(&bar_tfull[acc]);
+          if (++stage == (uint32_t)stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++acc == (uint32_t)kAccBufs) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+      }
+      umma_commit(&bar_drain);  // every MMA issued above has finished before TMEM is freed
+      mbar_wait_drain(&bar_drain, 0);
+    }
+  } else {
+    // -------------------------------- epilogue ----------------------------------
+    const int quad = warp & 3;  // TMEM lane quadrant this warp can access
+    const int row = quad * 32 + lane;
+    const int64_t words = (p.S + 31) / 32;
+    uint32_t acc = 0, acc_phase = 0;
+    bool ok = true;
+    int64_t b = t_begin / p.tiles_per_b;
+    int tile = (int)(t_begin % p.tiles_per_b) - 1;
+    for (int64_t t = t_begin; t < t_end && ok; ++t) {
+      if (++tile == p.tiles_per_b) {
+        tile = 0;
+        ++b;
+      }
+      const int64_t s = (int64_t)tile * kM + row;
+      const bool valid = s < p.S;
+      float m = -INFINITY;
+      for (int l = 0; l < L; ++l) {
+        // the chunk's scale is loaded before the wait so its latency overlaps it
+        const float sc = valid ? __ldg(p.k_scale + b * p.sstride_b + l * p.sstride_l + s) : 0.f;
+        if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN;
+        const float4* wl = reinterpret_cast<const float4*>(p.wq + (b * L + l) * kHeads);
+        float y = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // 32 heads at a time: their t1 and t2 dots
+          uint32_t r[32], u[32];
+          tmem_ld32(taddr + half * 32, r);
+          tmem_ld32(taddr + kHeads + half * 32, u);
+          float wr[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = __ldg(wl + half * 8 + i);
+            wr[4 * i] = v.x;
+            wr[4 * i + 1] = v.y;
+            wr[4 * i + 2] = v.z;
+            wr[4 * i + 3] = v.w;
+          }
+          tmem_ld_wait();
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(&bar_tempty[acc]);
+          }
+          // q_h . k = 2^e_h (t1 . k + t2 . k); 2^e_h is folded into w
+          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+          if (sc > 0.f) {  // ReLU(sc d) = sc ReLU(d): one multiply per chunk
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+              x0 = fmaf(wr[h], fmaxf(__uint_as_float(r[h]) + __uint_as_float(u[h]), 0.f), x0);
+              x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1]), 0.f), x1);
+              x2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(r[h + 2]) + __uint_as_float(u[h + 2]), 0.f), x2);
+              x3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(r[h + 3]) + __uint_as_float(u[h + 3]), 0.f), x3);
+            }
+            y += sc * ((x0 + x1) + (x2 + x3));
+          } else {
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+              x0 = fmaf(wr[h], fmaxf(sc * (__uint_as_float(r[h]) + __uint_as_float(u[h])), 0.f), x0);
+              x1 = fmaf(wr[h + 1], fmaxf(sc * (__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1])), 0.f), x1);
+              x2 = fmaf(wr[h + 2], fmaxf(sc * (__uint_as_float(r[h + 2]) + __uint_as_float(u[h + 2])), 0.f), x2);
+              x3 = fmaf(wr[h + 3], fmaxf(sc * (__uint_as_float(r[h + 3]) + __uint_as_float(u[h + 3])), 0.f), x3);
+            }
+            y += (x0 + x1) + (x2 + x3);
+          }
+        }
+        if (p.logits != nullptr && valid) p.logits[(b * L + l) * p.S + s] = y;
+        m = fmaxf(m, y);
+        if (++acc == (uint32_t)kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      const uint32_t bits = __ballot_sync(0xffffffffu, valid && m >= p.thr_logit);
+      const int64_t word = (int64_t)tile * (kM / 32) + quad;
+      if (lane == 0 && word < words) p.mask[b * words + word] = bits;
+      if (p.maxsig != nullptr && valid) p.maxsig[b * p.S + s] = 1.0f / (1.0f + expf(-m));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t memindex_fp8_workspace_bytes(int B, int L) {
+  return align256((size_t)B * L * kQLayerBytes) + align256((size_t)B * L * kHeads * 4);
+}
+
+namespace {
+
+struct Fp8Args {
+  const uint16_t* q;
+  const float* w;
+  const uint8_t* k8;
+  const float* k_scale;
+  int64_t key_stride_b, key_stride_l, sstride_b, sstride_l;
+  int B, L;
+  int64_t S;
+  float thr_logit;
+  uint32_t* mask;
+  float* maxsig;
+  float* logits;
+  void* workspace;
+};
+
+fm_status launch_memindex_fp8(const Fp8Args& a, int num_sms, unsigned int* status, cudaStream_t stream) {
+  const int tiles_per_b = (int)((a.S + kM - 1) / kM);
+  const int64_t total = (int64_t)a.B * tiles_per_b;
+  if (total == 0) return FM_OK;
+  uint8_t* qsplit = static_cast<uint8_t*>(a.workspace);
+  float* wq = reinterpret_cast<float*>(qsplit + align256((size_t)a.B * a.L * kQLayerBytes));
+  memindex_fp8_prep_kernel<<<a.B * a.L, kPrepThreads, 0, stream>>>(a.q, a.w, qsplit, wq);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "memindex fp8 prep: launch: %s", cudaGetErrorString(e));
+
+  CUtensorMap tmap_k, tmap_q;
+  {
+    // keys: dims (128 B, S, L, B), box (128, 128, 1, 1), 128-byte swizzle
+    const uint64_t dims[4] = {(uint64_t)kDim, (uint64_t)a.S, (uint64_t)a.L, (uint64_t)a.B};
+    const uint64_t strides[3] = {(uint64_t)kDim, (uint64_t)a.key_stride_l, (uint64_t)a.key_stride_b};
+    const uint32_t box[4] = {(uint32_t)kDim, (uint32_t)kM, 1, 1};
+    fm_status st = make_tmap(&tmap_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, a.k8, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  }
+  {
+    // split query: rows (B*L*128) x 128 B, one box of 128 rows per layer
+    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.B * a.L * kN};
+    const uint64_t strides[1] = {(uint64_t)kDim};
+    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)kN};
+    fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, qsplit, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  }
+  const int smem_cap = 227 * 1024;
+  const int fixed = 1024 + a.L * kQLayerBytes;
+  int stages = (smem_cap - fixed) / kTileBytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  const int smem = fixed + stages * kTileBytes;
+
+  Params p;
+  p.wq = wq;
+  p.k_scale = a.k_scale;
+  p.sstride_b = a.sstride_b;
+  p.sstride_l = a.sstride_l;
+  p.mask = a.mask;
+  p.maxsig = a.maxsig;
+  p.logits = a.logits;
+  p.status = status;
+  p.S = a.S;
+  p.total_tiles = total;
+  p.tiles_per_b = tiles_per_b;
+  p.L = a.L;
+  p.stages = stages;
+  p.thr_logit = a.thr_logit;
+  e = cudaFuncSetAttribute(memindex_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "memindex fp8: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  const int grid = (int)(total < num_sms ? total : num_sms);
+  memindex_fp8_kernel<<<grid, kThreads, smem, stream>>>(tmap_k, tmap_q, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "memindex fp8: launch: %s", cudaGetErrorString(e));
+  return FM_OK;
+}
+
+}  // namespace
+}  // namespace fm
+
+FM_API size_t fm_memindex_fp8_workspace(int B, int L) {
+  if (B < 0 || L < 1 || L > 4) return 0;
+  return fm::memindex_fp8_workspace_bytes(B, L);
+}
+
+FM_API fm_status fm_memindex_score_mask_fp8(const uint16_t* q, const float* w, const uint8_t* k8, const float* k_scale,
+                                            int64_t key_stride_b, int64_t key_stride_l, int64_t scale_stride_b,
+                                            int64_t scale_stride_l, int B, int L, int64_t S, int n_h, int d,
+                                            float threshold, uint32_t* mask_out, float* maxsig_out, float* logits_out,
+                                            void* workspace, size_t workspace_bytes, fm_stream_t stream) {
+  using namespace fm;
+  if (n_h != 64 || d != 128)
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask_fp8: n_h=%d d=%d (need 64, 128)", n_h, d);
+  if (B < 0 || L < 1 || L > 4 || S < 0 || S >= (int64_t(1) << 31))
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask_fp8: bad sizes B=%d L=%d S=%lld", B, L,
+                     (long long)S);
+  if (!(threshold > 0.0f && threshold < 1.0f))
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask_fp8: threshold %g not in (0, 1)", (double)threshold);
+  if (B == 0 || S == 0) return FM_OK;
+  if (!q || !w || !k8 || !k_scale || !mask_out)
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask_fp8: required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(k8, 16) || !aligned(k_scale, 4) || !aligned(mask_out, 4) ||
+      (maxsig_out && !aligned(maxsig_out, 4)) || (logits_out && !aligned(logits_out, 4)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask_fp8: misaligned pointer (q, w, k8: 16 bytes)");
+  // key rows are 128 contiguous bytes; layer and request strides must be
+  // multiples of 16 bytes and must not make rows of different (b, l) overlap
+  if (key_stride_l % 16 != 0 || key_stride_b % 16 != 0 || (L > 1 && key_stride_l < S * d) ||
+      (B > 1 && key_stride_b < (L > 1 ? key_stride_l * L : S * d)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask_fp8: bad key strides b=%lld l=%lld",
+                     (long long)key_stride_b, (long long)key_stride_l);
+  if ((L > 1 && scale_stride_l < S) || (B > 1 && scale_stride_b < (L > 1 ? scale_stride_l * L : S)) ||
+      scale_stride_l < 0 || scale_stride_b < 0)
+    return set_error(FM_ERR_INVALID_ARG, "fm_memindex_score_mask_fp8: bad scale strides b=%lld l=%lld",
+                     (long long)scale_stride_b, (long long)scale_stride_l);
+  const size_t need = memindex_fp8_workspace_bytes(B, L);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return set_error(FM_ERR_WORKSPACE, "fm_memindex_score_mask_fp8: workspace needs %zu bytes, 256-byte aligned",
+                     need);
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  unsigned int* status = nullptr;
+  st = status_word(&status);
+  if (st != FM_OK) return st;
+  Fp8Args a;
+  a.q = q;
+  a.w = w;
+  a.k8 = k8;
+  a.k_scale = k_scale;
+  a.key_stride_b = key_stride_b;
+  a.key_stride_l = key_stride_l;
+  a.sstride_b = scale_stride_b;
+  a.sstride_l = scale_stride_l;
+  a.B = B;
+  a.L = L;
+  a.S = S;
+  a.thr_logit = (float)log((double)threshold / (1.0 - (double)threshold));
+  a.mask = mask_out;
+  a.maxsig = maxsig_out;
+  a.logits = logits_out;
+  a.workspace = workspace;
+  return launch_memindex_fp8(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -27,12 +27,11 @@
 //     chunk) adds the two halves of its 128 dots, applies the chunk's scale,
 //     ReLU and w, and writes y to the workspace.
 //  3. the block top-k (topk.cuh), mapping candidate i to its chunk id.
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <math.h>
 
 #include "fm_common.cuh"
 #include "fm_internal.h"
+#include "fp8.cuh"
 
 namespace fm {
 namespace {
@@ -58,15 +57,6 @@ constexpr int kPrepThreads = 256;
 // --------------------------------------------------------------------------
 // 1. prep: sort pages, validate, split q
 // --------------------------------------------------------------------------
-
-// fp32 -> E4M3 code, round to nearest even (|f| <= 448 here).
-FM_DEV uint32_t e4m3_rne(float f) {
-  return (uint32_t)__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
-}
-FM_DEV float e4m3_value(uint32_t code) {
-  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
-  return __half2float(__half(h));
-}
 
 __global__ void __launch_bounds__(kPrepThreads)
     paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
@@ -184,32 +174,10 @@ __global__ void __launch_bounds__(kPrepThreads)
       n_valid[qi] = (int32_t)run;
     }
   }
-  // q split: warp handles heads warp, warp+8, ...; lane handles d = 4*lane..4*lane+3
-  for (int h = warp; h < kHeads; h += kPrepThreads / 32) {
-    const uint16_t* qh = q + ((int64_t)qi * kHeads + h) * kDim;
-    float v[4], amax = 0.f;
-    for (int j = 0; j < 4; ++j) {
-      v[j] = __uint_as_float((uint32_t)qh[4 * lane + j] << 16);
-      amax = fmaxf(amax, fabsf(v[j]));
-    }
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    // e: power of two putting amax * 2^-e in (224, 448] (E4M3's top binades)
-    int e = 0;
-    if (amax > 0.f && isfinite(amax)) {
-      e = ilogbf(amax) - 8;
-      if (ldexpf(amax, -e) > 448.f) e += 1;
-    }
-    uint8_t* t1 = qsplit + ((int64_t)qi * 2 * kHeads + h) * kDim;
-    uint8_t* t2 = t1 + (int64_t)kHeads * kDim;
-    for (int j = 0; j < 4; ++j) {
-      const float s = ldexpf(v[j], -e);
-      const uint32_t c1 = e4m3_rne(s);
-      const float r = s - e4m3_value(c1);
-      t1[4 * lane + j] = (uint8_t)c1;
-      t2[4 * lane + j] = (uint8_t)e4m3_rne(r);
-    }
-    if (lane == 0) wq[(int64_t)qi * kHeads + h] = ldexpf(w[(int64_t)qi * kHeads + h], e);
-  }
+  // q split: q_h = 2^e_h (t1 + t2), 2^e_h folded into w
+  uint8_t* t1 = qsplit + (int64_t)qi * 2 * kHeads * kDim;
+  split_query(q + (int64_t)qi * kHeads * kDim, w + (int64_t)qi * kHeads, kHeads, kPrepThreads, t1,
+              t1 + (int64_t)kHeads * kDim, wq + (int64_t)qi * kHeads);
 }
 
 // --------------------------------------------------------------------------
@@ -230,20 +198,6 @@ struct ScoreParams {
   int R;
   int stages;
 };
-
-// Instruction descriptor, kind::f8f6f4 with E4M3 A/B, fp32 accumulate, K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-FM_DEV void umma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 // kMasked: write only the resident chunks of each page, compacted (the
 // Level-2 resident mask); a separate instantiation so that the unmasked
