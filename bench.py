@@ -396,6 +396,12 @@ def run_ours(args):
     import sparse_attention_kv_c4_gb300 as fm
     fm.lib()
 
+    if args.only == "memindex_fp8":
+        v = Fp8MemIndex(torch, dev, fm, small=args.small)
+        r = v.measure(max(1, args.steps), args.warmup, peaks())
+        print(json.dumps({"profile_case": True, "only": args.only, "small": args.small, "ms_per_step": r["ms"],
+                          "device_status": fm.fm_device_status(reset=True)}), flush=True)
+        return
     cfgs = workload_cfgs(args.small)
     W, cfgs = build_inputs(torch, dev, cfgs, args.only)
     mi, pg, pf = cfgs
@@ -523,6 +529,16 @@ def run_ours(args):
     e2e_ms = reduce_max(e2e_ms, dev, world)
     e2e_value = world * cs_step / (e2e_ms / 1e3)
 
+    # ---- variant rows, each timed alone on its own inputs after the step ----
+    variants = None
+    if not args.no_variants:
+        del sets, host_in, host_out
+        v = Fp8MemIndex(torch, dev, fm)
+        variants = {"memindex_fp8": v.measure(10, 3, pk)}
+        del v
+        if fm.fm_device_status(reset=True) != 0:
+            raise RuntimeError("device status flagged an error in the variant rows")
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(cfgs)
@@ -541,11 +557,64 @@ def run_ours(args):
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": e2e_ms},
                 "gpu_launches": KERNELS_PER_STEP * K,
-                "roofline": roofline, "phases": phases, "clocks": clk, "cpu_baseline": cpu,
+                "roofline": roofline, "phases": phases, "variants": variants, "clocks": clk, "cpu_baseline": cpu,
                 "device_status": status, "sanity": chk}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+class Fp8MemIndex:
+    """The Memory Indexer over compressed keys (fm_memindex_score_mask_fp8):
+    the bench step's 30 requests x 3 layers x 262144 chunks with E4M3 codes
+    and one fp32 scale per chunk (3.1 GB streamed per call, far above L2).
+    Timed on its own after the step, not part of the step's value."""
+
+    def __init__(self, torch, dev, fm, small=False):
+        import gen
+        self.torch, self.fm = torch, fm
+        mi = gen.replace(gen.MEMINDEX_1M, B=4) if small else gen.MEMINDEX_1M
+        self.cfg = mi
+        q, w, hot = gen.memindex_qw(mi)
+        self.q = torch.from_numpy(q.view(np.int16)).to(dev)
+        self.w = torch.from_numpy(w).to(dev)
+        hot_d = torch.from_numpy(hot).to(dev)
+        own_d = torch.from_numpy(gen.memindex_fp8_owner(mi)).to(dev)
+        self.k8 = torch.empty((mi.B, mi.L, mi.S, mi.d), dtype=torch.uint8, device=dev)
+        self.sc = torch.empty((mi.B, mi.L, mi.S), dtype=torch.float32, device=dev)
+        gen.memindex_fp8_keys_device(mi, hot_d.data_ptr(), own_d.data_ptr(), self.k8.data_ptr(), self.sc.data_ptr())
+        self.mask = torch.empty((mi.B, (mi.S + 31) // 32), dtype=torch.int32, device=dev)
+        self.maxsig = torch.empty((mi.B, mi.S), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(fm.fm_memindex_fp8_workspace(mi.B, mi.L), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        self.fm.fm_memindex_score_mask_fp8(self.q, self.w, self.k8, self.sc, self.mask, self.maxsig,
+                                           workspace=self.ws)
+
+    def bytes(self):
+        mi = self.cfg
+        return (mi.B * mi.L * mi.S * (mi.d + 4) + mi.B * mi.S * 4 + mi.B * ((mi.S + 31) // 32) * 4
+                + mi.B * mi.L * mi.n_h * (mi.d * 2 + 4))
+
+    def measure(self, reps, warmup, pk):
+        torch = self.torch
+        for _ in range(warmup):
+            self.call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            self.call()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        ach = self.bytes() / (ms / 1e3) / 1e9
+        mi = self.cfg
+        return {"ms": round(ms, 4), "chunk_scores_per_s": mi.chunk_scores / (ms / 1e3), "bound": "hbm",
+                "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": self.bytes(), "launches": 2, "reps": reps,
+                "workload": f"memindex fp8 keys {mi.B}x{mi.L}x{mi.S}, E4M3 + per-chunk fp32 scale"}
 
 
 def run_profile_case(args, fm, torch, W, cfgs, ws):
@@ -574,7 +643,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["memindex", "paged", "prefill"], default=None,
+    ap.add_argument("--no-variants", action="store_true", help="skip the variant rows timed after the step")
+    ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8"], default=None,
                     help="profiling case: run one phase only")
     ap.add_argument("--small", action="store_true", help="profiling case: reduced sizes for ncu captures")
     args = ap.parse_args()

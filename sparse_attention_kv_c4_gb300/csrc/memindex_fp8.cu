@@ -19,15 +19,24 @@
 //   warp 0  TMA producer: the request's split q (L x 16 KB) once per request,
 //           then per layer a key tile [128 chunks x 128 B] (SWIZZLE_128B)
 //           into an N-stage ring.
-//   warp 1  UMMA issuer: per layer-tile 4 x tcgen05.mma M=128 (chunks) x
-//           N=128 (t1 and t2 rows of the 64 heads) x K=32 into one of four
-//           128-column TMEM accumulators taken in turn, so four layer-tiles
-//           can be in flight.
-//   warps 2-5  epilogue: thread = chunk row; loads its chunk's scale before
-//           waiting for the accumulator, reads the 64 (t1, t2) dot pairs,
-//           y = sum_h w_h 2^e_h ReLU(scale (t1.k + t2.k)), keeps the running
-//           max over the tile's layers, then ballots the mask word and
-//           writes max-sigmoid (and per-layer logits when asked).
+//   warps 1-2  UMMA issuers: per layer-tile 8 x tcgen05.mma M=128 (chunks)
+//           x N=64 (heads) x K=32: four K steps against the t1 rows, then
+//           four against the t2 rows into the same accumulator, so TMEM holds
+//           (t1 + t2).k directly.  One issuing thread alone cannot keep up
+//           with the key stream (each MMA costs it tens of cycles), so two
+//           issue in parallel.
+//   warps 3-10  epilogue, two groups of four warps (one warp per SM
+//           sub-partition would leave every latency exposed).  Issuer m and
+//           group m form pair m: the pair takes the CTA's tiles with local
+//           index = m (mod 2) and owns four of the eight 64-column
+//           accumulators.  Thread = chunk row; its chunk's scales are fetched
+//           with cp.async two of its pair's tiles ahead into a shared-memory
+//           ring (a load from HBM per layer-tile would stall the warp for its
+//           full latency), the head weights come from a per-warp shared copy,
+//           then y = sum_h w_h 2^e_h ReLU(scale (t1 + t2).k) from the 64
+//           accumulated dots, the running max over the tile's layers, the
+//           ballot of the mask word, max-sigmoid (and per-layer logits when
+//           asked).
 #include <math.h>
 
 #include "fm_common.cuh"
@@ -40,17 +49,42 @@ namespace fm {
 namespace {
 
 constexpr int kM = 128;                      // chunks per tile (UMMA M)
-constexpr int kHeads = 64;
-constexpr int kN = 2 * kHeads;               // t1 and t2 rows of the split query (UMMA N)
+constexpr int kHeads = 64;                   // UMMA N: t1.k + t2.k accumulate in one column per head
+constexpr int kQRows = 2 * kHeads;           // t1 rows 0..63, t2 rows 64..127 of the split query
 constexpr int kDim = 128;                    // E4M3 bytes per key (UMMA K, 4 steps of 32)
 constexpr int kMaxL = 4;
 constexpr int kTileBytes = kM * kDim;        // 16 KB of keys per layer-tile
-constexpr int kQLayerBytes = kN * kDim;      // 16 KB of split query per layer
-constexpr int kAccBufs = 4;                  // 128-column accumulators taken in turn
+constexpr int kQLayerBytes = kQRows * kDim;  // 16 KB of split query per layer
+constexpr int kAccBufs = 8;                  // 64-column accumulators
 constexpr int kMaxStages = 12;
-constexpr int kThreads = 192;
+// Issuer m and epilogue group m form pair m: the pair takes the CTA's tiles
+// with local index i = m (mod kPairs) and owns accumulators
+// [m * kRingAccs, (m + 1) * kRingAccs), a ring with one filler and one
+// reader, so every parity wait on it is unambiguous.  (Rings shared between
+// issuers or between epilogue groups let a waiter run two uses ahead of an
+// accumulator and pass a parity wait on a stale phase.)
+constexpr int kPairs = 2;
+constexpr int kMmaWarps = kPairs;
+constexpr int kEpiGroups = kPairs;
+constexpr int kRingAccs = kAccBufs / kPairs;
+constexpr int kFirstEpiWarp = 1 + kMmaWarps;
+constexpr int kThreads = kFirstEpiWarp * 32 + kEpiGroups * 128;
 constexpr int kPrepThreads = 256;
-constexpr uint32_t kTmemCols = kAccBufs * kN;  // 512
+constexpr uint32_t kTmemCols = kAccBufs * kHeads;  // 512
+constexpr int kScDepth = 2;                  // a group's tiles of scales in flight ahead of it
+constexpr int kScSlots = kScDepth + 1;
+constexpr int kScRingBytes = kEpiGroups * kScSlots * kMaxL * kM * 4;  // 12 KB
+
+// 4-byte asynchronous global -> shared copy; src_bytes = 0 writes a zero
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 struct Params {
   const float* wq;            // [B*L, 64] head weights with 2^e_h folded in
@@ -83,12 +117,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_smem = smem;
-  uint8_t* k_smem = smem + p.L * kQLayerBytes;
+  float* sc_ring = reinterpret_cast<float*>(smem + p.L * kQLayerBytes);  // [group][slot][layer][row]
+  uint8_t* k_smem = smem + p.L * kQLayerBytes + kScRingBytes;
 
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[kAccBufs], bar_tempty[kAccBufs], bar_qfull, bar_qempty, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  // one copy of the current request's head weights per epilogue warp, so a
+  // warp refreshes its own copy with __syncwarp alone
+  __shared__ __align__(16) float w_smem[kEpiGroups * 4][kMaxL * kHeads];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int L = p.L, stages = p.stages;
@@ -105,8 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_tempty[i], 128);
     }
     mbar_init(&bar_qfull, 1);
-    mbar_init(&bar_qempty, 1);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_qempty, kMmaWarps);
+    mbar_init(&bar_drain, kMmaWarps);  // each issuer arrives once its MMAs are done
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -146,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&bar_qfull, (uint32_t)(L * kQLayerBytes));
           for (int l = 0; l < L; ++l)
-            tma_load_2d(q_smem + l * kQLayerBytes, &tmap_q, &bar_qfull, 0, (int32_t)((b * L + l) * kN));
+            tma_load_2d(q_smem + l * kQLayerBytes, &tmap_q, &bar_qfull, 0, (int32_t)((b * L + l) * kQRows));
           q_issued = (q_issued + 1) & 1;
           cur_b = b;
         }
@@ -170,11 +208,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp < kFirstEpiWarp) {
     if (lane == 0) {
-      // ------------------------------ UMMA issuer -------------------------------
-      const uint32_t idesc = idesc_e4m3_f32(kM, kN);
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0;
+      // ------------------------------ UMMA issuers ------------------------------
+      // Issuer m takes its pair's tiles (all layers of each), so one issuer's
+      // barrier waits and commits overlap the other's MMAs.  The key stages
+      // are filled in CTA order: an issuer waiting for the stage of a tile has
+      // consumed its previous tile, at most (kPairs - 1) * L + 1 layer-tiles
+      // earlier, so stages >= (kPairs - 1) * kMaxL + 1 keeps that wait exact.
+      const int me = warp - 1;
+      const uint32_t idesc = idesc_e4m3_f32(kM, kHeads);
+      uint32_t stage = 0, phase = 0, racc = 0, acc_phase = 0, q_phase = 0;
       int64_t cur_b = -1;
       bool ok = true;
       const uint64_t a_desc0 = sdesc_sw128(smem_u32(k_smem));
@@ -193,29 +237,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           cur_b = b;
         }
+        if ((int)((t - t_begin) % kPairs) != me) {  // the other pair's tile
+          stage += L;
+          if (stage >= (uint32_t)stages) {  // L < stages: at most one wrap
+            stage -= stages;
+            phase ^= 1u;
+          }
+          continue;
+        }
         for (int l = 0; l < L; ++l) {
+          const uint32_t acc = me * kRingAccs + racc;
           if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status) ||
               !mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + acc * kN;
+          const uint32_t d_tmem = tmem_base + acc * kHeads;
           // descriptor start-address field counts 16-byte units; K steps of
           // 32 bytes advance it by 2 inside the 128-byte swizzle atom
           const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
           const uint64_t b_desc = b_desc0 + (uint64_t)(l * (kQLayerBytes >> 4));
+          // the t2 rows start 8 KB (eight 1 KB swizzle atoms) after the t1 rows
+          constexpr uint64_t kT2 = (kHeads * kDim) >> 4;
 #pragma unroll
           for (int k = 0; k < kDim / 32; ++k)
             umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k != 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < kDim / 32; ++k) umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc + kT2 + 2 * k, idesc, 1u);
           umma_commit(&bar_empty[stage]);
           umma_commit(&bar_tfull[acc]);
           if (++stage == (uint32_t)stages) {
             stage = 0;
             phase ^= 1u;
           }
-          if (++acc == (uint32_t)kAccBufs) {
-            acc = 0;
+          if (++racc == (uint32_t)kRingAccs) {
+            racc = 0;
             acc_phase ^= 1u;
           }
         }
@@ -225,77 +282,127 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------- epilogue ----------------------------------
+    // Group g (four warps, one per TMEM lane quadrant) is pair g's reader: it
+    // takes the CTA's tiles with local index i = g (mod kPairs).
+    const int group = (warp - kFirstEpiWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp can access
     const int row = quad * 32 + lane;
     const int64_t words = (p.S + 31) / 32;
-    uint32_t acc = 0, acc_phase = 0;
+    // The scales of the group's j-th tile go to its ring slot j % kScSlots.
+    // Each thread copies and later reads only its own row, so its own
+    // cp.async.wait_group is the only ordering needed.
+    float* ring = sc_ring + group * (kScSlots * kMaxL * kM);
+    int64_t pf_t = t_begin + group, pf_b = pf_t / p.tiles_per_b;
+    int pf_tile = (int)(pf_t % p.tiles_per_b), pf_slot = 0;
+    auto prefetch = [&]() {
+      if (pf_t < t_end) {
+        const int64_t s = (int64_t)pf_tile * kM + row;
+        const bool v = s < p.S;
+        const float* src = p.k_scale + pf_b * p.sstride_b + (v ? s : 0);
+        for (int l = 0; l < L; ++l)
+          cp_async4(ring + (pf_slot * kMaxL + l) * kM + row, src + l * p.sstride_l, v ? 4u : 0u);
+        pf_t += kEpiGroups;
+        pf_tile += kEpiGroups;
+        while (pf_tile >= p.tiles_per_b) {
+          pf_tile -= p.tiles_per_b;
+          ++pf_b;
+        }
+      }
+      cp_async_commit();  // an empty group past the end keeps the group count uniform
+      if (++pf_slot == kScSlots) pf_slot = 0;
+    };
+    for (int d = 0; d < kScDepth; ++d) prefetch();
+
+    // the pair's accumulator ring, read in the order its issuer fills it
+    uint32_t racc = 0, acc_phase = 0;
+    int slot = 0;
     bool ok = true;
-    int64_t b = t_begin / p.tiles_per_b;
+    int64_t b = t_begin / p.tiles_per_b, w_b = -1;
     int tile = (int)(t_begin % p.tiles_per_b) - 1;
+    float* w_mine = w_smem[warp - kFirstEpiWarp];
     for (int64_t t = t_begin; t < t_end && ok; ++t) {
       if (++tile == p.tiles_per_b) {
         tile = 0;
         ++b;
       }
+      if ((int)((t - t_begin) % kPairs) != group) continue;  // the other pair's tile
+      if (b != w_b) {  // a new request: its weights into this warp's copy
+        __syncwarp();
+        for (int i = lane; i < L * kHeads; i += 32) w_mine[i] = __ldg(p.wq + b * L * kHeads + i);
+        __syncwarp();
+        w_b = b;
+      }
+      prefetch();                  // the group's tile kScDepth ahead
+      cp_async_wait<kScDepth>();   // this tile's scales have landed
+      const float* sc_t = ring + slot * kMaxL * kM + row;
+      if (++slot == kScSlots) slot = 0;
       const int64_t s = (int64_t)tile * kM + row;
-      const bool valid = s < p.S;
+      const bool valid = s < p.S;  // rows past S read a zero scale and score 0
       float m = -INFINITY;
       for (int l = 0; l < L; ++l) {
-        // the chunk's scale is loaded before the wait so its latency overlaps it
-        const float sc = valid ? __ldg(p.k_scale + b * p.sstride_b + l * p.sstride_l + s) : 0.f;
+        const float sc = sc_t[l * kM];
+        const uint32_t acc = group * kRingAccs + racc;
         if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN;
-        const float4* wl = reinterpret_cast<const float4*>(p.wq + (b * L + l) * kHeads);
-        float y = 0.f;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kHeads;
+        uint32_t r0[32], r1[32];
+        tmem_ld32(taddr, r0);
+        tmem_ld32(taddr + 32, r1);
+        const float4* wl = reinterpret_cast<const float4*>(w_mine + l * kHeads);
+        float wr[kHeads];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {  // 32 heads at a time: their t1 and t2 dots
-          uint32_t r[32], u[32];
-          tmem_ld32(taddr + half * 32, r);
-          tmem_ld32(taddr + kHeads + half * 32, u);
-          float wr[32];
+        for (int i = 0; i < kHeads / 4; ++i) {
+          const float4 v = wl[i];
+          wr[4 * i] = v.x;
+          wr[4 * i + 1] = v.y;
+          wr[4 * i + 2] = v.z;
+          wr[4 * i + 3] = v.w;
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_tempty[acc]);  // the dots are in registers: the MMA may reuse the accumulator
+        // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, y;
+        if (sc > 0.f) {  // ReLU(sc d) = sc ReLU(d): one multiply per chunk
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = __ldg(wl + half * 8 + i);
-            wr[4 * i] = v.x;
-            wr[4 * i + 1] = v.y;
-            wr[4 * i + 2] = v.z;
-            wr[4 * i + 3] = v.w;
+          for (int h = 0; h < 32; h += 4) {
+            x0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), x0);
+            x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), x1);
+            x2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(r0[h + 2]), 0.f), x2);
+            x3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(r0[h + 3]), 0.f), x3);
           }
-          tmem_ld_wait();
-          if (half == 1) {
-            tc_fence_before();
-            mbar_arrive(&bar_tempty[acc]);
-          }
-          // q_h . k = 2^e_h (t1 . k + t2 . k); 2^e_h is folded into w
-          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-          if (sc > 0.f) {  // ReLU(sc d) = sc ReLU(d): one multiply per chunk
 #pragma unroll
-            for (int h = 0; h < 32; h += 4) {
-              x0 = fmaf(wr[h], fmaxf(__uint_as_float(r[h]) + __uint_as_float(u[h]), 0.f), x0);
-              x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1]), 0.f), x1);
-              x2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(r[h + 2]) + __uint_as_float(u[h + 2]), 0.f), x2);
-              x3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(r[h + 3]) + __uint_as_float(u[h + 3]), 0.f), x3);
-            }
-            y += sc * ((x0 + x1) + (x2 + x3));
-          } else {
-#pragma unroll
-            for (int h = 0; h < 32; h += 4) {
-              x0 = fmaf(wr[h], fmaxf(sc * (__uint_as_float(r[h]) + __uint_as_float(u[h])), 0.f), x0);
-              x1 = fmaf(wr[h + 1], fmaxf(sc * (__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1])), 0.f), x1);
-              x2 = fmaf(wr[h + 2], fmaxf(sc * (__uint_as_float(r[h + 2]) + __uint_as_float(u[h + 2])), 0.f), x2);
-              x3 = fmaf(wr[h + 3], fmaxf(sc * (__uint_as_float(r[h + 3]) + __uint_as_float(u[h + 3])), 0.f), x3);
-            }
-            y += (x0 + x1) + (x2 + x3);
+          for (int h = 0; h < 32; h += 4) {
+            x0 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), x0);
+            x1 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), x1);
+            x2 = fmaf(wr[34 + h], fmaxf(__uint_as_float(r1[h + 2]), 0.f), x2);
+            x3 = fmaf(wr[35 + h], fmaxf(__uint_as_float(r1[h + 3]), 0.f), x3);
           }
+          y = sc * ((x0 + x1) + (x2 + x3));
+        } else {
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            x0 = fmaf(wr[h], fmaxf(sc * __uint_as_float(r0[h]), 0.f), x0);
+            x1 = fmaf(wr[h + 1], fmaxf(sc * __uint_as_float(r0[h + 1]), 0.f), x1);
+            x2 = fmaf(wr[h + 2], fmaxf(sc * __uint_as_float(r0[h + 2]), 0.f), x2);
+            x3 = fmaf(wr[h + 3], fmaxf(sc * __uint_as_float(r0[h + 3]), 0.f), x3);
+          }
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            x0 = fmaf(wr[32 + h], fmaxf(sc * __uint_as_float(r1[h]), 0.f), x0);
+            x1 = fmaf(wr[33 + h], fmaxf(sc * __uint_as_float(r1[h + 1]), 0.f), x1);
+            x2 = fmaf(wr[34 + h], fmaxf(sc * __uint_as_float(r1[h + 2]), 0.f), x2);
+            x3 = fmaf(wr[35 + h], fmaxf(sc * __uint_as_float(r1[h + 3]), 0.f), x3);
+          }
+          y = (x0 + x1) + (x2 + x3);
         }
         if (p.logits != nullptr && valid) p.logits[(b * L + l) * p.S + s] = y;
         m = fmaxf(m, y);
-        if (++acc == (uint32_t)kAccBufs) {
-          acc = 0;
+        if (++racc == (uint32_t)kRingAccs) {
+          racc = 0;
           acc_phase ^= 1u;
         }
       }
@@ -305,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && word < words) p.mask[b * words + word] = bits;
       if (p.maxsig != nullptr && valid) p.maxsig[b * p.S + s] = 1.0f / (1.0f + expf(-m));
     }
+    cp_async_wait<0>();  // no copy may still target shared memory when the CTA exits
   }
 
   __syncthreads();
@@ -362,17 +470,20 @@ fm_status launch_memindex_fp8(const Fp8Args& a, int num_sms, unsigned int* statu
   }
   {
     // split query: rows (B*L*128) x 128 B, one box of 128 rows per layer
-    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.B * a.L * kN};
+    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.B * a.L * kQRows};
     const uint64_t strides[1] = {(uint64_t)kDim};
-    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)kN};
+    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)kQRows};
     fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, qsplit, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != FM_OK) return st;
   }
-  const int smem_cap = 227 * 1024;
-  const int fixed = 1024 + a.L * kQLayerBytes;
+  const int smem_cap = 227 * 1024 - 10 * 1024;  // less the kernel's static shared memory
+  const int fixed = 1024 + a.L * kQLayerBytes + kScRingBytes;
   int stages = (smem_cap - fixed) / kTileBytes;
   if (stages > kMaxStages) stages = kMaxStages;
+  static_assert(kMaxStages >= (kPairs - 1) * kMaxL + 1, "stage ring too short for the pairs");
+  if (stages < (kPairs - 1) * kMaxL + 1)
+    return set_error(FM_ERR_UNSUPPORTED, "memindex fp8: %d stages are too few for %d pairs", stages, kPairs);
   const int smem = fixed + stages * kTileBytes;
 
   Params p;

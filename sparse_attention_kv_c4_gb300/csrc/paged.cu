@@ -20,12 +20,13 @@
 //  2. paged_score_kernel (persistent, one CTA per SM): TMA loads two E4M3 pages
 //     (2 x 8 KB, SWIZZLE_128B) per 128-chunk tile straight into the UMMA A
 //     operand -- no conversion pass; tcgen05.mma kind::f8f6f4 M=128 chunks x
-//     N=128 ([t1; t2] for the 64 heads) x K=32, so the key tile is read from
-//     shared memory once.  The producer warp issues a batch of tiles at once
-//     (lane i fills the stage of tile i), four issuing threads and four
-//     epilogue warp groups take tiles in turn.  The epilogue (thread =
-//     chunk) adds the two halves of its 128 dots, applies the chunk's scale,
-//     ReLU and w, and writes y to the workspace.
+//     N=64 heads x K=32, four K steps against t1 and four against t2 into
+//     the same accumulator, so TMEM holds (t1 + t2).k per head.  The
+//     producer warp issues a batch of tiles at once (lane i fills the stage
+//     of tile i), four issuing threads and four epilogue warp groups take
+//     tiles in turn.  The epilogue (thread = chunk) reads its 64 dots, applies
+//     the chunk's scale, ReLU and w (from a per-warp shared-memory copy), and
+//     writes y to the workspace.
 //  3. the block top-k (topk.cuh), mapping candidate i to its chunk id.
 #include <math.h>
 
@@ -50,7 +51,7 @@ constexpr int kMmaWarps = 4;           // UMMA issuers, taking tiles in turn (is
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreads = kFirstEpiWarp * 32 + kEpiGroups * 128;
 constexpr int kAccBufs = 4;
-constexpr int kAccCols = 2 * kHeads;  // t1 dots in columns 0..63, t2 dots in 64..127
+constexpr int kAccCols = kHeads;  // one column per head: the t1 and t2 MMAs accumulate into it
 constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
 constexpr int kPrepThreads = 256;
 
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulator m, so the issuers' barrier waits and commits overlap each
       // other's MMAs.
       const uint32_t me = (uint32_t)(warp - 1);
-      const uint32_t idesc = idesc_e4m3_f32(kM, kAccCols);
+      const uint32_t idesc = idesc_e4m3_f32(kM, kHeads);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0, seq = 0;
       int64_t cur_q = -1;
       int nres = 0;
@@ -365,12 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kAccCols;
-          // descriptor start-address field counts 16-byte units; B = [t1; t2]
-          // (128 rows), so one N=128 MMA per K step reads the key tile once
+          // descriptor start-address field counts 16-byte units; the t2 rows
+          // start 8 KB (eight 1 KB swizzle atoms) after the t1 rows
           const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
+          constexpr uint64_t kT2 = (kHeads * kDim) >> 4;
 #pragma unroll
           for (int k = 0; k < kDim / 32; ++k)
             umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc0 + 2 * k, idesc, k != 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < kDim / 32; ++k) umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc0 + kT2 + 2 * k, idesc, 1u);
           umma_commit(&bar_tfull[acc]);  // also frees the stage: its epilogue releases it
         }
         if (++stage == (uint32_t)stages) {
@@ -393,6 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int group = (warp - kFirstEpiWarp) >> 2;
     const int row = quad * 32 + lane;
+    // one copy of the current query's head weights per epilogue warp, so a
+    // warp refreshes its own copy with __syncwarp alone
+    __shared__ __align__(16) float w_smem[kEpiGroups * 4][kHeads];
+    float* w_mine = w_smem[warp - kFirstEpiWarp];
     uint32_t acc = 0, acc_phase = 0, stage = 0, phase = 0, seq = 0;
     int64_t cur_q = -1;
     int nres = 0;
@@ -406,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qi != cur_q) {
         nres = p.nres_eff[qi];
         cur_q = qi;
+        __syncwarp();
+        for (int i = lane; i < kHeads; i += 32) w_mine[i] = __ldg(p.wq + qi * kHeads + i);
+        __syncwarp();
       }
       if (2 * tile >= nres) continue;
       const bool mine = (seq++ % kEpiGroups) == (uint32_t)group;
@@ -419,43 +430,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = valid ? scale_smem[stage * kM + row] : 0.f;
         mbar_arrive(&bar_empty[stage]);
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kAccCols;
-        const float4* wl = reinterpret_cast<const float4*>(p.wq + qi * kHeads);
+        const float4* wl = reinterpret_cast<const float4*>(w_mine);
         float y = 0.f;
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {  // 16 heads at a time
-          uint32_t r[16], u[16];
-          tmem_ld16(taddr + part * 16, r);
-          tmem_ld16(taddr + kHeads + part * 16, u);
-          float wr[16];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 v = __ldg(wl + part * 4 + i);
-            wr[4 * i] = v.x;
-            wr[4 * i + 1] = v.y;
-            wr[4 * i + 2] = v.z;
-            wr[4 * i + 3] = v.w;
-          }
+        for (int half = 0; half < 2; ++half) {  // 32 heads at a time keeps the thread within 80 registers
+          uint32_t r[32];
+          tmem_ld32(taddr + half * 32, r);
           tmem_ld_wait();
-          if (part == 3) {
+          if (half == 1) {
             tc_fence_before();
-            mbar_arrive(&bar_tempty[acc]);
+            mbar_arrive(&bar_tempty[acc]);  // the dots are in registers: the MMA may reuse the accumulator
           }
-          // q_h . k = 2^e_h (t1 . k + t2 . k); 2^e_h is folded into w
-          float x0 = 0.f, x1 = 0.f;
-          if (sc > 0.f) {
+          // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w
+          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+          if (sc > 0.f) {  // ReLU(sc d) = sc ReLU(d): one multiply per chunk
 #pragma unroll
-            for (int h = 0; h < 16; h += 2) {
-              x0 = fmaf(wr[h], fmaxf(__uint_as_float(r[h]) + __uint_as_float(u[h]), 0.f), x0);
-              x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1]), 0.f), x1);
+            for (int h = 0; h < 32; h += 4) {
+              const float4 wv = wl[half * 8 + h / 4];
+              x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
+              x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
+              x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
+              x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
             }
-            y += sc * (x0 + x1);
+            y += sc * ((x0 + x1) + (x2 + x3));
           } else {
 #pragma unroll
-            for (int h = 0; h < 16; h += 2) {
-              x0 = fmaf(wr[h], fmaxf(sc * (__uint_as_float(r[h]) + __uint_as_float(u[h])), 0.f), x0);
-              x1 = fmaf(wr[h + 1], fmaxf(sc * (__uint_as_float(r[h + 1]) + __uint_as_float(u[h + 1])), 0.f), x1);
+            for (int h = 0; h < 32; h += 4) {
+              const float4 wv = wl[half * 8 + h / 4];
+              x0 = fmaf(wv.x, fmaxf(sc * __uint_as_float(r[h]), 0.f), x0);
+              x1 = fmaf(wv.y, fmaxf(sc * __uint_as_float(r[h + 1]), 0.f), x1);
+              x2 = fmaf(wv.z, fmaxf(sc * __uint_as_float(r[h + 2]), 0.f), x2);
+              x3 = fmaf(wv.w, fmaxf(sc * __uint_as_float(r[h + 3]), 0.f), x3);
             }
-            y += x0 + x1;
+            y += (x0 + x1) + (x2 + x3);
           }
         }
         if constexpr (kMasked) {
@@ -555,7 +562,7 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   }
   const int tiles_per_q = (a.R + 1) / 2;
   const int64_t total = (int64_t)a.Q * tiles_per_q;
-  const int smem_cap = 227 * 1024;
+  const int smem_cap = 227 * 1024 - 6 * 1024;  // less the kernel's static shared memory
   const int fixed = 1024 + kQBytes + kMaxR * 4;
   const int per_stage = kTileBytes + kM * 4;
   int stages = (smem_cap - fixed) / per_stage;

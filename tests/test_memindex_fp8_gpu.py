@@ -30,7 +30,8 @@ def _run(torch, dev, q, w, k8d, scd, S, threshold=0.5, want_logits=True):
     ws = torch.empty(fm.fm_memindex_fp8_workspace(B, L), dtype=torch.uint8, device=dev)
     fm.fm_memindex_score_mask_fp8(qd, wd, k8d, scd, mask, maxsig, logits, threshold=threshold, workspace=ws)
     torch.cuda.synchronize()
-    assert fm.fm_device_status(reset=True) == 0
+    st = fm.fm_device_status(reset=True)
+    assert st == 0, f"device status {st:#x}"
     return (mask.cpu().numpy().view(np.uint32), maxsig.cpu().numpy(),
             None if logits is None else logits.cpu().numpy())
 
