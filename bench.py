@@ -49,7 +49,9 @@ WORKLOAD = ("lsa_c4_indexer_1m: memindex 30x3x262144 bf16 (12% hot) + paged top-
 PROFILE_CASES = {
     # phase: [(profile summary, kernel source files, units in the summary's case, units in the bench step)]
     "memindex": [("memindex_kernel_memindex_1m_b4_l3_s262144.md", ["memindex.cu", "fm_common.cuh"], 4, 30)],
-    "paged_topk": [("paged_score_kernel_paged_1m_q84_r384.md", ["paged.cu", "fm_common.cuh"], 84, 630)],
+    "paged_topk": [("paged_score_kernel_paged_1m_q84_r384.md", ["paged.cu", "fp8.cuh", "fm_common.cuh"], 84, 630)],
+    "memindex_fp8": [("memindex_fp8_kernel_memindex_fp8_1m_b4_l3_s262144.md", ["memindex_fp8.cu", "fp8.cuh", "fm_common.cuh"],
+                      4, 30)],
     "prefill_topk": [("prefill_score_kernel_prefill_t512_s65536.md", ["prefill.cu", "fm_common.cuh"], 512, 4096),
                      ("topk_rows_kernel_prefill_t512_s65536.md", ["topk.cu", "topk.cuh", "fm_common.cuh"], 512, 4096)],
 }
@@ -613,7 +615,8 @@ class Fp8MemIndex:
         mi = self.cfg
         return {"ms": round(ms, 4), "chunk_scores_per_s": mi.chunk_scores / (ms / 1e3), "bound": "hbm",
                 "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                "algorithmic_bytes": self.bytes(), "launches": 2, "reps": reps,
+                "algorithmic_bytes": self.bytes(), "traffic_bytes_est": profiled_traffic("memindex_fp8"),
+                "launches": 2, "reps": reps,
                 "workload": f"memindex fp8 keys {mi.B}x{mi.L}x{mi.S}, E4M3 + per-chunk fp32 scale"}
 
 
