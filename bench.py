@@ -398,8 +398,8 @@ def run_ours(args):
     import sparse_attention_kv_c4_gb300 as fm
     fm.lib()
 
-    if args.only == "memindex_fp8":
-        v = Fp8MemIndex(torch, dev, fm, small=args.small)
+    if args.only in ("memindex_fp8", "paged_full"):
+        v = (Fp8MemIndex if args.only == "memindex_fp8" else FullHistoryPaged)(torch, dev, fm, small=args.small)
         r = v.measure(max(1, args.steps), args.warmup, peaks())
         print(json.dumps({"profile_case": True, "only": args.only, "small": args.small, "ms_per_step": r["ms"],
                           "device_status": fm.fm_device_status(reset=True)}), flush=True)
@@ -538,6 +538,9 @@ def run_ours(args):
         v = Fp8MemIndex(torch, dev, fm)
         variants = {"memindex_fp8": v.measure(10, 3, pk)}
         del v
+        v = FullHistoryPaged(torch, dev, fm)
+        variants["paged_full_history"] = v.measure(10, 3, pk)
+        del v
         if fm.fm_device_status(reset=True) != 0:
             raise RuntimeError("device status flagged an error in the variant rows")
 
@@ -620,6 +623,63 @@ class Fp8MemIndex:
                 "workload": f"memindex fp8 keys {mi.B}x{mi.L}x{mi.S}, E4M3 + per-chunk fp32 scale"}
 
 
+class FullHistoryPaged:
+    """Full-history native top-512 (fm_native_topk_paged with every page
+    listed): 30 requests x 21 layers = 630 queries, each scoring all 4096
+    pages (262144 chunks) of its 1M-token history -- the path without
+    residency that the Memory Indexer's page recall replaces.  21.8 GB of
+    E4M3 keys and scales per call.  Timed on its own after the step."""
+
+    def __init__(self, torch, dev, fm, small=False):
+        import gen
+        self.torch, self.fm = torch, fm
+        cfg = gen.replace(gen.PAGED_FULL_1M, requests=2) if small else gen.PAGED_FULL_1M
+        self.cfg = cfg
+        logical, phys, owner = gen.paged_tables(cfg)
+        q, w = gen.paged_qw(cfg)
+        self.q = torch.from_numpy(q.view(np.int16)).to(dev)
+        self.w = torch.from_numpy(w).to(dev)
+        own_d = torch.from_numpy(owner).to(dev)
+        self.k8 = torch.empty((cfg.P, cfg.page, cfg.d), dtype=torch.uint8, device=dev)
+        self.sc = torch.empty((cfg.P, cfg.page), dtype=torch.float32, device=dev)
+        gen.paged_pool_device(cfg, own_d.data_ptr(), self.k8.data_ptr(), self.sc.data_ptr())
+        del own_d
+        self.phys = torch.from_numpy(phys).to(dev)
+        self.logical = torch.from_numpy(logical).to(dev)
+        self.idx = torch.empty((cfg.Q, cfg.k), dtype=torch.int32, device=dev)
+        self.score = torch.empty((cfg.Q, cfg.k), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(fm.fm_native_topk_paged_workspace(cfg.Q, cfg.R), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        self.fm.fm_native_topk_paged(self.q, self.w, self.k8, self.sc, self.phys, self.logical, self.cfg.k,
+                                     self.idx, self.score, workspace=self.ws)
+
+    def bytes(self):
+        c = self.cfg
+        return c.P * c.page * (c.d + 4) + c.Q * c.R * 8 + c.Q * c.k * 8
+
+    def measure(self, reps, warmup, pk):
+        torch = self.torch
+        for _ in range(warmup):
+            self.call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            self.call()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        ach = self.bytes() / (ms / 1e3) / 1e9
+        c = self.cfg
+        return {"ms": round(ms, 4), "chunk_scores_per_s": c.chunk_scores / (ms / 1e3),
+                "queries_per_s": c.Q / (ms / 1e3), "bound": "hbm", "achieved": round(ach, 2), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "algorithmic_bytes": self.bytes(),
+                "launches": 3, "reps": reps,
+                "workload": f"full-history paged top-{c.k}: {c.Q} queries x {c.R} pages (all of a 1M-token history), E4M3"}
+
+
 def run_profile_case(args, fm, torch, W, cfgs, ws):
     """--only / --small: run a reduced or single-phase case for ncu captures
     (prints the timing as one JSON line marked as a profiling case)."""
@@ -647,7 +707,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the variant rows timed after the step")
-    ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8"], default=None,
+    ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8", "paged_full"], default=None,
                     help="profiling case: run one phase only")
     ap.add_argument("--small", action="store_true", help="profiling case: reduced sizes for ncu captures")
     args = ap.parse_args()

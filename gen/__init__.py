@@ -202,6 +202,10 @@ PAGED_512K = PagedCfg("paged_512k_q1260_r192", requests=60, layers=21, n_pages=2
                       seed=BASE_SEED + 3)
 PAGED_1M = PagedCfg("paged_1m_q630_r384", requests=30, layers=21, n_pages=4096, R=384,
                     seed=BASE_SEED + 4)
+# Full-history native top-512 (the path without residency that LSA is
+# compared against): every one of a 1M-token request's 4096 pages is listed.
+PAGED_FULL_1M = PagedCfg("paged_full_1m_q630_r4096", requests=30, layers=21, n_pages=4096, R=4096,
+                         seed=BASE_SEED + 9)
 PREFILL = PrefillCfg("prefill_t4096_s65536", T=4096, S=65536, pos0=262144, seed=BASE_SEED + 5)
 RECALL_256K = RecallCfg("recall_256k_b76_s65536_k96", B=76, S=65536, kmax=96)
 RECALL_512K = RecallCfg("recall_512k_b60_s131072_k192", B=60, S=131072, kmax=192, seed=BASE_SEED + 7)
@@ -422,7 +426,7 @@ def prefill_host(cfg: PrefillCfg, pos=None):
 
 __all__ = [
     "BASE_SEED", "MemIndexCfg", "PagedCfg", "PrefillCfg", "TINY", "MEMINDEX_256K", "MEMINDEX_1M",
-    "PAGED_512K", "PAGED_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
+    "PAGED_512K", "PAGED_1M", "PAGED_FULL_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
     "memindex_keys_device", "planted", "paged_tables", "paged_qw", "paged_pool_host",
     "paged_chunk_rows", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
 ]

@@ -68,6 +68,7 @@ typedef enum {
 } fm_status;
 
 /* Bits of the device status word (fm_device_status). */
+#define FM_PAGED_MAX_R 4096       /* page-table entries per query of the paged calls     */
 #define FM_DEVERR_PAGE_RANGE 0x1u  /* page_phys outside [0, P): that page was skipped     */
 #define FM_DEVERR_TIMEOUT 0x2u     /* a bounded on-chip wait ran out: the launch gave up  */
 #define FM_DEVERR_DUP_PAGE 0x4u    /* repeated logical page in one query's page table     */
@@ -194,7 +195,9 @@ fm_status fm_page_recall(const uint32_t* mask, int B, int64_t S, int64_t sink, i
  *   page_logical [Q, R] int32 logical page id in [0, 2^25); distinct within
  *                a query (a repeat is flagged FM_DEVERR_DUP_PAGE)
  *   n_res        [Q] int32 entries used per query (clamped to [0, R]), or NULL = R
- *   1 <= R <= 2048, 1 <= k <= 1024, Q >= 0
+ *   1 <= R <= FM_PAGED_MAX_R (4096 pages = 262144 chunks: the whole history
+ *   of a 1M-token request, so the call also serves the full-history native
+ *   top-k that scores every chunk), 1 <= k <= 1024, Q >= 0
  *   idx_out      [Q, k] int32 chunk ids; score_out [Q, k] fp32 or NULL
  *   workspace    >= fm_native_topk_paged_workspace(Q, R) bytes, 256-byte aligned
  */

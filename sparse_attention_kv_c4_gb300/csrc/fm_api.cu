@@ -169,7 +169,7 @@ FM_API fm_status fm_topk_select(const float* scores, int64_t ld, const int32_t* 
 }
 
 FM_API size_t fm_native_topk_paged_workspace(int Q, int R) {
-  if (Q < 0 || R < 1 || R > 2048) return 0;
+  if (Q < 0 || R < 1 || R > FM_PAGED_MAX_R) return 0;
   return paged_workspace_bytes(Q, R);
 }
 
@@ -181,7 +181,7 @@ FM_API fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, cons
                                          size_t workspace_bytes, fm_stream_t stream) {
   if (n_h != 64 || d != 128)
     return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: n_h=%d d=%d (need 64, 128)", n_h, d);
-  if (Q < 0 || R < 1 || R > 2048 || k < 1 || k > 1024 || P < 0 || P > (int64_t(1) << 26))
+  if (Q < 0 || R < 1 || R > FM_PAGED_MAX_R || k < 1 || k > 1024 || P < 0 || P > (int64_t(1) << 26))
     return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: bad sizes Q=%d R=%d k=%d P=%lld", Q, R, k,
                      (long long)P);
   if (id_mode != 0 && id_mode != 1)

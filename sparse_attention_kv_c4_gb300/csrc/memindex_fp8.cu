@@ -18,7 +18,7 @@
 //           (fp8.cuh), 2^e_h folded into w.
 //   warp 0  TMA producer: the request's split q (L x 16 KB) once per request,
 //           then per layer a key tile [128 chunks x 128 B] (SWIZZLE_128B)
-//           into an N-stage ring.
+//           into the stage ring of the pair (below) that takes the tile.
 //   warps 1-2  UMMA issuers: per layer-tile 8 x tcgen05.mma M=128 (chunks)
 //           x N=64 (heads) x K=32: four K steps against the t1 rows, then
 //           four against the t2 rows into the same accumulator, so TMEM holds
@@ -98,7 +98,7 @@ struct Params {
   int64_t total_tiles;
   int tiles_per_b;
   int L;
-  int stages;
+  int stages;  // key stages per pair
   float thr_logit;
 };
 
@@ -129,12 +129,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float w_smem[kEpiGroups * 4][kMaxL * kHeads];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int L = p.L, stages = p.stages;
+  const int L = p.L, ring = p.stages;  // key stages per pair; pair m owns [m * ring, (m + 1) * ring)
   const int64_t t_begin = p.total_tiles * blockIdx.x / gridDim.x;
   const int64_t t_end = p.total_tiles * (blockIdx.x + 1) / gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
+    for (int s = 0; s < kPairs * ring; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
@@ -164,7 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------ TMA producer ------------------------------
-      uint32_t stage = 0, phase = 0, q_phase = 0;
+      // Each pair has its own ring of key stages, filled in the order its
+      // issuer consumes them.  (Key copies may complete out of order: with a
+      // ring shared by both issuers, an issuer could wait on a stage whose
+      // previous fill -- the other issuer's -- is still in flight and pass
+      // its parity wait on that older phase.)
+      uint32_t rstage[kPairs] = {}, rphase[kPairs] = {}, q_phase = 0;
       int issued[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
       int q_issued = -1;
@@ -188,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_issued = (q_issued + 1) & 1;
           cur_b = b;
         }
+        const int m = (int)((t - t_begin) % kPairs);
         for (int l = 0; l < L; ++l) {
+          const uint32_t stage = m * ring + rstage[m], phase = rphase[m];
           if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) {
             ok = false;
             break;
@@ -196,14 +203,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)kTileBytes);
           tma_load_4d(k_smem + stage * kTileBytes, &tmap_k, &bar_full[stage], 0, tile * kM, l, (int32_t)b);
           issued[stage] = (int)phase;
-          if (++stage == (uint32_t)stages) {
-            stage = 0;
-            phase ^= 1u;
+          if (++rstage[m] == (uint32_t)ring) {
+            rstage[m] = 0;
+            rphase[m] ^= 1u;
           }
         }
       }
       if (abort_flag) {  // let copies already in flight land before the CTA exits
-        for (int s = 0; s < stages; ++s)
+        for (int s = 0; s < kPairs * ring; ++s)
           if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
         if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
       }
@@ -211,14 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kFirstEpiWarp) {
     if (lane == 0) {
       // ------------------------------ UMMA issuers ------------------------------
-      // Issuer m takes its pair's tiles (all layers of each), so one issuer's
-      // barrier waits and commits overlap the other's MMAs.  The key stages
-      // are filled in CTA order: an issuer waiting for the stage of a tile has
-      // consumed its previous tile, at most (kPairs - 1) * L + 1 layer-tiles
-      // earlier, so stages >= (kPairs - 1) * kMaxL + 1 keeps that wait exact.
+      // Issuer m takes its pair's tiles (all layers of each) from its pair's
+      // stage ring, so one issuer's barrier waits and commits overlap the
+      // other's MMAs.
       const int me = warp - 1;
       const uint32_t idesc = idesc_e4m3_f32(kM, kHeads);
-      uint32_t stage = 0, phase = 0, racc = 0, acc_phase = 0, q_phase = 0;
+      uint32_t rstage = 0, phase = 0, racc = 0, acc_phase = 0, q_phase = 0;
       int64_t cur_b = -1;
       bool ok = true;
       const uint64_t a_desc0 = sdesc_sw128(smem_u32(k_smem));
@@ -237,16 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           cur_b = b;
         }
-        if ((int)((t - t_begin) % kPairs) != me) {  // the other pair's tile
-          stage += L;
-          if (stage >= (uint32_t)stages) {  // L < stages: at most one wrap
-            stage -= stages;
-            phase ^= 1u;
-          }
-          continue;
-        }
+        if ((int)((t - t_begin) % kPairs) != me) continue;  // the other pair's tile
         for (int l = 0; l < L; ++l) {
           const uint32_t acc = me * kRingAccs + racc;
+          const uint32_t stage = me * ring + rstage;
           if (!mbar_wait(&bar_tempty[acc], acc_phase ^ 1u, &abort_flag, p.status) ||
               !mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) {
             ok = false;
@@ -267,8 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kDim / 32; ++k) umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc + kT2 + 2 * k, idesc, 1u);
           umma_commit(&bar_empty[stage]);
           umma_commit(&bar_tfull[acc]);
-          if (++stage == (uint32_t)stages) {
-            stage = 0;
+          if (++rstage == (uint32_t)ring) {
+            rstage = 0;
             phase ^= 1u;
           }
           if (++racc == (uint32_t)kRingAccs) {
@@ -481,10 +480,9 @@ fm_status launch_memindex_fp8(const Fp8Args& a, int num_sms, unsigned int* statu
   const int fixed = 1024 + a.L * kQLayerBytes + kScRingBytes;
   int stages = (smem_cap - fixed) / kTileBytes;
   if (stages > kMaxStages) stages = kMaxStages;
-  static_assert(kMaxStages >= (kPairs - 1) * kMaxL + 1, "stage ring too short for the pairs");
-  if (stages < (kPairs - 1) * kMaxL + 1)
-    return set_error(FM_ERR_UNSUPPORTED, "memindex fp8: %d stages are too few for %d pairs", stages, kPairs);
-  const int smem = fixed + stages * kTileBytes;
+  const int ring = stages / kPairs;  // each pair's own stage ring
+  if (ring < 2) return set_error(FM_ERR_UNSUPPORTED, "memindex fp8: %d key stages per pair are too few", ring);
+  const int smem = fixed + kPairs * ring * kTileBytes;
 
   Params p;
   p.wq = wq;
@@ -499,7 +497,7 @@ fm_status launch_memindex_fp8(const Fp8Args& a, int num_sms, unsigned int* statu
   p.total_tiles = total;
   p.tiles_per_b = tiles_per_b;
   p.L = a.L;
-  p.stages = stages;
+  p.stages = ring;
   p.thr_logit = a.thr_logit;
   e = cudaFuncSetAttribute(memindex_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "memindex fp8: cudaFuncSetAttribute: %s", cudaGetErrorString(e));

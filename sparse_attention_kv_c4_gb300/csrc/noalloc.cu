@@ -65,7 +65,7 @@ FM_API fm_status fm_native_topk_paged_noalloc(const uint16_t* q, const float* w,
                                               fm_stream_t stream) {
   if (n_h != 64 || d != 128)
     return fm::set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged_noalloc: n_h=%d d=%d (need 64, 128)", n_h, d);
-  if (Q < 0 || R < 1 || R > 2048 || k < 1 || k > 1024 || P < 0 || P > (int64_t(1) << 26))
+  if (Q < 0 || R < 1 || R > FM_PAGED_MAX_R || k < 1 || k > 1024 || P < 0 || P > (int64_t(1) << 26))
     return fm::set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged_noalloc: bad sizes Q=%d R=%d k=%d P=%lld", Q, R,
                          k, (long long)P);
   if (Q == 0) return FM_OK;

@@ -44,7 +44,7 @@ constexpr int kDim = 128;                // bytes per E4M3 key row
 constexpr int kPageBytes = kPage * kDim; // 8 KB
 constexpr int kTileBytes = kM * kDim;    // 16 KB
 constexpr int kQBytes = 2 * kHeads * kDim;  // t1 rows 0..63, t2 rows 64..127
-constexpr int kMaxR = 2048;
+constexpr int kMaxR = FM_PAGED_MAX_R;  // 4096 pages: a 1M-token request's whole history
 constexpr int kMaxStages = 12;
 constexpr int kEpiGroups = 4;          // epilogue warp groups, taking tiles in turn
 constexpr int kMmaWarps = 4;           // UMMA issuers, taking tiles in turn (issuer m owns accumulator m)
@@ -212,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_smem = smem;                       // 16 KB
   uint8_t* a_smem = smem + kQBytes;             // stages x 16 KB
   float* scale_smem = reinterpret_cast<float*>(a_smem + p.stages * kTileBytes);            // stages x 128
-  int32_t* phys_s = reinterpret_cast<int32_t*>(scale_smem + p.stages * kM);                 // kMaxR
 
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[kAccBufs], bar_tempty[kAccBufs], bar_qfull, bar_qempty, bar_drain;
@@ -273,9 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (t < t_end) {
       if (qi != cur_q) {
         nres = p.nres_eff[qi];
-        __syncwarp();
-        for (int i = lane; i < nres; i += 32) phys_s[i] = p.s_phys[qi * p.R + i];
-        __syncwarp();
         cur_q = qi;
         if (nres > 0 && lane == 0) {
           if (q_issued >= 0) {
@@ -305,7 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int npg = nres - 2 * my_tile >= 2 ? 2 : 1;
           mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)(npg * (kPageBytes + kPage * 4)));
           for (int h = 0; h < npg; ++h) {
-            const int32_t ph = phys_s[2 * my_tile + h];
+            // the sorted page table is in the workspace (L2-resident): one
+            // load per page, issued by all lanes of the batch in parallel
+            const int32_t ph = __ldg(p.s_phys + qi * p.R + 2 * my_tile + h);
             tma_load_2d(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0, ph * kPage);
             bulk_load(scale_smem + stage * kM + h * kPage, p.k_scale + (int64_t)ph * kPage, kPage * 4,
                       &bar_full[stage]);
@@ -563,10 +561,18 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   const int tiles_per_q = (a.R + 1) / 2;
   const int64_t total = (int64_t)a.Q * tiles_per_q;
   const int smem_cap = 227 * 1024 - 6 * 1024;  // less the kernel's static shared memory
-  const int fixed = 1024 + kQBytes + kMaxR * 4;
+  const int fixed = 1024 + kQBytes;
   const int per_stage = kTileBytes + kM * 4;
   int stages = (smem_cap - fixed) / per_stage;
   if (stages > kMaxStages) stages = kMaxStages;
+  // Tile i uses stage i % stages and is consumed by issuer / epilogue group
+  // i % 4.  With stages a multiple of 4 every stage has a single consumer, so
+  // a consumer's parity wait on a stage's full barrier can only see that
+  // stage's previous fill completed (it consumed that fill itself).  Key
+  // copies may complete out of order; with another consumer's fill as the
+  // previous use, a wait could pass on the previous phase while that fill is
+  // still in flight.
+  stages -= stages % kMmaWarps;
   const int smem = fixed + stages * per_stage;
 
   ScoreParams p;

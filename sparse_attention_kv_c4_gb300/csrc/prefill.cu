@@ -341,6 +341,11 @@ fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status
     const int fixed = 1024 + kQBytes;
     int stages = (smem_cap - fixed) / kTileBytes;
     if (stages > kMaxStages) stages = kMaxStages;
+    // tile i uses stage i % stages and issuer i % 2: with an even stage count
+    // each stage has one consumer, whose parity wait on the stage's full
+    // barrier then cannot pass on a previous fill still in flight (key copies
+    // may complete out of order)
+    stages -= stages % kMmaWarps;
     const int smem = fixed + stages * kTileBytes;
     Params p;
     p.w = a.w;

@@ -94,3 +94,14 @@ def test_topk_workspace_size_contract(lib):
     lib.fm_topk_workspace.restype = ctypes.c_size_t
     for rows, n in ((8, 4096), (8, 65536), (0, 65536), (4096, 131073)):
         assert lib.fm_topk_workspace(rows, n) == 0
+
+
+def test_paged_workspace_accepts_a_whole_1m_history(lib):
+    """Page tables of up to 4096 entries (a 1M-token request's every page) are
+    accepted; one more is rejected (size 0)."""
+    lib.fm_native_topk_paged_workspace.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.fm_native_topk_paged_workspace.restype = ctypes.c_size_t
+    ws = lib.fm_native_topk_paged_workspace(630, 4096)
+    assert ws >= 630 * 4096 * 64 * 4  # the score rows alone
+    assert lib.fm_native_topk_paged_workspace(630, 4097) == 0
+    assert lib.fm_native_topk_paged_workspace(1, 0) == 0

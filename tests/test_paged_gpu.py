@@ -160,3 +160,43 @@ def test_paged_full_size_sampled(torch_dev, orc, cfg):
         sub_phys = np.arange(cfg.R, dtype=np.int32)[None, :]
         check_rows(orc, q[qi:qi + 1], w[qi:qi + 1], k8s, scs, sub_phys, logical[qi:qi + 1], idx[qi:qi + 1],
                    sc[qi:qi + 1], cfg.k)
+
+
+def test_paged_full_history_whole_rows(torch_dev, orc):
+    """Full-history scoring: every page of a 4096-page (1M-token) history is
+    listed, in a shuffled table order; each query's 262144 chunks are all
+    candidates and the whole rows are compared with the oracle."""
+    torch, dev = torch_dev
+    cfg, q, w, k8, scale, phys, logical = small_case(gen.BASE_SEED + 910, requests=1, layers=2, n_pages=4096,
+                                                     R=4096)
+    assert sorted(logical[0].tolist()) == list(range(4096))
+    idx, sc, status = run_paged(torch, dev, q, w, k8, scale, phys, logical, 512)
+    assert status == 0
+    check_rows(orc, q, w, k8, scale, phys, logical, idx, sc, 512)
+
+
+def test_paged_full_history_1m_sampled(torch_dev, orc):
+    """The full-history configuration at full size (630 queries x 4096 pages,
+    21.8 GB pool filled on the device); sampled queries recomputed by the
+    oracle over all 262144 of their chunks."""
+    torch, dev = torch_dev
+    cfg = gen.PAGED_FULL_1M
+    logical, phys, owner = gen.paged_tables(cfg)
+    q, w = gen.paged_qw(cfg)
+    own_d = torch.from_numpy(owner).to(dev)
+    k8d = torch.empty((cfg.P, cfg.page, cfg.d), dtype=torch.uint8, device=dev)
+    scd = torch.empty((cfg.P, cfg.page), dtype=torch.float32, device=dev)
+    gen.paged_pool_device(cfg, own_d.data_ptr(), k8d.data_ptr(), scd.data_ptr())
+    idx, sc, status = run_paged(torch, dev, q, w, None, None, phys, logical, cfg.k, pool_dev=(k8d, scd))
+    assert status == 0
+    del k8d, scd, own_d
+    torch.cuda.empty_cache()
+    rng = np.random.default_rng(cfg.seed)
+    for qi in rng.choice(cfg.Q, size=2, replace=False):
+        a, b = qi // cfg.layers, qi % cfg.layers
+        k8s, scs = gen.paged_chunk_rows(cfg, a, b, np.arange(cfg.n_pages * cfg.page))
+        k8s = k8s.reshape(cfg.n_pages, cfg.page, cfg.d)
+        scs = scs.reshape(cfg.n_pages, cfg.page)
+        # logical page j sits in local pool page j
+        check_rows(orc, q[qi:qi + 1], w[qi:qi + 1], k8s, scs, logical[qi:qi + 1], logical[qi:qi + 1],
+                   idx[qi:qi + 1], sc[qi:qi + 1], cfg.k)
