@@ -59,7 +59,10 @@ constexpr int kPrepThreads = 256;
 // 1. prep: sort pages, validate, split q
 // --------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kPrepThreads)
+// THREADS: 256, or 1024 for tables longer than 1024 entries (the bitonic
+// sort's passes then take four elements per thread instead of sixteen).
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
     paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                       const int32_t* __restrict__ page_phys, const int32_t* __restrict__ page_logical,
                       const int32_t* __restrict__ n_res, int R, int64_t P, int Rpow2,
@@ -69,20 +72,20 @@ __global__ void __launch_bounds__(kPrepThreads)
                       unsigned long long* __restrict__ pmask, int32_t* __restrict__ pprefix,
                       uint8_t* __restrict__ qsplit, float* __restrict__ wq, unsigned int* __restrict__ status) {
   __shared__ unsigned long long keys[kMaxR];
-  __shared__ uint32_t warp_tot[kPrepThreads / 32];
+  __shared__ uint32_t warp_tot[THREADS / 32];
   const int qi = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int nr = R;
   if (n_res != nullptr) {
     const int v = n_res[qi];
     nr = v < 0 ? 0 : (v > R ? R : v);
   }
-  for (int i = tid; i < Rpow2; i += kPrepThreads)
+  for (int i = tid; i < Rpow2; i += THREADS)
     keys[i] = i < nr ? (((unsigned long long)(uint32_t)page_logical[(int64_t)qi * R + i] << 32) | (uint32_t)i)
                      : ~0ull;
   __syncthreads();
   for (int k2 = 2; k2 <= Rpow2; k2 <<= 1)
     for (int j = k2 >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < Rpow2; i += kPrepThreads) {
+      for (int i = tid; i < Rpow2; i += THREADS) {
         const int ixj = i ^ j;
         if (ixj > i) {
           const unsigned long long a = keys[i], b = keys[ixj];
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(kPrepThreads)
       __syncthreads();
     }
   uint32_t base = 0;
-  for (int i0 = 0; i0 < Rpow2; i0 += kPrepThreads) {
+  for (int i0 = 0; i0 < Rpow2; i0 += THREADS) {
     const int i = i0 + tid;
     uint32_t valid = 0;
     int32_t lg = 0, ph = 0;
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     if (lane == 31) warp_tot[warp] = x;
     __syncthreads();
     uint32_t before = 0, total = 0;
-    for (int wi = 0; wi < kPrepThreads / 32; ++wi) {
+    for (int wi = 0; wi < THREADS / 32; ++wi) {
       if (wi < warp) before += warp_tot[wi];
       total += warp_tot[wi];
     }
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     // past the listed ones get an empty mask and the final count.
     const uint32_t* mrow = res_mask + (int64_t)(qi / mask_group) * mask_ld;
     uint32_t run = 0;
-    for (int j0 = 0; j0 < R; j0 += kPrepThreads) {
+    for (int j0 = 0; j0 < R; j0 += THREADS) {
       const int j = j0 + tid;
       unsigned long long m = 0ull;
       if (j < (int)base) {
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kPrepThreads)
       if (lane == 31) warp_tot[warp] = x;
       __syncthreads();
       uint32_t before = 0, total = 0;
-      for (int wi = 0; wi < kPrepThreads / 32; ++wi) {
+      for (int wi = 0; wi < THREADS / 32; ++wi) {
         if (wi < warp) before += warp_tot[wi];
         total += warp_tot[wi];
       }
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
   // q split: q_h = 2^e_h (t1 + t2), 2^e_h folded into w
   uint8_t* t1 = qsplit + (int64_t)qi * 2 * kHeads * kDim;
-  split_query(q + (int64_t)qi * kHeads * kDim, w + (int64_t)qi * kHeads, kHeads, kPrepThreads, t1,
+  split_query(q + (int64_t)qi * kHeads * kDim, w + (int64_t)qi * kHeads, kHeads, THREADS, t1,
               t1 + (int64_t)kHeads * kDim, wq + (int64_t)qi * kHeads);
 }
 
@@ -534,7 +537,8 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   PagedWs ws = paged_ws_layout(a.workspace, a.Q, a.R);
   int Rpow2 = 1;
   while (Rpow2 < a.R) Rpow2 <<= 1;
-  paged_prep_kernel<<<a.Q, kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
+  auto prep = a.R > 1024 ? paged_prep_kernel<1024> : paged_prep_kernel<kPrepThreads>;
+  prep<<<a.Q, a.R > 1024 ? 1024 : kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
                                                       Rpow2, a.res_mask, a.mask_ld, a.mask_group, ws.s_logical,
                                                       ws.s_phys, ws.nres_eff, ws.n_valid, ws.pmask, ws.pprefix,
                                                       ws.qsplit, ws.wq, status);

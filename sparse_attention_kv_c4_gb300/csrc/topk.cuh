@@ -77,9 +77,7 @@ FM_DEV void block_topk_radix(const float* __restrict__ row, int n, int k, IdxMap
           key = float_key(__ldg(row + i));
           act = (key & pmask) == prefix;
         }
-        const uint32_t digit = act ? ((key >> shift) & 0xFFu) : (0x100u + (uint32_t)lane);
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (act && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], (uint32_t)__popc(peers));
+        if (act) atomicAdd(&sm.hist[(key >> shift) & 0xFFu], 1u);
       }
       __syncthreads();
       if (tid < 32) {
@@ -203,6 +201,7 @@ struct TopkFastSmem {
   unsigned long long cmax;
   union {
     unsigned long long sample[kTopkSample];
+    uint32_t sample32[2 * kTopkSample];  // rows longer than kTopkBitmapN: twice the sample, keys only
     unsigned long long sel[1024];
     uint32_t bitmap[kTopkBitmapN / 32];
   } u;
@@ -239,8 +238,8 @@ FM_DEV int next_pow2(int x) {
   return p;
 }
 
-// Radix select of the r-th largest (1 <= r <= n) of the distinct values
-// a[0..n) in shared memory, all of which lie in [lo, hi]: 8-bit digits, most
+// Radix select of the r-th largest (1 <= r <= n) of the values a[0..n)
+// (32- or 64-bit) in shared memory, all of which lie in [lo, hi]: 8-bit digits, most
 // significant first, starting at the highest bit where lo and hi differ (the
 // bits above it are common to every value, so they need no pass).  It stops
 // once the deciding digit holds exactly the remaining need (then the result T
@@ -249,14 +248,14 @@ FM_DEV int next_pow2(int x) {
 // shared-memory atomics (cheaper here than aggregating them per warp with
 // __match_any_sync); the two histograms alternate so that each digit costs two
 // block barriers.  All threads call it.
-template <int THREADS>
-FM_DEV unsigned long long block_select_u64(const unsigned long long* a, int n, int r, unsigned long long lo,
-                                           unsigned long long hi, uint32_t loose, SelectSmem<THREADS>& sm) {
+template <int THREADS, typename T>
+FM_DEV T block_select(const T* a, int n, int r, T lo, T hi, uint32_t loose, SelectSmem<THREADS>& sm) {
+  constexpr int kBits = 8 * (int)sizeof(T);
   const int tid = threadIdx.x, lane = tid & 31;
   if (lo == hi) return lo;
-  const int hb = 63 - __clzll((long long)(lo ^ hi));
-  unsigned long long pmask = hb == 63 ? 0ull : (~0ull << (hb + 1));
-  unsigned long long prefix = lo & pmask;
+  const int hb = kBits == 64 ? 63 - __clzll((long long)(lo ^ hi)) : 31 - __clz((int)(lo ^ hi));
+  T pmask = hb == kBits - 1 ? T(0) : (~T(0) << (hb + 1));
+  T prefix = lo & pmask;
   uint32_t need = (uint32_t)r;
   for (int i = tid; i < 256; i += THREADS) sm.hist[0][i] = 0u;
   __syncthreads();
@@ -266,7 +265,7 @@ FM_DEV unsigned long long block_select_u64(const unsigned long long* a, int n, i
     uint32_t* hist = sm.hist[b];
     for (int i = tid; i < 256; i += THREADS) sm.hist[b ^ 1][i] = 0u;  // for the next digit
     for (int i = tid; i < n; i += THREADS) {
-      const unsigned long long v = a[i];
+      const T v = a[i];
       if ((v & pmask) == prefix) atomicAdd(&hist[(uint32_t)(v >> shift) & 0xFFu], 1u);
     }
     __syncthreads();
@@ -302,8 +301,8 @@ FM_DEV unsigned long long block_select_u64(const unsigned long long* a, int n, i
     __syncthreads();
     const uint32_t d = sm.digit[b], in_digit = sm.in_digit[b];
     need -= sm.above[b];
-    prefix |= (unsigned long long)d << shift;  // bits already decided agree with d
-    pmask |= 0xFFull << shift;
+    prefix |= (T)d << shift;  // bits already decided agree with d
+    pmask |= (T)0xFFu << shift;
     if (shift == 0 || in_digit == need || in_digit <= loose) break;
   }
   return prefix;
@@ -324,16 +323,34 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   // ---- 1. threshold from a sample --------------------------------------------
   unsigned long long theta = 0ull;
   if (n > kTopkCap) {
-    for (int i = tid; i < kTopkSample; i += THREADS) {
-      const int run = i >> 6, off = i & 63;
-      const int j = (int)(((long long)run * (n - 64)) / (kTopkRuns - 1)) + off;
-      sm.u.sample[i] = ((unsigned long long)float_key(__ldg(row + j)) << 32) | (uint32_t)(~(uint32_t)j);
-    }
-    __syncthreads();
     const long long want = 3 * kk < 2 * kTopkCap / 3 ? 3 * kk : 2 * kTopkCap / 3;  // expected candidates
-    int r = (int)((want * kTopkSample) / (long long)n);
-    r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
-    theta = block_select_u64<THREADS>(sm.u.sample, kTopkSample, r, 0ull, ~0ull, 4u, sm.sel);
+    if (n <= kTopkBitmapN) {
+      for (int i = tid; i < kTopkSample; i += THREADS) {
+        const int run = i >> 6, off = i & 63;
+        const int j = (int)(((long long)run * (n - 64)) / (kTopkRuns - 1)) + off;
+        sm.u.sample[i] = ((unsigned long long)float_key(__ldg(row + j)) << 32) | (uint32_t)(~(uint32_t)j);
+      }
+      __syncthreads();
+      int r = (int)((want * kTopkSample) / (long long)n);
+      r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
+      theta = block_select<THREADS>(sm.u.sample, kTopkSample, r, 0ull, ~0ull, 4u, sm.sel);
+    } else {
+      // Long rows (a whole 1M-token history is 262144 scores): with 2048
+      // samples only ~12 would lie above the threshold and about one row in
+      // a thousand would fall short of k candidates.  Twice the sample as
+      // plain 32-bit keys (same shared memory) keeps ~24 above it; the
+      // threshold then admits every score >= the sampled key (ties at it
+      // are not split by index).
+      for (int i = tid; i < 2 * kTopkSample; i += THREADS) {
+        const int run = i >> 6, off = i & 63;
+        const int j = (int)(((long long)run * (n - 64)) / (2 * kTopkRuns - 1)) + off;
+        sm.u.sample32[i] = float_key(__ldg(row + j));
+      }
+      __syncthreads();
+      int r = (int)((want * 2 * kTopkSample) / (long long)n);
+      r = r < 1 ? 1 : (r > 2 * kTopkSample ? 2 * kTopkSample : r);
+      theta = (unsigned long long)block_select<THREADS>(sm.u.sample32, 2 * kTopkSample, r, 0u, ~0u, 4u, sm.sel) << 32;
+    }
   }
   // the sample is dead from here: its space becomes the (cleared) bitmap
   if (n <= kTopkBitmapN) {
@@ -450,7 +467,7 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   }
   // ---- 3. exact select among the candidates -------------------------------------
   // every candidate lies in [theta, cmax]
-  const unsigned long long T = block_select_u64<THREADS>(sm.cand, cnt, kk, theta, sm.cmax, 0u, sm.sel);
+  const unsigned long long T = block_select<THREADS>(sm.cand, cnt, kk, theta, sm.cmax, 0u, sm.sel);
   // ---- 4. emit in index order -------------------------------------------------
   if (n <= kTopkBitmapN) {
     const int words = (n + 31) >> 5;
