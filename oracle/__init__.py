@@ -70,6 +70,8 @@ class Oracle:
         lib.orc_memindex_logits_fp8.argtypes = [u16p, f32p, u8p, f32p, I64, I64, I64, I64, I64, I64, I64, I32, I32,
                                                 f64p]
         lib.orc_memindex_select.argtypes = [f64p, I64, I64, I64, D, u32p, f64p]
+        lib.orc_unpack_compressed_k.argtypes = [u8p, I64, I32, u8p, f32p]
+        lib.orc_memindex_ensemble.argtypes = [f64p, I64, I64, I64, I32, D, u32p, f64p]
         lib.orc_topk.argtypes = [i64p, f64p, I64, I32, i32p, f64p]
         lib.orc_topk.restype = ctypes.c_int
         lib.orc_paged_topk.argtypes = [u16p, f32p, u8p, f32p, i32p, i32p, i32p, I64, I64, I32, I32, I32,
@@ -138,6 +140,26 @@ class Oracle:
         maxsig = np.empty((B, S), dtype=np.float64)
         self.lib.orc_memindex_select(_p(x, f64p), B, L, S, float(thr), _p(mask, u32p), _p(maxsig, f64p))
         return mask, maxsig
+
+    def unpack_compressed_k(self, ck):
+        """ck [..., d + 4] uint8 packed rows -> k8 [..., d] uint8, scale [...] fp32."""
+        ck = _c(ck, np.uint8)
+        d = ck.shape[-1] - 4
+        n = ck.size // (d + 4)
+        k8 = np.empty(ck.shape[:-1] + (d,), dtype=np.uint8)
+        sc = np.empty(ck.shape[:-1], dtype=np.float32)
+        self.lib.orc_unpack_compressed_k(_p(ck, u8p), n, d, _p(k8, u8p), _p(sc, f32p))
+        return k8, sc
+
+    def memindex_ensemble(self, x, mode: int = 0, thr: float = 0.5):
+        """x [B,L,S] -> mask [B, ceil(S/32)] uint32, ensembled score [B,S] fp64
+        (mode 0: max over layers, mode 1: mean over layers of the sigmoids)."""
+        x = _c(x, np.float64)
+        B, L, S = x.shape
+        mask = np.empty((B, (S + 31) // 32), dtype=np.uint32)
+        ens = np.empty((B, S), dtype=np.float64)
+        self.lib.orc_memindex_ensemble(_p(x, f64p), B, L, S, int(mode), float(thr), _p(mask, u32p), _p(ens, f64p))
+        return mask, ens
 
     # -- top-k -------------------------------------------------------------------
     def topk(self, ids, x, k: int = 512):

@@ -166,6 +166,45 @@ ORC_API void orc_memindex_select(const double* x, int64_t B, int64_t L, int64_t 
     }
 }
 
+/* The retriever's packed compressed_k rows ([RM] "compressed_k format"): a
+ * chunk is d + 4 bytes, bytes [0, d) its E4M3 key and bytes [d, d + 4) its
+ * fp32 dequant scale, read in the machine's byte order as a tensor view of
+ * those bytes reads it.  Splits n packed rows into k8 [n][d] and scale [n]. */
+ORC_API void orc_unpack_compressed_k(const uint8_t* ck, int64_t n, int d, uint8_t* k8_out, float* scale_out) {
+  for (int64_t i = 0; i < n; ++i) {
+    const uint8_t* row = ck + (size_t)i * (size_t)(d + 4);
+    memcpy(k8_out + (size_t)i * (size_t)d, row, (size_t)d);
+    memcpy(&scale_out[i], row + d, sizeof(float));
+  }
+}
+
+/* [RM] "Joint checkpoint + ensemble": the per-layer sigmoid scores of a chunk
+ * are ensembled -- mode 0: max (the union, the default), mode 1: mean -- into
+ * one score e[b][s]; the chunk is resident iff e >= thr.  The mean sums the
+ * L sigmoids in layer order and divides by L. */
+ORC_API void orc_memindex_ensemble(const double* x, int64_t B, int64_t L, int64_t S, int mode, double thr,
+                                   uint32_t* mask, double* ens) {
+  int64_t words = (S + 31) / 32;
+  memset(mask, 0, sizeof(uint32_t) * (size_t)(B * words));
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t s = 0; s < S; ++s) {
+      double e;
+      if (mode == 0) {
+        e = -1.0;
+        for (int64_t l = 0; l < L; ++l) {
+          double sig = orc_sigmoid(x[((size_t)b * L + l) * S + s]);
+          if (sig > e) e = sig;
+        }
+      } else {
+        double sum = 0.0;
+        for (int64_t l = 0; l < L; ++l) sum += orc_sigmoid(x[((size_t)b * L + l) * S + s]);
+        e = sum / (double)L;
+      }
+      if (e >= thr) mask[b * words + (s >> 5)] |= 1u << (s & 31);
+      if (ens) ens[b * S + s] = e;
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Top-k select                                                               */
 /* ------------------------------------------------------------------------- */

@@ -444,6 +444,70 @@ def pin_memindex_fp8_equals_bf16_on_exact_keys(orc):
                 assert xs[b, l, s] == orc.score_bf16(q[b, l], w[b, l], kk), (b, l, s)
 
 
+def pin_unpack_compressed_k(orc):
+    """[RM] "compressed_k format": a chunk is 132 bytes, [:128] E4M3 codes and
+    [128:132] an fp32 scale.  Rows built field by field with a numpy record
+    type (an independent construction) unpack to their fields; IEEE-754
+    binary32 fixes 1.0 as bytes 00 00 80 3f and -2.5 as 00 00 20 c0 in
+    little-endian order."""
+    rng = np.random.default_rng(41)
+    n, d = 37, 128
+    rec = np.zeros(n, dtype=np.dtype([("k", np.uint8, (d,)), ("s", "<f4")]))
+    assert rec.dtype.itemsize == d + 4
+    rec["k"] = rng.integers(0, 256, (n, d))
+    rec["s"] = rng.standard_normal(n).astype(np.float32)
+    rec["s"][0], rec["s"][1] = 1.0, -2.5
+    ck = rec.view(np.uint8).reshape(n, d + 4)
+    assert list(ck[0, d:]) == [0x00, 0x00, 0x80, 0x3F] and list(ck[1, d:]) == [0x00, 0x00, 0x20, 0xC0]
+    k8, sc = orc.unpack_compressed_k(ck)
+    assert np.array_equal(k8, rec["k"]) and np.array_equal(sc.view(np.uint32), rec["s"].view(np.uint32))
+    # a [B, L, S, 132] block unpacks row by row
+    k8b, scb = orc.unpack_compressed_k(ck[:36].reshape(2, 3, 6, d + 4))
+    assert k8b.shape == (2, 3, 6, d) and np.array_equal(k8b.reshape(36, d), rec["k"][:36])
+    assert np.array_equal(scb.reshape(36), rec["s"][:36])
+
+
+def pin_ensemble_closed_forms(orc):
+    """[RM] "Joint checkpoint + ensemble": max (the union) or mean of the
+    per-layer sigmoid scores.  sigma(0) = 1/2 and sigma(ln 3) = 3/4, so layers
+    with logits (0, ln 3) ensemble to 3/4 by max and 5/8 by mean (the sigmoid
+    of the mean logit would be 0.634); sigma(a) + sigma(-a) = 1 gives a mean
+    of 1/2 for (a, -a); an ensembled score equal to the threshold is resident
+    (the threshold test is inclusive); one layer makes both modes sigma(x); the max mode is
+    the union rule; the mean lies between the smallest and largest layer
+    score and does not depend on layer order."""
+    x = np.array([[[0.0], [math.log(3.0)]]])  # B=1, L=2, S=1
+    _, emax = orc.memindex_ensemble(x, 0)
+    _, emean = orc.memindex_ensemble(x, 1)
+    assert abs(emax[0, 0] - 0.75) < 1e-15 and abs(emean[0, 0] - 0.625) < 1e-15, (emax, emean)
+    for thr, want in ((0.62, 1), (0.63, 0)):
+        m, _ = orc.memindex_ensemble(x, 1, thr)
+        assert int(m[0, 0]) & 1 == want
+    z = np.zeros((1, 2, 3))  # sigma(0) = 1/2 exactly: the inclusive threshold keeps it
+    for mode in (0, 1):
+        m, e = orc.memindex_ensemble(z, mode, 0.5)
+        assert np.all(e == 0.5) and int(m[0, 0]) == 0b111, (mode, e, m)
+    a = np.array([[[7.25, -3.0], [-7.25, 3.0]]])
+    _, e = orc.memindex_ensemble(a, 1)
+    assert np.all(np.abs(e - 0.5) < 1e-15)
+    rng = np.random.default_rng(43)
+    x1 = rng.normal(0, 3, (2, 1, 50))
+    for mode in (0, 1):
+        _, e1 = orc.memindex_ensemble(x1, mode)
+        assert np.all(np.abs(e1 - 1 / (1 + np.exp(-x1[:, 0]))) < 1e-15)
+    xr = rng.normal(0, 3, (3, 4, 77))
+    m0, e0 = orc.memindex_ensemble(xr, 0, 0.6)
+    ms, es = orc.memindex_select(xr, 0.6)
+    assert np.array_equal(m0, ms) and np.array_equal(e0, es)
+    m1, e1 = orc.memindex_ensemble(xr, 1, 0.6)
+    sig = 1 / (1 + np.exp(-xr))
+    assert np.all(e1 <= sig.max(axis=1) + 1e-15) and np.all(e1 >= sig.min(axis=1) - 1e-15)
+    m2, e2 = orc.memindex_ensemble(xr[:, ::-1], 1, 0.6)
+    assert np.allclose(e2, e1, rtol=0, atol=1e-15)
+    bits = np.unpackbits(m1.view(np.uint8), bitorder="little").reshape(3, -1)[:, :77].astype(bool)
+    assert np.array_equal(bits, e1 >= 0.6)
+
+
 # ---------------------------------------------------------------------------
 # page recall (densest resident pages)
 # ---------------------------------------------------------------------------

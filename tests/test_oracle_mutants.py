@@ -30,7 +30,10 @@ MUTANTS = {
     "threshold_strict": ("if (best >= thr)", "if (best > thr)"),
     "union_by_min": ("if (sig > best) best = sig;", "if (l == 0 || sig < best) best = sig;"),
     "sigmoid_sign": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));"),
-    "mask_bit_reversed": ("|= 1u << (s & 31);", "|= 1u << (31 - (s & 31));"),
+    "mask_bit_reversed": ("if (best >= thr) mask[b * words + (s >> 5)] |= 1u << (s & 31);",
+                          "if (best >= thr) mask[b * words + (s >> 5)] |= 1u << (31 - (s & 31));"),
+    "ensemble_mask_bit_reversed": ("if (e >= thr) mask[b * words + (s >> 5)] |= 1u << (s & 31);",
+                                   "if (e >= thr) mask[b * words + (s >> 5)] |= 1u << (31 - (s & 31));"),
     "tie_higher_id_first": ("return a->id < b->id ? -1 : 1;", "return a->id > b->id ? -1 : 1;"),
     "rank_ascending": ("if (xa > xb) return -1;\n  if (xa < xb) return 1;",
                        "if (xa < xb) return -1;\n  if (xa > xb) return 1;"),
@@ -67,6 +70,16 @@ MUTANTS = {
     "recall_sink_long": ("if (s < sink || s >= S - recent) resident = 1;",
                          "if (s <= sink || s >= S - recent) resident = 1;"),
     "recall_partial_page_overrun": ("s < (p + 1) * page_size && s < S; ++s)", "s < (p + 1) * page_size; ++s)"),
+    "ensemble_sigmoid_of_mean_logit": (
+        "for (int64_t l = 0; l < L; ++l) sum += orc_sigmoid(x[((size_t)b * L + l) * S + s]);\n        e = sum / (double)L;",
+        "for (int64_t l = 0; l < L; ++l) sum += x[((size_t)b * L + l) * S + s];\n        e = orc_sigmoid(sum / (double)L);"),
+    "ensemble_mode_ignored": ("      if (mode == 0) {\n        e = -1.0;", "      if (1) {\n        e = -1.0;"),
+    "ensemble_sum_not_mean": ("e = sum / (double)L;", "e = sum;"),
+    "ensemble_threshold_strict": ("if (e >= thr) mask", "if (e > thr) mask"),
+    "unpack_scale_offset": ("memcpy(&scale_out[i], row + d, sizeof(float));",
+                            "memcpy(&scale_out[i], row + d - 4, sizeof(float));"),
+    "unpack_row_stride_d": ("const uint8_t* row = ck + (size_t)i * (size_t)(d + 4);",
+                            "const uint8_t* row = ck + (size_t)i * (size_t)d;"),
     "recall_bit_reversed": ("int resident = (mask[b * words + (s >> 5)] >> (s & 31)) & 1u;",
                             "int resident = (mask[b * words + (s >> 5)] >> (31 - (s & 31))) & 1u;"),
 }
