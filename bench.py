@@ -398,8 +398,9 @@ def run_ours(args):
     import sparse_attention_kv_c4_gb300 as fm
     fm.lib()
 
-    if args.only in ("memindex_fp8", "paged_full"):
-        v = (Fp8MemIndex if args.only == "memindex_fp8" else FullHistoryPaged)(torch, dev, fm, small=args.small)
+    if args.only in ("memindex_fp8", "paged_full", "retriever"):
+        v = {"memindex_fp8": Fp8MemIndex, "paged_full": FullHistoryPaged,
+             "retriever": RetrieverMemIndex}[args.only](torch, dev, fm, small=args.small)
         r = v.measure(max(1, args.steps), args.warmup, peaks())
         print(json.dumps({"profile_case": True, "only": args.only, "small": args.small, "ms_per_step": r["ms"],
                           "device_status": fm.fm_device_status(reset=True)}), flush=True)
@@ -541,6 +542,10 @@ def run_ours(args):
         v = FullHistoryPaged(torch, dev, fm)
         variants["paged_full_history"] = v.measure(10, 3, pk)
         del v
+        for mode, name in ((0, "retriever_max"), (1, "retriever_mean")):
+            v = RetrieverMemIndex(torch, dev, fm, mode=mode)
+            variants[name] = v.measure(10, 3, pk)
+            del v
         if fm.fm_device_status(reset=True) != 0:
             raise RuntimeError("device status flagged an error in the variant rows")
 
@@ -621,6 +626,62 @@ class Fp8MemIndex:
                 "algorithmic_bytes": self.bytes(), "traffic_bytes_est": profiled_traffic("memindex_fp8"),
                 "launches": 2, "reps": reps,
                 "workload": f"memindex fp8 keys {mi.B}x{mi.L}x{mi.S}, E4M3 + per-chunk fp32 scale"}
+
+
+class RetrieverMemIndex:
+    """The trained retriever's Memory Indexer (fm_retriever_score_mask): the
+    1M workload's 30 requests x 3 layers x 262144 chunks, 128 heads, keys in
+    packed 132-byte compressed_k rows (3.1 GB per call), max or mean layer
+    ensemble.  Timed on its own after the step."""
+
+    def __init__(self, torch, dev, fm, small=False, mode=0):
+        import gen
+        self.torch, self.fm, self.mode = torch, fm, mode
+        cfg = gen.replace(gen.RETRIEVER_1M, B=4) if small else gen.RETRIEVER_1M
+        self.cfg = cfg
+        q, w, hot = gen.memindex_qw(cfg)
+        self.q = torch.from_numpy(q.view(np.int16)).to(dev)
+        self.w = torch.from_numpy(w).to(dev)
+        hot_d = torch.from_numpy(hot).to(dev)
+        own_d = torch.from_numpy(gen.memindex_fp8_owner(cfg)).to(dev)
+        k8 = torch.empty((cfg.B, cfg.L, cfg.S, cfg.d), dtype=torch.uint8, device=dev)
+        sc = torch.empty((cfg.B, cfg.L, cfg.S), dtype=torch.float32, device=dev)
+        gen.memindex_fp8_keys_device(cfg, hot_d.data_ptr(), own_d.data_ptr(), k8.data_ptr(), sc.data_ptr())
+        self.ck = torch.cat([k8, sc.view(torch.uint8).view(cfg.B, cfg.L, cfg.S, 4)], dim=-1)
+        del k8, sc
+        self.mask = torch.empty((cfg.B, (cfg.S + 31) // 32), dtype=torch.int32, device=dev)
+        self.ens = torch.empty((cfg.B, cfg.S), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(fm.fm_retriever_workspace(cfg.B, cfg.L, cfg.n_h), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        self.fm.fm_retriever_score_mask(self.q, self.w, self.ck, self.mask, self.ens, ensemble=self.mode,
+                                        workspace=self.ws)
+
+    def bytes(self):
+        c = self.cfg
+        return (c.B * c.L * c.S * (c.d + 4) + c.B * c.S * 4 + c.B * ((c.S + 31) // 32) * 4
+                + c.B * c.L * c.n_h * (c.d * 2 + 4))
+
+    def measure(self, reps, warmup, pk):
+        torch = self.torch
+        for _ in range(warmup):
+            self.call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            self.call()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        ach = self.bytes() / (ms / 1e3) / 1e9
+        c = self.cfg
+        return {"ms": round(ms, 4), "chunk_scores_per_s": c.chunk_scores / (ms / 1e3), "bound": "hbm",
+                "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": self.bytes(), "launches": 2, "reps": reps,
+                "workload": (f"retriever {c.B}x{c.L}x{c.S}, {c.n_h} heads, packed 132-byte compressed_k rows, "
+                             f"{'max' if self.mode == 0 else 'mean'} ensemble")}
 
 
 class FullHistoryPaged:
@@ -707,7 +768,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the variant rows timed after the step")
-    ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8", "paged_full"], default=None,
+    ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8", "paged_full", "retriever"], default=None,
                     help="profiling case: run one phase only")
     ap.add_argument("--small", action="store_true", help="profiling case: reduced sizes for ncu captures")
     args = ap.parse_args()

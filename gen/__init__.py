@@ -202,6 +202,9 @@ PAGED_512K = PagedCfg("paged_512k_q1260_r192", requests=60, layers=21, n_pages=2
                       seed=BASE_SEED + 3)
 PAGED_1M = PagedCfg("paged_1m_q630_r384", requests=30, layers=21, n_pages=4096, R=384,
                     seed=BASE_SEED + 4)
+# The trained retriever's Memory Indexer: 128 heads over packed compressed_k
+# rows, at the 1M workload's sizes.
+RETRIEVER_1M = MemIndexCfg("retriever_1m_b30_l3_s262144_h128", B=30, L=3, S=262144, n_h=128, seed=BASE_SEED + 10)
 # Full-history native top-512 (the path without residency that LSA is
 # compared against): every one of a 1M-token request's 4096 pages is listed.
 PAGED_FULL_1M = PagedCfg("paged_full_1m_q630_r4096", requests=30, layers=21, n_pages=4096, R=4096,
@@ -324,6 +327,13 @@ def memindex_fp8_keys_device(cfg: MemIndexCfg, hot_dev_ptr: int, owner_dev_ptr: 
         raise RuntimeError(f"gen_cuda_fill_k_fp8_pool failed: cuda error {rc}")
 
 
+def pack_compressed_k(k8: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """The retriever's packed rows: [..., 128] E4M3 codes and [...] fp32 scales
+    -> [..., 132] bytes (codes, then the scale's little-endian bytes)."""
+    sc = np.ascontiguousarray(scale, dtype="<f4")
+    return np.concatenate([np.asarray(k8, dtype=np.uint8), sc.view(np.uint8).reshape(sc.shape + (4,))], axis=-1)
+
+
 def memindex_fp8_owner(cfg: MemIndexCfg) -> np.ndarray:
     """owner [B*L*S/64, 3] int32: (request, layer, block) of each 64-chunk block."""
     nb = cfg.S // 64
@@ -426,7 +436,7 @@ def prefill_host(cfg: PrefillCfg, pos=None):
 
 __all__ = [
     "BASE_SEED", "MemIndexCfg", "PagedCfg", "PrefillCfg", "TINY", "MEMINDEX_256K", "MEMINDEX_1M",
-    "PAGED_512K", "PAGED_1M", "PAGED_FULL_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
-    "memindex_keys_device", "planted", "paged_tables", "paged_qw", "paged_pool_host",
+    "PAGED_512K", "PAGED_1M", "PAGED_FULL_1M", "RETRIEVER_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
+    "memindex_keys_device", "planted", "pack_compressed_k", "paged_tables", "paged_qw", "paged_pool_host",
     "paged_chunk_rows", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
 ]

@@ -133,6 +133,40 @@ fm_status fm_memindex_score_mask_fp8(const uint16_t* q, const float* w, const ui
                                      void* workspace, size_t workspace_bytes, fm_stream_t stream);
 
 /*
+ * The trained retriever's Memory Indexer ([RM] "Retriever architecture",
+ * "compressed_k format", "Joint checkpoint + ensemble"): the logits of
+ * fm_memindex_score_mask_fp8 with n_h = 128 (the retriever) or 64 heads, read
+ * from packed compressed_k rows, and the per-layer sigmoid scores ensembled
+ * per chunk by max (the union) or mean:
+ *     e[b,s] = max_l sigmoid(x[b,l,s])  or  (1/L) sum_l sigmoid(x[b,l,s])
+ *     resident[b,s] = e[b,s] >= threshold
+ *
+ *   q             [B, L, n_h, 128] bf16; w [B, L, n_h] fp32 (fused weights)
+ *   compressed_k  chunk (b,l,s) is the 132 bytes at compressed_k +
+ *                 b*ck_stride_b + l*ck_stride_l + s*132: 128 E4M3 key bytes,
+ *                 then the fp32 scale (little-endian).  Byte strides are
+ *                 multiples of 16 (so S % 4 == 0); 16-byte aligned.
+ *   ensemble      FM_ENSEMBLE_MAX or FM_ENSEMBLE_MEAN
+ *   threshold     in (0, 1)
+ *   mask_out      as fm_memindex_score_mask (required)
+ *   ens_out       [B, S] fp32 e[b,s], or NULL
+ *   logits_out    [B, L, S] fp32 x, or NULL
+ *   workspace     >= fm_retriever_workspace(B, L, n_h) bytes, 256-byte aligned
+ *                 (the split query and weights: 32.5 KB per (request, layer)
+ *                 at 128 heads)
+ * Errors: FM_ERR_INVALID_ARG for n_h not 64/128, d != 128, L outside 1..4,
+ * S % 4 != 0, a bad ensemble, threshold, pointer or stride; FM_ERR_WORKSPACE
+ * for a missing or short workspace.
+ */
+#define FM_ENSEMBLE_MAX 0
+#define FM_ENSEMBLE_MEAN 1
+size_t fm_retriever_workspace(int B, int L, int n_h);
+fm_status fm_retriever_score_mask(const uint16_t* q, const float* w, const uint8_t* compressed_k,
+                                  int64_t ck_stride_b, int64_t ck_stride_l, int B, int L, int64_t S, int n_h,
+                                  int d, int ensemble, float threshold, uint32_t* mask_out, float* ens_out,
+                                  float* logits_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
+
+/*
  * Top-k select over caller-provided scores ([FM] sec. 3 "Top-k" of the native
  * score; [V4] sec. 3 CSA-2 top-512).
  *

@@ -79,6 +79,11 @@ def lib() -> ctypes.CDLL:
             L.fm_memindex_fp8_workspace.restype = _SZ
             L.fm_memindex_score_mask_fp8.argtypes = [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I32, _I32, _I64,
                                                      _I32, _I32, _F, _VP, _VP, _VP, _VP, _SZ, _VP]
+        if hasattr(L, "fm_retriever_score_mask"):
+            L.fm_retriever_workspace.argtypes = [_I32, _I32, _I32]
+            L.fm_retriever_workspace.restype = _SZ
+            L.fm_retriever_score_mask.argtypes = [_VP, _VP, _VP, _I64, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _F,
+                                                  _VP, _VP, _VP, _VP, _SZ, _VP]
         if hasattr(L, "fm_page_recall"):
             L.fm_page_recall.argtypes = [_VP, _I32, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _VP]
         for name in ("fm_memindex_score_mask", "fm_topk_select", "fm_native_topk_paged", "fm_index_prefill_topk",
@@ -152,6 +157,31 @@ def fm_memindex_score_mask_fp8(q, w, k8, k_scale, mask_out, maxsig_out=None, log
                                             k_scale.stride(0), k_scale.stride(1), B, L, S, n_h, d, float(threshold),
                                             _ptr(mask_out), _ptr(maxsig_out), _ptr(logits_out), _ptr(workspace),
                                             ws_bytes, _stream(stream)))
+
+
+ENSEMBLE_MAX, ENSEMBLE_MEAN = 0, 1
+
+
+def fm_retriever_workspace(B: int, L: int, n_h: int = 128) -> int:
+    return lib().fm_retriever_workspace(B, L, n_h)
+
+
+def fm_retriever_score_mask(q, w, compressed_k, mask_out, ens_out=None, logits_out=None, ensemble: int = ENSEMBLE_MAX,
+                            threshold: float = 0.5, workspace=None, stream=None) -> None:
+    """q [B,L,n_h,128] bf16 (n_h 64 or 128), w [B,L,n_h] fp32, compressed_k
+    [B,L,S,132] uint8 packed rows (any b/l strides, rows dense), mask_out
+    [B, ceil(S/32)], ens_out [B,S] or None, logits_out [B,L,S] or None,
+    ensemble ENSEMBLE_MAX or ENSEMBLE_MEAN, workspace >=
+    fm_retriever_workspace(B, L, n_h)."""
+    B, L, n_h, d = q.shape
+    S = compressed_k.shape[2]
+    if compressed_k.stride(3) != 1 or compressed_k.stride(2) != d + 4:
+        raise ValueError("compressed_k rows must be dense [.., S, 132]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_retriever_score_mask(_ptr(q), _ptr(w), _ptr(compressed_k), compressed_k.stride(0),
+                                         compressed_k.stride(1), B, L, S, n_h, d, int(ensemble), float(threshold),
+                                         _ptr(mask_out), _ptr(ens_out), _ptr(logits_out), _ptr(workspace), ws_bytes,
+                                         _stream(stream)))
 
 
 def fm_topk_workspace(rows: int, n: int) -> int:

@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfm_index.so")
-SOURCES = ["fm_api.cu", "memindex.cu", "memindex_fp8.cu", "topk.cu", "paged.cu", "prefill.cu", "noalloc.cu",
+SOURCES = ["fm_api.cu", "memindex.cu", "memindex_fp8.cu", "retriever.cu", "topk.cu", "paged.cu", "prefill.cu", "noalloc.cu",
            "recall.cu"]
 ARCH = ["-gencode=arch=compute_103a,code=sm_103a"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")

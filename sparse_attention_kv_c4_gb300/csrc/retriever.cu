@@ -1,0 +1,579 @@
+// retriever.cu -- the trained retriever's Memory Indexer, reading the packed
+// compressed_k rows directly.
+//
+// Computes ("FlashMemory-DeepSeek-V4" README, "Retriever architecture",
+// "compressed_k format", "Joint checkpoint + ensemble"; "FlashMemory-
+// DeepSeek-V4: Lightning Index Ultra-Long Context via Lookahead Sparse
+// Attention", sec. 3 "Memory Indexer scoring function"):
+//     x[b,l,s] = sum_{h < n_h} w[b,l,h] * ReLU(q[b,l,h,:] . (scale * e4m3(k8)))
+// where chunk s of (request b, layer l) is one 132-byte row: its 128 E4M3
+// key bytes, then its fp32 dequant scale; then per chunk the layers' sigmoid
+// scores are ensembled, e[b,s] = max_l sigma(x) (the union) or mean_l
+// sigma(x), and the chunk is resident iff e >= threshold.  n_h is 128 (the
+// retriever's heads) or 64.
+//
+// GB300 mapping.  A 132-byte row pitch is not a multiple of 16 bytes, so no
+// tensor map can describe the keys and no UMMA shared-memory layout can use
+// them in place.  Instead:
+//   warp 0  producer: per request the split query (L x 2 n_h rows of 128 B,
+//           SWIZZLE_128B TMA); per layer-tile one bulk copy of its 128 packed
+//           rows (16,896 contiguous bytes) into the stage ring of the pair
+//           (below) that takes the tile.
+//   warps 3-10  two epilogue groups of four warps (one per TMEM lane
+//           quadrant).  A group first unpacks a layer-tile: thread = chunk
+//           row reads its 33 words from shared memory (a 33-word row stride
+//           spreads a warp over all 32 banks), keeps the scale and writes
+//           the 128 key bytes into TMEM (tcgen05.st, lane = row): the MMA's
+//           A operand, with no shared-memory re-layout.  It then reads the
+//           previous layer-tile's n_h dots and computes y = sum_h w_h 2^e_h
+//           ReLU(scale (t1 + t2).k), the per-layer logits, the ensemble,
+//           the mask word (ballot) and the ensembled score.
+//   warps 1-2  UMMA issuers: per layer-tile 8 x tcgen05.mma kind::f8f6f4
+//           M=128 N=n_h K=32 with A from TMEM, four K steps against the
+//           query's t1 rows and four against its t2 rows into one
+//           accumulator (the query split of fp8.cuh).
+// Issuer m and group m form pair m: the pair takes the CTA's tiles with
+// local index = m (mod 2) and owns its stage ring, two TMEM A slots and
+// its accumulators (256 TMEM columns), so every ring has a single filler and
+// a single reader and each parity wait is exact.
+#include <math.h>
+
+#include "fm_common.cuh"
+#include "fm_internal.h"
+#include "fp8.cuh"
+
+#define FM_API extern "C" __attribute__((visibility("default")))
+
+namespace fm {
+namespace {
+
+constexpr int kM = 128;                    // chunks per tile (UMMA M, TMEM lanes)
+constexpr int kDim = 128;                  // E4M3 key bytes per chunk
+constexpr int kRowBytes = kDim + 4;        // packed compressed_k row
+constexpr int kRowWords = kRowBytes / 4;   // 33
+constexpr int kTileBytes = kM * kRowBytes;  // 16,896 bytes per layer-tile
+constexpr int kMaxL = 4;
+constexpr int kPairs = 2;
+constexpr int kMmaWarps = kPairs;
+constexpr int kFirstEpiWarp = 1 + kMmaWarps;
+constexpr int kThreads = kFirstEpiWarp * 32 + kPairs * 128;
+constexpr int kASlots = 2;                 // TMEM A slots per pair
+constexpr int kACols = kDim / 4;           // 32 columns: 128 E4M3 bytes per lane
+constexpr int kPairCols = 256;             // TMEM columns per pair
+constexpr uint32_t kTmemCols = kPairs * kPairCols;
+constexpr int kMaxRing = 6;                // key stages per pair
+constexpr int kMaxDAccs = 3;
+constexpr int kPrepThreads = 256;
+
+template <int NH>
+struct Cfg {
+  static constexpr int kDAccs = (kPairCols - kASlots * kACols) / NH;  // 1 for 128 heads, 3 for 64
+  static constexpr int kQLayerBytes = 2 * NH * kDim;                  // t1 and t2 rows of one layer
+};
+
+struct Params {
+  const uint8_t* ck;         // packed rows
+  int64_t ck_stride_b, ck_stride_l;  // bytes
+  const float* wq;           // [B*L, n_h] head weights with 2^e_h folded in
+  uint32_t* mask;
+  float* ens;                // [B, S] ensembled score, or null
+  float* logits;             // [B, L, S], or null
+  unsigned int* status;
+  int64_t S;
+  int64_t total_tiles;
+  int tiles_per_b;
+  int L;
+  int ring;                  // key stages per pair
+  int mode;                  // 0 max, 1 mean
+  float thr, thr_logit;
+};
+
+template <int NH>
+__global__ void __launch_bounds__(kPrepThreads)
+    retriever_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w, uint8_t* __restrict__ qsplit,
+                          float* __restrict__ wq) {
+  const int64_t bl = blockIdx.x;
+  uint8_t* t1 = qsplit + bl * Cfg<NH>::kQLayerBytes;
+  split_query(q + bl * NH * kDim, w + bl * NH, NH, kPrepThreads, t1, t1 + NH * kDim, wq + bl * NH);
+}
+
+// Position of a pair's j-th layer-tile: tile t = t_begin + pair + 2i of
+// request b, tile index `tile` within it, layer l (j = i*L + l).
+struct Cursor {
+  int64_t t, b;
+  int tile, l;
+  FM_DEV void init(int64_t t0, int tiles_per_b) {
+    t = t0;
+    b = t0 / tiles_per_b;
+    tile = (int)(t0 % tiles_per_b);
+    l = 0;
+  }
+  FM_DEV void next(int L, int tiles_per_b) {
+    if (++l < L) return;
+    l = 0;
+    t += kPairs;
+    tile += kPairs;
+    while (tile >= tiles_per_b) {
+      tile -= tiles_per_b;
+      ++b;
+    }
+  }
+};
+
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    retriever_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
+  using C = Cfg<NH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_smem = smem;
+  uint8_t* k_smem = smem + p.L * C::kQLayerBytes;  // [pair][ring] stages of kTileBytes
+
+  __shared__ __align__(8) uint64_t bar_full[kPairs * kMaxRing], bar_empty[kPairs * kMaxRing];
+  __shared__ __align__(8) uint64_t bar_afull[kPairs * kASlots], bar_aempty[kPairs * kASlots];
+  __shared__ __align__(8) uint64_t bar_tfull[kPairs * kMaxDAccs], bar_tempty[kPairs * kMaxDAccs];
+  __shared__ __align__(8) uint64_t bar_qfull, bar_qempty, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  // one copy of the current request's head weights per epilogue warp, so a
+  // warp refreshes its own copy with __syncwarp alone
+  __shared__ __align__(16) float w_smem[kPairs * 4][kMaxL * NH];
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int L = p.L, ring = p.ring;
+  const int64_t t_begin = p.total_tiles * blockIdx.x / gridDim.x;
+  const int64_t t_end = p.total_tiles * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairs * ring; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 128);  // the group read the stage's rows
+    }
+    for (int i = 0; i < kPairs * kASlots; ++i) {
+      mbar_init(&bar_afull[i], 128);  // the group wrote the A slot
+      mbar_init(&bar_aempty[i], 1);   // the MMAs reading it finished
+    }
+    for (int i = 0; i < kPairs * C::kDAccs; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 128);
+    }
+    mbar_init(&bar_qfull, 1);
+    mbar_init(&bar_qempty, kMmaWarps);
+    mbar_init(&bar_drain, kMmaWarps);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch(&tmap_q);
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ producer ---------------------------------
+      uint32_t rstage[kPairs] = {}, rphase[kPairs] = {}, q_phase = 0;
+      int issued[kPairs * kMaxRing];
+      for (int s = 0; s < kPairs * kMaxRing; ++s) issued[s] = -1;
+      int q_issued = -1;
+      int64_t cur_b = -1;
+      bool ok = true;
+      int64_t b = t_begin / p.tiles_per_b;
+      int tile = (int)(t_begin % p.tiles_per_b) - 1;
+      for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        if (++tile == p.tiles_per_b) {
+          tile = 0;
+          ++b;
+        }
+        if (b != cur_b) {
+          if (cur_b >= 0) {
+            if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) break;
+            q_phase ^= 1;
+          }
+          mbar_arrive_expect_tx(&bar_qfull, (uint32_t)(L * C::kQLayerBytes));
+          for (int l = 0; l < L; ++l)
+            tma_load_2d(q_smem + l * C::kQLayerBytes, &tmap_q, &bar_qfull, 0, (int32_t)((b * L + l) * 2 * NH));
+          q_issued = (q_issued + 1) & 1;
+          cur_b = b;
+        }
+        const int m = (int)((t - t_begin) % kPairs);
+        const int64_t rows = p.S - (int64_t)tile * kM < kM ? p.S - (int64_t)tile * kM : kM;
+        const uint32_t bytes = (uint32_t)(rows * kRowBytes);  // S % 4 == 0: a multiple of 16
+        for (int l = 0; l < L; ++l) {
+          const uint32_t stage = m * ring + rstage[m], phase = rphase[m];
+          if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar_full[stage], bytes);
+          bulk_load(k_smem + stage * kTileBytes,
+                    p.ck + b * p.ck_stride_b + l * p.ck_stride_l + (int64_t)tile * kTileBytes, bytes,
+                    &bar_full[stage]);
+          issued[stage] = (int)phase;
+          if (++rstage[m] == (uint32_t)ring) {
+            rstage[m] = 0;
+            rphase[m] ^= 1u;
+          }
+        }
+      }
+      if (abort_flag) {  // let copies already in flight land before the CTA exits
+        for (int s = 0; s < kPairs * ring; ++s)
+          if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
+        if (q_issued >= 0) mbar_wait_drain(&bar_qfull, (uint32_t)q_issued);
+      }
+    }
+  } else if (warp < kFirstEpiWarp) {
+    if (lane == 0) {
+      // ------------------------------ UMMA issuers ------------------------------
+      const int me = warp - 1;
+      const uint32_t idesc = idesc_e4m3_f32(kM, NH);
+      uint32_t aslot = 0, a_phase = 0, dacc = 0, d_phase = 0, q_phase = 0;
+      int64_t cur_b = -1;
+      bool ok = true;
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(q_smem));
+      const uint32_t pair_base = tmem_base + (uint32_t)(me * kPairCols);
+      int64_t b = t_begin / p.tiles_per_b;
+      int tile = (int)(t_begin % p.tiles_per_b) - 1;
+      for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        if (++tile == p.tiles_per_b) {
+          tile = 0;
+          ++b;
+        }
+        if (b != cur_b) {
+          if (cur_b >= 0) umma_commit(&bar_qempty);
+          if (!mbar_wait(&bar_qfull, q_phase, &abort_flag, p.status)) break;
+          q_phase ^= 1;
+          tc_fence_after();
+          cur_b = b;
+        }
+        if ((int)((t - t_begin) % kPairs) != me) continue;  // the other pair's tile
+        for (int l = 0; l < L; ++l) {
+          const int ai = me * kASlots + (int)aslot, di = me * C::kDAccs + (int)dacc;
+          if (!mbar_wait(&bar_afull[ai], a_phase, &abort_flag, p.status) ||
+              !mbar_wait(&bar_tempty[di], d_phase ^ 1u, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = pair_base + aslot * kACols;
+          const uint32_t d_tmem = pair_base + kASlots * kACols + dacc * NH;
+          // B: the layer's t1 rows, then its t2 rows NH * 128 bytes later
+          // (descriptor addresses count 16-byte units); A: 8 TMEM columns
+          // (32 E4M3 values per lane) per K step
+          const uint64_t b_desc = b_desc0 + (uint64_t)(l * (C::kQLayerBytes >> 4));
+          constexpr uint64_t kT2 = (uint64_t)(NH * kDim) >> 4;
+#pragma unroll
+          for (int k = 0; k < kDim / 32; ++k)
+            umma_e4m3_ts(d_tmem, a_tmem + 8 * k, b_desc + 2 * k, idesc, k != 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < kDim / 32; ++k) umma_e4m3_ts(d_tmem, a_tmem + 8 * k, b_desc + kT2 + 2 * k, idesc, 1u);
+          umma_commit(&bar_aempty[ai]);
+          umma_commit(&bar_tfull[di]);
+          if (++aslot == (uint32_t)kASlots) {
+            aslot = 0;
+            a_phase ^= 1u;
+          }
+          if (++dacc == (uint32_t)C::kDAccs) {
+            dacc = 0;
+            d_phase ^= 1u;
+          }
+        }
+      }
+      umma_commit(&bar_drain);  // every MMA issued above has finished before TMEM is freed
+      mbar_wait_drain(&bar_drain, 0);
+    }
+  } else {
+    // -------------------------------- epilogue ----------------------------------
+    const int group = (warp - kFirstEpiWarp) >> 2;
+    const int quad = warp & 3;  // TMEM lane quadrant this warp can access
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(group * kPairCols);
+    const int64_t words = (p.S + 31) / 32;
+    float* w_mine = w_smem[warp - kFirstEpiWarp];
+    const int64_t span = t_end - t_begin;
+    const int64_t n_lt = (span > group ? (span - group + kPairs - 1) / kPairs : 0) * L;  // the pair's layer-tiles
+
+    // unpack one layer-tile (the loader cursor's) into the pair's next A slot
+    Cursor lc;
+    lc.init(t_begin + group, p.tiles_per_b);
+    uint32_t lstage = 0, lphase = 0, aslot = 0, a_phase = 0;
+    float sc_next = 0.f;
+    auto load = [&]() -> bool {
+      const uint32_t stage = group * ring + lstage;
+      if (!mbar_wait(&bar_full[stage], lphase, &abort_flag, p.status)) return false;
+      const bool valid = (int64_t)lc.tile * kM + row < p.S;  // rows past S hold stale bytes
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(k_smem + stage * kTileBytes) + row * kRowWords;
+      uint32_t kw[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) kw[i] = valid ? src[i] : 0u;
+      sc_next = valid ? __uint_as_float(src[32]) : 0.f;
+      mbar_arrive(&bar_empty[stage]);
+      if (++lstage == (uint32_t)ring) {
+        lstage = 0;
+        lphase ^= 1u;
+      }
+      const int ai = group * kASlots + (int)aslot;
+      if (!mbar_wait(&bar_aempty[ai], a_phase ^ 1u, &abort_flag, p.status)) return false;
+      tc_fence_after();
+      tmem_st32(lane_base + aslot * kACols, kw);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_afull[ai]);
+      if (++aslot == (uint32_t)kASlots) {
+        aslot = 0;
+        a_phase ^= 1u;
+      }
+      lc.next(L, p.tiles_per_b);
+      return true;
+    };
+
+    // score one layer-tile (the compute cursor's) and, at its last layer, the chunk
+    Cursor cc;
+    cc.init(t_begin + group, p.tiles_per_b);
+    uint32_t dacc = 0, d_phase = 0;
+    int64_t w_b = -1;
+    float acc_m = -INFINITY, acc_sum = 0.f;
+    auto compute = [&](float sc) -> bool {
+      const int64_t b = cc.b;
+      const int l = cc.l;
+      if (b != w_b) {  // a new request: its weights into this warp's copy
+        __syncwarp();
+        for (int i = lane; i < L * NH; i += 32) w_mine[i] = __ldg(p.wq + b * L * NH + i);
+        __syncwarp();
+        w_b = b;
+      }
+      const int di = group * C::kDAccs + (int)dacc;
+      if (!mbar_wait(&bar_tfull[di], d_phase, &abort_flag, p.status)) return false;
+      tc_fence_after();
+      const uint32_t taddr = lane_base + kASlots * kACols + dacc * NH;
+      const float4* wl = reinterpret_cast<const float4*>(w_mine + l * NH);
+      float y = 0.f;
+#pragma unroll
+      for (int c = 0; c < NH / 32; ++c) {  // 32 heads at a time
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+        if (c == NH / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bar_tempty[di]);  // the dots are in registers: the MMA may reuse the accumulator
+        }
+        // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        if (sc > 0.f) {  // ReLU(sc d) = sc ReLU(d): one multiply per chunk
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 wv = wl[c * 8 + h / 4];
+            x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
+            x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
+            x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
+            x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
+          }
+          y += sc * ((x0 + x1) + (x2 + x3));
+        } else {
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 wv = wl[c * 8 + h / 4];
+            x0 = fmaf(wv.x, fmaxf(sc * __uint_as_float(r[h]), 0.f), x0);
+            x1 = fmaf(wv.y, fmaxf(sc * __uint_as_float(r[h + 1]), 0.f), x1);
+            x2 = fmaf(wv.z, fmaxf(sc * __uint_as_float(r[h + 2]), 0.f), x2);
+            x3 = fmaf(wv.w, fmaxf(sc * __uint_as_float(r[h + 3]), 0.f), x3);
+          }
+          y += (x0 + x1) + (x2 + x3);
+        }
+      }
+      if (++dacc == (uint32_t)C::kDAccs) {
+        dacc = 0;
+        d_phase ^= 1u;
+      }
+      const int64_t s = (int64_t)cc.tile * kM + row;
+      const bool valid = s < p.S;
+      if (p.logits != nullptr && valid) p.logits[(b * L + l) * p.S + s] = y;
+      if (l == 0) {
+        acc_m = -INFINITY;
+        acc_sum = 0.f;
+      }
+      if (p.mode == 0)
+        acc_m = fmaxf(acc_m, y);
+      else
+        acc_sum += 1.0f / (1.0f + expf(-y));
+      if (l == L - 1) {  // the ensemble over the tile's layers
+        float e;
+        bool res;
+        if (p.mode == 0) {  // max of sigmoids = sigmoid of the max: compare the logit
+          e = 1.0f / (1.0f + expf(-acc_m));
+          res = valid && acc_m >= p.thr_logit;
+        } else {
+          e = acc_sum / (float)L;
+          res = valid && e >= p.thr;
+        }
+        const uint32_t bits = __ballot_sync(0xffffffffu, res);
+        const int64_t word = (int64_t)cc.tile * (kM / 32) + quad;
+        if (lane == 0 && word < words) p.mask[b * words + word] = bits;
+        if (p.ens != nullptr && valid) p.ens[b * p.S + s] = e;
+      }
+      cc.next(L, p.tiles_per_b);
+      return true;
+    };
+
+    // the unpack of layer-tile j + 1 runs ahead of the scoring of j, so the
+    // pair's MMAs for j + 1 overlap this group's arithmetic for j
+    if (n_lt > 0 && load()) {
+      for (int64_t j = 0; j < n_lt; ++j) {
+        const float sc = sc_next;
+        if (j + 1 < n_lt && !load()) break;
+        if (!compute(sc)) break;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t retriever_ws_bytes(int B, int L, int n_h) {
+  return align256((size_t)B * L * 2 * n_h * kDim) + align256((size_t)B * L * n_h * 4);
+}
+
+struct RetrieverArgs {
+  const uint16_t* q;
+  const float* w;
+  const uint8_t* ck;
+  int64_t ck_stride_b, ck_stride_l;
+  int B, L, n_h, mode;
+  int64_t S;
+  float thr;
+  uint32_t* mask;
+  float* ens;
+  float* logits;
+  void* workspace;
+};
+
+template <int NH>
+fm_status launch_retriever(const RetrieverArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
+  using C = Cfg<NH>;
+  const int tiles_per_b = (int)((a.S + kM - 1) / kM);
+  const int64_t total = (int64_t)a.B * tiles_per_b;
+  if (total == 0) return FM_OK;
+  uint8_t* qsplit = static_cast<uint8_t*>(a.workspace);
+  float* wq = reinterpret_cast<float*>(qsplit + align256((size_t)a.B * a.L * C::kQLayerBytes));
+  retriever_prep_kernel<NH><<<a.B * a.L, kPrepThreads, 0, stream>>>(a.q, a.w, qsplit, wq);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever prep: launch: %s", cudaGetErrorString(e));
+
+  CUtensorMap tmap_q;
+  {
+    // split query: rows (B*L*2*n_h) x 128 B, one box of 2*n_h rows per layer
+    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.B * a.L * 2 * NH};
+    const uint64_t strides[1] = {(uint64_t)kDim};
+    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)(2 * NH)};
+    fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, qsplit, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  }
+  const int smem_cap = 227 * 1024 - (int)sizeof(float) * kPairs * 4 * kMaxL * NH - 2048;  // less static
+  const int fixed = 1024 + a.L * C::kQLayerBytes;
+  int ring = (smem_cap - fixed) / (kPairs * kTileBytes);
+  if (ring > kMaxRing) ring = kMaxRing;
+  if (ring < 2) return set_error(FM_ERR_UNSUPPORTED, "retriever: %d key stages per pair are too few", ring);
+  const int smem = fixed + kPairs * ring * kTileBytes;
+
+  Params p;
+  p.ck = a.ck;
+  p.ck_stride_b = a.ck_stride_b;
+  p.ck_stride_l = a.ck_stride_l;
+  p.wq = wq;
+  p.mask = a.mask;
+  p.ens = a.ens;
+  p.logits = a.logits;
+  p.status = status;
+  p.S = a.S;
+  p.total_tiles = total;
+  p.tiles_per_b = tiles_per_b;
+  p.L = a.L;
+  p.ring = ring;
+  p.mode = a.mode;
+  p.thr = a.thr;
+  p.thr_logit = logf(a.thr / (1.0f - a.thr));
+  e = cudaFuncSetAttribute(retriever_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  const int grid = (int)(total < num_sms ? total : num_sms);
+  retriever_kernel<NH><<<grid, kThreads, smem, stream>>>(tmap_q, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever: launch: %s", cudaGetErrorString(e));
+  return FM_OK;
+}
+
+}  // namespace
+}  // namespace fm
+
+FM_API size_t fm_retriever_workspace(int B, int L, int n_h) {
+  if (B < 0 || L < 1 || L > 4 || (n_h != 64 && n_h != 128)) return 0;
+  return fm::retriever_ws_bytes(B, L, n_h);
+}
+
+FM_API fm_status fm_retriever_score_mask(const uint16_t* q, const float* w, const uint8_t* compressed_k,
+                                         int64_t ck_stride_b, int64_t ck_stride_l, int B, int L, int64_t S, int n_h,
+                                         int d, int ensemble, float threshold, uint32_t* mask_out, float* ens_out,
+                                         float* logits_out, void* workspace, size_t workspace_bytes,
+                                         fm_stream_t stream) {
+  using namespace fm;
+  if ((n_h != 64 && n_h != 128) || d != 128)
+    return set_error(FM_ERR_INVALID_ARG, "fm_retriever_score_mask: n_h=%d d=%d (need 64 or 128, 128)", n_h, d);
+  if (B < 0 || L < 1 || L > 4 || S < 0 || S >= (int64_t(1) << 31) || S % 4 != 0)
+    return set_error(FM_ERR_INVALID_ARG, "fm_retriever_score_mask: bad sizes B=%d L=%d S=%lld (S %% 4 == 0)", B, L,
+                     (long long)S);
+  if (ensemble != FM_ENSEMBLE_MAX && ensemble != FM_ENSEMBLE_MEAN)
+    return set_error(FM_ERR_INVALID_ARG, "fm_retriever_score_mask: ensemble %d is not max (0) or mean (1)", ensemble);
+  if (!(threshold > 0.0f && threshold < 1.0f))
+    return set_error(FM_ERR_INVALID_ARG, "fm_retriever_score_mask: threshold %g not in (0, 1)", (double)threshold);
+  if (B == 0 || S == 0) return FM_OK;
+  if (!q || !w || !compressed_k || !mask_out)
+    return set_error(FM_ERR_INVALID_ARG, "fm_retriever_score_mask: required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(compressed_k, 16) || !aligned(mask_out, 4) ||
+      (ens_out && !aligned(ens_out, 4)) || (logits_out && !aligned(logits_out, 4)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_retriever_score_mask: misaligned pointer (q, w, compressed_k: 16 bytes)");
+  // packed rows are 132 contiguous bytes; layer and request strides must be
+  // multiples of 16 bytes and must not make rows of different (b, l) overlap
+  const int64_t rows_bytes = S * (d + 4);
+  if (ck_stride_l % 16 != 0 || ck_stride_b % 16 != 0 || (L > 1 && ck_stride_l < rows_bytes) ||
+      (B > 1 && ck_stride_b < (L > 1 ? ck_stride_l * L : rows_bytes)))
+    return set_error(FM_ERR_INVALID_ARG, "fm_retriever_score_mask: bad strides b=%lld l=%lld",
+                     (long long)ck_stride_b, (long long)ck_stride_l);
+  const size_t need = retriever_ws_bytes(B, L, n_h);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return set_error(FM_ERR_WORKSPACE, "fm_retriever_score_mask: workspace needs %zu bytes, 256-byte aligned", need);
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  unsigned int* status = nullptr;
+  st = status_word(&status);
+  if (st != FM_OK) return st;
+  RetrieverArgs a;
+  a.q = q;
+  a.w = w;
+  a.ck = compressed_k;
+  a.ck_stride_b = ck_stride_b;
+  a.ck_stride_l = ck_stride_l;
+  a.B = B;
+  a.L = L;
+  a.n_h = n_h;
+  a.mode = ensemble;
+  a.S = S;
+  a.thr = threshold;
+  a.mask = mask_out;
+  a.ens = ens_out;
+  a.logits = logits_out;
+  a.workspace = workspace;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return n_h == 128 ? launch_retriever<128>(a, sms, status, s) : launch_retriever<64>(a, sms, status, s);
+}

@@ -29,6 +29,7 @@ def test_header_declares_the_boundary():
     names = declared()
     for n in ("fm_memindex_score_mask", "fm_native_topk_paged", "fm_index_prefill_topk", "fm_topk_select",
               "fm_native_topk_paged_workspace", "fm_index_prefill_workspace", "fm_topk_workspace",
+              "fm_retriever_score_mask", "fm_retriever_workspace",
               "fm_last_error", "fm_device_status", "fm_version"):
         assert n in names
 
@@ -105,3 +106,30 @@ def test_paged_workspace_accepts_a_whole_1m_history(lib):
     assert ws >= 630 * 4096 * 64 * 4  # the score rows alone
     assert lib.fm_native_topk_paged_workspace(630, 4097) == 0
     assert lib.fm_native_topk_paged_workspace(1, 0) == 0
+
+
+def test_retriever_workspace_and_host_checks(lib):
+    """Workspace sizing is host arithmetic; bad arguments are rejected before
+    any device work (no GPU needed)."""
+    lib.fm_retriever_workspace.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.fm_retriever_workspace.restype = ctypes.c_size_t
+    assert lib.fm_retriever_workspace(30, 3, 128) >= 30 * 3 * (2 * 128 * 128 + 128 * 4)
+    assert lib.fm_retriever_workspace(30, 3, 64) >= 30 * 3 * (2 * 64 * 128 + 64 * 4)
+    assert lib.fm_retriever_workspace(1, 3, 96) == 0 and lib.fm_retriever_workspace(1, 5, 128) == 0
+    f = lib.fm_retriever_score_mask
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 2 + [ctypes.c_int] * 2 + [ctypes.c_int64] + \
+        [ctypes.c_int] * 3 + [ctypes.c_float] + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p]
+    INVALID = 1
+    base = dict(B=1, L=3, S=64, n_h=128, d=128, ens=0, thr=0.5)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(8, 8, 8, 0, 0, a["B"], a["L"], a["S"], a["n_h"], a["d"], a["ens"], a["thr"], 8, None, None, 256, 1 << 20,
+                 None)
+    assert call(n_h=96) == INVALID
+    assert call(d=64) == INVALID
+    assert call(S=30) == INVALID        # packed rows need S % 4 == 0
+    assert call(L=5) == INVALID
+    assert call(ens=2) == INVALID
+    assert call(thr=0.0) == INVALID
