@@ -24,7 +24,9 @@
 //           row reads its 33 words from shared memory (a 33-word row stride
 //           spreads a warp over all 32 banks), keeps the scale and writes
 //           the 128 key bytes into TMEM (tcgen05.st, lane = row): the MMA's
-//           A operand, with no shared-memory re-layout.  It then reads the
+//           A operand, with no shared-memory re-layout.  A negative scale
+//           becomes positive with every key sign bit flipped (the same
+//           dequantised key), so the scoring needs only ReLU(sc d) = sc ReLU(d).  It then reads the
 //           previous layer-tile's n_h dots and computes y = sum_h w_h 2^e_h
 //           ReLU(scale (t1 + t2).k), the per-layer logits, the ensemble,
 //           the mask word (ballot) and the ensembled score.
@@ -310,7 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kw[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) kw[i] = valid ? src[i] : 0u;
-      sc_next = valid ? __uint_as_float(src[32]) : 0.f;
+      float sc = valid ? __uint_as_float(src[32]) : 0.f;
+      if (sc < 0.f) {  // scale * e4m3(k) == (-scale) * e4m3(-k): flip every sign bit, keep the scale positive
+        sc = -sc;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) kw[i] ^= 0x80808080u;
+      }
+      sc_next = sc;
       mbar_arrive(&bar_empty[stage]);
       if (++lstage == (uint32_t)ring) {
         lstage = 0;
@@ -362,28 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bar_tempty[di]);  // the dots are in registers: the MMA may reuse the accumulator
         }
         // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w
+        // the scale is >= 0 (the unpack moved its sign into the key), so
+        // ReLU(sc d) = sc ReLU(d): one multiply per chunk
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-        if (sc > 0.f) {  // ReLU(sc d) = sc ReLU(d): one multiply per chunk
 #pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            const float4 wv = wl[c * 8 + h / 4];
-            x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
-            x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
-            x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
-            x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
-          }
-          y += sc * ((x0 + x1) + (x2 + x3));
-        } else {
-#pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            const float4 wv = wl[c * 8 + h / 4];
-            x0 = fmaf(wv.x, fmaxf(sc * __uint_as_float(r[h]), 0.f), x0);
-            x1 = fmaf(wv.y, fmaxf(sc * __uint_as_float(r[h + 1]), 0.f), x1);
-            x2 = fmaf(wv.z, fmaxf(sc * __uint_as_float(r[h + 2]), 0.f), x2);
-            x3 = fmaf(wv.w, fmaxf(sc * __uint_as_float(r[h + 3]), 0.f), x3);
-          }
-          y += (x0 + x1) + (x2 + x3);
+        for (int h = 0; h < 32; h += 4) {
+          const float4 wv = wl[c * 8 + h / 4];
+          x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
+          x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
+          x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
+          x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
         }
+        y += sc * ((x0 + x1) + (x2 + x3));
       }
       if (++dacc == (uint32_t)C::kDAccs) {
         dacc = 0;
