@@ -71,6 +71,13 @@ class Oracle:
                                                 f64p]
         lib.orc_memindex_select.argtypes = [f64p, I64, I64, I64, D, u32p, f64p]
         lib.orc_unpack_compressed_k.argtypes = [u8p, I64, I32, u8p, f32p]
+        lib.orc_rmsnorm.argtypes = [f64p, u16p, I32, D, f64p]
+        lib.orc_yarn_freq.argtypes = [I32, I32, D, D, D, D, D]
+        lib.orc_yarn_freq.restype = D
+        lib.orc_rope_yarn.argtypes = [f64p, I32, I32, I64, D, D, D, D, D]
+        lib.orc_hadamard.argtypes = [f64p, I32, f64p]
+        lib.orc_query_chain.argtypes = [u16p, u16p, u16p, u16p, u16p, i64p, I64, I32, I32, I32, I32, I32, D, D, D, D,
+                                        D, D, f64p, f64p]
         lib.orc_memindex_ensemble.argtypes = [f64p, I64, I64, I64, I32, D, u32p, f64p]
         lib.orc_topk.argtypes = [i64p, f64p, I64, I32, i32p, f64p]
         lib.orc_topk.restype = ctypes.c_int
@@ -150,6 +157,50 @@ class Oracle:
         sc = np.empty(ck.shape[:-1], dtype=np.float32)
         self.lib.orc_unpack_compressed_k(_p(ck, u8p), n, d, _p(k8, u8p), _p(sc, f32p))
         return k8, sc
+
+    # -- query projection chain -------------------------------------------------
+    ROPE = dict(rope_dim=64, base=160000.0, factor=16.0, orig_len=65536.0, beta_fast=32.0, beta_slow=1.0)
+
+    def rmsnorm(self, x, g, eps: float = 1e-6) -> np.ndarray:
+        x = _c(x, np.float64); g = _c(g, np.uint16)
+        y = np.empty_like(x)
+        self.lib.orc_rmsnorm(_p(x, f64p), _p(g, u16p), len(x), float(eps), _p(y, f64p))
+        return y
+
+    def yarn_freq(self, i: int, rope_dim=64, base=160000.0, factor=16.0, orig_len=65536.0, beta_fast=32.0,
+                  beta_slow=1.0) -> float:
+        return self.lib.orc_yarn_freq(int(i), int(rope_dim), float(base), float(factor), float(orig_len),
+                                      float(beta_fast), float(beta_slow))
+
+    def rope_yarn(self, x, pos: int, rope_dim=64, base=160000.0, factor=16.0, orig_len=65536.0, beta_fast=32.0,
+                  beta_slow=1.0) -> np.ndarray:
+        y = _c(np.array(x, dtype=np.float64), np.float64)
+        self.lib.orc_rope_yarn(_p(y, f64p), len(y), int(rope_dim), int(pos), float(base), float(factor),
+                               float(orig_len), float(beta_fast), float(beta_slow))
+        return y
+
+    def hadamard(self, x) -> np.ndarray:
+        x = _c(x, np.float64)
+        y = np.empty_like(x)
+        self.lib.orc_hadamard(_p(x, f64p), len(x), _p(y, f64p))
+        return y
+
+    def query_chain(self, hidden, wq_a, q_norm, wq_b, w_proj, pos, n_h: int, head_dim: int = 128,
+                    eps: float = 1e-6, **rope):
+        """hidden [T,dim] bf16 bits; wq_a [r,dim], q_norm [r], wq_b [n_h*head_dim, r],
+        w_proj [n_h, dim] bf16 bits; pos [T] -> q [T,n_h,head_dim], w [T,n_h] fp64."""
+        cfg = dict(self.ROPE, **rope)
+        hidden = _c(hidden, np.uint16); wq_a = _c(wq_a, np.uint16); q_norm = _c(q_norm, np.uint16)
+        wq_b = _c(wq_b, np.uint16); w_proj = _c(w_proj, np.uint16); pos = _c(pos, np.int64)
+        T, dim = hidden.shape
+        r = wq_a.shape[0]
+        q = np.empty((T, n_h, head_dim), dtype=np.float64)
+        w = np.empty((T, n_h), dtype=np.float64)
+        self.lib.orc_query_chain(_p(hidden, u16p), _p(wq_a, u16p), _p(q_norm, u16p), _p(wq_b, u16p),
+                                 _p(w_proj, u16p), _p(pos, i64p), T, dim, r, n_h, head_dim, cfg["rope_dim"],
+                                 cfg["base"], cfg["factor"], cfg["orig_len"], cfg["beta_fast"], cfg["beta_slow"],
+                                 float(eps), _p(q, f64p), _p(w, f64p))
+        return q, w
 
     def memindex_ensemble(self, x, mode: int = 0, thr: float = 0.5):
         """x [B,L,S] -> mask [B, ceil(S/32)] uint32, ensembled score [B,S] fp64

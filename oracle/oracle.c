@@ -416,6 +416,114 @@ ORC_API void orc_page_recall(const uint32_t* mask, int64_t B, int64_t S, int64_t
   }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Query-side projection chain of one CSA layer ([RM] "Retriever            */
+/* architecture" and "Hyperparameters")                                       */
+/* ------------------------------------------------------------------------- */
+
+/* RMSNorm: y = x / sqrt(mean(x^2) + eps) * g. */
+ORC_API void orc_rmsnorm(const double* x, const uint16_t* g, int n, double eps, double* y) {
+  double ss = 0.0;
+  for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+  double inv = 1.0 / sqrt(ss / (double)n + eps);
+  for (int i = 0; i < n; ++i) y[i] = x[i] * inv * orc_bf16(g[i]);
+}
+
+/* YaRN frequency of rotary pair i of a rope_dim-wide rotary part, the
+ * "NTK-by-parts" rule of the YaRN method (Peng et al., 2023): the base
+ * frequency theta_i = base^(-2i / rope_dim) has wavelength 2 pi / theta_i and
+ * turns r = orig_len / wavelength times over the original context; pairs
+ * turning fewer than beta_slow times are interpolated (theta / factor), pairs
+ * turning more than beta_fast times keep theta, and in between
+ * gamma = (r - beta_slow) / (beta_fast - beta_slow) blends the two:
+ * theta' = (1 - gamma) theta / factor + gamma theta. */
+ORC_API double orc_yarn_freq(int i, int rope_dim, double base, double factor, double orig_len, double beta_fast,
+                             double beta_slow) {
+  const double two_pi = 6.283185307179586476925286766559;
+  double theta = pow(base, -2.0 * (double)i / (double)rope_dim);
+  double r = orig_len * theta / two_pi;
+  double gamma = (r - beta_slow) / (beta_fast - beta_slow);
+  if (gamma < 0.0) gamma = 0.0;
+  if (gamma > 1.0) gamma = 1.0;
+  return (1.0 - gamma) * theta / factor + gamma * theta;
+}
+
+/* Rotary embedding of the last rope_dim entries of a head_dim vector at
+ * position pos: consecutive entries (2i, 2i+1) of the rotary part form pair i
+ * and turn by the angle pos * theta'_i (the complex-pair form of rotary
+ * embeddings). */
+ORC_API void orc_rope_yarn(double* x, int head_dim, int rope_dim, int64_t pos, double base, double factor,
+                           double orig_len, double beta_fast, double beta_slow) {
+  double* xr = x + head_dim - rope_dim;
+  for (int i = 0; i < rope_dim / 2; ++i) {
+    double a = (double)pos * orc_yarn_freq(i, rope_dim, base, factor, orig_len, beta_fast, beta_slow);
+    double c = cos(a), sn = sin(a);
+    double x0 = xr[2 * i], x1 = xr[2 * i + 1];
+    xr[2 * i] = x0 * c - x1 * sn;
+    xr[2 * i + 1] = x0 * sn + x1 * c;
+  }
+}
+
+/* Normalised Walsh-Hadamard transform (Sylvester order): y = H x / sqrt(n),
+ * H[i][j] = (-1)^popcount(i & j), n a power of two. */
+ORC_API void orc_hadamard(const double* x, int n, double* y) {
+  double norm = 1.0 / sqrt((double)n);
+  for (int i = 0; i < n; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < n; ++j) acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -x[j] : x[j];
+    y[i] = acc * norm;
+  }
+}
+
+/* The chain for T tokens: for token t,
+ *   a = wq_a . hidden_t                     (Linear dim -> r, no bias)
+ *   c = RMSNorm(a; q_norm, eps)
+ *   u = wq_b . c                            (Linear r -> n_h * head_dim)
+ *   q_h = Hadamard(RoPE_yarn(u_h, pos_t))   per head h (u reshaped [n_h, head_dim])
+ *   w = (w_proj . hidden_t) * head_dim^-1/2 * n_h^-1/2
+ * Weights are row-major [out][in] bf16 (a Linear's weight), hidden [T][dim]
+ * bf16; everything is accumulated in fp64 with no intermediate rounding. */
+ORC_API void orc_query_chain(const uint16_t* hidden, const uint16_t* wq_a, const uint16_t* q_norm, const uint16_t* wq_b,
+                             const uint16_t* w_proj, const int64_t* pos, int64_t T, int dim, int r, int n_h,
+                             int head_dim, int rope_dim, double base, double factor, double orig_len, double beta_fast,
+                             double beta_slow, double eps, double* q_out, double* w_out) {
+  for (int64_t t = 0; t < T; ++t) {
+    double* h = (double*)malloc(sizeof(double) * (size_t)dim);
+    double* a = (double*)malloc(sizeof(double) * (size_t)r);
+    double* c = (double*)malloc(sizeof(double) * (size_t)r);
+    double* u = (double*)malloc(sizeof(double) * (size_t)n_h * head_dim);
+    for (int i = 0; i < dim; ++i) h[i] = orc_bf16(hidden[(size_t)t * dim + i]);
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < dim; ++i) acc += orc_bf16(wq_a[(size_t)j * dim + i]) * h[i];
+      a[j] = acc;
+    }
+    orc_rmsnorm(a, q_norm, r, eps, c);
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < n_h * head_dim; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < r; ++i) acc += orc_bf16(wq_b[(size_t)j * r + i]) * c[i];
+      u[j] = acc;
+    }
+    for (int hh = 0; hh < n_h; ++hh) {
+      double* uh = u + (size_t)hh * head_dim;
+      orc_rope_yarn(uh, head_dim, rope_dim, pos[t], base, factor, orig_len, beta_fast, beta_slow);
+      orc_hadamard(uh, head_dim, q_out + ((size_t)t * n_h + hh) * head_dim);
+    }
+    double ws = 1.0 / sqrt((double)head_dim) / sqrt((double)n_h);
+    for (int hh = 0; hh < n_h; ++hh) {
+      double acc = 0.0;
+      for (int i = 0; i < dim; ++i) acc += orc_bf16(w_proj[(size_t)hh * dim + i]) * h[i];
+      w_out[(size_t)t * n_h + hh] = acc * ws;
+    }
+    free(h);
+    free(a);
+    free(c);
+    free(u);
+  }
+}
+
 ORC_API int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -509,6 +509,124 @@ def pin_ensemble_closed_forms(orc):
 
 
 # ---------------------------------------------------------------------------
+# query projection chain ([RM] "Retriever architecture", "Hyperparameters")
+# ---------------------------------------------------------------------------
+
+def pin_rmsnorm_closed_forms(orc):
+    """RMSNorm divides by the root mean square: (3, 4) has mean square 12.5,
+    so with unit gain and eps = 0 it maps to (3, 4) / sqrt(12.5); a constant
+    vector maps to +-1; scaling the input does not change the output (eps = 0);
+    the gain multiplies element by element; eps sits inside the root."""
+    one = f32_to_bf16_bits(np.ones(2, np.float32))
+    y = orc.rmsnorm(np.array([3.0, 4.0]), one, eps=0.0)
+    assert np.allclose(y, np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15)
+    g8 = f32_to_bf16_bits(np.ones(8, np.float32))
+    assert np.allclose(orc.rmsnorm(np.full(8, -2.5), g8, eps=0.0), -1.0, rtol=1e-15)
+    rng = np.random.default_rng(51)
+    x = rng.standard_normal(64)
+    g = f32_to_bf16_bits(rng.standard_normal(64).astype(np.float32))
+    y1 = orc.rmsnorm(x, g, eps=0.0)
+    assert np.allclose(orc.rmsnorm(7.5 * x, g, eps=0.0), y1, rtol=1e-13)
+    ones = f32_to_bf16_bits(np.ones(64, np.float32))
+    assert np.allclose(y1, orc.rmsnorm(x, ones, eps=0.0) * bf16_bits_to_f64(g), rtol=1e-15)
+    # eps inside the root: mean square 1 with eps = 3 halves the output
+    assert np.allclose(orc.rmsnorm(np.ones(4), f32_to_bf16_bits(np.ones(4, np.float32)), eps=3.0), 0.5, rtol=1e-15)
+
+
+def pin_yarn_frequencies(orc):
+    """YaRN's NTK-by-parts frequencies at the pages' hyperparameters (64
+    rotary dims, base 160000, factor 16, original length 65536, beta 32 / 1):
+    pair 0 (theta = 1) turns 65536 / 2 pi times in the original context, far
+    above beta_fast, and keeps its frequency; the slowest pairs turn less than
+    once and are divided by the factor; factor 1 leaves every frequency at
+    base^(-2i/64); the scale theta'/theta never leaves [1/16, 1], decreases
+    with i, and is linear in the number of turns r inside the blend region."""
+    f = [orc.yarn_freq(i) for i in range(32)]
+    th = [160000.0 ** (-2.0 * i / 64) for i in range(32)]
+    assert f[0] == 1.0
+    turns = [65536 * t / (2 * math.pi) for t in th]
+    ratio = [a / b for a, b in zip(f, th)]
+    for i in range(32):
+        assert 1 / 16 - 1e-15 <= ratio[i] <= 1 + 1e-15
+        if turns[i] >= 32:
+            assert abs(ratio[i] - 1) < 1e-15
+        if turns[i] <= 1:
+            assert abs(ratio[i] - 1 / 16) < 1e-15
+    assert all(ratio[i] >= ratio[i + 1] - 1e-15 for i in range(31))
+    blend = [i for i in range(32) if 1 < turns[i] < 32]
+    assert len(blend) >= 3
+    i0, i1, i2 = blend[0], blend[len(blend) // 2], blend[-1]
+    slope01 = (ratio[i1] - ratio[i0]) / (turns[i1] - turns[i0])
+    slope12 = (ratio[i2] - ratio[i1]) / (turns[i2] - turns[i1])
+    assert abs(slope01 - slope12) < 1e-12 and abs(slope01 - (1 - 1 / 16) / 31) < 1e-12
+    assert all(abs(orc.yarn_freq(i, factor=1.0) - th[i]) <= 1e-15 * th[i] for i in range(32))
+
+
+def pin_rope_rotation(orc):
+    """Rotary embedding on the last 64 of 128 entries: position 0 is the
+    identity; the first 64 entries never change; each rotary pair keeps its
+    length; positions add (rotating by p1 then p2 equals rotating by p1 + p2);
+    the unit vector on entry 64 (pair 0, frequency 1) lands on
+    (cos p, sin p) in entries 64 and 65."""
+    rng = np.random.default_rng(53)
+    x = rng.standard_normal(128)
+    assert np.array_equal(orc.rope_yarn(x, 0), x)
+    y = orc.rope_yarn(x, 12345)
+    assert np.array_equal(y[:64], x[:64])
+    assert np.allclose(np.hypot(y[64::2], y[65::2]), np.hypot(x[64::2], x[65::2]), rtol=1e-13)
+    assert np.allclose(orc.rope_yarn(orc.rope_yarn(x, 700), 1234), orc.rope_yarn(x, 1934), rtol=0, atol=1e-11)
+    e = np.zeros(128)
+    e[64] = 1.0
+    for p in (1, 7, 100000):
+        z = orc.rope_yarn(e, p)
+        assert abs(z[64] - math.cos(p)) < 1e-12 and abs(z[65] - math.sin(p)) < 1e-12
+        assert np.count_nonzero(z) <= 2
+
+
+def pin_hadamard_transform(orc):
+    """The normalised Walsh-Hadamard transform equals scipy's Sylvester
+    Hadamard matrix divided by sqrt(n) (a library routine), is its own
+    inverse, keeps lengths, and maps e_0 to the constant 1/sqrt(n)."""
+    from scipy.linalg import hadamard
+    n = 128
+    rng = np.random.default_rng(57)
+    x = rng.standard_normal(n)
+    assert np.allclose(orc.hadamard(x), hadamard(n) @ x / math.sqrt(n), rtol=0, atol=1e-12)
+    assert np.allclose(orc.hadamard(orc.hadamard(x)), x, rtol=0, atol=1e-12)
+    assert abs(np.linalg.norm(orc.hadamard(x)) - np.linalg.norm(x)) < 1e-12
+    e0 = np.zeros(n)
+    e0[0] = 1.0
+    assert np.allclose(orc.hadamard(e0), 1 / math.sqrt(n), rtol=1e-15)
+
+
+def pin_query_chain_composition(orc):
+    """The chain is the composition of its steps in the pages' order: Linear
+    (weights [out, in]) -> RMSNorm -> Linear -> per-head rotary -> per-head
+    Hadamard; the head weights are a Linear of the hidden state times
+    head_dim^-1/2 n_h^-1/2 (here 1 / sqrt(16 * 3)).  Matrix products from
+    numpy, the steps from their pinned oracle functions."""
+    rng = np.random.default_rng(59)
+    T, dim, r, n_h, hd = 3, 24, 16, 3, 16
+    hidden = f32_to_bf16_bits(rng.standard_normal((T, dim)).astype(np.float32))
+    wa = f32_to_bf16_bits((rng.standard_normal((r, dim)) / 5).astype(np.float32))
+    gn = f32_to_bf16_bits(rng.uniform(0.5, 1.5, r).astype(np.float32))
+    wb = f32_to_bf16_bits((rng.standard_normal((n_h * hd, r)) / 4).astype(np.float32))
+    wp = f32_to_bf16_bits(rng.standard_normal((n_h, dim)).astype(np.float32))
+    pos = np.array([0, 17, 262143], dtype=np.int64)
+    rope = dict(rope_dim=8, base=10000.0, factor=4.0, orig_len=64.0, beta_fast=8.0, beta_slow=1.0)
+    q, w = orc.query_chain(hidden, wa, gn, wb, wp, pos, n_h=n_h, head_dim=hd, eps=1e-6, **rope)
+    h = bf16_bits_to_f64(hidden)
+    for t in range(T):
+        a = bf16_bits_to_f64(wa) @ h[t]
+        c = orc.rmsnorm(a, gn, eps=1e-6)
+        u = (bf16_bits_to_f64(wb) @ c).reshape(n_h, hd)
+        for hh in range(n_h):
+            want = orc.hadamard(orc.rope_yarn(u[hh], int(pos[t]), **rope))
+            assert np.allclose(q[t, hh], want, rtol=1e-12, atol=1e-12), (t, hh)
+        assert np.allclose(w[t], bf16_bits_to_f64(wp) @ h[t] / math.sqrt(hd * n_h), rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # page recall (densest resident pages)
 # ---------------------------------------------------------------------------
 

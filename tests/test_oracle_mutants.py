@@ -80,6 +80,26 @@ MUTANTS = {
                             "memcpy(&scale_out[i], row + d - 4, sizeof(float));"),
     "unpack_row_stride_d": ("const uint8_t* row = ck + (size_t)i * (size_t)(d + 4);",
                             "const uint8_t* row = ck + (size_t)i * (size_t)d;"),
+    "rmsnorm_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)n + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
+    "rmsnorm_eps_outside": ("double inv = 1.0 / sqrt(ss / (double)n + eps);", "double inv = 1.0 / (sqrt(ss / (double)n) + eps);"),
+    "rmsnorm_gain_ignored": ("y[i] = x[i] * inv * orc_bf16(g[i]);", "y[i] = x[i] * inv;"),
+    "yarn_blend_swapped": ("return (1.0 - gamma) * theta / factor + gamma * theta;",
+                           "return gamma * theta / factor + (1.0 - gamma) * theta;"),
+    "yarn_turns_without_2pi": ("double r = orig_len * theta / two_pi;", "double r = orig_len * theta;"),
+    "yarn_exponent_per_dim": ("double theta = pow(base, -2.0 * (double)i / (double)rope_dim);",
+                              "double theta = pow(base, -(double)i / (double)rope_dim);"),
+    "rope_half_split_pairs": ("double x0 = xr[2 * i], x1 = xr[2 * i + 1];\n    xr[2 * i] = x0 * c - x1 * sn;\n    xr[2 * i + 1] = x0 * sn + x1 * c;",
+                              "double x0 = xr[i], x1 = xr[i + rope_dim / 2];\n    xr[i] = x0 * c - x1 * sn;\n    xr[i + rope_dim / 2] = x0 * sn + x1 * c;"),
+    "rope_on_first_dims": ("double* xr = x + head_dim - rope_dim;", "double* xr = x;"),
+    "rope_reverse_turn": ("xr[2 * i] = x0 * c - x1 * sn;", "xr[2 * i] = x0 * c + x1 * sn;"),
+    "hadamard_unnormalised": ("double norm = 1.0 / sqrt((double)n);", "double norm = 1.0;"),
+    "hadamard_or_not_and": ("__builtin_popcount((unsigned)(i & j))", "__builtin_popcount((unsigned)(i | j))"),
+    "chain_wq_b_transposed": ("acc += orc_bf16(wq_b[(size_t)j * r + i]) * c[i];",
+                              "acc += orc_bf16(wq_b[(size_t)i * (n_h * head_dim) + j]) * c[i];"),
+    "chain_weight_scale_missing": ("w_out[(size_t)t * n_h + hh] = acc * ws;", "w_out[(size_t)t * n_h + hh] = acc;"),
+    "chain_hadamard_before_rope": (
+        "      orc_rope_yarn(uh, head_dim, rope_dim, pos[t], base, factor, orig_len, beta_fast, beta_slow);\n      orc_hadamard(uh, head_dim, q_out + ((size_t)t * n_h + hh) * head_dim);",
+        "      double* qo = q_out + ((size_t)t * n_h + hh) * head_dim;\n      orc_hadamard(uh, head_dim, qo);\n      orc_rope_yarn(qo, head_dim, rope_dim, pos[t], base, factor, orig_len, beta_fast, beta_slow);"),
     "recall_bit_reversed": ("int resident = (mask[b * words + (s >> 5)] >> (s & 31)) & 1u;",
                             "int resident = (mask[b * words + (s >> 5)] >> (31 - (s & 31))) & 1u;"),
 }
