@@ -546,6 +546,9 @@ def run_ours(args):
             v = RetrieverMemIndex(torch, dev, fm, mode=mode)
             variants[name] = v.measure(10, 3, pk)
             del v
+        v = QueryChain(torch, dev, fm)
+        variants["query_chain"] = v.measure(20, 3, pk)
+        del v
         if fm.fm_device_status(reset=True) != 0:
             raise RuntimeError("device status flagged an error in the variant rows")
 
@@ -739,6 +742,58 @@ class FullHistoryPaged:
                 "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "algorithmic_bytes": self.bytes(),
                 "launches": 3, "reps": reps,
                 "workload": f"full-history paged top-{c.k}: {c.Q} queries x {c.R} pages (all of a 1M-token history), E4M3"}
+
+
+class QueryChain:
+    """The query side of the retriever's three indexer layers (fm_query_chain:
+    wq_a -> RMSNorm -> wq_b -> YaRN rotary -> Walsh-Hadamard, plus the head
+    weights) for one decode token of each of the 1M workload's 30 requests.
+    Each layer has its own synthetic weights (dim 4096, rank 2048, 128 heads of
+    128): 86 MB of bf16 weights per layer, 258 MB per call over the three
+    layers, above the 129 MB L2.  Timed on its own after the step."""
+
+    def __init__(self, torch, dev, fm, small=False, T=30, layers=3):
+        import gen
+        self.torch, self.fm = torch, fm
+        self.T, self.layers, self.dim, self.r, self.n_h = T, layers, 4096, 2048, 128
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).to(dev)
+        self.sets = []
+        for l in range(layers):
+            ins = gen.query_chain_inputs(T, dim=self.dim, r=self.r, n_h=self.n_h, seed=gen.BASE_SEED + 600 + l)
+            self.sets.append([t(a) for a in ins])
+        self.q = torch.empty((layers, T, self.n_h, 128), dtype=torch.int16, device=dev)
+        self.w = torch.empty((layers, T, self.n_h), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(fm.fm_query_chain_workspace(T, self.r, self.n_h), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        for l, (hidden, wq_a, q_norm, wq_b, w_proj, pos) in enumerate(self.sets):
+            self.fm.fm_query_chain(hidden, wq_a, q_norm, wq_b, w_proj, pos, self.q[l], self.w[l], workspace=self.ws)
+
+    def bytes(self):
+        T, dim, r, n_h = self.T, self.dim, self.r, self.n_h
+        weights = (r * dim + r + n_h * 128 * r + n_h * dim) * 2
+        io = T * dim * 2 + T * 8 + T * n_h * 128 * 2 + T * n_h * 4
+        return self.layers * (weights + io)
+
+    def measure(self, reps, warmup, pk):
+        torch = self.torch
+        for _ in range(warmup):
+            self.call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            self.call()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        ach = self.bytes() / (ms / 1e3) / 1e9
+        return {"ms": round(ms, 4), "tokens_per_s": self.T * self.layers / (ms / 1e3), "bound": "hbm",
+                "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": self.bytes(), "launches": "3 cuBLAS GEMMs + 2 kernels per layer", "reps": reps,
+                "workload": (f"query chain: {self.T} decode tokens x {self.layers} indexer layers, dim {self.dim}, "
+                             f"rank {self.r}, {self.n_h} heads x 128 (bf16 weights, fp32 accumulate)")}
 
 
 def run_profile_case(args, fm, torch, W, cfgs, ws):

@@ -334,6 +334,28 @@ def pack_compressed_k(k8: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return np.concatenate([np.asarray(k8, dtype=np.uint8), sc.view(np.uint8).reshape(sc.shape + (4,))], axis=-1)
 
 
+def query_chain_inputs(T: int, dim: int = 4096, r: int = 2048, n_h: int = 128, head_dim: int = 128,
+                       seed: int = BASE_SEED + 11, pos=None):
+    """Synthetic weights and inputs of one CSA layer's query chain (bf16 bits):
+    hidden [T,dim] ~ N(0,1), wq_a [r,dim] ~ N(0,1/dim), q_norm [r] ~ U(0.5,1.5),
+    wq_b [n_h*head_dim, r] ~ N(0,1/r), w_proj [n_h,dim] ~ N(0,1/dim); pos [T]
+    int64 spread over a 1M-token context unless given."""
+    rng = np.random.default_rng(seed)
+
+    def bf16(a):
+        u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    hidden = bf16(rng.standard_normal((T, dim)))
+    wq_a = bf16(rng.standard_normal((r, dim)) / np.sqrt(dim))
+    q_norm = bf16(rng.uniform(0.5, 1.5, r))
+    wq_b = bf16(rng.standard_normal((n_h * head_dim, r)) / np.sqrt(r))
+    w_proj = bf16(rng.standard_normal((n_h, dim)) / np.sqrt(dim))
+    if pos is None:
+        pos = rng.integers(0, 1 << 20, T)
+        pos[: min(T, 3)] = [0, 65535, (1 << 20) - 1][: min(T, 3)]
+    return hidden, wq_a, q_norm, wq_b, w_proj, np.asarray(pos, dtype=np.int64)
+
+
 def memindex_fp8_owner(cfg: MemIndexCfg) -> np.ndarray:
     """owner [B*L*S/64, 3] int32: (request, layer, block) of each 64-chunk block."""
     nb = cfg.S // 64
@@ -437,6 +459,6 @@ def prefill_host(cfg: PrefillCfg, pos=None):
 __all__ = [
     "BASE_SEED", "MemIndexCfg", "PagedCfg", "PrefillCfg", "TINY", "MEMINDEX_256K", "MEMINDEX_1M",
     "PAGED_512K", "PAGED_1M", "PAGED_FULL_1M", "RETRIEVER_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
-    "memindex_keys_device", "planted", "pack_compressed_k", "paged_tables", "paged_qw", "paged_pool_host",
+    "memindex_keys_device", "planted", "pack_compressed_k", "query_chain_inputs", "paged_tables", "paged_qw", "paged_pool_host",
     "paged_chunk_rows", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
 ]

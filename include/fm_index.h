@@ -167,6 +167,42 @@ fm_status fm_retriever_score_mask(const uint16_t* q, const float* w, const uint8
                                   float* logits_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
 
 /*
+ * The query side of a CSA layer's indexer ([RM] "Retriever architecture",
+ * "Hyperparameters"): from T tokens' hidden states to the query heads and head
+ * weights the Memory Indexer / retriever score with.  For token t:
+ *     a = wq_a . h_t                  Linear dim -> r, no bias
+ *     c = RMSNorm(a; q_norm, eps)     c = a / sqrt(mean(a^2) + eps) * q_norm
+ *     u = wq_b . c                    Linear r -> n_h * 128, reshaped [n_h, 128]
+ *     q_h = H(RoPE(u_h, pos_t))       rotary (YaRN) on entries 64..127, pairs
+ *                                     (64+2i, 65+2i), angle pos_t * theta'_i,
+ *                                     then the normalised Walsh-Hadamard
+ *                                     transform H (Sylvester order, / sqrt(128))
+ *     w = (w_proj . h_t) / sqrt(128 * n_h)
+ * theta'_i is YaRN's NTK-by-parts frequency of base^(-2i/64) (rope_base,
+ * rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow; the retriever
+ * uses 160000, 16, 65536, 32, 1).  The GEMMs take bf16 inputs with fp32
+ * accumulation; the RMSNorm output is rounded to bf16 (wq_b's input type).
+ *
+ *   hidden   [T, dim] bf16;  wq_a [r, dim], q_norm [r], wq_b [n_h*128, r],
+ *            w_proj [n_h, dim] bf16 (row-major [out, in]; 16-byte aligned)
+ *   pos      [T] int64 token positions
+ *   dim, r   multiples of 8; head_dim == 128; rope_dim == 64
+ *   q_out    [T, n_h, 128] bf16 (required); q_out_f32 [T, n_h, 128] or NULL
+ *   w_out    [T, n_h] fp32 (required)
+ *   workspace >= fm_query_chain_workspace(T, r, n_h) bytes, 256-byte aligned
+ * The projections run in cuBLAS (one handle per device, created on first
+ * use, shared by callers; its stream is set to `stream` for each call).
+ * Errors: FM_ERR_INVALID_ARG for bad sizes, parameters or pointers;
+ * FM_ERR_WORKSPACE; FM_ERR_CUDA for a cuBLAS failure.
+ */
+size_t fm_query_chain_workspace(int T, int r, int n_h);
+fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, const uint16_t* q_norm, const uint16_t* wq_b,
+                         const uint16_t* w_proj, const int64_t* pos, int T, int dim, int r, int n_h, int head_dim,
+                         int rope_dim, double rope_base, double rope_factor, double rope_orig_len,
+                         double rope_beta_fast, double rope_beta_slow, float eps, uint16_t* q_out, float* q_out_f32,
+                         float* w_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
+
+/*
  * Top-k select over caller-provided scores ([FM] sec. 3 "Top-k" of the native
  * score; [V4] sec. 3 CSA-2 top-512).
  *

@@ -84,6 +84,12 @@ def lib() -> ctypes.CDLL:
             L.fm_retriever_workspace.restype = _SZ
             L.fm_retriever_score_mask.argtypes = [_VP, _VP, _VP, _I64, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _F,
                                                   _VP, _VP, _VP, _VP, _SZ, _VP]
+        if hasattr(L, "fm_query_chain"):
+            L.fm_query_chain_workspace.argtypes = [_I32, _I32, _I32]
+            L.fm_query_chain_workspace.restype = _SZ
+            _D = ctypes.c_double
+            L.fm_query_chain.argtypes = [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _I32, _D, _D, _D,
+                                         _D, _D, _F, _VP, _VP, _VP, _VP, _SZ, _VP]
         if hasattr(L, "fm_page_recall"):
             L.fm_page_recall.argtypes = [_VP, _I32, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _VP]
         for name in ("fm_memindex_score_mask", "fm_topk_select", "fm_native_topk_paged", "fm_index_prefill_topk",
@@ -157,6 +163,30 @@ def fm_memindex_score_mask_fp8(q, w, k8, k_scale, mask_out, maxsig_out=None, log
                                             k_scale.stride(0), k_scale.stride(1), B, L, S, n_h, d, float(threshold),
                                             _ptr(mask_out), _ptr(maxsig_out), _ptr(logits_out), _ptr(workspace),
                                             ws_bytes, _stream(stream)))
+
+
+# The retriever's rotary hyperparameters ("FlashMemory-DeepSeek-V4" README, "Hyperparameters").
+RETRIEVER_ROPE = dict(rope_base=160000.0, rope_factor=16.0, rope_orig_len=65536.0, rope_beta_fast=32.0,
+                      rope_beta_slow=1.0)
+
+
+def fm_query_chain_workspace(T: int, r: int, n_h: int) -> int:
+    return lib().fm_query_chain_workspace(T, r, n_h)
+
+
+def fm_query_chain(hidden, wq_a, q_norm, wq_b, w_proj, pos, q_out, w_out, q_out_f32=None, eps: float = 1e-6,
+                   workspace=None, stream=None, **rope) -> None:
+    """hidden [T,dim] bf16, wq_a [r,dim], q_norm [r], wq_b [n_h*128, r], w_proj [n_h,dim] bf16,
+    pos [T] int64 -> q_out [T,n_h,128] bf16, w_out [T,n_h] fp32 (q_out_f32 optional)."""
+    cfg = dict(RETRIEVER_ROPE, **rope)
+    T, dim = hidden.shape
+    r = wq_a.shape[0]
+    n_h = w_proj.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_query_chain(_ptr(hidden), _ptr(wq_a), _ptr(q_norm), _ptr(wq_b), _ptr(w_proj), _ptr(pos), T, dim,
+                                r, n_h, 128, 64, cfg["rope_base"], cfg["rope_factor"], cfg["rope_orig_len"],
+                                cfg["rope_beta_fast"], cfg["rope_beta_slow"], float(eps), _ptr(q_out),
+                                _ptr(q_out_f32), _ptr(w_out), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 ENSEMBLE_MAX, ENSEMBLE_MEAN = 0, 1

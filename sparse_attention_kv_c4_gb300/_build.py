@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfm_index.so")
 SOURCES = ["fm_api.cu", "memindex.cu", "memindex_fp8.cu", "retriever.cu", "topk.cu", "paged.cu", "prefill.cu", "noalloc.cu",
-           "recall.cu"]
+           "recall.cu", "query_chain.cu"]
 ARCH = ["-gencode=arch=compute_103a,code=sm_103a"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
@@ -39,7 +39,7 @@ def build(verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    cmd = [NVCC, *ARCH, "-shared", "--cudart", "shared", "-o", LIB, *objs,
+    cmd = [NVCC, *ARCH, "-shared", "--cudart", "shared", "-o", LIB, *objs, "-lcublas",
            "-Xlinker", f"-rpath={os.path.join(CUDA_HOME, 'lib64')}"]
     subprocess.run(cmd, check=True)
     return LIB
