@@ -29,6 +29,42 @@ FM_DEV float e4m3_value(uint32_t code) {
   return __half2float(__half(h));
 }
 
+// One head of the query split.  `raw` holds the lane's four bf16 elements
+// 4l .. 4l+3 of the head (the low half of raw.x is element 4l); r1 / r2 are
+// the head's t1 / t2 rows (128 bytes each); wq_h receives w_h * 2^e_h.  All
+// lanes of the warp call it.
+FM_DEV void split_head(uint2 raw, float w_h, uint8_t* __restrict__ r1, uint8_t* __restrict__ r2,
+                       float* __restrict__ wq_h) {
+  const int lane = threadIdx.x & 31;
+  const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+  float amax = 0.f;
+  for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int e = 0;
+  if (amax > 0.f && isfinite(amax)) {
+    e = ilogbf(amax) - 8;
+    if (ldexpf(amax, -e) > 448.f) e += 1;
+  }
+  uint32_t c1w = 0, c2w = 0;
+  for (int j = 0; j < 4; ++j) {
+    const float s = ldexpf(v[j], -e);
+    const uint32_t c1 = e4m3_rne(s);
+    const float r = s - e4m3_value(c1);
+    c1w |= c1 << (8 * j);
+    c2w |= e4m3_rne(r) << (8 * j);
+  }
+  reinterpret_cast<uint32_t*>(r1)[lane] = c1w;
+  reinterpret_cast<uint32_t*>(r2)[lane] = c2w;
+  if (lane == 0) *wq_h = ldexpf(w_h, e);
+}
+
+// The lane's slice of head h of a query block (16-byte aligned rows of 128
+// bf16 elements), as split_head takes it.
+FM_DEV uint2 load_head_slice(const uint16_t* __restrict__ q, int h) {
+  return __ldg(reinterpret_cast<const uint2*>(q + (int64_t)h * 128) + (threadIdx.x & 31));
+}
+
 // Split the n_heads x 128 bf16 query block q into t1 (rows 0..n_heads-1) and
 // t2 (rows n_heads..2 n_heads-1), 128 bytes per row, and write
 // wq[h] = w[h] * 2^e_h.  Called by every thread of a CTA of `nthreads`
@@ -36,31 +72,9 @@ FM_DEV float e4m3_value(uint32_t code) {
 // elements 4l .. 4l+3.
 FM_DEV void split_query(const uint16_t* __restrict__ q, const float* __restrict__ w, int n_heads, int nthreads,
                         uint8_t* __restrict__ t1, uint8_t* __restrict__ t2, float* __restrict__ wq) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int h = warp; h < n_heads; h += nthreads / 32) {
-    const uint16_t* qh = q + (int64_t)h * 128;
-    float v[4], amax = 0.f;
-    for (int j = 0; j < 4; ++j) {
-      v[j] = __uint_as_float((uint32_t)qh[4 * lane + j] << 16);
-      amax = fmaxf(amax, fabsf(v[j]));
-    }
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    int e = 0;
-    if (amax > 0.f && isfinite(amax)) {
-      e = ilogbf(amax) - 8;
-      if (ldexpf(amax, -e) > 448.f) e += 1;
-    }
-    uint8_t* r1 = t1 + (int64_t)h * 128;
-    uint8_t* r2 = t2 + (int64_t)h * 128;
-    for (int j = 0; j < 4; ++j) {
-      const float s = ldexpf(v[j], -e);
-      const uint32_t c1 = e4m3_rne(s);
-      const float r = s - e4m3_value(c1);
-      r1[4 * lane + j] = (uint8_t)c1;
-      r2[4 * lane + j] = (uint8_t)e4m3_rne(r);
-    }
-    if (lane == 0) wq[h] = ldexpf(w[h], e);
-  }
+  const int warp = threadIdx.x >> 5;
+  for (int h = warp; h < n_heads; h += nthreads / 32)
+    split_head(load_head_slice(q, h), __ldg(w + h), t1 + (int64_t)h * 128, t2 + (int64_t)h * 128, wq + h);
 }
 
 // Instruction descriptor, kind::f8f6f4 with E4M3 A/B, fp32 accumulate, K-major.

@@ -26,7 +26,9 @@
 //     of tile i), four issuing threads and four epilogue warp groups take
 //     tiles in turn.  The epilogue (thread = chunk) reads its 64 dots, applies
 //     the chunk's scale, ReLU and w (from a per-warp shared-memory copy), and
-//     writes y to the workspace.
+//     writes y to the workspace.  Key copies carry an L2 evict-first hint and
+//     score stores an evict-last hint, so the scores are still in L2 when
+//     the top-k reads them.
 //  3. the block top-k (topk.cuh), mapping candidate i to its chunk id.
 #include <math.h>
 
@@ -55,6 +57,41 @@ constexpr int kAccCols = kHeads;  // one column per head: the t1 and t2 MMAs acc
 constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
 constexpr int kPrepThreads = 256;
 
+// L2 priorities.  The keys are read once per call and the scores are read
+// back by the top-k right after: the key copies go in as evict-first and the
+// score stores as evict-last, so the [Q, R*64] score block (62 MB for 630
+// queries x 384 pages) stays in the 129 MB L2 for the top-k instead of being
+// evicted by the key stream.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void st_f32_hint(float* addr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy) : "memory");
+}
+
 // --------------------------------------------------------------------------
 // 1. prep: sort pages, validate, split q
 // --------------------------------------------------------------------------
@@ -62,7 +99,7 @@ constexpr int kPrepThreads = 256;
 // THREADS: 256, or 1024 for tables longer than 1024 entries (the bitonic
 // sort's passes then take four elements per thread instead of sixteen).
 template <int THREADS>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threads: 760 queries per wave
     paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                       const int32_t* __restrict__ page_phys, const int32_t* __restrict__ page_logical,
                       const int32_t* __restrict__ n_res, int R, int64_t P, int Rpow2,
@@ -74,6 +111,16 @@ __global__ void __launch_bounds__(THREADS)
   __shared__ unsigned long long keys[kMaxR];
   __shared__ uint32_t warp_tot[THREADS / 32];
   const int qi = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the query and head weights are loaded first, so that their latency
+  // overlaps the page-table sort (warp i splits heads i, i + THREADS/32, ...)
+  constexpr int kWarps = THREADS / 32, kHeadsPerWarp = kHeads / kWarps;
+  uint2 qraw[kHeadsPerWarp];
+  float wraw[kHeadsPerWarp];
+#pragma unroll
+  for (int i = 0; i < kHeadsPerWarp; ++i) {
+    qraw[i] = load_head_slice(q + (int64_t)qi * kHeads * kDim, warp + i * kWarps);
+    wraw[i] = __ldg(w + (int64_t)qi * kHeads + warp + i * kWarps);
+  }
   int nr = R;
   if (n_res != nullptr) {
     const int v = n_res[qi];
@@ -180,8 +227,12 @@ __global__ void __launch_bounds__(THREADS)
   }
   // q split: q_h = 2^e_h (t1 + t2), 2^e_h folded into w
   uint8_t* t1 = qsplit + (int64_t)qi * 2 * kHeads * kDim;
-  split_query(q + (int64_t)qi * kHeads * kDim, w + (int64_t)qi * kHeads, kHeads, THREADS, t1,
-              t1 + (int64_t)kHeads * kDim, wq + (int64_t)qi * kHeads);
+#pragma unroll
+  for (int i = 0; i < kHeadsPerWarp; ++i) {
+    const int h = warp + i * kWarps;
+    split_head(qraw[i], wraw[i], t1 + (int64_t)h * kDim, t1 + (int64_t)(kHeads + h) * kDim,
+               wq + (int64_t)qi * kHeads + h);
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -261,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // query: lane i waits for the stage of the batch's i-th tile and issues its
     // copies, so the per-copy issue latency is paid once per batch.
     constexpr int kBatch = 8;
+    const uint64_t stream_policy = l2_policy_evict_first();
     __shared__ int issued_ph[kMaxStages];
     for (int s = lane; s < kMaxStages; s += 32) issued_ph[s] = -1;
     uint32_t seq = 0, q_phase = 0;
@@ -307,9 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the sorted page table is in the workspace (L2-resident): one
             // load per page, issued by all lanes of the batch in parallel
             const int32_t ph = __ldg(p.s_phys + qi * p.R + 2 * my_tile + h);
-            tma_load_2d(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0, ph * kPage);
-            bulk_load(scale_smem + stage * kM + h * kPage, p.k_scale + (int64_t)ph * kPage, kPage * 4,
-                      &bar_full[stage]);
+            tma_load_2d_hint(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0,
+                             ph * kPage, stream_policy);
+            bulk_load_hint(scale_smem + stage * kM + h * kPage, p.k_scale + (int64_t)ph * kPage, kPage * 4,
+                           &bar_full[stage], stream_policy);
           }
           issued_ph[stage] = (int)phase;
         }
@@ -407,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nres = 0;
     int64_t qi = t_begin / p.tiles_per_q;
     int tile = (int)(t_begin % p.tiles_per_q) - 1;
+    const uint64_t keep_policy = l2_policy_evict_last();
     for (int64_t t = t_begin; t < t_end; ++t) {
       if (++tile == p.tiles_per_q) {
         tile = 0;
@@ -471,10 +525,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned long long m = __ldg(p.pmask + qi * p.R + j);
             const int o = row & (kPage - 1);
             if ((m >> o) & 1ull)
-              p.scores[qi * ld + __ldg(p.pprefix + qi * (p.R + 1) + j) + __popcll(m & ((1ull << o) - 1ull))] = y;
+              st_f32_hint(p.scores + qi * ld + __ldg(p.pprefix + qi * (p.R + 1) + j) + __popcll(m & ((1ull << o) - 1ull)),
+                          y, keep_policy);
           }
         } else {
-          if (valid) p.scores[qi * ld + (int64_t)tile * kM + row] = y;
+          if (valid) st_f32_hint(p.scores + qi * ld + (int64_t)tile * kM + row, y, keep_policy);
         }
       }
       if (++acc == (uint32_t)kAccBufs) {

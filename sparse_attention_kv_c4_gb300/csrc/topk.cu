@@ -54,15 +54,19 @@ FM_DEV int row_len(const int32_t* __restrict__ n_valid, int64_t r, int n) {
 
 // kMap: 0 = candidate index, 1 = paged rows (PageMap), 2 = paged rows
 // compacted to resident chunks (MaskedPageMap); one instantiation each so the
-// id maps do not share a register allocation.
-template <int kMap>
-__global__ void __launch_bounds__(kTopkThreads, 4)  // four CTAs per SM (shared memory allows four)
+// id maps do not share a register allocation.  kShort: rows of at most
+// kTopkShortN scores take a smaller candidate list (kTopkCapShort), which lets
+// five CTAs share an SM instead of four (760 rows per wave on 152 SMs, so the
+// 630 queries of a 1M-context decode batch run in one wave).
+template <int kMap, bool kShort>
+__global__ void __launch_bounds__(kTopkThreads, kShort ? 5 : 4)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid, int n, int k,
                      const int32_t* __restrict__ page_ids, int64_t page_ld, const int32_t* __restrict__ page_prefix,
                      const unsigned long long* __restrict__ page_mask, int32_t* __restrict__ idx_out,
                      float* __restrict__ score_out) {
+  constexpr int kCap = kShort ? kTopkCapShort : kTopkCap;
   extern __shared__ uint8_t topk_smem_raw[];
-  TopkFastSmem<kTopkThreads>& sm = *reinterpret_cast<TopkFastSmem<kTopkThreads>*>(topk_smem_raw);
+  TopkFastSmem<kTopkThreads, kCap>& sm = *reinterpret_cast<TopkFastSmem<kTopkThreads, kCap>*>(topk_smem_raw);
   const int64_t r = blockIdx.x;
   const int nr = row_len(n_valid, r, n);
   const float* row = scores + r * ld;
@@ -72,11 +76,11 @@ __global__ void __launch_bounds__(kTopkThreads, 4)  // four CTAs per SM (shared 
     // all page_ld pages are searched: pages past the listed ones are empty
     const MaskedPageMap map{page_ids + r * page_ld, page_prefix + r * (page_ld + 1), page_mask + r * page_ld,
                             (int)page_ld};
-    block_topk<kTopkThreads>(row, nr, k, map, io, so, sm);
+    block_topk<kTopkThreads, kCap>(row, nr, k, map, io, so, sm);
   } else if constexpr (kMap == 1) {
-    block_topk<kTopkThreads>(row, nr, k, PageMap{page_ids + r * page_ld}, io, so, sm);
+    block_topk<kTopkThreads, kCap>(row, nr, k, PageMap{page_ids + r * page_ld}, io, so, sm);
   } else {
-    block_topk<kTopkThreads>(row, nr, k, IdentityMap{}, io, so, sm);
+    block_topk<kTopkThreads, kCap>(row, nr, k, IdentityMap{}, io, so, sm);
   }
 }
 
@@ -94,11 +98,23 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
                            const unsigned long long* page_mask, int32_t* idx_out, float* score_out,
                            cudaStream_t stream) {
   if (rows == 0) return FM_OK;
-  const int smem = (int)sizeof(TopkFastSmem<kTopkThreads>);
-  auto* kernel = page_mask != nullptr ? topk_rows_kernel<2> : (page_ids != nullptr ? topk_rows_kernel<1>
-                                                                                      : topk_rows_kernel<0>);
+  const bool short_rows = n <= kTopkShortN;
+  const int smem = short_rows ? (int)sizeof(TopkFastSmem<kTopkThreads, kTopkCapShort>)
+                              : (int)sizeof(TopkFastSmem<kTopkThreads, kTopkCap>);
+  void (*kernel)(const float*, int64_t, const int32_t*, int, int, const int32_t*, int64_t, const int32_t*,
+                 const unsigned long long*, int32_t*, float*);
+  if (short_rows)
+    kernel = page_mask != nullptr ? topk_rows_kernel<2, true>
+                                  : (page_ids != nullptr ? topk_rows_kernel<1, true> : topk_rows_kernel<0, true>);
+  else
+    kernel = page_mask != nullptr ? topk_rows_kernel<2, false>
+                                  : (page_ids != nullptr ? topk_rows_kernel<1, false> : topk_rows_kernel<0, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  // the whole shared-memory carveout, so that the occupancy shared memory
+  // allows (four or five CTAs) is not cut by a smaller L1 split
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: carveout: %s", cudaGetErrorString(e));
   kernel<<<rows, kTopkThreads, smem, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, page_prefix, page_mask,
                                                idx_out, score_out);
   e = cudaGetLastError();

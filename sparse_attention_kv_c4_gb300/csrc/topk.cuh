@@ -185,6 +185,8 @@ namespace fm {
 //     second read of the row (longer rows sort the selection instead).
 // Scores are reported from their keys: -0 reads as +0 and NaN as -inf.
 constexpr int kTopkCap = 4096;       // candidate slots (32 KB of shared memory)
+constexpr int kTopkCapShort = 3072;  // for rows of at most kTopkShortN scores (24 KB: five CTAs per SM)
+constexpr int kTopkShortN = 32768;
 constexpr int kTopkRuns = 32;        // sample: 32 runs x 64 scores
 constexpr int kTopkSample = kTopkRuns * 64;
 constexpr int kTopkBitmapN = 131072;  // rows up to this length emit ids via a bitmap
@@ -195,9 +197,9 @@ struct SelectSmem {
   uint32_t digit[2], above[2], in_digit[2];
 };
 
-template <int THREADS>
+template <int THREADS, int CAP = kTopkCap>
 struct TopkFastSmem {
-  unsigned long long cand[kTopkCap];
+  unsigned long long cand[CAP];
   unsigned long long cmax;
   union {
     unsigned long long sample[kTopkSample];
@@ -308,9 +310,9 @@ FM_DEV T block_select(const T* a, int n, int r, T lo, T hi, uint32_t loose, Sele
   return prefix;
 }
 
-template <int THREADS, typename IdxMap>
+template <int THREADS, int CAP, typename IdxMap>
 FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
-                       float* __restrict__ score_out, TopkFastSmem<THREADS>& sm) {
+                       float* __restrict__ score_out, TopkFastSmem<THREADS, CAP>& sm) {
   const int tid = threadIdx.x;
   const int kk = n < k ? n : k;
   if (kk == 0) {
@@ -322,8 +324,8 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   }
   // ---- 1. threshold from a sample --------------------------------------------
   unsigned long long theta = 0ull;
-  if (n > kTopkCap) {
-    const long long want = 3 * kk < 2 * kTopkCap / 3 ? 3 * kk : 2 * kTopkCap / 3;  // expected candidates
+  if (n > CAP) {
+    const long long want = 3 * kk < 2 * CAP / 3 ? 3 * kk : 2 * CAP / 3;  // expected candidates
     if (n <= kTopkBitmapN) {
       for (int i = tid; i < kTopkSample; i += THREADS) {
         const int run = i >> 6, off = i & 63;
@@ -408,7 +410,7 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   unsigned long long tmax = 0ull;  // this thread's largest stored composite
   auto store = [&](uint32_t slot, float v, int i) {
     const unsigned long long c = composite_of(v, i);
-    if (slot < (uint32_t)kTopkCap) {
+    if (slot < (uint32_t)CAP) {
       sm.cand[slot] = c;
       tmax = c > tmax ? c : tmax;
     } else {
