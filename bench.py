@@ -791,7 +791,7 @@ class QueryChain:
         ach = self.bytes() / (ms / 1e3) / 1e9
         return {"ms": round(ms, 4), "tokens_per_s": self.T * self.layers / (ms / 1e3), "bound": "hbm",
                 "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                "algorithmic_bytes": self.bytes(), "launches": "3 cuBLAS GEMMs + 2 kernels per layer", "reps": reps,
+                "algorithmic_bytes": self.bytes(), "launches": "2 projection GEMMs + 2 kernels per layer", "reps": reps,
                 "workload": (f"query chain: {self.T} decode tokens x {self.layers} indexer layers, dim {self.dim}, "
                              f"rank {self.r}, {self.n_h} heads x 128 (bf16 weights, fp32 accumulate)")}
 

@@ -190,10 +190,11 @@ fm_status fm_retriever_score_mask(const uint16_t* q, const float* w, const uint8
  *   q_out    [T, n_h, 128] bf16 (required); q_out_f32 [T, n_h, 128] or NULL
  *   w_out    [T, n_h] fp32 (required)
  *   workspace >= fm_query_chain_workspace(T, r, n_h) bytes, 256-byte aligned
- * The projections run in cuBLAS (one handle per device, created on first
- * use, shared by callers; its stream is set to `stream` for each call).
+ * The projections run on the tensor cores with the weights streamed once
+ * per 256 tokens; their K-split partial sums (in the workspace) are reduced
+ * in a fixed order, so results do not depend on scheduling.
  * Errors: FM_ERR_INVALID_ARG for bad sizes, parameters or pointers;
- * FM_ERR_WORKSPACE; FM_ERR_CUDA for a cuBLAS failure.
+ * FM_ERR_WORKSPACE; FM_ERR_CUDA for a launch failure.
  */
 size_t fm_query_chain_workspace(int T, int r, int n_h);
 fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, const uint16_t* q_norm, const uint16_t* wq_b,

@@ -39,7 +39,7 @@ def build(verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    cmd = [NVCC, *ARCH, "-shared", "--cudart", "shared", "-o", LIB, *objs, "-lcublas",
+    cmd = [NVCC, *ARCH, "-shared", "--cudart", "shared", "-o", LIB, *objs,
            "-Xlinker", f"-rpath={os.path.join(CUDA_HOME, 'lib64')}"]
     subprocess.run(cmd, check=True)
     return LIB

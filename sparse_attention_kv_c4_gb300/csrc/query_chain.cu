@@ -11,24 +11,39 @@
 //     w = (w_proj . h) * 128^-1/2 * n_h^-1/2
 //
 // GB300 mapping.  For a decode batch (tens of tokens) the three projections
-// stream 81 MB of bf16 weights per layer and are plain GEMMs: they run in
-// cuBLAS (bf16 inputs, fp32 accumulate and fp32 outputs).  The rest are two
-// small kernels:
-//   rmsnorm_kernel        one CTA per token: sum of squares in fp32, the
-//                         normalised row rounded to bf16 (wq_b's input type).
+// stream 86 MB of bf16 weights per layer against a few kilobytes of
+// activations: HBM-bound matrix products with 30 to 60 FLOP per weight byte,
+// more than the CUDA cores can sustain at full bandwidth.  They run on the
+// tensor cores with the weights as the streamed operand:
+//   proj_gemm_kernel      one CTA per (128-row weight tile, K split): a TMA
+//                         producer streams [128 rows x 64] weight chunks
+//                         (the UMMA A operand, SWIZZLE_128B) and the matching
+//                         [tokens x 64] activation chunks (B, tokens padded to
+//                         a multiple of 16 by the copy's zero fill); one thread
+//                         issues tcgen05.mma kind::f16 M=128 N=tokens K=16 into
+//                         a TMEM accumulator; four epilogue warps write the
+//                         fp32 partial sums (thread = weight row).  wq_a and
+//                         w_proj share the hidden state, so they are one launch
+//                         (w_proj's tile after wq_a's).  Each GEMM is split
+//                         along K so that tiles x splits fills the SMs once.
+//   rmsnorm_kernel        one CTA per token: sums the K-split partials of a in
+//                         a fixed order, RMSNorm in fp32, the normalised row
+//                         rounded to bf16 (wq_b's input type); also the head
+//                         weights w from w_proj's partials.
 //   rope_hadamard_kernel  one warp per (token, head), four entries per lane:
-//                         the rotary angles pos * theta'_i are formed and
-//                         reduced in fp64 (positions reach 2^20, where an
-//                         fp32 angle would lose whole radians), the
-//                         Walsh-Hadamard butterflies run in registers (strides
+//                         sums u's partials, forms and reduces the rotary
+//                         angles pos * theta'_i in fp64 (positions reach 2^20,
+//                         where an fp32 angle would lose whole radians), runs
+//                         the Walsh-Hadamard butterflies in registers (strides
 //                         1 and 2 inside a lane, 4..64 across lanes by
-//                         shuffles), and q is written as bf16 (and fp32 when
+//                         shuffles), and writes q as bf16 (and fp32 when
 //                         asked).
-#include <cublas_v2.h>
+// Partial sums are reduced in a fixed order, so results do not depend on
+// scheduling.
 #include <cuda_bf16.h>
 #include <math.h>
 
-#include <mutex>
+#include <cmath>
 
 #include "fm_common.cuh"
 #include "fm_internal.h"
@@ -40,22 +55,342 @@ namespace {
 
 constexpr int kHeadDim = 128;
 constexpr int kRopeDim = 64;
-constexpr int kNormThreads = 256;
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-struct RopeCfg {
-  double base, factor, orig_len, beta_fast, beta_slow;
+// Programmatic dependent launch.  The chain's second to fourth kernels are
+// launched with programmatic stream serialisation: each may start while its
+// predecessor finishes, and waits (griddepcontrol.wait) for the predecessor's
+// completion and memory before it reads that kernel's output or writes
+// anything.  The first GEMM is launched normally, so nothing of the chain
+// starts before the caller's earlier work has finished.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Rotary frequencies theta'_i of the 32 pairs, computed once per call on the
+// host (fp64) and passed by value.
+struct RopeFreqs {
+  double f[kRopeDim / 2];
 };
 
+// ---------------------------------------------------------------------------
+// Projection GEMM for a few tokens:
+//     part[split][t][col] = sum_{k in split} X[t, k] * W[col, k]
+// W is W0 (tiles 0 .. nt0-1) then W1 (tiles nt0 ..), 128 rows per tile.
+// ---------------------------------------------------------------------------
+constexpr int kGM = 128;                  // weight rows per tile (UMMA M, TMEM lanes)
+constexpr int kGK = 64;                   // K elements per chunk: one 128-byte swizzle atom
+constexpr int kGAtomA = kGM * kGK * 2;    // 16 KB of weights per chunk
+constexpr int kGThreads = 192;            // producer warp, issuer warp, four epilogue warps
+constexpr int kGMaxStages = 8;
+constexpr int kGMaxTokens = 256;          // tokens per launch (UMMA N <= 256)
+constexpr int kGMaxSplits = 16;
+constexpr int kGSizingSms = 160;          // workspace sizing bound on the SM count (GB300: 152)
+
+struct GemmParams {
+  float* part;
+  unsigned int* status;
+  int64_t ld_part;     // columns of part: (nt0 + nt1) * 128
+  int64_t t_rows;      // rows of one split's block of part (all tokens of the call)
+  int t_base;          // first token of this launch
+  int T;               // tokens in this launch (<= kGMaxTokens)
+  int tpad;            // UMMA N: T rounded up to 16
+  int kc;              // K chunks
+  int nt0;             // tiles of W0
+  int splits;
+  int stages;
+  uint32_t tmem_cols;
+};
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    proj_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w0, const __grid_constant__ CUtensorMap tmap_w1,
+                     const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int b_bytes = p.tpad * 128;
+  const int stage_bytes = kGAtomA + b_bytes;  // both multiples of 1 KB (the swizzle atom)
+
+  __shared__ __align__(8) uint64_t bar_full[kGMaxStages], bar_empty[kGMaxStages], bar_tfull, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  const int c_begin = (int)((int64_t)p.kc * split / p.splits);
+  const int c_end = (int)((int64_t)p.kc * (split + 1) / p.splits);  // > c_begin: splits <= kc
+  const bool second = tile >= p.nt0;
+  const int row0 = (second ? tile - p.nt0 : tile) * kGM;
+  const CUtensorMap* wmap = second ? &tmap_w1 : &tmap_w0;
+  const int stages = p.stages;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_tfull, 1);
+    mbar_init(&bar_drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(wmap);
+    tma_prefetch(&tmap_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+  grid_dep_launch_dependents();  // the next kernel may start (it waits for this one's completion)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ TMA producer ------------------------------
+      int issued[kGMaxStages];
+      for (int s = 0; s < kGMaxStages; ++s) issued[s] = -1;
+      // The first stages' weight chunks go out before the dependency wait:
+      // weights are never written by the kernels this one may overlap.  The
+      // activation chunks (the previous kernel's output) follow the wait.
+      const int pre = c_end - c_begin < stages ? c_end - c_begin : stages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&bar_full[i], (uint32_t)stage_bytes);
+        tma_load_2d(smem + i * stage_bytes, wmap, &bar_full[i], (c_begin + i) * kGK, row0);
+        issued[i] = 0;
+      }
+      grid_dep_wait();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(smem + i * stage_bytes + kGAtomA, &tmap_x, &bar_full[i], (c_begin + i) * kGK, p.t_base);
+      uint32_t stage = (uint32_t)(pre % stages), phase = pre == stages ? 1u : 0u;
+      for (int c = c_begin + pre; c < c_end; ++c) {
+        if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)stage_bytes);
+        uint8_t* st = smem + stage * stage_bytes;
+        tma_load_2d(st, wmap, &bar_full[stage], c * kGK, row0);
+        tma_load_2d(st + kGAtomA, &tmap_x, &bar_full[stage], c * kGK, p.t_base);
+        issued[stage] = (int)phase;
+        if (++stage == (uint32_t)stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (abort_flag) {  // let copies already in flight land before the CTA exits
+        for (int s = 0; s < stages; ++s)
+          if (issued[s] >= 0) mbar_wait_drain(&bar_full[s], (uint32_t)issued[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------ UMMA issuer -------------------------------
+      const uint32_t idesc = idesc_bf16_f32(kGM, p.tpad);
+      const uint64_t desc0 = sdesc_sw128(smem_u32(smem));
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int c = c_begin; c < c_end; ++c) {
+        if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // descriptor start-address field counts 16-byte units; K=16 steps are
+        // 32 bytes apart inside the 128-byte swizzle atom
+        const uint64_t a_desc = desc0 + (uint64_t)(stage * (stage_bytes >> 4));
+        const uint64_t b_desc = a_desc + (uint64_t)(kGAtomA >> 4);
+#pragma unroll
+        for (int k = 0; k < kGK / 16; ++k)
+          umma_bf16_ss(tmem_base, a_desc + 2 * k, b_desc + 2 * k, idesc, (c > c_begin || k > 0) ? 1u : 0u);
+        umma_commit(&bar_empty[stage]);
+        if (++stage == (uint32_t)stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) umma_commit(&bar_tfull);
+      umma_commit(&bar_drain);
+      mbar_wait_drain(&bar_drain, 0);
+    }
+  } else {
+    // ------------------------------ epilogue -------------------------------------
+    // warp w reads TMEM lanes 32 (w % 4) ..: thread = weight row of the tile
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    if (mbar_wait(&bar_tfull, 0, &abort_flag, p.status)) {
+      tc_fence_after();
+      float* out = p.part + ((int64_t)split * p.t_rows + p.t_base) * p.ld_part + (int64_t)tile * kGM + row;
+      for (int t0 = 0; t0 < p.tpad; t0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)t0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (t0 + j < p.T) out[(int64_t)(t0 + j) * p.ld_part] = __uint_as_float(r[j]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// K splits of a projection with `tiles` weight tiles: enough that
+// tiles x splits fills the SMs once, at most one per K chunk.
+int gemm_splits(int tiles, int kc, int num_sms) {
+  int s = num_sms / tiles;
+  const int cap = kGSizingSms / tiles < kGMaxSplits ? kGSizingSms / tiles : kGMaxSplits;
+  if (s > cap) s = cap;
+  if (s > kc) s = kc;
+  return s < 1 ? 1 : s;
+}
+// Upper bound of gemm_splits over devices and K (sizes the workspace).
+int gemm_splits_max(int tiles) {
+  const int cap = kGSizingSms / tiles < kGMaxSplits ? kGSizingSms / tiles : kGMaxSplits;
+  return cap < 1 ? 1 : cap;
+}
+
+// part[s][t][col] for the T tokens of X [T, K] against W0 [N0, K] and W1
+// [N1, K] (W1 may be null); ld_part = (ceil(N0/128) + ceil(N1/128)) * 128.
+// Launches one grid per 256 tokens.
+fm_status proj_gemm(const uint16_t* X, int T, int K, const uint16_t* W0, int N0, const uint16_t* W1, int N1,
+                    int num_sms, float* part, int* splits_out, unsigned int* status, bool pdl, cudaStream_t stream) {
+  const int nt0 = (N0 + kGM - 1) / kGM, nt1 = W1 != nullptr ? (N1 + kGM - 1) / kGM : 0;
+  const int kc = (K + kGK - 1) / kGK;
+  const int splits = gemm_splits(nt0 + nt1, kc, num_sms);
+  *splits_out = splits;
+  CUtensorMap tw0, tw1, tx;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N0};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {(uint32_t)kGK, (uint32_t)kGM};
+    fm_status st = make_tmap(&tw0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W0, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  }
+  if (W1 != nullptr) {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N1};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {(uint32_t)kGK, (uint32_t)kGM};
+    fm_status st = make_tmap(&tw1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W1, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  } else {
+    tw1 = tw0;
+  }
+  for (int t_base = 0; t_base < T; t_base += kGMaxTokens) {
+    const int Tb = T - t_base < kGMaxTokens ? T - t_base : kGMaxTokens;
+    const int tpad = (Tb + 15) / 16 * 16;
+    {
+      // rows past T read as zeros (the copy's out-of-bounds fill)
+      const uint64_t dims[2] = {(uint64_t)K, (uint64_t)T};
+      const uint64_t strides[1] = {(uint64_t)K * 2};
+      const uint32_t box[2] = {(uint32_t)kGK, (uint32_t)tpad};
+      fm_status st = make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != FM_OK) return st;
+    }
+    GemmParams gp;
+    gp.part = part;
+    gp.status = status;
+    gp.ld_part = (int64_t)(nt0 + nt1) * kGM;
+    gp.t_rows = T;
+    gp.t_base = t_base;
+    gp.T = Tb;
+    gp.tpad = tpad;
+    gp.kc = kc;
+    gp.nt0 = nt0;
+    gp.splits = splits;
+    const int stage_bytes = kGAtomA + tpad * 128;
+    int stages = (200 * 1024) / stage_bytes;
+    if (stages > kGMaxStages) stages = kGMaxStages;
+    gp.stages = stages;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)tpad) cols <<= 1;
+    gp.tmem_cols = cols;
+    const int smem = 1024 + stages * stage_bytes;
+    cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "query chain: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    const unsigned grid = (unsigned)((nt0 + nt1) * splits);
+    if (pdl) {
+      e = launch_pdl(proj_gemm_kernel, grid, kGThreads, (size_t)smem, stream, tw0, tw1, tx, gp);
+    } else {
+      proj_gemm_kernel<<<grid, kGThreads, smem, stream>>>(tw0, tw1, tx, gp);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "query chain: GEMM launch: %s", cudaGetErrorString(e));
+  }
+  return FM_OK;
+}
+
+// One CTA per token t: a = sum of the splits of part[., t, 0..r), RMSNorm,
+// rounded to bf16; w[t, h] = w_scale * sum of the splits of part[., t, w_col0 + h].
+// The splits are summed in order 0, 1, ...  A thread takes its elements two at
+// a time with the partial loads of up to eight splits issued together, so the
+// row's reduction costs a few memory round trips, not one per split.
+constexpr int kNormThreads = 1024;
+constexpr int kNormUnroll = 2;
+constexpr int kNormSplitBatch = 8;
 __global__ void __launch_bounds__(kNormThreads)
-    rmsnorm_kernel(const float* __restrict__ a, const uint16_t* __restrict__ g, int r, float eps,
-                   uint16_t* __restrict__ out) {
+    rmsnorm_kernel(const float* __restrict__ part, int splits, int64_t ld, int64_t T, int r,
+                   const uint16_t* __restrict__ g, float eps, uint16_t* __restrict__ out, int n_h, int64_t w_col0,
+                   float w_scale, float* __restrict__ w_out) {
   __shared__ float warp_ss[kNormThreads / 32];
-  const int t = blockIdx.x, tid = threadIdx.x;
-  const float* row = a + (int64_t)t * r;
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // part is the previous kernel's output
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const float* row = part + t * ld;
+  const int64_t split_stride = T * ld;
+  // a[j] = the sum over splits of column c0 + j * kNormThreads (0 where that is >= n)
+  auto sums = [&](int64_t c0, int64_t n, float (&a)[kNormUnroll]) {
+#pragma unroll
+    for (int j = 0; j < kNormUnroll; ++j) a[j] = 0.f;
+    for (int s0 = 0; s0 < splits; s0 += kNormSplitBatch) {
+      float x[kNormSplitBatch][kNormUnroll];
+#pragma unroll
+      for (int u = 0; u < kNormSplitBatch; ++u)
+#pragma unroll
+        for (int j = 0; j < kNormUnroll; ++j) {
+          const int64_t c = c0 + j * kNormThreads;
+          x[u][j] = (s0 + u < splits && c < n) ? __ldg(row + (s0 + u) * split_stride + c) : 0.f;
+        }
+#pragma unroll
+      for (int u = 0; u < kNormSplitBatch; ++u)
+#pragma unroll
+        for (int j = 0; j < kNormUnroll; ++j) a[j] += x[u][j];
+    }
+  };
   float ss = 0.f;
-  for (int i = tid; i < r; i += kNormThreads) ss = fmaf(row[i], row[i], ss);
+  for (int i0 = tid; i0 < r; i0 += kNormThreads * kNormUnroll) {
+    float a[kNormUnroll];
+    sums(i0, r, a);
+#pragma unroll
+    for (int j = 0; j < kNormUnroll; ++j) ss = fmaf(a[j], a[j], ss);
+  }
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
   __syncthreads();
@@ -63,45 +398,80 @@ __global__ void __launch_bounds__(kNormThreads)
 #pragma unroll
   for (int i = 0; i < kNormThreads / 32; ++i) tot += warp_ss[i];
   const float inv = rsqrtf(tot / (float)r + eps);
-  for (int i = tid; i < r; i += kNormThreads) {
-    const float gv = __uint_as_float((uint32_t)g[i] << 16);
-    out[(int64_t)t * r + i] = f32_to_bf16_rne(row[i] * inv * gv);
+  for (int i0 = tid; i0 < r; i0 += kNormThreads * kNormUnroll) {
+    float a[kNormUnroll];
+    sums(i0, r, a);
+#pragma unroll
+    for (int j = 0; j < kNormUnroll; ++j) {
+      const int i = i0 + j * kNormThreads;
+      if (i < r) out[t * r + i] = f32_to_bf16_rne(a[j] * inv * __uint_as_float((uint32_t)g[i] << 16));
+    }
+  }
+  for (int h0 = tid; h0 < n_h; h0 += kNormThreads * kNormUnroll) {
+    float a[kNormUnroll];
+    sums(w_col0 + h0, w_col0 + n_h, a);
+#pragma unroll
+    for (int j = 0; j < kNormUnroll; ++j) {
+      const int h = h0 + j * kNormThreads;
+      if (h < n_h) w_out[t * n_h + h] = w_scale * a[j];
+    }
   }
 }
 
-// YaRN NTK-by-parts frequency of rotary pair i (see the oracle's reading).
-__device__ double yarn_freq(int i, const RopeCfg& c) {
+// YaRN NTK-by-parts frequency of rotary pair i: theta_i = base^(-2i/64);
+// pairs that turn fewer than beta_slow times over the original context take
+// theta_i / factor, pairs that turn more than beta_fast times keep theta_i,
+// and the ones between blend the two linearly in the number of turns.
+RopeFreqs yarn_freqs(double base, double factor, double orig_len, double beta_fast, double beta_slow) {
   const double two_pi = 6.283185307179586476925286766559;
-  const double theta = pow(c.base, -2.0 * (double)i / (double)kRopeDim);
-  const double turns = c.orig_len * theta / two_pi;
-  double gamma = (turns - c.beta_slow) / (c.beta_fast - c.beta_slow);
-  gamma = gamma < 0.0 ? 0.0 : (gamma > 1.0 ? 1.0 : gamma);
-  return (1.0 - gamma) * theta / c.factor + gamma * theta;
+  RopeFreqs r;
+  for (int i = 0; i < kRopeDim / 2; ++i) {
+    const double theta = std::pow(base, -2.0 * (double)i / (double)kRopeDim);
+    const double turns = orig_len * theta / two_pi;
+    double gamma = (turns - beta_slow) / (beta_fast - beta_slow);
+    gamma = gamma < 0.0 ? 0.0 : (gamma > 1.0 ? 1.0 : gamma);
+    r.f[i] = (1.0 - gamma) * theta / factor + gamma * theta;
+  }
+  return r;
 }
 
+// u = the splits of part summed in order; part is [splits][rows * 128] with
+// row = (token, head).
 __global__ void __launch_bounds__(256)
-    rope_hadamard_kernel(const float* __restrict__ u, const int64_t* __restrict__ pos, int64_t rows, int n_h,
-                         RopeCfg rc, uint16_t* __restrict__ q_out, float* __restrict__ q_out_f32) {
+    rope_hadamard_kernel(const float* __restrict__ part, int splits, const int64_t* __restrict__ pos, int64_t rows,
+                         int n_h, RopeFreqs rf, uint16_t* __restrict__ q_out, float* __restrict__ q_out_f32) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head)
+  grid_dep_wait();  // part is the previous kernel's output
   if (row >= rows) return;
   const int64_t t = row / n_h;
-  const float4 in = *reinterpret_cast<const float4*>(u + row * kHeadDim + 4 * lane);
+  float4 in = *reinterpret_cast<const float4*>(part + row * kHeadDim + 4 * lane);
+  for (int s = 1; s < splits; ++s) {
+    const float4 x = *reinterpret_cast<const float4*>(part + (s * rows + row) * kHeadDim + 4 * lane);
+    in.x += x.x;
+    in.y += x.y;
+    in.z += x.z;
+    in.w += x.w;
+  }
   float v[4] = {in.x, in.y, in.z, in.w};
   // rotary on entries 64..127 (lanes 16..31): pairs (2i, 2i+1), i = 2 lane - 32 + {0, 1}
+  // The angle pos * theta'_i is formed and reduced modulo 2 pi in fp64 (it
+  // reaches 2^31 radians); sine and cosine of the reduced angle and the
+  // rotation itself run in fp32.
   if (lane >= 16) {
     const double p = (double)pos[t];
     const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int i = 2 * lane - 32 + k;
-      double a = p * yarn_freq(i, rc);
-      a -= two_pi * floor(a / two_pi);
-      double s, c;
-      sincos(a, &s, &c);
+      double a = p * rf.f[i];
+      a -= two_pi * floor(a * inv_two_pi);
+      float s, c;
+      sincosf((float)a, &s, &c);
       const float x0 = v[2 * k], x1 = v[2 * k + 1];
-      v[2 * k] = (float)((double)x0 * c - (double)x1 * s);
-      v[2 * k + 1] = (float)((double)x0 * s + (double)x1 * c);
+      v[2 * k] = x0 * c - x1 * s;
+      v[2 * k + 1] = x0 * s + x1 * c;
     }
   }
   // Walsh-Hadamard butterflies: strides 1, 2 inside the lane, 4..64 across lanes
@@ -132,37 +502,22 @@ __global__ void __launch_bounds__(256)
     *reinterpret_cast<float4*>(q_out_f32 + row * kHeadDim + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
-// One cuBLAS handle per device, created on first use; calls that enqueue on
-// it are serialised (the handle's stream is set per call).
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {};
-
-fm_status blas_for(int device, cublasHandle_t* out) {
-  if (device < 0 || device >= 64) return set_error(FM_ERR_UNSUPPORTED, "query chain: device %d", device);
-  if (g_blas[device] == nullptr) {
-    cublasHandle_t h = nullptr;
-    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return set_error(FM_ERR_CUDA, "query chain: cublasCreate failed");
-    g_blas[device] = h;
-  }
-  *out = g_blas[device];
-  return FM_OK;
-}
-
-// Y[T, N] (ldy = N, row-major) = alpha * X[T, K] . W[N, K]^T (both bf16, row-major).
-fm_status gemm_xwt(cublasHandle_t h, const uint16_t* X, const uint16_t* W, int T, int N, int K, float alpha,
-                   float* Y) {
-  const float beta = 0.f;
-  const cublasStatus_t st =
-      cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, T, K, &alpha, W, CUDA_R_16BF, K, X, CUDA_R_16BF, K, &beta, Y,
-                   CUDA_R_32F, N, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (st != CUBLAS_STATUS_SUCCESS) return set_error(FM_ERR_CUDA, "query chain: cublasGemmEx status %d", (int)st);
-  return FM_OK;
-}
-
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t chain_ws_bytes(int T, int r, int n_h) {
-  return align256((size_t)T * r * 4) + align256((size_t)T * r * 2) + align256((size_t)T * n_h * kHeadDim * 4);
+// Workspace: the K-split partials of [a | w] (tiles of wq_a then w_proj), the
+// bf16 RMSNorm output, the K-split partials of u.
+struct ChainWs {
+  size_t part1, c, part2, bytes;
+};
+ChainWs chain_ws(int T, int r, int n_h) {
+  const int nt1 = (r + kGM - 1) / kGM + (n_h + kGM - 1) / kGM;
+  const int nt2 = n_h;  // n_h * 128 rows
+  ChainWs w;
+  w.part1 = 0;
+  w.c = align256((size_t)gemm_splits_max(nt1) * T * nt1 * kGM * 4);
+  w.part2 = w.c + align256((size_t)T * r * 2);
+  w.bytes = w.part2 + align256((size_t)gemm_splits_max(nt2) * T * nt2 * kGM * 4);
+  return w;
 }
 
 }  // namespace
@@ -170,7 +525,7 @@ size_t chain_ws_bytes(int T, int r, int n_h) {
 
 FM_API size_t fm_query_chain_workspace(int T, int r, int n_h) {
   if (T < 0 || r < 1 || n_h < 1) return 0;
-  return fm::chain_ws_bytes(T, r, n_h);
+  return fm::chain_ws(T, r, n_h).bytes;
 }
 
 FM_API fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, const uint16_t* q_norm,
@@ -196,36 +551,35 @@ FM_API fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, co
       !aligned(q_norm, 2) || !aligned(pos, 8) || !aligned(q_out, 8) || !aligned(w_out, 4) ||
       (q_out_f32 && !aligned(q_out_f32, 16)))
     return set_error(FM_ERR_INVALID_ARG, "fm_query_chain: misaligned pointer");
-  const size_t need = chain_ws_bytes(T, r, n_h);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
-    return set_error(FM_ERR_WORKSPACE, "fm_query_chain: workspace needs %zu bytes, 256-byte aligned", need);
+  const ChainWs lay = chain_ws(T, r, n_h);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes)
+    return set_error(FM_ERR_WORKSPACE, "fm_query_chain: workspace needs %zu bytes, 256-byte aligned", lay.bytes);
   int sms = 0;
   fm_status st = check_device(&sms);
   if (st != FM_OK) return st;
-  int dev = 0;
-  cudaGetDevice(&dev);
+  unsigned int* status = nullptr;
+  if ((st = status_word(&status)) != FM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* a = static_cast<float*>(workspace);
-  uint16_t* c = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + align256((size_t)T * r * 4));
-  float* u = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(c) + align256((size_t)T * r * 2));
-  {
-    std::lock_guard<std::mutex> lock(g_blas_mu);
-    cublasHandle_t h = nullptr;
-    if ((st = blas_for(dev, &h)) != FM_OK) return st;
-    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return set_error(FM_ERR_CUDA, "fm_query_chain: cublasSetStream");
-    if ((st = gemm_xwt(h, hidden, wq_a, T, r, dim, 1.0f, a)) != FM_OK) return st;
-    // head weights: w_proj . h scaled by head_dim^-1/2 n_h^-1/2
-    const float ws = (float)(1.0 / sqrt((double)head_dim) / sqrt((double)n_h));
-    if ((st = gemm_xwt(h, hidden, w_proj, T, n_h, dim, ws, w_out)) != FM_OK) return st;
-    rmsnorm_kernel<<<T, kNormThreads, 0, s>>>(a, q_norm, r, eps, c);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_query_chain: rmsnorm launch: %s", cudaGetErrorString(e));
-    if ((st = gemm_xwt(h, c, wq_b, T, n_h * kHeadDim, r, 1.0f, u)) != FM_OK) return st;
-  }
-  RopeCfg rc{rope_base, rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow};
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  float* part1 = reinterpret_cast<float*>(base + lay.part1);
+  uint16_t* c = reinterpret_cast<uint16_t*>(base + lay.c);
+  float* part2 = reinterpret_cast<float*>(base + lay.part2);
+  // [a | w] = h . [wq_a | w_proj]^T
+  int splits1 = 1, splits2 = 1;
+  if ((st = proj_gemm(hidden, T, dim, wq_a, r, w_proj, n_h, sms, part1, &splits1, status, false, s)) != FM_OK) return st;
+  // RMSNorm of a, and the head weights w_proj . h scaled by head_dim^-1/2 n_h^-1/2
+  const int nt_a = (r + kGM - 1) / kGM;
+  const int64_t ld1 = (int64_t)(nt_a + (n_h + kGM - 1) / kGM) * kGM;
+  const float w_scale = (float)(1.0 / sqrt((double)head_dim) / sqrt((double)n_h));
+  cudaError_t e = launch_pdl(rmsnorm_kernel, (unsigned)T, kNormThreads, 0, s, (const float*)part1, splits1, ld1,
+                             (int64_t)T, r, q_norm, eps, c, n_h, (int64_t)nt_a * kGM, w_scale, w_out);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_query_chain: rmsnorm launch: %s", cudaGetErrorString(e));
+  // u = c . wq_b^T
+  if ((st = proj_gemm(c, T, r, wq_b, n_h * kHeadDim, nullptr, 0, sms, part2, &splits2, status, true, s)) != FM_OK) return st;
+  const RopeFreqs rf = yarn_freqs(rope_base, rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow);
   const int64_t rows = (int64_t)T * n_h;
-  rope_hadamard_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(u, pos, rows, n_h, rc, q_out, q_out_f32);
-  cudaError_t e = cudaGetLastError();
+  e = launch_pdl(rope_hadamard_kernel, (unsigned)((rows + 7) / 8), 256, 0, s, (const float*)part2, splits2, pos, rows,
+                 n_h, rf, q_out, q_out_f32);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_query_chain: rope launch: %s", cudaGetErrorString(e));
   return FM_OK;
 }

@@ -55,6 +55,26 @@ def test_query_chain_matches_oracle(torch_dev, orc, T, n_h):
     _check(q_ref, w_ref, *_run(torch, dev, inputs, n_h))
 
 
+def test_query_chain_decode_batch(torch_dev, orc):
+    """A decode batch of 30 tokens (one per request of the 1M-context
+    workload) at the retriever's sizes: the projections' token operand spans
+    two 16-row groups and the K splits of both GEMMs are summed."""
+    torch, dev = torch_dev
+    inputs = gen.query_chain_inputs(30, seed=gen.BASE_SEED + 560)
+    q_ref, w_ref = orc.query_chain(*inputs, n_h=128)
+    _check(q_ref, w_ref, *_run(torch, dev, inputs, 128))
+
+
+@pytest.mark.parametrize("T", [40, 256, 300])
+def test_query_chain_many_tokens(torch_dev, orc, T):
+    """More tokens than one projection launch takes (256): 300 tokens run as
+    blocks of 256 and 44; dims not multiples of 64 leave ragged K chunks."""
+    torch, dev = torch_dev
+    inputs = gen.query_chain_inputs(T, dim=520, r=264, n_h=8, seed=gen.BASE_SEED + 570 + T)
+    q_ref, w_ref = orc.query_chain(*inputs, n_h=8)
+    _check(q_ref, w_ref, *_run(torch, dev, inputs, 8))
+
+
 def test_query_chain_small_dims_and_positions(torch_dev, orc):
     """Other widths (dim 512, rank 256) and positions across the whole range,
     including ones where fp32 angles would be off by whole radians."""
