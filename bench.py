@@ -49,9 +49,12 @@ WORKLOAD = ("lsa_c4_indexer_1m: memindex 30x3x262144 bf16 (12% hot) + paged top-
 PROFILE_CASES = {
     # phase: [(profile summary, kernel source files, units in the summary's case, units in the bench step)]
     "memindex": [("memindex_kernel_memindex_1m_b4_l3_s262144.md", ["memindex.cu", "fm_common.cuh"], 4, 30)],
-    "paged_topk": [("paged_score_kernel_paged_1m_q84_r384.md", ["paged.cu", "fp8.cuh", "fm_common.cuh"], 84, 630)],
+    "paged_topk": [("paged_score_kernel_paged_1m_q84_r384.md", ["paged.cu", "fp8.cuh", "fm_common.cuh"], 84, 630),
+                   ("topk_rows_kernel_paged_1m_q84_r384.md", ["topk.cu", "topk.cuh", "fm_common.cuh"], 84, 630)],
     "memindex_fp8": [("memindex_fp8_kernel_memindex_fp8_1m_b4_l3_s262144.md", ["memindex_fp8.cu", "fp8.cuh", "fm_common.cuh"],
                       4, 30)],
+    "retriever": [("retriever_kernel_retriever_1m_b4_l3_s262144.md", ["retriever.cu", "fp8.cuh", "fm_common.cuh"], 4, 30)],
+    "query_chain": [("proj_gemm_kernel_query_chain_t30.md", ["query_chain.cu", "fm_common.cuh"], 1, 3)],
     "prefill_topk": [("prefill_score_kernel_prefill_t512_s65536.md", ["prefill.cu", "fm_common.cuh"], 512, 4096),
                      ("topk_rows_kernel_prefill_t512_s65536.md", ["topk.cu", "topk.cuh", "fm_common.cuh"], 512, 4096)],
 }
@@ -70,7 +73,7 @@ def profiled_traffic(phase: str):
             return None
         text = open(path).read()
         m_hash = re.search(r"first 16 hex\): `([0-9a-f]+)`", text)
-        m_traf = re.search(r"\| traffic \(read \+ write\) per launch \| ([0-9.]+) MB \|", text)
+        m_traf = re.findall(r"\| traffic \(read \+ write\) per launch \| ([0-9.]+) MB \|", text)
         if not m_hash or not m_traf:
             return None
         h = hashlib.sha256()
@@ -79,7 +82,7 @@ def profiled_traffic(phase: str):
                 h.update(fh.read())
         if h.hexdigest()[:16] != m_hash.group(1):
             return None
-        total += float(m_traf.group(1)) * 1e6 * units_step / units_case
+        total += sum(float(x) for x in m_traf) * 1e6 * units_step / units_case  # every launch of the summary
     return total or None
 
 
@@ -398,9 +401,9 @@ def run_ours(args):
     import sparse_attention_kv_c4_gb300 as fm
     fm.lib()
 
-    if args.only in ("memindex_fp8", "paged_full", "retriever"):
-        v = {"memindex_fp8": Fp8MemIndex, "paged_full": FullHistoryPaged,
-             "retriever": RetrieverMemIndex}[args.only](torch, dev, fm, small=args.small)
+    if args.only in ("memindex_fp8", "paged_full", "retriever", "query_chain"):
+        v = {"memindex_fp8": Fp8MemIndex, "paged_full": FullHistoryPaged, "retriever": RetrieverMemIndex,
+             "query_chain": QueryChain}[args.only](torch, dev, fm, small=args.small)
         r = v.measure(max(1, args.steps), args.warmup, peaks())
         print(json.dumps({"profile_case": True, "only": args.only, "small": args.small, "ms_per_step": r["ms"],
                           "device_status": fm.fm_device_status(reset=True)}), flush=True)
@@ -682,7 +685,8 @@ class RetrieverMemIndex:
         c = self.cfg
         return {"ms": round(ms, 4), "chunk_scores_per_s": c.chunk_scores / (ms / 1e3), "bound": "hbm",
                 "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                "algorithmic_bytes": self.bytes(), "launches": 2, "reps": reps,
+                "algorithmic_bytes": self.bytes(), "traffic_bytes_est": profiled_traffic("retriever"),
+                "launches": 2, "reps": reps,
                 "workload": (f"retriever {c.B}x{c.L}x{c.S}, {c.n_h} heads, packed 132-byte compressed_k rows, "
                              f"{'max' if self.mode == 0 else 'mean'} ensemble")}
 
@@ -791,7 +795,8 @@ class QueryChain:
         ach = self.bytes() / (ms / 1e3) / 1e9
         return {"ms": round(ms, 4), "tokens_per_s": self.T * self.layers / (ms / 1e3), "bound": "hbm",
                 "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                "algorithmic_bytes": self.bytes(), "launches": "2 projection GEMMs + 2 kernels per layer", "reps": reps,
+                "algorithmic_bytes": self.bytes(), "traffic_bytes_est": profiled_traffic("query_chain"),
+                "launches": "2 projection GEMMs + 2 kernels per layer", "reps": reps,
                 "workload": (f"query chain: {self.T} decode tokens x {self.layers} indexer layers, dim {self.dim}, "
                              f"rank {self.r}, {self.n_h} heads x 128 (bf16 weights, fp32 accumulate)")}
 
@@ -823,7 +828,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the variant rows timed after the step")
-    ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8", "paged_full", "retriever"], default=None,
+    ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8", "paged_full", "retriever",
+                                       "query_chain"], default=None,
                     help="profiling case: run one phase only")
     ap.add_argument("--small", action="store_true", help="profiling case: reduced sizes for ncu captures")
     args = ap.parse_args()
