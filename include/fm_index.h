@@ -356,6 +356,18 @@ fm_status fm_native_topk_paged_noalloc(const uint16_t* q, const float* w, const 
  *   workspace >= fm_index_prefill_workspace(T, S) bytes, 256-byte aligned
  */
 size_t fm_index_prefill_workspace(int T, int64_t S);
+
+/*
+ * The prefill call's dense scores alone ([V4] sec. 3 CSA-1, the score the
+ * CSA-2 top-512 ranks), for callers that select or inspect them themselves:
+ *     logits_out[t, s] = Y[t,s]  for s < min(S, floor(pos[t] / ratio)),
+ *                        -inf    otherwise.
+ * Arguments as fm_index_prefill_topk; logits_out [T, S] fp32, row stride S,
+ * 4-byte aligned (caller-owned; every element is written).  Two kernel
+ * launches (the scores, then -inf past each token's limit), no workspace.
+ */
+fm_status fm_index_prefill_scores(const uint16_t* q, const float* w, const int64_t* pos, const uint16_t* keys,
+                                  int T, int64_t S, int n_h, int d, int ratio, float* logits_out, fm_stream_t stream);
 fm_status fm_index_prefill_topk(const uint16_t* q, const float* w, const int64_t* pos, const uint16_t* keys,
                                 int T, int64_t S, int n_h, int d, int ratio, int k, int32_t* idx_out,
                                 float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);

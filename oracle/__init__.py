@@ -243,6 +243,22 @@ class Oracle:
     def causal_limit(self, pos: int, S: int, ratio: int = 4) -> int:
         return self.lib.orc_causal_limit(int(pos), int(S), int(ratio))
 
+    def prefill_logits(self, q, w, pos, K, ratio: int = 4) -> np.ndarray:
+        """The prefill scores ([V4] sec. 3 CSA-1): Y[t,s] = sum_h w[t,h] ReLU(q[t,h].K[s])
+        for s < causal_limit(pos[t]), -inf beyond.  q [T,n_h,d] bf16 bits,
+        w [T,n_h], pos [T], K [S,d] bf16 bits -> [T,S] fp64.  The Memory
+        Indexer's logits with every query row reading the same keys (request
+        stride 0)."""
+        q = _c(q, np.uint16); w = _c(w, np.float32); K = _c(K, np.uint16)
+        T, n_h, d = q.shape
+        S = K.shape[0]
+        x = np.empty((T, 1, S), dtype=np.float64)
+        self.lib.orc_memindex_logits(_p(q, u16p), _p(w, f32p), _p(K, u16p), 0, S * d, T, 1, S, n_h, d, _p(x, f64p))
+        x = x[:, 0, :]
+        for t in range(T):
+            x[t, self.causal_limit(int(pos[t]), S, ratio):] = -np.inf
+        return x
+
     def prefill_topk(self, q, w, pos, K, ratio: int = 4, k: int = 512):
         q = _c(q, np.uint16); w = _c(w, np.float32); pos = _c(pos, np.int64); K = _c(K, np.uint16)
         T, n_h, d = q.shape

@@ -18,7 +18,8 @@ __all__ = [
     "fm_topk_workspace", "fm_topk_select", "fm_native_topk_paged_workspace", "fm_native_topk_paged",
     "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "fm_page_recall",
     "fm_native_topk_paged_ex", "fm_memindex_fp8_workspace", "fm_memindex_score_mask_fp8",
-    "LIB_PATH",
+    "fm_index_prefill_scores", "fm_retriever_workspace", "fm_retriever_score_mask", "fm_query_chain_workspace",
+    "fm_query_chain", "LIB_PATH",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +75,9 @@ def lib() -> ctypes.CDLL:
             L.fm_index_prefill_workspace.restype = _SZ
             L.fm_index_prefill_topk.argtypes = [_VP, _VP, _VP, _VP, _I32, _I64, _I32, _I32, _I32, _I32, _VP, _VP,
                                                 _VP, _SZ, _VP]
+        if hasattr(L, "fm_index_prefill_scores"):
+            L.fm_index_prefill_scores.argtypes = [_VP, _VP, _VP, _VP, _I32, _I64, _I32, _I32, _I32, _VP, _VP]
+            L.fm_index_prefill_scores.restype = ctypes.c_int
         if hasattr(L, "fm_memindex_score_mask_fp8"):
             L.fm_memindex_fp8_workspace.argtypes = [_I32, _I32]
             L.fm_memindex_fp8_workspace.restype = _SZ
@@ -290,6 +294,16 @@ def fm_index_prefill_topk(q, w, pos, keys, k: int, idx_out, score_out=None, rati
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().fm_index_prefill_topk(_ptr(q), _ptr(w), _ptr(pos), _ptr(keys), T, S, n_h, d, ratio, k,
                                        _ptr(idx_out), _ptr(score_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_index_prefill_scores(q, w, pos, keys, logits_out, ratio: int = 4, stream=None) -> None:
+    """q [T,64,128] bf16, w [T,64] fp32, pos [T] int64, keys [S,128] bf16,
+    logits_out [T,S] fp32 (contiguous): the dense scores, -inf past each
+    token's causal limit."""
+    T, n_h, d = q.shape
+    S = keys.shape[0]
+    _check(lib().fm_index_prefill_scores(_ptr(q), _ptr(w), _ptr(pos), _ptr(keys), T, S, n_h, d, ratio,
+                                         _ptr(logits_out), _stream(stream)))
 
 
 def fm_page_recall(mask, S: int, kmax: int, pages_out, density_out=None, n_out=None, sink: int = 0, recent: int = 0,

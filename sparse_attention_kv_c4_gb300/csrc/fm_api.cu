@@ -279,3 +279,33 @@ FM_API fm_status fm_index_prefill_topk(const uint16_t* q, const float* w, const 
   a.workspace = workspace;
   return launch_prefill(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
 }
+
+FM_API fm_status fm_index_prefill_scores(const uint16_t* q, const float* w, const int64_t* pos, const uint16_t* keys,
+                                         int T, int64_t S, int n_h, int d, int ratio, float* logits_out,
+                                         fm_stream_t stream) {
+  if (n_h != 64 || d != 128)
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_scores: n_h=%d d=%d (need 64, 128)", n_h, d);
+  if (T < 0 || S < 0 || S >= (int64_t(1) << 31) || ratio < 1)
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_scores: bad sizes T=%d S=%lld ratio=%d", T, (long long)S,
+                     ratio);
+  if (T == 0 || S == 0) return FM_OK;
+  if (!q || !w || !pos || !keys || !logits_out)
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_scores: required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(pos, 8) || !aligned(keys, 16) || !aligned(logits_out, 4))
+    return set_error(FM_ERR_INVALID_ARG, "fm_index_prefill_scores: q/w/keys need 16-byte alignment");
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  unsigned int* status = nullptr;
+  st = status_word(&status);
+  if (st != FM_OK) return st;
+  PrefillArgs a = {};
+  a.q = q;
+  a.w = w;
+  a.pos = pos;
+  a.keys = keys;
+  a.T = T;
+  a.S = S;
+  a.ratio = ratio;
+  return launch_prefill_scores(a, logits_out, true, sms, status, reinterpret_cast<cudaStream_t>(stream));
+}

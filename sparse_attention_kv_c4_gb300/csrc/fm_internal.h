@@ -87,6 +87,10 @@ struct PrefillArgs {
 };
 size_t prefill_workspace_bytes(int T, int64_t S);
 fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
+// The dense scores Y [T, S] alone into `logits` (row stride S); with
+// fill_masked, -inf wherever s >= the token's causal limit.
+fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, bool fill_masked, int num_sms,
+                                unsigned int* status, cudaStream_t stream);
 fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
 
 }  // namespace fm

@@ -21,7 +21,9 @@
 // accumulator, and turn it into Y with fp32 max/FMA against the token's head
 // weights (kept in shared memory per query block); tiles wholly past a
 // block's causal limit are skipped.  The block top-k then reads
-// each row up to its causal limit.
+// each row up to its causal limit.  Called for the scores alone, a second
+// small kernel writes -inf wherever s >= the token's limit (the score kernel
+// itself is the same either way).
 #include <math.h>
 
 #include "fm_common.cuh"
@@ -302,21 +304,23 @@ __global__ void causal_limits_kernel(const int64_t* __restrict__ pos, int T, int
   if (t < T) n_valid[t] = (int32_t)causal_limit(pos[t], S, ratio);
 }
 
+// logits[t, s] = -inf for s >= the causal limit of token t (one CTA per row).
+__global__ void causal_fill_kernel(const int64_t* __restrict__ pos, int64_t S, int ratio, float* __restrict__ logits) {
+  const int64_t t = blockIdx.x;
+  float* row = logits + t * S;
+  for (int64_t s = causal_limit(__ldg(pos + t), S, ratio) + threadIdx.x; s < S; s += blockDim.x) row[s] = -INFINITY;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
 size_t prefill_workspace_bytes(int T, int64_t S) { return align256((size_t)T * S * 4) + align256((size_t)T * 4); }
 
-fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
-  if (a.T == 0) return FM_OK;
-  float* logits = static_cast<float*>(a.workspace);
-  int32_t* n_valid = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + align256((size_t)a.T * a.S * 4));
-  causal_limits_kernel<<<(a.T + 255) / 256, 256, 0, stream>>>(a.pos, a.T, a.S, a.ratio, n_valid);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill limits: launch: %s", cudaGetErrorString(e));
-
-  if (a.S > 0) {
+fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, bool fill_masked, int num_sms,
+                                unsigned int* status, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (a.T > 0 && a.S > 0) {
     CUtensorMap tmap_k, tmap_q;
     {
       const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.S};
@@ -364,7 +368,24 @@ fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status
     prefill_score_kernel<<<grid, kThreads, smem, stream>>>(tmap_k, tmap_q, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill score: launch: %s", cudaGetErrorString(e));
+    if (fill_masked) {
+      causal_fill_kernel<<<a.T, 256, 0, stream>>>(a.pos, a.S, a.ratio, logits);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill fill: launch: %s", cudaGetErrorString(e));
+    }
   }
+  return FM_OK;
+}
+
+fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
+  if (a.T == 0) return FM_OK;
+  float* logits = static_cast<float*>(a.workspace);
+  int32_t* n_valid = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + align256((size_t)a.T * a.S * 4));
+  causal_limits_kernel<<<(a.T + 255) / 256, 256, 0, stream>>>(a.pos, a.T, a.S, a.ratio, n_valid);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill limits: launch: %s", cudaGetErrorString(e));
+  fm_status st = launch_prefill_scores(a, logits, false, num_sms, status, stream);
+  if (st != FM_OK) return st;
   return launch_topk_rows(logits, a.S, n_valid, a.T, (int)a.S, a.k, nullptr, 0, nullptr, nullptr, a.idx_out,
                           a.score_out, stream);
 }

@@ -388,6 +388,27 @@ def pin_prefill_causal(orc):
     assert list(idx[2]) == [0, -1, -1, -1, -1]
 
 
+def pin_prefill_logits(orc):
+    """The prefill scores are the definition element by element: each finite
+    entry equals the single-score routine (n_h heads, one key), every entry at
+    or past the causal limit is -inf, and the scores' own top-k (by score desc,
+    id asc) is the prefill top-k."""
+    rng = np.random.default_rng(37)
+    T, S, n_h, d, k = 7, 19, 3, 8, 4
+    q = f32_to_bf16_bits(rng.standard_normal((T, n_h, d)).astype(np.float32))
+    w = rng.standard_normal((T, n_h)).astype(np.float32)
+    K = f32_to_bf16_bits(rng.standard_normal((S, d)).astype(np.float32))
+    pos = np.array([0, 5, 12, 33, 75, 76, 400], np.int64)
+    y = orc.prefill_logits(q, w, pos, K, ratio=4)
+    idx, _ = orc.prefill_topk(q, w, pos, K, ratio=4, k=k)
+    for t in range(T):
+        lim = min(S, int(pos[t]) // 4)
+        assert np.all(np.isneginf(y[t, lim:]))
+        for s in range(lim):
+            assert y[t, s] == orc.score_bf16(q[t], w[t], K[s])
+        assert list(idx[t]) == expected_topk(list(range(lim)), list(y[t, :lim]), k), t
+
+
 # ---------------------------------------------------------------------------
 # planted construction (the generator's promise, checked through the oracle)
 # ---------------------------------------------------------------------------

@@ -27,7 +27,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared()
-    for n in ("fm_memindex_score_mask", "fm_native_topk_paged", "fm_index_prefill_topk", "fm_topk_select",
+    for n in ("fm_memindex_score_mask", "fm_native_topk_paged", "fm_index_prefill_topk", "fm_index_prefill_scores",
+              "fm_topk_select",
               "fm_native_topk_paged_workspace", "fm_index_prefill_workspace", "fm_topk_workspace",
               "fm_retriever_score_mask", "fm_retriever_workspace",
               "fm_query_chain", "fm_query_chain_workspace",
@@ -80,6 +81,21 @@ def test_page_recall_rejects_bad_args_on_host(lib):
     assert f(fake, 2, 1024, 0, 0, 8, None, None, None, None) == 1  # NULL pages_out
     assert f(fake + 2, 2, 1024, 0, 0, 8, fake, None, None, None) == 1  # misaligned mask
     assert f(None, 0, 1024, 0, 0, 8, None, None, None, None) == 0  # empty work is OK without a device
+
+
+def test_prefill_scores_rejects_bad_args_on_host(lib):
+    import sparse_attention_kv_c4_gb300 as fm
+    fm.lib()  # sets argtypes
+    f = lib.fm_index_prefill_scores
+    fake = 4096  # never dereferenced: validation fails first
+    assert f(fake, fake, fake, fake, 8, 100, 32, 128, 4, fake, None) == 1  # n_h != 64
+    assert "n_h" in fm.fm_last_error()
+    assert f(fake, fake, fake, fake, 8, 100, 64, 128, 0, fake, None) == 1  # ratio < 1
+    assert f(fake, fake, fake, fake, 8, 1 << 31, 64, 128, 4, fake, None) == 1  # S too large
+    assert f(fake, fake, fake, fake, 8, 100, 64, 128, 4, None, None) == 1  # NULL logits_out
+    assert f(fake + 8, fake, fake, fake, 8, 100, 64, 128, 4, fake, None) == 1  # misaligned q
+    assert f(fake, fake, fake, fake, 8, 100, 64, 128, 4, fake + 2, None) == 1  # misaligned logits_out
+    assert f(None, None, None, None, 0, 100, 64, 128, 4, None, None) == 0  # T = 0: nothing to do
 
 
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):

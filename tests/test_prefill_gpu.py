@@ -97,3 +97,46 @@ def test_prefill_full_size_sampled(torch_dev, orc, variant):
     rng = np.random.default_rng(11)
     rows = sorted(set(rng.choice(cfg.T, size=6, replace=False).tolist()) | {0, cfg.T - 1})
     check(orc, q, w, pos, K, idx, sc, cfg.k, rows=rows)
+
+
+@pytest.mark.parametrize("T,S,start", [(37, 1000, None), (9, 4097, 0), (6, 300, -3)])
+def test_prefill_scores_match_oracle(torch_dev, orc, T, S, start):
+    """fm_index_prefill_scores: every element against the oracle's scores,
+    -inf exactly where s >= the token's causal limit.  start=None puts every
+    position past 4S (nothing masked); 0 makes the limit bite inside the row
+    and skip whole 128-chunk tiles; negative positions mask the whole row."""
+    torch, dev = torch_dev
+    import sparse_attention_kv_c4_gb300 as fm
+    pos = None if start is None else np.arange(start, start + T, dtype=np.int64) * 97
+    q, w, pos, K = small(T, S, seed=T * 11 + S, pos=pos)
+    ref = orc.prefill_logits(q, w, pos, K)
+    out = torch.full((T, S), 7.0, dtype=torch.float32, device=dev)
+    fm.fm_index_prefill_scores(torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).to(dev),
+                               torch.from_numpy(np.ascontiguousarray(w)).to(dev),
+                               torch.from_numpy(np.ascontiguousarray(pos, dtype=np.int64)).to(dev),
+                               torch.from_numpy(np.ascontiguousarray(K).view(np.int16)).to(dev), out)
+    torch.cuda.synchronize()
+    assert fm.fm_device_status(reset=True) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    masked = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), masked)
+    parity.assert_logits_close(got[~masked], ref[~masked])
+
+
+def test_prefill_scores_full_size_sampled(torch_dev, orc):
+    """The bench's launch (4096 tokens x 65536 chunks): sampled rows against
+    the oracle."""
+    torch, dev = torch_dev
+    import sparse_attention_kv_c4_gb300 as fm
+    cfg = gen.PREFILL
+    q, w, pos, K = gen.prefill_host(cfg)
+    out = torch.empty((cfg.T, cfg.S), dtype=torch.float32, device=dev)
+    fm.fm_index_prefill_scores(torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).to(dev),
+                               torch.from_numpy(np.ascontiguousarray(w)).to(dev),
+                               torch.from_numpy(np.ascontiguousarray(pos, dtype=np.int64)).to(dev),
+                               torch.from_numpy(np.ascontiguousarray(K).view(np.int16)).to(dev), out)
+    torch.cuda.synchronize()
+    assert fm.fm_device_status(reset=True) == 0
+    rows = [0, 1, 2, 3, 1021, 2050, 4095]
+    ref = orc.prefill_logits(q[rows], w[rows], pos[rows], K)
+    parity.assert_logits_close(out[rows].cpu().numpy(), ref)
