@@ -58,12 +58,16 @@ constexpr int kRopeDim = 64;
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-// Programmatic dependent launch.  The chain's second to fourth kernels are
-// launched with programmatic stream serialisation: each may start while its
-// predecessor finishes, and waits (griddepcontrol.wait) for the predecessor's
-// completion and memory before it reads that kernel's output or writes
-// anything.  The first GEMM is launched normally, so nothing of the chain
-// starts before the caller's earlier work has finished.
+// Programmatic dependent launch.  The chain's kernels are launched with
+// programmatic stream serialisation: each may start while its predecessor
+// finishes, and waits (griddepcontrol.wait) for the predecessor's completion
+// and memory before it reads or writes global memory -- except that the
+// second GEMM issues its first weight chunks before its wait (the weights are
+// inputs of the call, never written by the kernels it can overlap: the
+// chain's own RMSNorm and first GEMM).  A predecessor that does not trigger
+// early (any kernel outside the chain) completes before the chain's first
+// GEMM starts; the rotary kernel triggers early, so a following call's first
+// GEMM sets up while it runs.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -118,6 +122,7 @@ struct GemmParams {
   int splits;
   int stages;
   uint32_t tmem_cols;
+  int prefetch_weights;  // issue the first stages' weight chunks before the dependency wait
 };
 
 __global__ void __launch_bounds__(kGThreads, 1)
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       // The first stages' weight chunks go out before the dependency wait:
       // weights are never written by the kernels this one may overlap.  The
       // activation chunks (the previous kernel's output) follow the wait.
-      const int pre = c_end - c_begin < stages ? c_end - c_begin : stages;
+      const int pre = !p.prefetch_weights ? 0 : (c_end - c_begin < stages ? c_end - c_begin : stages);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&bar_full[i], (uint32_t)stage_bytes);
         tma_load_2d(smem + i * stage_bytes, wmap, &bar_full[i], (c_begin + i) * kGK, row0);
@@ -277,7 +282,8 @@ int gemm_splits_max(int tiles) {
 // [N1, K] (W1 may be null); ld_part = (ceil(N0/128) + ceil(N1/128)) * 128.
 // Launches one grid per 256 tokens.
 fm_status proj_gemm(const uint16_t* X, int T, int K, const uint16_t* W0, int N0, const uint16_t* W1, int N1,
-                    int num_sms, float* part, int* splits_out, unsigned int* status, bool pdl, cudaStream_t stream) {
+                    int num_sms, float* part, int* splits_out, unsigned int* status, bool pdl, bool prefetch,
+                    cudaStream_t stream) {
   const int nt0 = (N0 + kGM - 1) / kGM, nt1 = W1 != nullptr ? (N1 + kGM - 1) / kGM : 0;
   const int kc = (K + kGK - 1) / kGK;
   const int splits = gemm_splits(nt0 + nt1, kc, num_sms);
@@ -331,6 +337,7 @@ fm_status proj_gemm(const uint16_t* X, int T, int K, const uint16_t* W0, int N0,
     uint32_t cols = 32;
     while (cols < (uint32_t)tpad) cols <<= 1;
     gp.tmem_cols = cols;
+    gp.prefetch_weights = prefetch ? 1 : 0;
     const int smem = 1024 + stages * stage_bytes;
     cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "query chain: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -442,6 +449,7 @@ __global__ void __launch_bounds__(256)
                          int n_h, RopeFreqs rf, uint16_t* __restrict__ q_out, float* __restrict__ q_out_f32) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head)
+  grid_dep_launch_dependents();
   grid_dep_wait();  // part is the previous kernel's output
   if (row >= rows) return;
   const int64_t t = row / n_h;
@@ -566,7 +574,7 @@ FM_API fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, co
   float* part2 = reinterpret_cast<float*>(base + lay.part2);
   // [a | w] = h . [wq_a | w_proj]^T
   int splits1 = 1, splits2 = 1;
-  if ((st = proj_gemm(hidden, T, dim, wq_a, r, w_proj, n_h, sms, part1, &splits1, status, false, s)) != FM_OK) return st;
+  if ((st = proj_gemm(hidden, T, dim, wq_a, r, w_proj, n_h, sms, part1, &splits1, status, true, false, s)) != FM_OK) return st;
   // RMSNorm of a, and the head weights w_proj . h scaled by head_dim^-1/2 n_h^-1/2
   const int nt_a = (r + kGM - 1) / kGM;
   const int64_t ld1 = (int64_t)(nt_a + (n_h + kGM - 1) / kGM) * kGM;
@@ -575,7 +583,7 @@ FM_API fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, co
                              (int64_t)T, r, q_norm, eps, c, n_h, (int64_t)nt_a * kGM, w_scale, w_out);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_query_chain: rmsnorm launch: %s", cudaGetErrorString(e));
   // u = c . wq_b^T
-  if ((st = proj_gemm(c, T, r, wq_b, n_h * kHeadDim, nullptr, 0, sms, part2, &splits2, status, true, s)) != FM_OK) return st;
+  if ((st = proj_gemm(c, T, r, wq_b, n_h * kHeadDim, nullptr, 0, sms, part2, &splits2, status, true, true, s)) != FM_OK) return st;
   const RopeFreqs rf = yarn_freqs(rope_base, rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow);
   const int64_t rows = (int64_t)T * n_h;
   e = launch_pdl(rope_hadamard_kernel, (unsigned)((rows + 7) / 8), 256, 0, s, (const float*)part2, splits2, pos, rows,

@@ -89,3 +89,57 @@ def test_decode_and_prefill_in_one_graph(torch_dev):
     assert fm.fm_device_status(reset=True) == 0
     # the graph is live: the recalled pages and the masked selection are non-trivial
     assert int(n_rec.min()) > 0 and int((pidx >= 0).sum()) > 0
+
+
+def test_query_chain_layers_in_one_graph(torch_dev):
+    """Three layers of the query chain (its second to fourth kernels use
+    programmatic dependent launch) captured in one CUDA graph, followed by
+    the retriever over the chain's output: replays reproduce the eager
+    results bit for bit (the K-split partials are summed in a fixed order)."""
+    torch, dev = torch_dev
+    import sparse_attention_kv_c4_gb300 as fm
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).to(dev)
+    T, L, n_h, dim, r = 6, 3, 128, 1024, 512
+    sets = [[t(a) for a in gen.query_chain_inputs(T, dim=dim, r=r, n_h=n_h, seed=gen.BASE_SEED + 700 + l)]
+            for l in range(L)]
+    q = torch.empty((T, L, n_h, 128), dtype=torch.int16, device=dev)
+    w = torch.empty((T, L, n_h), dtype=torch.float32, device=dev)
+    ws = torch.empty(fm.fm_query_chain_workspace(T, r, n_h), dtype=torch.uint8, device=dev)
+    S = 1024
+    cfg = gen.MemIndexCfg("gq", B=T, L=L, S=S, n_h=n_h, seed=gen.BASE_SEED + 710)
+    k8, sc = gen.memindex_fp8_keys_host(cfg, np.zeros((T, L, n_h), np.float32))
+    ck = torch.from_numpy(gen.pack_compressed_k(k8, sc)).to(dev)
+    mask = torch.empty((T, S // 32), dtype=torch.int32, device=dev)
+    ens = torch.empty((T, S), dtype=torch.float32, device=dev)
+    rws = torch.empty(fm.fm_retriever_workspace(T, L, n_h), dtype=torch.uint8, device=dev)
+    # the chain's per-layer outputs are strided views of q / w ([T, L, ...])
+    q_l = [torch.empty((T, n_h, 128), dtype=torch.int16, device=dev) for _ in range(L)]
+    w_l = [torch.empty((T, n_h), dtype=torch.float32, device=dev) for _ in range(L)]
+
+    def run():
+        for l, (hidden, wq_a, q_norm, wq_b, w_proj, pos) in enumerate(sets):
+            fm.fm_query_chain(hidden, wq_a, q_norm, wq_b, w_proj, pos, q_l[l], w_l[l], workspace=ws)
+        for l in range(L):
+            q[:, l].copy_(q_l[l])
+            w[:, l].copy_(w_l[l])
+        fm.fm_retriever_score_mask(q, w, ck, mask, ens, workspace=rws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    ref = [x.clone() for x in (q, w, mask, ens)]
+    for x in (q, w, mask, ens):
+        x.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    for _ in range(3):
+        for x in (q, w, mask, ens):
+            x.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip((q, w, mask, ens), ref):
+            assert torch.equal(a, b)
+    assert fm.fm_device_status(reset=True) == 0
