@@ -815,14 +815,18 @@ class QueryChain:
         for l in range(layers):
             ins = gen.query_chain_inputs(T, dim=self.dim, r=self.r, n_h=self.n_h, seed=gen.BASE_SEED + 600 + l)
             self.sets.append([t(a) for a in ins])
-        self.q = torch.empty((layers, T, self.n_h, 128), dtype=torch.int16, device=dev)
-        self.w = torch.empty((layers, T, self.n_h), dtype=torch.float32, device=dev)
-        self.ws = torch.empty(fm.fm_query_chain_workspace(T, self.r, self.n_h), dtype=torch.uint8, device=dev)
+        # one call for the three layers: q [T, L, n_h, 128], w [T, L, n_h] (the retriever's q / w layout);
+        # the layers share the tokens' positions
+        self.q = torch.empty((T, layers, self.n_h, 128), dtype=torch.int16, device=dev)
+        self.w = torch.empty((T, layers, self.n_h), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(fm.fm_query_chain_layers_workspace(layers, T, self.r, self.n_h), dtype=torch.uint8,
+                              device=dev)
         torch.cuda.synchronize()
 
     def call(self):
-        for l, (hidden, wq_a, q_norm, wq_b, w_proj, pos) in enumerate(self.sets):
-            self.fm.fm_query_chain(hidden, wq_a, q_norm, wq_b, w_proj, pos, self.q[l], self.w[l], workspace=self.ws)
+        S = self.sets
+        self.fm.fm_query_chain_layers([x[0] for x in S], [x[1] for x in S], [x[2] for x in S], [x[3] for x in S],
+                                      [x[4] for x in S], S[0][5], self.q, self.w, workspace=self.ws)
 
     def bytes(self):
         T, dim, r, n_h = self.T, self.dim, self.r, self.n_h
@@ -846,7 +850,8 @@ class QueryChain:
         return {"ms": round(ms, 4), "tokens_per_s": self.T * self.layers / (ms / 1e3), "bound": "hbm",
                 "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                 "algorithmic_bytes": self.bytes(), "traffic_bytes_est": profiled_traffic("query_chain"),
-                "launches": "2 projection GEMMs + 2 kernels per layer", "reps": reps,
+                "launches": "one fm_query_chain_layers call: 2 projection GEMMs + RMSNorm + rotary/Hadamard for all layers",
+                "reps": reps,
                 "workload": (f"query chain: {self.T} decode tokens x {self.layers} indexer layers, dim {self.dim}, "
                              f"rank {self.r}, {self.n_h} heads x 128 (bf16 weights, fp32 accumulate)")}
 

@@ -197,6 +197,34 @@ fm_status fm_retriever_score_mask(const uint16_t* q, const float* w, const uint8
  * FM_ERR_WORKSPACE; FM_ERR_CUDA for a launch failure.
  */
 size_t fm_query_chain_workspace(int T, int r, int n_h);
+
+/*
+ * The query chain of L indexer layers (1 <= L <= 4) in one call: the layers'
+ * projections share launches, so the fixed cost of a launch is paid once per
+ * call rather than once per layer (the retriever scores its three indexer
+ * layers together, [RM] "Retriever architecture").  Layer l computes
+ * fm_query_chain from hidden[l] with its own weights wq_a[l], q_norm[l],
+ * wq_b[l] and w_proj[l]; the T tokens and their positions are shared.
+ *
+ *   hidden, wq_a, q_norm, wq_b, w_proj   HOST arrays of L device pointers,
+ *            each as in fm_query_chain
+ *   q_out    [T, L, n_h, 128] bf16 (required) -- the layout
+ *            fm_retriever_score_mask takes as q with B = T;
+ *            q_out_f32 the same in fp32, or NULL
+ *   w_out    [T, L, n_h] fp32 (required)
+ *   workspace >= fm_query_chain_layers_workspace(L, T, r, n_h) bytes,
+ *            256-byte aligned
+ * fm_query_chain is this call with L = 1.  Errors as fm_query_chain, and
+ * FM_ERR_INVALID_ARG for L outside 1..4.
+ */
+size_t fm_query_chain_layers_workspace(int L, int T, int r, int n_h);
+fm_status fm_query_chain_layers(int L, const uint16_t* const* hidden, const uint16_t* const* wq_a,
+                                const uint16_t* const* q_norm, const uint16_t* const* wq_b,
+                                const uint16_t* const* w_proj, const int64_t* pos, int T, int dim, int r, int n_h,
+                                int head_dim, int rope_dim, double rope_base, double rope_factor,
+                                double rope_orig_len, double rope_beta_fast, double rope_beta_slow, float eps,
+                                uint16_t* q_out, float* q_out_f32, float* w_out, void* workspace,
+                                size_t workspace_bytes, fm_stream_t stream);
 fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, const uint16_t* q_norm, const uint16_t* wq_b,
                          const uint16_t* w_proj, const int64_t* pos, int T, int dim, int r, int n_h, int head_dim,
                          int rope_dim, double rope_base, double rope_factor, double rope_orig_len,

@@ -19,7 +19,7 @@ __all__ = [
     "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "fm_page_recall",
     "fm_native_topk_paged_ex", "fm_memindex_fp8_workspace", "fm_memindex_score_mask_fp8",
     "fm_index_prefill_scores", "fm_retriever_workspace", "fm_retriever_score_mask", "fm_query_chain_workspace",
-    "fm_query_chain", "LIB_PATH",
+    "fm_query_chain", "fm_query_chain_layers_workspace", "fm_query_chain_layers", "LIB_PATH",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -94,6 +94,13 @@ def lib() -> ctypes.CDLL:
             _D = ctypes.c_double
             L.fm_query_chain.argtypes = [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _I32, _D, _D, _D,
                                          _D, _D, _F, _VP, _VP, _VP, _VP, _SZ, _VP]
+        if hasattr(L, "fm_query_chain_layers"):
+            _D = ctypes.c_double
+            L.fm_query_chain_layers_workspace.argtypes = [_I32, _I32, _I32, _I32]
+            L.fm_query_chain_layers_workspace.restype = _SZ
+            L.fm_query_chain_layers.argtypes = [_I32, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32,
+                                                _I32, _D, _D, _D, _D, _D, _F, _VP, _VP, _VP, _VP, _SZ, _VP]
+            L.fm_query_chain_layers.restype = ctypes.c_int
         if hasattr(L, "fm_page_recall"):
             L.fm_page_recall.argtypes = [_VP, _I32, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _VP]
         for name in ("fm_memindex_score_mask", "fm_topk_select", "fm_native_topk_paged", "fm_index_prefill_topk",
@@ -191,6 +198,29 @@ def fm_query_chain(hidden, wq_a, q_norm, wq_b, w_proj, pos, q_out, w_out, q_out_
                                 r, n_h, 128, 64, cfg["rope_base"], cfg["rope_factor"], cfg["rope_orig_len"],
                                 cfg["rope_beta_fast"], cfg["rope_beta_slow"], float(eps), _ptr(q_out),
                                 _ptr(q_out_f32), _ptr(w_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_query_chain_layers_workspace(L: int, T: int, r: int, n_h: int) -> int:
+    return lib().fm_query_chain_layers_workspace(L, T, r, n_h)
+
+
+def fm_query_chain_layers(hidden, wq_a, q_norm, wq_b, w_proj, pos, q_out, w_out, q_out_f32=None, eps: float = 1e-6,
+                          workspace=None, stream=None, **rope) -> None:
+    """hidden, wq_a, q_norm, wq_b, w_proj: sequences of L device tensors (one
+    per layer, shapes as fm_query_chain); pos [T] int64 -> q_out [T,L,n_h,128]
+    bf16, w_out [T,L,n_h] fp32 (q_out_f32 optional)."""
+    cfg = dict(RETRIEVER_ROPE, **rope)
+    L = len(hidden)
+    T, dim = hidden[0].shape
+    r = wq_a[0].shape[0]
+    n_h = w_proj[0].shape[0]
+    arr = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fm_query_chain_layers(L, arr(hidden), arr(wq_a), arr(q_norm), arr(wq_b), arr(w_proj), _ptr(pos), T,
+                                       dim, r, n_h, 128, 64, cfg["rope_base"], cfg["rope_factor"],
+                                       cfg["rope_orig_len"], cfg["rope_beta_fast"], cfg["rope_beta_slow"], float(eps),
+                                       _ptr(q_out), _ptr(q_out_f32), _ptr(w_out), _ptr(workspace), ws_bytes,
+                                       _stream(stream)))
 
 
 ENSEMBLE_MAX, ENSEMBLE_MEAN = 0, 1

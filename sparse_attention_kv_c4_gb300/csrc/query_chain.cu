@@ -74,10 +74,10 @@ __device__ __forceinline__ void grid_dep_launch_dependents() {
 }
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, unsigned block, size_t smem, cudaStream_t stream,
                        Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -89,6 +89,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// One device pointer per layer (by value).
+struct LayerPtrs {
+  const uint16_t* p[4];
+};
+
 // Rotary frequencies theta'_i of the 32 pairs, computed once per call on the
 // host (fp64) and passed by value.
 struct RopeFreqs {
@@ -96,9 +101,11 @@ struct RopeFreqs {
 };
 
 // ---------------------------------------------------------------------------
-// Projection GEMM for a few tokens:
-//     part[split][t][col] = sum_{k in split} X[t, k] * W[col, k]
-// W is W0 (tiles 0 .. nt0-1) then W1 (tiles nt0 ..), 128 rows per tile.
+// Projection GEMM for a few tokens, over up to kGMaxMats weight matrices of
+// up to kGMaxLayers layers in one launch:
+//     part[layer][split][t][col] = sum_{k in split} X_layer[t, k] * W_m[row, k]
+// with matrix m's 128-row tiles numbered from mat_tile0[m], its rows placed at
+// column (mat_col_tile[m] + tile) * 128 + row of its layer's part rows.
 // ---------------------------------------------------------------------------
 constexpr int kGM = 128;                  // weight rows per tile (UMMA M, TMEM lanes)
 constexpr int kGK = 64;                   // K elements per chunk: one 128-byte swizzle atom
@@ -108,17 +115,27 @@ constexpr int kGMaxStages = 8;
 constexpr int kGMaxTokens = 256;          // tokens per launch (UMMA N <= 256)
 constexpr int kGMaxSplits = 16;
 constexpr int kGSizingSms = 160;          // workspace sizing bound on the SM count (GB300: 152)
+constexpr int kGMaxLayers = 4;
+constexpr int kGMaxMats = 2 * kGMaxLayers;
+
+struct GemmMaps {
+  CUtensorMap w[kGMaxMats];   // weight matrices [rows, K] bf16
+  CUtensorMap x[kGMaxLayers]; // each layer's activations [T, K] bf16
+};
 
 struct GemmParams {
   float* part;
   unsigned int* status;
-  int64_t ld_part;     // columns of part: (nt0 + nt1) * 128
-  int64_t t_rows;      // rows of one split's block of part (all tokens of the call)
+  int64_t ld_part;     // columns of one layer's part rows
+  int64_t t_rows;      // rows of one (layer, split) block of part (all tokens of the call)
   int t_base;          // first token of this launch
   int T;               // tokens in this launch (<= kGMaxTokens)
   int tpad;            // UMMA N: T rounded up to 16
   int kc;              // K chunks
-  int nt0;             // tiles of W0
+  int n_mats;
+  int mat_tile0[kGMaxMats + 1];  // first tile of each matrix (prefix over the matrices)
+  int mat_layer[kGMaxMats];
+  int mat_col_tile[kGMaxMats];   // the matrix's first column tile in its layer's part rows
   int splits;
   int stages;
   uint32_t tmem_cols;
@@ -126,8 +143,7 @@ struct GemmParams {
 };
 
 __global__ void __launch_bounds__(kGThreads, 1)
-    proj_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w0, const __grid_constant__ CUtensorMap tmap_w1,
-                     const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
+    proj_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_bytes = p.tpad * 128;
@@ -141,9 +157,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
   const int c_begin = (int)((int64_t)p.kc * split / p.splits);
   const int c_end = (int)((int64_t)p.kc * (split + 1) / p.splits);  // > c_begin: splits <= kc
-  const bool second = tile >= p.nt0;
-  const int row0 = (second ? tile - p.nt0 : tile) * kGM;
-  const CUtensorMap* wmap = second ? &tmap_w1 : &tmap_w0;
+  int m = 0;
+  while (m + 1 < p.n_mats && tile >= p.mat_tile0[m + 1]) ++m;
+  const int tile_in = tile - p.mat_tile0[m];
+  const int layer = p.mat_layer[m];
+  const int row0 = tile_in * kGM;
+  const CUtensorMap* wmap = &maps.w[m];
+  const CUtensorMap* xmap = &maps.x[layer];
   const int stages = p.stages;
 
   if (threadIdx.x == 0) {
@@ -158,7 +178,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch(wmap);
-    tma_prefetch(&tmap_x);
+    tma_prefetch(xmap);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, p.tmem_cols);
@@ -186,14 +206,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
       }
       grid_dep_wait();
       for (int i = 0; i < pre; ++i)
-        tma_load_2d(smem + i * stage_bytes + kGAtomA, &tmap_x, &bar_full[i], (c_begin + i) * kGK, p.t_base);
+        tma_load_2d(smem + i * stage_bytes + kGAtomA, xmap, &bar_full[i], (c_begin + i) * kGK, p.t_base);
       uint32_t stage = (uint32_t)(pre % stages), phase = pre == stages ? 1u : 0u;
       for (int c = c_begin + pre; c < c_end; ++c) {
         if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)stage_bytes);
         uint8_t* st = smem + stage * stage_bytes;
         tma_load_2d(st, wmap, &bar_full[stage], c * kGK, row0);
-        tma_load_2d(st + kGAtomA, &tmap_x, &bar_full[stage], c * kGK, p.t_base);
+        tma_load_2d(st + kGAtomA, xmap, &bar_full[stage], c * kGK, p.t_base);
         issued[stage] = (int)phase;
         if (++stage == (uint32_t)stages) {
           stage = 0;
@@ -242,7 +262,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int row = quad * 32 + lane;
     if (mbar_wait(&bar_tfull, 0, &abort_flag, p.status)) {
       tc_fence_after();
-      float* out = p.part + ((int64_t)split * p.t_rows + p.t_base) * p.ld_part + (int64_t)tile * kGM + row;
+      float* out = p.part + (((int64_t)layer * p.splits + split) * p.t_rows + p.t_base) * p.ld_part +
+                   (int64_t)(p.mat_col_tile[m] + tile_in) * kGM + row;
       for (int t0 = 0; t0 < p.tpad; t0 += 16) {
         uint32_t r[16];
         tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)t0, r);
@@ -278,57 +299,62 @@ int gemm_splits_max(int tiles) {
   return cap < 1 ? 1 : cap;
 }
 
-// part[s][t][col] for the T tokens of X [T, K] against W0 [N0, K] and W1
-// [N1, K] (W1 may be null); ld_part = (ceil(N0/128) + ceil(N1/128)) * 128.
+// One projection launch set: up to kGMaxMats weight matrices [rows, K] (matrix
+// m of layer mats[m].layer, its tiles at column tile mats[m].col_tile of that
+// layer's part rows) against each layer's activations X[layer] [T, K].
+struct ProjMat {
+  const uint16_t* w;
+  int rows;
+  int layer;
+  int col_tile;
+};
+
+// part[layer][s][t][col]; ld_part = the column tiles of one layer * 128.
 // Launches one grid per 256 tokens.
-fm_status proj_gemm(const uint16_t* X, int T, int K, const uint16_t* W0, int N0, const uint16_t* W1, int N1,
-                    int num_sms, float* part, int* splits_out, unsigned int* status, bool pdl, bool prefetch,
-                    cudaStream_t stream) {
-  const int nt0 = (N0 + kGM - 1) / kGM, nt1 = W1 != nullptr ? (N1 + kGM - 1) / kGM : 0;
+fm_status proj_gemm(const uint16_t* const* X, int n_layers, int T, int K, const ProjMat* mats, int n_mats,
+                    int64_t ld_part, int num_sms, float* part, int* splits_out, unsigned int* status, bool pdl,
+                    bool prefetch, cudaStream_t stream) {
+  GemmParams gp = {};
+  GemmMaps maps;
+  int tiles = 0;
+  for (int m = 0; m < n_mats; ++m) {
+    gp.mat_tile0[m] = tiles;
+    gp.mat_layer[m] = mats[m].layer;
+    gp.mat_col_tile[m] = mats[m].col_tile;
+    tiles += (mats[m].rows + kGM - 1) / kGM;
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)mats[m].rows};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {(uint32_t)kGK, (uint32_t)kGM};
+    fm_status st = make_tmap(&maps.w[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mats[m].w, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != FM_OK) return st;
+  }
+  gp.mat_tile0[n_mats] = tiles;
+  for (int m = n_mats; m < kGMaxMats; ++m) maps.w[m] = maps.w[0];
   const int kc = (K + kGK - 1) / kGK;
-  const int splits = gemm_splits(nt0 + nt1, kc, num_sms);
+  const int splits = gemm_splits(tiles, kc, num_sms);
   *splits_out = splits;
-  CUtensorMap tw0, tw1, tx;
-  {
-    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N0};
-    const uint64_t strides[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {(uint32_t)kGK, (uint32_t)kGM};
-    fm_status st = make_tmap(&tw0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W0, dims, strides, box,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != FM_OK) return st;
-  }
-  if (W1 != nullptr) {
-    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N1};
-    const uint64_t strides[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {(uint32_t)kGK, (uint32_t)kGM};
-    fm_status st = make_tmap(&tw1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W1, dims, strides, box,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != FM_OK) return st;
-  } else {
-    tw1 = tw0;
-  }
   for (int t_base = 0; t_base < T; t_base += kGMaxTokens) {
     const int Tb = T - t_base < kGMaxTokens ? T - t_base : kGMaxTokens;
     const int tpad = (Tb + 15) / 16 * 16;
-    {
+    for (int l = 0; l < kGMaxLayers; ++l) {
       // rows past T read as zeros (the copy's out-of-bounds fill)
       const uint64_t dims[2] = {(uint64_t)K, (uint64_t)T};
       const uint64_t strides[1] = {(uint64_t)K * 2};
       const uint32_t box[2] = {(uint32_t)kGK, (uint32_t)tpad};
-      fm_status st = make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, dims, strides, box,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+      fm_status st = make_tmap(&maps.x[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X[l < n_layers ? l : 0], dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
       if (st != FM_OK) return st;
     }
-    GemmParams gp;
     gp.part = part;
     gp.status = status;
-    gp.ld_part = (int64_t)(nt0 + nt1) * kGM;
+    gp.ld_part = ld_part;
     gp.t_rows = T;
     gp.t_base = t_base;
     gp.T = Tb;
     gp.tpad = tpad;
     gp.kc = kc;
-    gp.nt0 = nt0;
+    gp.n_mats = n_mats;
     gp.splits = splits;
     const int stage_bytes = kGAtomA + tpad * 128;
     int stages = (200 * 1024) / stage_bytes;
@@ -341,11 +367,11 @@ fm_status proj_gemm(const uint16_t* X, int T, int K, const uint16_t* W0, int N0,
     const int smem = 1024 + stages * stage_bytes;
     cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "query chain: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    const unsigned grid = (unsigned)((nt0 + nt1) * splits);
+    const unsigned grid = (unsigned)(tiles * splits);
     if (pdl) {
-      e = launch_pdl(proj_gemm_kernel, grid, kGThreads, (size_t)smem, stream, tw0, tw1, tx, gp);
+      e = launch_pdl(proj_gemm_kernel, dim3(grid), kGThreads, (size_t)smem, stream, maps, gp);
     } else {
-      proj_gemm_kernel<<<grid, kGThreads, smem, stream>>>(tw0, tw1, tx, gp);
+      proj_gemm_kernel<<<grid, kGThreads, smem, stream>>>(maps, gp);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "query chain: GEMM launch: %s", cudaGetErrorString(e));
@@ -353,8 +379,9 @@ fm_status proj_gemm(const uint16_t* X, int T, int K, const uint16_t* W0, int N0,
   return FM_OK;
 }
 
-// One CTA per token t: a = sum of the splits of part[., t, 0..r), RMSNorm,
-// rounded to bf16; w[t, h] = w_scale * sum of the splits of part[., t, w_col0 + h].
+// One CTA per (token t, layer l): a = sum of the splits of part[l, ., t, 0..r),
+// RMSNorm with layer l's gain, rounded to bf16 into c[l, t]; w[t, l, h] =
+// w_scale * sum of the splits of part[l, ., t, w_col0 + h].
 // The splits are summed in order 0, 1, ...  A thread takes its elements two at
 // a time with the partial loads of up to eight splits issued together, so the
 // row's reduction costs a few memory round trips, not one per split.
@@ -362,16 +389,19 @@ constexpr int kNormThreads = 1024;
 constexpr int kNormUnroll = 2;
 constexpr int kNormSplitBatch = 8;
 __global__ void __launch_bounds__(kNormThreads)
-    rmsnorm_kernel(const float* __restrict__ part, int splits, int64_t ld, int64_t T, int r,
-                   const uint16_t* __restrict__ g, float eps, uint16_t* __restrict__ out, int n_h, int64_t w_col0,
-                   float w_scale, float* __restrict__ w_out) {
+    rmsnorm_kernel(const float* __restrict__ part, int splits, int64_t ld, int64_t T, int r, LayerPtrs gains,
+                   float eps, uint16_t* __restrict__ c_out, int n_h, int64_t w_col0, float w_scale,
+                   float* __restrict__ w_out) {
   __shared__ float warp_ss[kNormThreads / 32];
   grid_dep_launch_dependents();
   grid_dep_wait();  // part is the previous kernel's output
   const int64_t t = blockIdx.x;
+  const int layer = blockIdx.y, n_layers = gridDim.y;
   const int tid = threadIdx.x;
-  const float* row = part + t * ld;
   const int64_t split_stride = T * ld;
+  const float* row = part + (int64_t)layer * splits * split_stride + t * ld;
+  const uint16_t* g = gains.p[layer];
+  uint16_t* out = c_out + (int64_t)layer * T * r;
   // a[j] = the sum over splits of column c0 + j * kNormThreads (0 where that is >= n)
   auto sums = [&](int64_t c0, int64_t n, float (&a)[kNormUnroll]) {
 #pragma unroll
@@ -420,7 +450,7 @@ __global__ void __launch_bounds__(kNormThreads)
 #pragma unroll
     for (int j = 0; j < kNormUnroll; ++j) {
       const int h = h0 + j * kNormThreads;
-      if (h < n_h) w_out[t * n_h + h] = w_scale * a[j];
+      if (h < n_h) w_out[(t * n_layers + layer) * n_h + h] = w_scale * a[j];
     }
   }
 }
@@ -442,20 +472,25 @@ RopeFreqs yarn_freqs(double base, double factor, double orig_len, double beta_fa
   return r;
 }
 
-// u = the splits of part summed in order; part is [splits][rows * 128] with
-// row = (token, head).
+// u = the splits of part summed in order; part is [layers][splits][T * n_h * 128]
+// (rows of one layer's split block: (token, head)).  q_out is [T, layers, n_h, 128].
 __global__ void __launch_bounds__(256)
-    rope_hadamard_kernel(const float* __restrict__ part, int splits, const int64_t* __restrict__ pos, int64_t rows,
-                         int n_h, RopeFreqs rf, uint16_t* __restrict__ q_out, float* __restrict__ q_out_f32) {
+    rope_hadamard_kernel(const float* __restrict__ part, int splits, const int64_t* __restrict__ pos, int64_t T,
+                         int n_layers, int n_h, RopeFreqs rf, uint16_t* __restrict__ q_out,
+                         float* __restrict__ q_out_f32) {
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head)
+  const int64_t rows = T * n_h;                                         // per layer
+  const int64_t grow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);    // (layer, token, head)
   grid_dep_launch_dependents();
   grid_dep_wait();  // part is the previous kernel's output
-  if (row >= rows) return;
-  const int64_t t = row / n_h;
-  float4 in = *reinterpret_cast<const float4*>(part + row * kHeadDim + 4 * lane);
+  if (grow >= rows * n_layers) return;
+  const int64_t layer = grow / rows, prow = grow % rows;
+  const int64_t t = prow / n_h, hh = prow % n_h;
+  const int64_t row = (t * n_layers + layer) * n_h + hh;               // output row
+  const float* lp = part + layer * splits * rows * kHeadDim;
+  float4 in = *reinterpret_cast<const float4*>(lp + prow * kHeadDim + 4 * lane);
   for (int s = 1; s < splits; ++s) {
-    const float4 x = *reinterpret_cast<const float4*>(part + (s * rows + row) * kHeadDim + 4 * lane);
+    const float4 x = *reinterpret_cast<const float4*>(lp + (s * rows + prow) * kHeadDim + 4 * lane);
     in.x += x.x;
     in.y += x.y;
     in.z += x.z;
@@ -512,20 +547,95 @@ __global__ void __launch_bounds__(256)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: the K-split partials of [a | w] (tiles of wq_a then w_proj), the
-// bf16 RMSNorm output, the K-split partials of u.
+// Workspace: per layer, the K-split partials of [a | w] (tiles of wq_a then
+// w_proj), the bf16 RMSNorm output, the K-split partials of u.
 struct ChainWs {
   size_t part1, c, part2, bytes;
 };
-ChainWs chain_ws(int T, int r, int n_h) {
-  const int nt1 = (r + kGM - 1) / kGM + (n_h + kGM - 1) / kGM;
-  const int nt2 = n_h;  // n_h * 128 rows
+ChainWs chain_ws(int L, int T, int r, int n_h) {
+  const int nt1 = (r + kGM - 1) / kGM + (n_h + kGM - 1) / kGM;  // per layer
+  const int nt2 = n_h;                                           // n_h * 128 rows per layer
   ChainWs w;
   w.part1 = 0;
-  w.c = align256((size_t)gemm_splits_max(nt1) * T * nt1 * kGM * 4);
-  w.part2 = w.c + align256((size_t)T * r * 2);
-  w.bytes = w.part2 + align256((size_t)gemm_splits_max(nt2) * T * nt2 * kGM * 4);
+  w.c = align256((size_t)L * gemm_splits_max(L * nt1) * T * nt1 * kGM * 4);
+  w.part2 = w.c + align256((size_t)L * T * r * 2);
+  w.bytes = w.part2 + align256((size_t)L * gemm_splits_max(L * nt2) * T * nt2 * kGM * 4);
   return w;
+}
+
+fm_status run_chain(int L, const uint16_t* const* hidden, const uint16_t* const* wq_a, const uint16_t* const* q_norm,
+                    const uint16_t* const* wq_b, const uint16_t* const* w_proj, const int64_t* pos, int T, int dim,
+                    int r, int n_h, int head_dim, int rope_dim, double rope_base, double rope_factor,
+                    double rope_orig_len, double rope_beta_fast, double rope_beta_slow, float eps, uint16_t* q_out,
+                    float* q_out_f32, float* w_out, void* workspace, size_t workspace_bytes, cudaStream_t s,
+                    const char* who) {
+  if (L < 1 || L > kGMaxLayers)
+    return set_error(FM_ERR_INVALID_ARG, "%s: L=%d (1..%d layers)", who, L, kGMaxLayers);
+  if (head_dim != kHeadDim || rope_dim != kRopeDim)
+    return set_error(FM_ERR_INVALID_ARG, "%s: head_dim=%d rope_dim=%d (need 128, 64)", who, head_dim, rope_dim);
+  if (T < 0 || dim < 8 || r < 8 || n_h < 1 || dim % 8 != 0 || r % 8 != 0 || n_h > 1024)
+    return set_error(FM_ERR_INVALID_ARG, "%s: bad sizes T=%d dim=%d r=%d n_h=%d (dim, r: multiples of 8)", who, T,
+                     dim, r, n_h);
+  if (!(rope_base > 1.0) || !(rope_factor >= 1.0) || !(rope_orig_len > 0.0) || !(rope_beta_fast > rope_beta_slow) ||
+      !(eps >= 0.0f))
+    return set_error(FM_ERR_INVALID_ARG, "%s: bad rotary or norm parameters", who);
+  if (T == 0) return FM_OK;
+  if (!hidden || !wq_a || !q_norm || !wq_b || !w_proj || !pos || !q_out || !w_out)
+    return set_error(FM_ERR_INVALID_ARG, "%s: required pointer is NULL", who);
+  for (int l = 0; l < L; ++l) {
+    if (!hidden[l] || !wq_a[l] || !q_norm[l] || !wq_b[l] || !w_proj[l])
+      return set_error(FM_ERR_INVALID_ARG, "%s: layer %d: required pointer is NULL", who, l);
+    if (!aligned(hidden[l], 16) || !aligned(wq_a[l], 16) || !aligned(wq_b[l], 16) || !aligned(w_proj[l], 16) ||
+        !aligned(q_norm[l], 2))
+      return set_error(FM_ERR_INVALID_ARG, "%s: layer %d: misaligned pointer", who, l);
+  }
+  if (!aligned(pos, 8) || !aligned(q_out, 8) || !aligned(w_out, 4) || (q_out_f32 && !aligned(q_out_f32, 16)))
+    return set_error(FM_ERR_INVALID_ARG, "%s: misaligned pointer", who);
+  const ChainWs lay = chain_ws(L, T, r, n_h);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes)
+    return set_error(FM_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 256-byte aligned", who, lay.bytes);
+  int sms = 0;
+  fm_status st = check_device(&sms);
+  if (st != FM_OK) return st;
+  unsigned int* status = nullptr;
+  if ((st = status_word(&status)) != FM_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  float* part1 = reinterpret_cast<float*>(base + lay.part1);
+  uint16_t* c = reinterpret_cast<uint16_t*>(base + lay.c);
+  float* part2 = reinterpret_cast<float*>(base + lay.part2);
+  // [a | w] = h . [wq_a | w_proj]^T, every layer in one launch
+  const int nt_a = (r + kGM - 1) / kGM;
+  const int64_t ld1 = (int64_t)(nt_a + (n_h + kGM - 1) / kGM) * kGM;
+  ProjMat mats[kGMaxMats];
+  for (int l = 0; l < L; ++l) {
+    mats[2 * l] = ProjMat{wq_a[l], r, l, 0};
+    mats[2 * l + 1] = ProjMat{w_proj[l], n_h, l, nt_a};
+  }
+  int splits1 = 1, splits2 = 1;
+  if ((st = proj_gemm(hidden, L, T, dim, mats, 2 * L, ld1, sms, part1, &splits1, status, true, false, s)) != FM_OK)
+    return st;
+  // RMSNorm of a, and the head weights w_proj . h scaled by head_dim^-1/2 n_h^-1/2
+  LayerPtrs gains = {};
+  for (int l = 0; l < L; ++l) gains.p[l] = q_norm[l];
+  const float w_scale = (float)(1.0 / sqrt((double)head_dim) / sqrt((double)n_h));
+  cudaError_t e = launch_pdl(rmsnorm_kernel, dim3((unsigned)T, (unsigned)L), kNormThreads, 0, s, (const float*)part1,
+                             splits1, ld1, (int64_t)T, r, gains, eps, c, n_h, (int64_t)nt_a * kGM, w_scale, w_out);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "%s: rmsnorm launch: %s", who, cudaGetErrorString(e));
+  // u = c . wq_b^T, every layer in one launch (layer l's rows of c start at l * T)
+  const uint16_t* c_l[kGMaxLayers];
+  for (int l = 0; l < L; ++l) {
+    c_l[l] = c + (int64_t)l * T * r;
+    mats[l] = ProjMat{wq_b[l], n_h * kHeadDim, l, 0};
+  }
+  if ((st = proj_gemm(c_l, L, T, r, mats, L, (int64_t)n_h * kHeadDim, sms, part2, &splits2, status, true, true, s)) !=
+      FM_OK)
+    return st;
+  const RopeFreqs rf = yarn_freqs(rope_base, rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow);
+  const int64_t rows = (int64_t)L * T * n_h;
+  e = launch_pdl(rope_hadamard_kernel, dim3((unsigned)((rows + 7) / 8)), 256, 0, s, (const float*)part2, splits2, pos,
+                 (int64_t)T, L, n_h, rf, q_out, q_out_f32);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "%s: rope launch: %s", who, cudaGetErrorString(e));
+  return FM_OK;
 }
 
 }  // namespace
@@ -533,7 +643,12 @@ ChainWs chain_ws(int T, int r, int n_h) {
 
 FM_API size_t fm_query_chain_workspace(int T, int r, int n_h) {
   if (T < 0 || r < 1 || n_h < 1) return 0;
-  return fm::chain_ws(T, r, n_h).bytes;
+  return fm::chain_ws(1, T, r, n_h).bytes;
+}
+
+FM_API size_t fm_query_chain_layers_workspace(int L, int T, int r, int n_h) {
+  if (L < 1 || L > fm::kGMaxLayers || T < 0 || r < 1 || n_h < 1) return 0;
+  return fm::chain_ws(L, T, r, n_h).bytes;
 }
 
 FM_API fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, const uint16_t* q_norm,
@@ -542,52 +657,19 @@ FM_API fm_status fm_query_chain(const uint16_t* hidden, const uint16_t* wq_a, co
                                 double rope_orig_len, double rope_beta_fast, double rope_beta_slow, float eps,
                                 uint16_t* q_out, float* q_out_f32, float* w_out, void* workspace,
                                 size_t workspace_bytes, fm_stream_t stream) {
-  using namespace fm;
-  if (head_dim != kHeadDim || rope_dim != kRopeDim)
-    return set_error(FM_ERR_INVALID_ARG, "fm_query_chain: head_dim=%d rope_dim=%d (need 128, 64)", head_dim,
-                     rope_dim);
-  if (T < 0 || dim < 8 || r < 8 || n_h < 1 || dim % 8 != 0 || r % 8 != 0 || n_h > 1024)
-    return set_error(FM_ERR_INVALID_ARG, "fm_query_chain: bad sizes T=%d dim=%d r=%d n_h=%d (dim, r: multiples of 8)",
-                     T, dim, r, n_h);
-  if (!(rope_base > 1.0) || !(rope_factor >= 1.0) || !(rope_orig_len > 0.0) || !(rope_beta_fast > rope_beta_slow) ||
-      !(eps >= 0.0f))
-    return set_error(FM_ERR_INVALID_ARG, "fm_query_chain: bad rotary or norm parameters");
-  if (T == 0) return FM_OK;
-  if (!hidden || !wq_a || !q_norm || !wq_b || !w_proj || !pos || !q_out || !w_out)
-    return set_error(FM_ERR_INVALID_ARG, "fm_query_chain: required pointer is NULL");
-  if (!aligned(hidden, 16) || !aligned(wq_a, 16) || !aligned(wq_b, 16) || !aligned(w_proj, 16) ||
-      !aligned(q_norm, 2) || !aligned(pos, 8) || !aligned(q_out, 8) || !aligned(w_out, 4) ||
-      (q_out_f32 && !aligned(q_out_f32, 16)))
-    return set_error(FM_ERR_INVALID_ARG, "fm_query_chain: misaligned pointer");
-  const ChainWs lay = chain_ws(T, r, n_h);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes)
-    return set_error(FM_ERR_WORKSPACE, "fm_query_chain: workspace needs %zu bytes, 256-byte aligned", lay.bytes);
-  int sms = 0;
-  fm_status st = check_device(&sms);
-  if (st != FM_OK) return st;
-  unsigned int* status = nullptr;
-  if ((st = status_word(&status)) != FM_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* base = static_cast<uint8_t*>(workspace);
-  float* part1 = reinterpret_cast<float*>(base + lay.part1);
-  uint16_t* c = reinterpret_cast<uint16_t*>(base + lay.c);
-  float* part2 = reinterpret_cast<float*>(base + lay.part2);
-  // [a | w] = h . [wq_a | w_proj]^T
-  int splits1 = 1, splits2 = 1;
-  if ((st = proj_gemm(hidden, T, dim, wq_a, r, w_proj, n_h, sms, part1, &splits1, status, true, false, s)) != FM_OK) return st;
-  // RMSNorm of a, and the head weights w_proj . h scaled by head_dim^-1/2 n_h^-1/2
-  const int nt_a = (r + kGM - 1) / kGM;
-  const int64_t ld1 = (int64_t)(nt_a + (n_h + kGM - 1) / kGM) * kGM;
-  const float w_scale = (float)(1.0 / sqrt((double)head_dim) / sqrt((double)n_h));
-  cudaError_t e = launch_pdl(rmsnorm_kernel, (unsigned)T, kNormThreads, 0, s, (const float*)part1, splits1, ld1,
-                             (int64_t)T, r, q_norm, eps, c, n_h, (int64_t)nt_a * kGM, w_scale, w_out);
-  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_query_chain: rmsnorm launch: %s", cudaGetErrorString(e));
-  // u = c . wq_b^T
-  if ((st = proj_gemm(c, T, r, wq_b, n_h * kHeadDim, nullptr, 0, sms, part2, &splits2, status, true, true, s)) != FM_OK) return st;
-  const RopeFreqs rf = yarn_freqs(rope_base, rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow);
-  const int64_t rows = (int64_t)T * n_h;
-  e = launch_pdl(rope_hadamard_kernel, (unsigned)((rows + 7) / 8), 256, 0, s, (const float*)part2, splits2, pos, rows,
-                 n_h, rf, q_out, q_out_f32);
-  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_query_chain: rope launch: %s", cudaGetErrorString(e));
-  return FM_OK;
+  return fm::run_chain(1, &hidden, &wq_a, &q_norm, &wq_b, &w_proj, pos, T, dim, r, n_h, head_dim, rope_dim, rope_base,
+                       rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow, eps, q_out, q_out_f32, w_out,
+                       workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), "fm_query_chain");
+}
+
+FM_API fm_status fm_query_chain_layers(int L, const uint16_t* const* hidden, const uint16_t* const* wq_a,
+                                       const uint16_t* const* q_norm, const uint16_t* const* wq_b,
+                                       const uint16_t* const* w_proj, const int64_t* pos, int T, int dim, int r,
+                                       int n_h, int head_dim, int rope_dim, double rope_base, double rope_factor,
+                                       double rope_orig_len, double rope_beta_fast, double rope_beta_slow, float eps,
+                                       uint16_t* q_out, float* q_out_f32, float* w_out, void* workspace,
+                                       size_t workspace_bytes, fm_stream_t stream) {
+  return fm::run_chain(L, hidden, wq_a, q_norm, wq_b, w_proj, pos, T, dim, r, n_h, head_dim, rope_dim, rope_base,
+                       rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow, eps, q_out, q_out_f32, w_out,
+                       workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), "fm_query_chain_layers");
 }

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
               "fm_topk_select",
               "fm_native_topk_paged_workspace", "fm_index_prefill_workspace", "fm_topk_workspace",
               "fm_retriever_score_mask", "fm_retriever_workspace",
-              "fm_query_chain", "fm_query_chain_workspace",
+              "fm_query_chain", "fm_query_chain_workspace", "fm_query_chain_layers", "fm_query_chain_layers_workspace",
               "fm_last_error", "fm_device_status", "fm_version"):
         assert n in names
 

@@ -119,3 +119,30 @@ def test_query_chain_feeds_the_retriever(torch_dev, orc):
     q_ref_bits = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     x_ref = orc.memindex_logits_fp8(q_ref_bits, w_ref, k8, sc)
     assert np.all(np.abs(x_gpu - x_ref) <= 2.0 ** -5 * (np.abs(x_ref) + np.abs(x_ref).mean()) + 1e-3)
+
+
+@pytest.mark.parametrize("L,T,n_h,dim,r", [(3, 30, 128, 4096, 2048), (2, 5, 64, 1024, 512), (4, 300, 8, 520, 264)])
+def test_query_chain_layers_match_oracle(torch_dev, orc, L, T, n_h, dim, r):
+    """fm_query_chain_layers: every layer against the oracle's chain for that
+    layer (its own weights, the shared positions), outputs in [T, L, ...]."""
+    torch, dev = torch_dev
+    import sparse_attention_kv_c4_gb300 as fm
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).to(dev)
+    ins = [gen.query_chain_inputs(T, dim=dim, r=r, n_h=n_h, seed=gen.BASE_SEED + 800 + 10 * L + l) for l in range(L)]
+    pos = ins[0][5]
+    dev_in = [[t(a) for a in x[:5]] for x in ins]
+    q = torch.zeros((T, L, n_h, 128), dtype=torch.int16, device=dev)
+    q32 = torch.zeros((T, L, n_h, 128), dtype=torch.float32, device=dev)
+    w = torch.zeros((T, L, n_h), dtype=torch.float32, device=dev)
+    ws = torch.empty(fm.fm_query_chain_layers_workspace(L, T, r, n_h), dtype=torch.uint8, device=dev)
+    fm.fm_query_chain_layers([x[0] for x in dev_in], [x[1] for x in dev_in], [x[2] for x in dev_in],
+                             [x[3] for x in dev_in], [x[4] for x in dev_in], t(pos), q, w, q_out_f32=q32,
+                             workspace=ws)
+    torch.cuda.synchronize()
+    assert fm.fm_device_status(reset=True) == 0
+    qb_all = (q.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for l in range(L):
+        hidden, wq_a, q_norm, wq_b, w_proj, _ = ins[l]
+        q_ref, w_ref = orc.query_chain(hidden, wq_a, q_norm, wq_b, w_proj, pos, n_h=n_h)
+        _check(q_ref, w_ref, qb_all[:, l], q32[:, l].cpu().numpy().astype(np.float64),
+               w[:, l].cpu().numpy().astype(np.float64))
