@@ -54,7 +54,7 @@ PROFILE_CASES = {
     "memindex_fp8": [("memindex_fp8_kernel_memindex_fp8_1m_b4_l3_s262144.md", ["memindex_fp8.cu", "fp8.cuh", "fm_common.cuh"],
                       4, 30)],
     "retriever": [("retriever_kernel_retriever_1m_b4_l3_s262144.md", ["retriever.cu", "fp8.cuh", "fm_common.cuh"], 4, 30)],
-    "query_chain": [("proj_gemm_kernel_query_chain_t30.md", ["query_chain.cu", "fm_common.cuh"], 1, 3)],
+    "query_chain": [("proj_gemm_kernel_query_chain_t30.md", ["query_chain.cu", "fm_common.cuh"], 1, 1)],
     "prefill_scores": [("prefill_score_kernel_prefill_t4096_s65536_dram.md", ["prefill.cu", "fm_common.cuh"], 1, 1)],
     "prefill_topk": [("prefill_score_kernel_prefill_t512_s65536.md", ["prefill.cu", "fm_common.cuh"], 512, 4096),
                      ("topk_rows_kernel_prefill_t512_s65536.md", ["topk.cu", "topk.cuh", "fm_common.cuh"], 512, 4096)],
