@@ -16,13 +16,14 @@
 // more than the CUDA cores can sustain at full bandwidth.  They run on the
 // tensor cores with the weights as the streamed operand:
 //   proj_gemm_kernel      one CTA per (128-row weight tile, K split): a TMA
-//                         producer streams [128 rows x 64] weight chunks
-//                         (the UMMA A operand, SWIZZLE_128B) and the matching
-//                         [tokens x 64] activation chunks (B, tokens padded to
-//                         a multiple of 16 by the copy's zero fill); one thread
-//                         issues tcgen05.mma kind::f16 M=128 N=tokens K=16 into
-//                         a TMEM accumulator; four epilogue warps write the
-//                         fp32 partial sums (thread = weight row).  wq_a and
+//                         producer streams [128 rows x 128] weight chunks as
+//                         two SWIZZLE_128B atoms (the UMMA A operand) and the
+//                         matching [tokens x 128] activation chunks (B, tokens
+//                         padded to a multiple of 16 by the copy's zero fill);
+//                         one thread issues 8 tcgen05.mma kind::f16 M=128
+//                         N=tokens K=16 per chunk into a TMEM accumulator;
+//                         four epilogue warps write the fp32 partial sums
+//                         (thread = weight row).  wq_a and
 //                         w_proj share the hidden state, so they are one launch
 //                         (w_proj's tile after wq_a's).  Each GEMM is split
 //                         along K so that tiles x splits fills the SMs once.
@@ -108,8 +109,10 @@ struct RopeFreqs {
 // column (mat_col_tile[m] + tile) * 128 + row of its layer's part rows.
 // ---------------------------------------------------------------------------
 constexpr int kGM = 128;                  // weight rows per tile (UMMA M, TMEM lanes)
-constexpr int kGK = 64;                   // K elements per chunk: one 128-byte swizzle atom
-constexpr int kGAtomA = kGM * kGK * 2;    // 16 KB of weights per chunk
+constexpr int kGK = 64;                   // K elements of one 128-byte swizzle atom
+constexpr int kGAtomA = kGM * kGK * 2;    // 16 KB of weights per atom
+constexpr int kGAtoms = 2;                // atoms per stage: a chunk is 128 K elements (8 MMAs per barrier round trip)
+constexpr int kGKStage = kGK * kGAtoms;
 constexpr int kGThreads = 192;            // producer warp, issuer warp, four epilogue warps
 constexpr int kGMaxStages = 8;
 constexpr int kGMaxTokens = 256;          // tokens per launch (UMMA N <= 256)
@@ -146,8 +149,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     proj_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int b_bytes = p.tpad * 128;
-  const int stage_bytes = kGAtomA + b_bytes;  // both multiples of 1 KB (the swizzle atom)
+  const int b_bytes = p.tpad * 128;                  // one activation atom
+  const int stage_bytes = kGAtoms * (kGAtomA + b_bytes);  // A atoms, then B atoms; all multiples of 1 KB
 
   __shared__ __align__(8) uint64_t bar_full[kGMaxStages], bar_empty[kGMaxStages], bar_tfull, bar_drain;
   __shared__ uint32_t tmem_slot;
@@ -201,19 +204,25 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const int pre = !p.prefetch_weights ? 0 : (c_end - c_begin < stages ? c_end - c_begin : stages);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&bar_full[i], (uint32_t)stage_bytes);
-        tma_load_2d(smem + i * stage_bytes, wmap, &bar_full[i], (c_begin + i) * kGK, row0);
+        for (int a = 0; a < kGAtoms; ++a)
+          tma_load_2d(smem + i * stage_bytes + a * kGAtomA, wmap, &bar_full[i], (c_begin + i) * kGKStage + a * kGK,
+                      row0);
         issued[i] = 0;
       }
       grid_dep_wait();
       for (int i = 0; i < pre; ++i)
-        tma_load_2d(smem + i * stage_bytes + kGAtomA, xmap, &bar_full[i], (c_begin + i) * kGK, p.t_base);
+        for (int a = 0; a < kGAtoms; ++a)
+          tma_load_2d(smem + i * stage_bytes + kGAtoms * kGAtomA + a * b_bytes, xmap, &bar_full[i],
+                      (c_begin + i) * kGKStage + a * kGK, p.t_base);
       uint32_t stage = (uint32_t)(pre % stages), phase = pre == stages ? 1u : 0u;
       for (int c = c_begin + pre; c < c_end; ++c) {
         if (!mbar_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)stage_bytes);
         uint8_t* st = smem + stage * stage_bytes;
-        tma_load_2d(st, wmap, &bar_full[stage], c * kGK, row0);
-        tma_load_2d(st + kGAtomA, xmap, &bar_full[stage], c * kGK, p.t_base);
+        for (int a = 0; a < kGAtoms; ++a) {
+          tma_load_2d(st + a * kGAtomA, wmap, &bar_full[stage], c * kGKStage + a * kGK, row0);
+          tma_load_2d(st + kGAtoms * kGAtomA + a * b_bytes, xmap, &bar_full[stage], c * kGKStage + a * kGK, p.t_base);
+        }
         issued[stage] = (int)phase;
         if (++stage == (uint32_t)stages) {
           stage = 0;
@@ -240,11 +249,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
         tc_fence_after();
         // descriptor start-address field counts 16-byte units; K=16 steps are
         // 32 bytes apart inside the 128-byte swizzle atom
-        const uint64_t a_desc = desc0 + (uint64_t)(stage * (stage_bytes >> 4));
-        const uint64_t b_desc = a_desc + (uint64_t)(kGAtomA >> 4);
+        const uint64_t s_desc = desc0 + (uint64_t)(stage * (stage_bytes >> 4));
 #pragma unroll
-        for (int k = 0; k < kGK / 16; ++k)
-          umma_bf16_ss(tmem_base, a_desc + 2 * k, b_desc + 2 * k, idesc, (c > c_begin || k > 0) ? 1u : 0u);
+        for (int a = 0; a < kGAtoms; ++a) {
+          const uint64_t a_desc = s_desc + (uint64_t)((a * kGAtomA) >> 4);
+          const uint64_t b_desc = s_desc + (uint64_t)((kGAtoms * kGAtomA + a * b_bytes) >> 4);
+#pragma unroll
+          for (int k = 0; k < kGK / 16; ++k)
+            umma_bf16_ss(tmem_base, a_desc + 2 * k, b_desc + 2 * k, idesc, (c > c_begin || a > 0 || k > 0) ? 1u : 0u);
+        }
         umma_commit(&bar_empty[stage]);
         if (++stage == (uint32_t)stages) {
           stage = 0;
@@ -331,7 +344,7 @@ fm_status proj_gemm(const uint16_t* const* X, int n_layers, int T, int K, const 
   }
   gp.mat_tile0[n_mats] = tiles;
   for (int m = n_mats; m < kGMaxMats; ++m) maps.w[m] = maps.w[0];
-  const int kc = (K + kGK - 1) / kGK;
+  const int kc = (K + kGKStage - 1) / kGKStage;
   const int splits = gemm_splits(tiles, kc, num_sms);
   *splits_out = splits;
   for (int t_base = 0; t_base < T; t_base += kGMaxTokens) {
@@ -356,7 +369,7 @@ fm_status proj_gemm(const uint16_t* const* X, int n_layers, int T, int K, const 
     gp.kc = kc;
     gp.n_mats = n_mats;
     gp.splits = splits;
-    const int stage_bytes = kGAtomA + tpad * 128;
+    const int stage_bytes = kGAtoms * (kGAtomA + tpad * 128);
     int stages = (200 * 1024) / stage_bytes;
     if (stages > kGMaxStages) stages = kGMaxStages;
     gp.stages = stages;
