@@ -303,10 +303,46 @@ def phase_figures(cfgs):
     }
 
 
+def resident_fraction(torch, mask, B, S):
+    """Fraction of the B x S chunks set in a packed resident mask (a popcount
+    through a byte table; a reported statistic, not part of the path)."""
+    lut = torch.tensor([bin(i).count("1") for i in range(256)], dtype=torch.int64, device=mask.device)
+    return float(lut[mask.contiguous().view(torch.uint8).long()].sum().item()) / (B * S)
+
+
+def memindex_hot_variant(torch, dev, fm, W, mi, hot, pk, reps=10, warmup=3):
+    """The 1M Memory-Indexer workload at another planted-hot fraction: the
+    step's key buffer refilled in place (after the step), timed alone."""
+    import gen
+    cfg = gen.replace(mi, hot_frac=hot)
+    q, w, hv = gen.memindex_qw(cfg)
+    W["mi_q"].copy_(torch.from_numpy(q.view(np.int16)))
+    W["mi_w"].copy_(torch.from_numpy(w))
+    hot_d = torch.from_numpy(hv).to(dev)
+    gen.memindex_keys_device(cfg, hot_d.data_ptr(), W["mi_K"].data_ptr(), cfg.L * cfg.S * cfg.d, cfg.S * cfg.d)
+    call = lambda: fm.fm_memindex_score_mask(W["mi_q"], W["mi_w"], W["mi_K"], W["mi_mask"], W["mi_maxsig"])
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    nbytes = cfg.B * cfg.L * cfg.S * 256 + cfg.B * cfg.S * 4 + cfg.B * ((cfg.S + 31) // 32) * 4
+    ach = nbytes / (ms / 1e3) / 1e9
+    return {"ms": round(ms, 4), "chunk_scores_per_s": cfg.B * cfg.L * cfg.S / (ms / 1e3), "bound": "hbm",
+            "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+            "algorithmic_bytes": nbytes, "hot_frac": hot,
+            "resident_fraction": round(resident_fraction(torch, W["mi_mask"], cfg.B, cfg.S), 4), "reps": reps,
+            "workload": f"memindex {cfg.B}x{cfg.L}x{cfg.S} bf16, {int(round(hot * 100))}% planted hot"}
+
+
 def sanity(torch, W, cfgs):
     mi, pg, pf = cfgs
-    frac = float(torch.bitwise_count(W["mi_mask"]).sum().item()) / (mi.B * mi.S) if hasattr(torch, "bitwise_count") \
-        else None
+    frac = resident_fraction(torch, W["mi_mask"], mi.B, mi.S)
     ok = bool((W["pg_idx"] >= 0).all().item()) and bool((W["pf_idx"] >= 0).all().item())
     recalled = float(W["rc_n"].float().mean().item())
     return {"resident_fraction": frac, "topk_full": ok, "pages_recalled_mean": recalled}
@@ -602,6 +638,8 @@ def run_ours(args):
         v = QueryChain(torch, dev, fm)
         variants["query_chain"] = v.measure(20, 3, pk)
         del v
+        for hot in (0.05, 0.25):  # the 1M workload's other hot fractions (the step runs 12%)
+            variants[f"memindex_hot{int(round(hot * 100))}"] = memindex_hot_variant(torch, dev, fm, W, mi, hot, pk)
         if fm.fm_device_status(reset=True) != 0:
             raise RuntimeError("device status flagged an error in the variant rows")
 
