@@ -98,6 +98,33 @@ def test_prefill_scores_rejects_bad_args_on_host(lib):
     assert f(None, None, None, None, 0, 100, 64, 128, 4, None, None) == 0  # T = 0: nothing to do
 
 
+def test_query_chain_layers_rejects_bad_args_on_host(lib):
+    import ctypes
+    import sparse_attention_kv_c4_gb300 as fm
+    fm.lib()  # sets argtypes
+    f = lib.fm_query_chain_layers
+    fake = 4096  # never dereferenced: validation fails first
+    ptrs = (ctypes.c_void_p * 4)(fake, fake, fake, fake)
+    rope = (160000.0, 16.0, 65536.0, 32.0, 1.0, 1e-6)
+
+    def call(L, T=4, dim=512, r=256, n_h=8, hd=128, rd=64, arrs=ptrs, q=fake, w=fake, ws=None, wsb=0):
+        return f(L, arrs, arrs, arrs, arrs, arrs, fake, T, dim, r, n_h, hd, rd, *rope, q, None, w, ws, wsb, None)
+    assert call(0) == 1 and "L=0" in fm.fm_last_error()          # no layers
+    assert call(5) == 1                                          # more than four layers
+    assert call(2, hd=64) == 1                                   # head_dim must be 128
+    assert call(2, dim=516) == 1                                 # dim not a multiple of 8
+    assert call(2, q=None) == 1                                  # NULL q_out
+    null_layer = (ctypes.c_void_p * 4)(fake, None, fake, fake)
+    assert call(2, arrs=null_layer) == 1 and "layer 1" in fm.fm_last_error()
+    misaligned = (ctypes.c_void_p * 4)(fake, fake + 8, fake, fake)
+    assert call(2, arrs=misaligned) == 1
+    assert call(2) == 4                                          # no workspace: FM_ERR_WORKSPACE
+    assert call(2, T=0) == 0                                     # nothing to do
+    assert fm.fm_query_chain_layers_workspace(3, 30, 2048, 128) > fm.fm_query_chain_workspace(30, 2048, 128)
+    assert fm.fm_query_chain_layers_workspace(1, 30, 2048, 128) == fm.fm_query_chain_workspace(30, 2048, 128)
+    assert fm.fm_query_chain_layers_workspace(5, 30, 2048, 128) == 0
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import sparse_attention_kv_c4_gb300 as fm
     monkeypatch.setattr(fm, "_lib", None)
