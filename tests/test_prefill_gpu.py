@@ -99,8 +99,8 @@ def test_prefill_full_size_sampled(torch_dev, orc, variant):
     check(orc, q, w, pos, K, idx, sc, cfg.k, rows=rows)
 
 
-@pytest.mark.parametrize("T,S,start", [(37, 1000, None), (9, 4097, 0), (6, 300, -3)])
-def test_prefill_scores_match_oracle(torch_dev, orc, T, S, start):
+@pytest.mark.parametrize("T,S,start,ratio", [(37, 1000, None, 4), (9, 4097, 0, 4), (6, 300, -3, 4), (11, 900, 0, 3)])
+def test_prefill_scores_match_oracle(torch_dev, orc, T, S, start, ratio):
     """fm_index_prefill_scores: every element against the oracle's scores,
     -inf exactly where s >= the token's causal limit.  start=None puts every
     position past 4S (nothing masked); 0 makes the limit bite inside the row
@@ -109,12 +109,12 @@ def test_prefill_scores_match_oracle(torch_dev, orc, T, S, start):
     import sparse_attention_kv_c4_gb300 as fm
     pos = None if start is None else np.arange(start, start + T, dtype=np.int64) * 97
     q, w, pos, K = small(T, S, seed=T * 11 + S, pos=pos)
-    ref = orc.prefill_logits(q, w, pos, K)
+    ref = orc.prefill_logits(q, w, pos, K, ratio=ratio)
     out = torch.full((T, S), 7.0, dtype=torch.float32, device=dev)
     fm.fm_index_prefill_scores(torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).to(dev),
                                torch.from_numpy(np.ascontiguousarray(w)).to(dev),
                                torch.from_numpy(np.ascontiguousarray(pos, dtype=np.int64)).to(dev),
-                               torch.from_numpy(np.ascontiguousarray(K).view(np.int16)).to(dev), out)
+                               torch.from_numpy(np.ascontiguousarray(K).view(np.int16)).to(dev), out, ratio=ratio)
     torch.cuda.synchronize()
     assert fm.fm_device_status(reset=True) == 0
     got = out.cpu().numpy().astype(np.float64)
