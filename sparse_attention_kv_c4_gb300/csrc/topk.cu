@@ -55,9 +55,11 @@ FM_DEV int row_len(const int32_t* __restrict__ n_valid, int64_t r, int n) {
 // kMap: 0 = candidate index, 1 = paged rows (PageMap), 2 = paged rows
 // compacted to resident chunks (MaskedPageMap); one instantiation each so the
 // id maps do not share a register allocation.  kShort: rows of at most
-// kTopkShortN scores take a smaller candidate list (kTopkCapShort), which lets
-// five CTAs share an SM instead of four (760 rows per wave on 152 SMs, so the
-// 630 queries of a 1M-context decode batch run in one wave).
+// kTopkShortN scores (every row up to a 1M-token history) take a smaller
+// candidate list (kTopkCapShort), which lets five CTAs share an SM instead of
+// four (760 rows per wave on 152 SMs, so the 630 queries of a 1M-context
+// decode batch run in one wave); a list that overflows falls back to the
+// exact radix path, so the cap affects only speed.
 template <int kMap, bool kShort>
 __global__ void __launch_bounds__(kTopkThreads, kShort ? 5 : 4)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid, int n, int k,

@@ -186,7 +186,7 @@ namespace fm {
 // Scores are reported from their keys: -0 reads as +0 and NaN as -inf.
 constexpr int kTopkCap = 4096;       // candidate slots (32 KB of shared memory)
 constexpr int kTopkCapShort = 3072;  // for rows of at most kTopkShortN scores (24 KB: five CTAs per SM)
-constexpr int kTopkShortN = 32768;
+constexpr int kTopkShortN = 1 << 18;  // every row up to a 1M-token history (262144 chunks)
 constexpr int kTopkRuns = 32;        // sample: 32 runs x 64 scores
 constexpr int kTopkSample = kTopkRuns * 64;
 constexpr int kTopkBitmapN = 131072;  // rows up to this length emit ids via a bitmap
