@@ -59,7 +59,7 @@ def test_topk_random(torch_dev, orc, rows, n, k):
     check_rows(orc, s, k, idx, sc)
 
 
-@pytest.mark.parametrize("n", [20000, 65536])
+@pytest.mark.parametrize("n", [20000, 65536, 262144])
 def test_topk_heavy_ties_and_specials(torch_dev, orc, n):
     torch, dev = torch_dev
     rng = np.random.default_rng(3)
