@@ -96,8 +96,9 @@ __device__ __forceinline__ void st_f32_hint(float* addr, float v, uint64_t polic
 // 1. prep: sort pages, validate, split q
 // --------------------------------------------------------------------------
 
-// THREADS: 256, or 1024 for tables longer than 1024 entries (the bitonic
-// sort's passes then take four elements per thread instead of sixteen).
+// THREADS: 256, or 1024 for tables longer than 1024 entries when the queries
+// fit one wave of such CTAs (the bitonic sort's passes then take four
+// elements per thread instead of sixteen).
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threads: 760 queries per wave
     paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
@@ -592,8 +593,12 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   PagedWs ws = paged_ws_layout(a.workspace, a.Q, a.R);
   int Rpow2 = 1;
   while (Rpow2 < a.R) Rpow2 <<= 1;
-  auto prep = a.R > 1024 ? paged_prep_kernel<1024> : paged_prep_kernel<kPrepThreads>;
-  prep<<<a.Q, a.R > 1024 ? 1024 : kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
+  // Tables longer than 1024 entries sort faster per query with 1024 threads,
+  // but only two such CTAs fit an SM: when the queries exceed one wave of
+  // them, 256 threads (five per SM) finish the batch sooner.
+  const bool wide = a.R > 1024 && a.Q <= 2 * num_sms;
+  auto prep = wide ? paged_prep_kernel<1024> : paged_prep_kernel<kPrepThreads>;
+  prep<<<a.Q, wide ? 1024 : kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
                                                       Rpow2, a.res_mask, a.mask_ld, a.mask_group, ws.s_logical,
                                                       ws.s_phys, ws.nres_eff, ws.n_valid, ws.pmask, ws.pprefix,
                                                       ws.qsplit, ws.wq, status);
