@@ -72,9 +72,25 @@ FM_DEV uint2 load_head_slice(const uint16_t* __restrict__ q, int h) {
 // elements 4l .. 4l+3.
 FM_DEV void split_query(const uint16_t* __restrict__ q, const float* __restrict__ w, int n_heads, int nthreads,
                         uint8_t* __restrict__ t1, uint8_t* __restrict__ t2, float* __restrict__ wq) {
-  const int warp = threadIdx.x >> 5;
-  for (int h = warp; h < n_heads; h += nthreads / 32)
-    split_head(load_head_slice(q, h), __ldg(w + h), t1 + (int64_t)h * 128, t2 + (int64_t)h * 128, wq + h);
+  const int warp = threadIdx.x >> 5, nw = nthreads / 32;
+  // four heads' loads in flight at a time: one memory round trip per four heads
+  for (int h0 = warp; h0 < n_heads; h0 += 4 * nw) {
+    uint2 raw[4];
+    float wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int h = h0 + u * nw;
+      if (h < n_heads) {
+        raw[u] = load_head_slice(q, h);
+        wv[u] = __ldg(w + h);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int h = h0 + u * nw;
+      if (h < n_heads) split_head(raw[u], wv[u], t1 + (int64_t)h * 128, t2 + (int64_t)h * 128, wq + h);
+    }
+  }
 }
 
 // Instruction descriptor, kind::f8f6f4 with E4M3 A/B, fp32 accumulate, K-major.

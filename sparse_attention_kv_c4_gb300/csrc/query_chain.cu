@@ -27,18 +27,22 @@
 //                         w_proj share the hidden state, so they are one launch
 //                         (w_proj's tile after wq_a's).  Each GEMM is split
 //                         along K so that tiles x splits fills the SMs once.
-//   rmsnorm_kernel        one CTA per token: sums the K-split partials of a in
-//                         a fixed order, RMSNorm in fp32, the normalised row
-//                         rounded to bf16 (wq_b's input type); also the head
-//                         weights w from w_proj's partials.
-//   rope_hadamard_kernel  one warp per (token, head), four entries per lane:
-//                         sums u's partials, forms and reduces the rotary
-//                         angles pos * theta'_i in fp64 (positions reach 2^20,
-//                         where an fp32 angle would lose whole radians), runs
-//                         the Walsh-Hadamard butterflies in registers (strides
-//                         1 and 2 inside a lane, 4..64 across lanes by
-//                         shuffles), and writes q as bf16 (and fp32 when
-//                         asked).
+//   rmsnorm_kernel        one CTA per (token, layer): sums the K-split
+//                         partials of a in a fixed order, RMSNorm in fp32,
+//                         the normalised row rounded to bf16 (wq_b's input
+//                         type); the head weights w from w_proj's partials;
+//                         and, once per token, the rotary (cos, sin) of its
+//                         32 pairs: the angle pos * theta'_i formed and
+//                         reduced modulo 2 pi in fp64 (positions reach 2^20
+//                         and beyond, where an fp32 angle would lose whole
+//                         radians), sine and cosine of the reduced angle in
+//                         fp32.
+//   rope_hadamard_kernel  one warp per (layer, token, head), four entries per
+//                         lane: sums u's partials, rotates the last 64 entries
+//                         with the token's (cos, sin), runs the Walsh-Hadamard
+//                         butterflies in registers (strides 1 and 2 inside a
+//                         lane, 4..64 across lanes by shuffles), and writes q
+//                         as bf16 (and fp32 when asked).
 // Partial sums are reduced in a fixed order, so results do not depend on
 // scheduling.
 #include <cuda_bf16.h>
@@ -404,13 +408,26 @@ constexpr int kNormSplitBatch = 8;
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const float* __restrict__ part, int splits, int64_t ld, int64_t T, int r, LayerPtrs gains,
                    float eps, uint16_t* __restrict__ c_out, int n_h, int64_t w_col0, float w_scale,
-                   float* __restrict__ w_out) {
+                   float* __restrict__ w_out, const int64_t* __restrict__ pos, RopeFreqs rf,
+                   float2* __restrict__ trig) {
   __shared__ float warp_ss[kNormThreads / 32];
   grid_dep_launch_dependents();
   grid_dep_wait();  // part is the previous kernel's output
   const int64_t t = blockIdx.x;
   const int layer = blockIdx.y, n_layers = gridDim.y;
   const int tid = threadIdx.x;
+  if (layer == 0 && tid < kRopeDim / 2) {
+    // the token's rotary (cos, sin) for the rotary kernel, once per token:
+    // the angle pos * theta'_i is formed and reduced modulo 2 pi in fp64 (it
+    // reaches 2^31 radians); sine and cosine of the reduced angle in fp32
+    const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
+    double a = (double)pos[t] * rf.f[tid];
+    a -= two_pi * floor(a * inv_two_pi);
+    float sn, cs;
+    sincosf((float)a, &sn, &cs);
+    trig[t * (kRopeDim / 2) + tid] = make_float2(cs, sn);
+  }
   const int64_t split_stride = T * ld;
   const float* row = part + (int64_t)layer * splits * split_stride + t * ld;
   const uint16_t* g = gains.p[layer];
@@ -488,9 +505,8 @@ RopeFreqs yarn_freqs(double base, double factor, double orig_len, double beta_fa
 // u = the splits of part summed in order; part is [layers][splits][T * n_h * 128]
 // (rows of one layer's split block: (token, head)).  q_out is [T, layers, n_h, 128].
 __global__ void __launch_bounds__(256)
-    rope_hadamard_kernel(const float* __restrict__ part, int splits, const int64_t* __restrict__ pos, int64_t T,
-                         int n_layers, int n_h, RopeFreqs rf, uint16_t* __restrict__ q_out,
-                         float* __restrict__ q_out_f32) {
+    rope_hadamard_kernel(const float* __restrict__ part, int splits, const float2* __restrict__ trig, int64_t T,
+                         int n_layers, int n_h, uint16_t* __restrict__ q_out, float* __restrict__ q_out_f32) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = T * n_h;                                         // per layer
   const int64_t grow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);    // (layer, token, head)
@@ -510,24 +526,16 @@ __global__ void __launch_bounds__(256)
     in.w += x.w;
   }
   float v[4] = {in.x, in.y, in.z, in.w};
-  // rotary on entries 64..127 (lanes 16..31): pairs (2i, 2i+1), i = 2 lane - 32 + {0, 1}
-  // The angle pos * theta'_i is formed and reduced modulo 2 pi in fp64 (it
-  // reaches 2^31 radians); sine and cosine of the reduced angle and the
-  // rotation itself run in fp32.
+  // rotary on entries 64..127 (lanes 16..31): pairs (2i, 2i+1), i = 2 lane - 32 + {0, 1},
+  // with the token's (cos, sin) from the RMSNorm kernel; the rotation in fp32
   if (lane >= 16) {
-    const double p = (double)pos[t];
-    const double two_pi = 6.283185307179586476925286766559;
-    const double inv_two_pi = 0.15915494309189533576888376337251;
+    const float4 cs = *reinterpret_cast<const float4*>(trig + t * (kRopeDim / 2) + 2 * lane - 32);
+    const float c[2] = {cs.x, cs.z}, sn[2] = {cs.y, cs.w};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int i = 2 * lane - 32 + k;
-      double a = p * rf.f[i];
-      a -= two_pi * floor(a * inv_two_pi);
-      float s, c;
-      sincosf((float)a, &s, &c);
       const float x0 = v[2 * k], x1 = v[2 * k + 1];
-      v[2 * k] = x0 * c - x1 * s;
-      v[2 * k + 1] = x0 * s + x1 * c;
+      v[2 * k] = x0 * c[k] - x1 * sn[k];
+      v[2 * k + 1] = x0 * sn[k] + x1 * c[k];
     }
   }
   // Walsh-Hadamard butterflies: strides 1, 2 inside the lane, 4..64 across lanes
@@ -563,7 +571,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Workspace: per layer, the K-split partials of [a | w] (tiles of wq_a then
 // w_proj), the bf16 RMSNorm output, the K-split partials of u.
 struct ChainWs {
-  size_t part1, c, part2, bytes;
+  size_t part1, c, part2, trig, bytes;
 };
 ChainWs chain_ws(int L, int T, int r, int n_h) {
   const int nt1 = (r + kGM - 1) / kGM + (n_h + kGM - 1) / kGM;  // per layer
@@ -572,7 +580,8 @@ ChainWs chain_ws(int L, int T, int r, int n_h) {
   w.part1 = 0;
   w.c = align256((size_t)L * gemm_splits_max(L * nt1) * T * nt1 * kGM * 4);
   w.part2 = w.c + align256((size_t)L * T * r * 2);
-  w.bytes = w.part2 + align256((size_t)L * gemm_splits_max(L * nt2) * T * nt2 * kGM * 4);
+  w.trig = w.part2 + align256((size_t)L * gemm_splits_max(L * nt2) * T * nt2 * kGM * 4);
+  w.bytes = w.trig + align256((size_t)T * (kRopeDim / 2) * 8);  // per token, (cos, sin) of the 32 rotary pairs
   return w;
 }
 
@@ -616,6 +625,7 @@ fm_status run_chain(int L, const uint16_t* const* hidden, const uint16_t* const*
   float* part1 = reinterpret_cast<float*>(base + lay.part1);
   uint16_t* c = reinterpret_cast<uint16_t*>(base + lay.c);
   float* part2 = reinterpret_cast<float*>(base + lay.part2);
+  float2* trig = reinterpret_cast<float2*>(base + lay.trig);
   // [a | w] = h . [wq_a | w_proj]^T, every layer in one launch
   const int nt_a = (r + kGM - 1) / kGM;
   const int64_t ld1 = (int64_t)(nt_a + (n_h + kGM - 1) / kGM) * kGM;
@@ -631,8 +641,10 @@ fm_status run_chain(int L, const uint16_t* const* hidden, const uint16_t* const*
   LayerPtrs gains = {};
   for (int l = 0; l < L; ++l) gains.p[l] = q_norm[l];
   const float w_scale = (float)(1.0 / sqrt((double)head_dim) / sqrt((double)n_h));
+  const RopeFreqs rf = yarn_freqs(rope_base, rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow);
   cudaError_t e = launch_pdl(rmsnorm_kernel, dim3((unsigned)T, (unsigned)L), kNormThreads, 0, s, (const float*)part1,
-                             splits1, ld1, (int64_t)T, r, gains, eps, c, n_h, (int64_t)nt_a * kGM, w_scale, w_out);
+                             splits1, ld1, (int64_t)T, r, gains, eps, c, n_h, (int64_t)nt_a * kGM, w_scale, w_out,
+                             pos, rf, trig);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "%s: rmsnorm launch: %s", who, cudaGetErrorString(e));
   // u = c . wq_b^T, every layer in one launch (layer l's rows of c start at l * T)
   const uint16_t* c_l[kGMaxLayers];
@@ -643,10 +655,9 @@ fm_status run_chain(int L, const uint16_t* const* hidden, const uint16_t* const*
   if ((st = proj_gemm(c_l, L, T, r, mats, L, (int64_t)n_h * kHeadDim, sms, part2, &splits2, status, true, true, s)) !=
       FM_OK)
     return st;
-  const RopeFreqs rf = yarn_freqs(rope_base, rope_factor, rope_orig_len, rope_beta_fast, rope_beta_slow);
   const int64_t rows = (int64_t)L * T * n_h;
-  e = launch_pdl(rope_hadamard_kernel, dim3((unsigned)((rows + 7) / 8)), 256, 0, s, (const float*)part2, splits2, pos,
-                 (int64_t)T, L, n_h, rf, q_out, q_out_f32);
+  e = launch_pdl(rope_hadamard_kernel, dim3((unsigned)((rows + 7) / 8)), 256, 0, s, (const float*)part2, splits2,
+                 (const float2*)trig, (int64_t)T, L, n_h, q_out, q_out_f32);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "%s: rope launch: %s", who, cudaGetErrorString(e));
   return FM_OK;
 }
