@@ -26,7 +26,7 @@
 namespace fm {
 namespace {
 
-constexpr int kRecallThreads = 256;
+constexpr int kRecallThreads = 1024;  // four 64-chunk pages per thread at 1M context
 constexpr int kPageChunks = 64;
 
 // Bits [lo, hi) of the 64-chunk window starting at chunk a, as a mask.
