@@ -103,6 +103,26 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def read_peak_gbs(torch, dev, gib: int = 4, reps: int = 10) -> float:
+    """A read-only streaming rate for the read-dominated kernels (the Memory
+    Indexer reads ~250 bytes for every byte it writes): torch's sum over a
+    `gib` GiB fp32 buffer, best of `reps`, CUDA events.  MEASURED_PEAKS.json's
+    hbm_gbs is a copy (read + write) and stays the roofline's denominator;
+    this is reported beside it."""
+    x = torch.ones((gib << 28,), dtype=torch.float32, device=dev)
+    best = None
+    for _ in range(reps + 2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        x.sum()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    del x
+    return (gib << 30) / (best / 1e3) / 1e9
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
 
@@ -549,6 +569,9 @@ def run_ours(args):
                         "queries_per_s": (f["queries"] / (m / 1e3)) if f["queries"] else None,
                         "bound": f["bound"], "achieved": round(ach, 2), "peak": peak, "unit": unit,
                         "frac": round(ach / peak, 4), "algorithmic_bytes": f["bytes"], "flops": f["flops"]}
+    read_gbs = read_peak_gbs(torch, dev)
+    for name in ("memindex", "page_recall"):
+        phases[name]["frac_of_read_peak"] = round(phases[name]["achieved"] / read_gbs, 4)
     dom = max(phases, key=lambda n: phases[n]["ms"])
     d = phases[dom]
     for name in phases:
@@ -625,8 +648,14 @@ def run_ours(args):
     variants = None
     if not args.no_variants:
         del sets, host_in, host_out
+        variants = {}
+        for name, cls, reps in (("tiny", TinyConfig, 50), ("memindex_256k", MemIndex256K, 10),
+                                ("paged_512k", Paged512K, 10)):
+            v = cls(torch, dev, fm)
+            variants[name] = v.measure(reps, 3, pk)
+            del v
         v = Fp8MemIndex(torch, dev, fm)
-        variants = {"memindex_fp8": v.measure(10, 3, pk)}
+        variants["memindex_fp8"] = v.measure(10, 3, pk)
         del v
         v = FullHistoryPaged(torch, dev, fm)
         variants["paged_full_history"] = v.measure(10, 3, pk)
@@ -640,6 +669,9 @@ def run_ours(args):
         del v
         for hot in (0.05, 0.25):  # the 1M workload's other hot fractions (the step runs 12%)
             variants[f"memindex_hot{int(round(hot * 100))}"] = memindex_hot_variant(torch, dev, fm, W, mi, hot, pk)
+        for name in ("memindex_256k", "memindex_fp8", "retriever_max", "retriever_mean", "memindex_hot5",
+                     "memindex_hot25"):
+            variants[name]["frac_of_read_peak"] = round(variants[name]["achieved"] / read_gbs, 4)
         if fm.fm_device_status(reset=True) != 0:
             raise RuntimeError("device status flagged an error in the variant rows")
 
@@ -662,10 +694,138 @@ def run_ours(args):
                         "ms_per_step": e2e_ms},
                 "gpu_launches": KERNELS_PER_STEP * K,
                 "roofline": roofline, "phases": phases, "variants": variants, "clocks": clk, "cpu_baseline": cpu,
+                "read_peak": {"value": round(read_gbs, 1), "unit": "GB/s",
+                              "how": "torch sum over 4 GiB fp32, best of 10 (read-only); the HBM fractions above "
+                                     "use the measured copy peak, frac_of_read_peak this one"},
                 "device_status": status, "sanity": chk}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def time_call(torch, call, reps, warmup):
+    """Mean device time of one call (ms): CUDA events around each of `reps`
+    calls on the current stream, after `warmup` untimed calls."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+class TinyConfig:
+    """The tiny workload (1 query, 1 indexer layer, S = 4096 chunks, 12%
+    planted): the Memory Indexer's mask and logits, then the top-512 over all
+    4096 chunks (fm_topk_select on the logits).  1 MB of keys: launch-bound,
+    and L2-resident after the first call, so its fraction of the HBM roofline
+    is not a bandwidth claim."""
+
+    def __init__(self, torch, dev, fm):
+        import gen
+        self.torch, self.fm, self.cfg = torch, fm, gen.TINY
+        c = self.cfg
+        q, w, hot = gen.memindex_qw(c)
+        K = gen.memindex_keys_host(c, hot)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.q, self.w, self.K = t(q.view(np.int16)), t(w), t(K.view(np.int16))
+        self.mask = torch.empty((1, c.S // 32), dtype=torch.int32, device=dev)
+        self.logits = torch.empty((1, 1, c.S), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((1, 512), dtype=torch.int32, device=dev)
+        self.sc = torch.empty((1, 512), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        self.fm.fm_memindex_score_mask(self.q, self.w, self.K, self.mask, None, self.logits)
+        self.fm.fm_topk_select(self.logits[0], 512, self.idx, self.sc)
+
+    def measure(self, reps, warmup, pk):
+        c = self.cfg
+        ms = time_call(self.torch, self.call, reps, warmup)
+        nbytes = c.S * c.d * 2 + c.S * 4 * 2 + (c.S // 32) * 4 + 512 * 8
+        ach = nbytes / (ms / 1e3) / 1e9
+        return {"ms": round(ms, 5), "chunk_scores_per_s": c.S / (ms / 1e3), "queries_per_s": 1 / (ms / 1e3),
+                "bound": "launch", "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 5), "algorithmic_bytes": nbytes, "launches": 2, "reps": reps,
+                "workload": "tiny: 1 query x 1 layer x 4096 chunks bf16 (12% planted): mask + logits, then top-512"}
+
+
+class MemIndex256K:
+    """The Memory Indexer at 256K-token context: 76 requests x 3 layers x
+    65536 chunks, bf16 keys, 12% planted (3.8 GB per call, far above L2),
+    OR-union mask and max-sigmoid."""
+
+    def __init__(self, torch, dev, fm):
+        import gen
+        self.torch, self.fm, self.cfg = torch, fm, gen.MEMINDEX_256K
+        c = self.cfg
+        q, w, hot = gen.memindex_qw(c)
+        self.q = torch.from_numpy(q.view(np.int16)).to(dev)
+        self.w = torch.from_numpy(w).to(dev)
+        hot_d = torch.from_numpy(hot).to(dev)
+        self.K = torch.empty((c.B, c.L, c.S, c.d), dtype=torch.int16, device=dev)
+        gen.memindex_keys_device(c, hot_d.data_ptr(), self.K.data_ptr(), c.L * c.S * c.d, c.S * c.d)
+        self.mask = torch.empty((c.B, (c.S + 31) // 32), dtype=torch.int32, device=dev)
+        self.maxsig = torch.empty((c.B, c.S), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        self.fm.fm_memindex_score_mask(self.q, self.w, self.K, self.mask, self.maxsig)
+
+    def measure(self, reps, warmup, pk):
+        c = self.cfg
+        ms = time_call(self.torch, self.call, reps, warmup)
+        nbytes = c.B * c.L * c.S * c.d * 2 + c.B * c.S * 4 + c.B * ((c.S + 31) // 32) * 4
+        ach = nbytes / (ms / 1e3) / 1e9
+        return {"ms": round(ms, 4), "chunk_scores_per_s": c.chunk_scores / (ms / 1e3), "bound": "hbm",
+                "achieved": round(ach, 2), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": nbytes, "launches": 1, "reps": reps,
+                "resident_fraction": round(resident_fraction(self.torch, self.mask, c.B, c.S), 4),
+                "workload": f"memindex 256K: {c.B}x{c.L}x{c.S} bf16 (12% planted), mask + max-sigmoid"}
+
+
+class Paged512K:
+    """The native paged top-512 at 512K-token context: 60 requests x 21 CSA
+    layers = 1260 queries, 192 resident E4M3 pages each (2.0 GB of keys and
+    scales per call)."""
+
+    def __init__(self, torch, dev, fm):
+        import gen
+        self.torch, self.fm, self.cfg = torch, fm, gen.PAGED_512K
+        c = self.cfg
+        logical, phys, owner = gen.paged_tables(c)
+        q, w = gen.paged_qw(c)
+        self.q = torch.from_numpy(q.view(np.int16)).to(dev)
+        self.w = torch.from_numpy(w).to(dev)
+        own_d = torch.from_numpy(owner).to(dev)
+        self.k8 = torch.empty((c.P, c.page, c.d), dtype=torch.uint8, device=dev)
+        self.sc = torch.empty((c.P, c.page), dtype=torch.float32, device=dev)
+        gen.paged_pool_device(c, own_d.data_ptr(), self.k8.data_ptr(), self.sc.data_ptr())
+        del own_d
+        self.phys = torch.from_numpy(phys).to(dev)
+        self.logical = torch.from_numpy(logical).to(dev)
+        self.idx = torch.empty((c.Q, c.k), dtype=torch.int32, device=dev)
+        self.score = torch.empty((c.Q, c.k), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(fm.fm_native_topk_paged_workspace(c.Q, c.R), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        self.fm.fm_native_topk_paged(self.q, self.w, self.k8, self.sc, self.phys, self.logical, self.cfg.k,
+                                     self.idx, self.score, workspace=self.ws)
+
+    def measure(self, reps, warmup, pk):
+        c = self.cfg
+        ms = time_call(self.torch, self.call, reps, warmup)
+        nbytes = c.P * c.page * (c.d + 4) + c.Q * c.R * 8 + c.Q * c.k * 8
+        ach = nbytes / (ms / 1e3) / 1e9
+        return {"ms": round(ms, 4), "chunk_scores_per_s": c.chunk_scores / (ms / 1e3),
+                "queries_per_s": c.Q / (ms / 1e3), "bound": "hbm", "achieved": round(ach, 2), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "algorithmic_bytes": nbytes, "launches": 3,
+                "reps": reps, "workload": f"paged top-{c.k} 512K: {c.Q} queries x {c.R} pages, E4M3 + fp32 scale"}
 
 
 class Fp8MemIndex:

@@ -418,6 +418,28 @@ def paged_pool_host(cfg: PagedCfg, owner: np.ndarray):
     return k8, scale
 
 
+def paged_pool_rows(cfg: PagedCfg, logical: np.ndarray, phys: np.ndarray, queries=None, n_pool=None):
+    """The pool pages that the listed queries' tables name, filled with the
+    values of paged_pool_host: one host call per query (all its pages at once).
+
+    queries: query ids (default all); phys: pool page per table entry (the
+    caller may pass a remapped, local numbering).  Returns k8 [n_pool, page, d]
+    and scale [n_pool, page]; pages no listed query names stay zero.
+    """
+    queries = range(cfg.Q) if queries is None else queries
+    n_pool = cfg.P if n_pool is None else n_pool
+    k8 = np.zeros((n_pool, cfg.page, cfg.d), dtype=np.uint8)
+    scale = np.zeros((n_pool, cfg.page), dtype=np.float32)
+    off = np.arange(cfg.page, dtype=np.int64)
+    for qi in queries:
+        a, b = int(qi) // cfg.layers, int(qi) % cfg.layers
+        s = (logical[qi].astype(np.int64)[:, None] * cfg.page + off[None, :]).reshape(-1)
+        rows, sc = paged_chunk_rows(cfg, a, b, s)
+        k8[phys[qi]] = rows.reshape(-1, cfg.page, cfg.d)
+        scale[phys[qi]] = sc.reshape(-1, cfg.page)
+    return k8, scale
+
+
 def paged_chunk_rows(cfg: PagedCfg, a: int, b: int, s_list):
     """E4M3 codes [n,d] and scales [n] of chunks s_list of stream (request a, layer b)."""
     s = np.ascontiguousarray(np.asarray(s_list, dtype=np.int64))
@@ -460,5 +482,5 @@ __all__ = [
     "BASE_SEED", "MemIndexCfg", "PagedCfg", "PrefillCfg", "TINY", "MEMINDEX_256K", "MEMINDEX_1M",
     "PAGED_512K", "PAGED_1M", "PAGED_FULL_1M", "RETRIEVER_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
     "memindex_keys_device", "planted", "pack_compressed_k", "query_chain_inputs", "paged_tables", "paged_qw", "paged_pool_host",
-    "paged_chunk_rows", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
+    "paged_chunk_rows", "paged_pool_rows", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
 ]

@@ -43,7 +43,8 @@
  *   - Kernels never trap and never spin without a bound.  A device-detected
  *     problem (an out-of-range page id, a bounded wait that ran out) sets a
  *     bit in the library's device status word and the affected work is
- *     skipped; read it with fm_device_status().
+ *     skipped; read it with fm_device_status() or, as a status code,
+ *     fm_check_device_status().
  *   - Thread-safety: calls may be issued from several host threads; the last
  *     error message is thread-local.
  */
@@ -61,10 +62,15 @@ typedef struct CUstream_st* fm_stream_t; /* == cudaStream_t */
 
 typedef enum {
   FM_OK = 0,
-  FM_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, unsupported n_h/d/k   */
-  FM_ERR_UNSUPPORTED = 2, /* current device is not an sm_103 GPU                       */
-  FM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (see fm_last_error)     */
-  FM_ERR_WORKSPACE = 4    /* workspace pointer null/misaligned or smaller than needed  */
+  FM_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, unsupported n_h/d/k    */
+  FM_ERR_UNSUPPORTED = 2,    /* current device is not an sm_103 GPU                        */
+  FM_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed (see fm_last_error)      */
+  FM_ERR_DEVICE_BOUNDS = 4,  /* a kernel met an out-of-range or repeated page id and      */
+                             /* skipped it (fm_check_device_status; FM_DEVERR_PAGE_RANGE,  */
+                             /* FM_DEVERR_DUP_PAGE)                                        */
+  FM_ERR_WORKSPACE = 5,      /* workspace pointer null/misaligned or smaller than needed   */
+  FM_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded on-chip wait ran out and the launch     */
+                             /* gave up (fm_check_device_status; FM_DEVERR_TIMEOUT)        */
 } fm_status;
 
 /* Bits of the device status word (fm_device_status). */
@@ -355,8 +361,10 @@ fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const uint8
  * device image: every GPU that loads the library holds it until the process
  * exits.  Sizes whose workspace (fm_native_topk_paged_workspace(Q, R)) exceeds
  * it are rejected with FM_ERR_INVALID_ARG before anything is enqueued (e.g.
- * R = 384 allows about 140 queries per call).  The first call on a device
- * resolves the array's device address with that device current; make that
+ * R = 384 allows 136 queries per call).  Every call looks up the
+ * array's device address (cudaGetSymbolAddress) with the calling thread's
+ * current device, so the address stays right after a device reset; the first
+ * call on a device also loads the library's device image there, so make that
  * first call before any stream capture.  All calls share the array and it
  * keeps the last call's contents (nothing in it needs to start at zero), so
  * calls that overlap on the GPU -- different streams or host threads -- race
@@ -406,6 +414,17 @@ fm_status fm_index_prefill_topk(const uint16_t* q, const float* w, const int64_t
  * reset != 0 the word is cleared after reading.  status_out is HOST memory.
  */
 fm_status fm_device_status(uint32_t* status_out, int reset, fm_stream_t stream);
+
+/*
+ * The device status word as a status code: synchronises `stream`, reads the
+ * word, clears it, and returns FM_OK when no bit was set,
+ * FM_ERR_DEVICE_TIMEOUT when FM_DEVERR_TIMEOUT was set (a launch gave up: its
+ * outputs are incomplete), otherwise FM_ERR_DEVICE_BOUNDS (page ids were
+ * skipped; the outputs are those of the table without them).  fm_last_error
+ * names the bits.  Kernels on other streams may set bits at any time: call it
+ * where the caller's own work is known to be complete.
+ */
+fm_status fm_check_device_status(fm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -14,7 +14,7 @@ import ctypes
 import os
 
 __all__ = [
-    "FmError", "lib", "fm_version", "fm_last_error", "fm_device_status", "fm_memindex_score_mask",
+    "FmError", "lib", "fm_version", "fm_last_error", "fm_device_status", "fm_check_device_status", "fm_memindex_score_mask",
     "fm_topk_workspace", "fm_topk_select", "fm_native_topk_paged_workspace", "fm_native_topk_paged",
     "fm_index_prefill_workspace", "fm_index_prefill_topk", "fm_native_topk_paged_noalloc", "fm_page_recall",
     "fm_native_topk_paged_ex", "fm_memindex_fp8_workspace", "fm_memindex_score_mask_fp8",
@@ -25,8 +25,10 @@ __all__ = [
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfm_index.so")
 
-FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_CUDA, FM_ERR_WORKSPACE = 0, 1, 2, 3, 4
+FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_CUDA = 0, 1, 2, 3
+FM_ERR_DEVICE_BOUNDS, FM_ERR_WORKSPACE, FM_ERR_DEVICE_TIMEOUT = 4, 5, 6
 FM_DEVERR_PAGE_RANGE, FM_DEVERR_TIMEOUT, FM_DEVERR_DUP_PAGE = 0x1, 0x2, 0x4
+FM_NOALLOC_SCRATCH_BYTES = 16 << 20  # the no-allocation paged top-k's built-in scratch (fm_index.h)
 
 _VP, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 
@@ -50,6 +52,8 @@ def lib() -> ctypes.CDLL:
         L.fm_version.restype = ctypes.c_int
         L.fm_last_error.restype = ctypes.c_char_p
         L.fm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), _I32, _VP]
+        L.fm_check_device_status.argtypes = [_VP]
+        L.fm_check_device_status.restype = ctypes.c_int
         L.fm_memindex_score_mask.argtypes = [_VP, _VP, _VP, _I64, _I64, _I32, _I32, _I64, _I32, _I32, _F, _VP,
                                              _VP, _VP, _VP]
         for name in ("fm_topk_workspace",):
@@ -139,6 +143,12 @@ def fm_device_status(reset: bool = True, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().fm_device_status(ctypes.byref(v), int(reset), _stream(stream)))
     return v.value
+
+
+def fm_check_device_status(stream=None) -> None:
+    """Raise FmError (FM_ERR_DEVICE_BOUNDS or FM_ERR_DEVICE_TIMEOUT) when a
+    kernel flagged the device status word since its last reset; clears it."""
+    _check(lib().fm_check_device_status(_stream(stream)))
 
 
 def fm_memindex_score_mask(q, w, keys, mask_out, maxsig_out=None, logits_out=None, threshold: float = 0.5,

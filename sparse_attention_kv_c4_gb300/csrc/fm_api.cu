@@ -75,7 +75,7 @@ fm_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const
 
 using namespace fm;
 
-FM_API int fm_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+FM_API int fm_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 FM_API const char* fm_last_error(void) { return t_last_error; }
 
@@ -93,6 +93,19 @@ FM_API fm_status fm_device_status(uint32_t* status_out, int reset, fm_stream_t s
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "fm_device_status: %s", cudaGetErrorString(e));
   *status_out = v;
   return FM_OK;
+}
+
+FM_API fm_status fm_check_device_status(fm_stream_t stream) {
+  uint32_t v = 0;
+  const fm_status st = fm_device_status(&v, 1, stream);
+  if (st != FM_OK) return st;
+  if (v == 0) return FM_OK;
+  const bool timeout = (v & FM_DEVERR_TIMEOUT) != 0;
+  set_error(timeout ? FM_ERR_DEVICE_TIMEOUT : FM_ERR_DEVICE_BOUNDS,
+            "device status 0x%x:%s%s%s", v, (v & FM_DEVERR_TIMEOUT) ? " a bounded wait ran out;" : "",
+            (v & FM_DEVERR_PAGE_RANGE) ? " a page id was out of range;" : "",
+            (v & FM_DEVERR_DUP_PAGE) ? " a logical page was repeated in a page table;" : "");
+  return timeout ? FM_ERR_DEVICE_TIMEOUT : FM_ERR_DEVICE_BOUNDS;
 }
 
 FM_API fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const uint16_t* keys,

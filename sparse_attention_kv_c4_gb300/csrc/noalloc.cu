@@ -12,16 +12,15 @@
 // Properties of that scratch (also stated in include/fm_index.h):
 //  - it is FM_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU that loads the
 //    library, held until the process exits;
-//  - its device address is resolved once per device, on the first call made
-//    with that device current (so make that first call before any stream
-//    capture);
+//  - every call resolves its device address with the calling thread's
+//    current device (cudaGetSymbolAddress); the first call on a device also
+//    loads the library's device image there, so make that first call before
+//    any stream capture;
 //  - every call shares it and it keeps the last call's contents: nothing in
 //    it has to start at zero (each launch writes every byte it later reads),
 //    but calls that overlap on the GPU -- on different streams, or from
 //    different host threads -- race on it and must be serialised by the
 //    caller.
-#include <mutex>
-
 #include "fm_common.cuh"
 #include "fm_internal.h"
 
@@ -33,26 +32,17 @@ constexpr size_t kScratchBytes = FM_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device (resolved once).
+// Device address of g_noalloc_scratch on the current device.  It is looked up
+// on every call rather than cached: after a cudaDeviceReset, or when the
+// primary context is destroyed and created again, the library's device image
+// is loaded anew and the array may sit at another address, so a cached
+// pointer could send the kernels' scratch writes to unmapped memory.
 fm_status scratch_for_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fm::set_error(FM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fm::set_error(FM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr)
-      return fm::set_error(FM_ERR_CUDA, "cudaGetSymbolAddress(scratch) on device %d: %s", dev,
-                           cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr)
+    return fm::set_error(FM_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  *out = p;
   return FM_OK;
 }
 

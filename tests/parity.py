@@ -70,3 +70,47 @@ def assert_topk_parity(got_idx, ref_idx, score_of, k, fp8=False, got_scores=None
         assert_logits_close(gs, ref, fp8, "top-k scores")
         assert np.all(np.isneginf(np.asarray(got_scores[n_got:], dtype=np.float64)))
     return exempt
+
+
+def assert_topk_rows_parity(got_idx, got_scores, ref_idx, cand_ids, cand_x, fp8=False):
+    """Whole rows at once.  got_idx / ref_idx [Q, k] int32 (ascending, -1
+    padded); got_scores [Q, k] fp32 or None; cand_ids [Q, n] int64 candidate
+    ids of each row (-1 = no candidate) and cand_x [Q, n] their oracle fp64
+    scores.  Every selected id must be a candidate, the id sets may differ
+    only inside the tolerance band around the oracle's k-th score, and every
+    returned score must match the oracle's score of its id.  Returns the
+    number of ids exempted by the band."""
+    got_idx = np.asarray(got_idx)
+    ref_idx = np.asarray(ref_idx)
+    exempt = 0
+    for r in range(got_idx.shape[0]):
+        n_ref = int((ref_idx[r] >= 0).sum())
+        n_got = int((got_idx[r] >= 0).sum())
+        assert n_got == n_ref, f"row {r}: selected {n_got} ids, oracle {n_ref}"
+        sel = got_idx[r, :n_got].astype(np.int64)
+        assert (got_idx[r, n_got:] == -1).all(), f"row {r}: padding must be -1"
+        assert n_got == 0 or (np.diff(sel) > 0).all(), f"row {r}: ids not strictly ascending"
+        ids = np.asarray(cand_ids[r], dtype=np.int64)
+        xs = np.asarray(cand_x[r], dtype=np.float64)
+        keep = ids >= 0
+        ids, xs = ids[keep], xs[keep]
+        order = np.argsort(ids, kind="stable")
+        ids, xs = ids[order], xs[order]
+        pos = np.searchsorted(ids, sel)
+        assert n_got == 0 or ((pos < len(ids)) & (ids[np.minimum(pos, len(ids) - 1)] == sel)).all(), \
+            f"row {r}: a selected id is not a candidate"
+        x_sel = xs[pos] if n_got else np.empty(0)
+        ref_sel = ref_idx[r, :n_ref].astype(np.int64)
+        diff = np.setxor1d(sel, ref_sel)
+        if diff.size:
+            kth = xs[np.searchsorted(ids, ref_sel)].min()
+            x_diff = xs[np.searchsorted(ids, diff)]
+            bad = ~(np.abs(x_diff - kth) <= tol(kth, fp8))
+            assert not bad.any(), (f"row {r}: ids {diff[bad][:4]} (scores {x_diff[bad][:4]}) differ from the "
+                                   f"oracle's set outside the band around its k-th score {kth}")
+            exempt += int(diff.size)
+        if got_scores is not None:
+            gs = np.asarray(got_scores[r], dtype=np.float64)
+            assert_logits_close(gs[:n_got], x_sel, fp8, f"row {r} top-k scores")
+            assert np.isneginf(gs[n_got:]).all(), f"row {r}: score padding must be -inf"
+    return exempt

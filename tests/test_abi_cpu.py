@@ -118,7 +118,7 @@ def test_query_chain_layers_rejects_bad_args_on_host(lib):
     assert call(2, arrs=null_layer) == 1 and "layer 1" in fm.fm_last_error()
     misaligned = (ctypes.c_void_p * 4)(fake, fake + 8, fake, fake)
     assert call(2, arrs=misaligned) == 1
-    assert call(2) == 4                                          # no workspace: FM_ERR_WORKSPACE
+    assert call(2) == 5                                          # no workspace: FM_ERR_WORKSPACE
     assert call(2, T=0) == 0                                     # nothing to do
     assert fm.fm_query_chain_layers_workspace(3, 30, 2048, 128) > fm.fm_query_chain_workspace(30, 2048, 128)
     assert fm.fm_query_chain_layers_workspace(1, 30, 2048, 128) == fm.fm_query_chain_workspace(30, 2048, 128)
@@ -177,3 +177,22 @@ def test_retriever_workspace_and_host_checks(lib):
     assert call(L=5) == INVALID
     assert call(ens=2) == INVALID
     assert call(thr=0.0) == INVALID
+
+
+def test_python_constants_match_header():
+    """The binding's status codes, device-status bits and the no-allocation
+    scratch size are the header's."""
+    import sparse_attention_kv_c4_gb300 as fm
+    src = open(HEADER).read()
+    enum = dict((k, int(v)) for k, v in re.findall(r"\b(FM_(?:OK|ERR_[A-Z_]+))\s*=\s*(\d+)", src))
+    assert enum, "no status codes found"
+    for k, v in enum.items():
+        assert getattr(fm, k) == v, k
+    for k, v in re.findall(r"#define (FM_DEVERR_[A-Z_]+) (0x[0-9a-f]+)u", src):
+        assert getattr(fm, k) == int(v, 16), k
+    m = re.search(r"#define FM_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", src)
+    assert m and fm.FM_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_check_device_status_is_exported(lib):
+    assert hasattr(lib, "fm_check_device_status")

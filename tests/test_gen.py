@@ -97,3 +97,19 @@ def test_pool_host_rows_consistent():
     k8r, scr = gen.paged_chunk_rows(cfg, a, b, np.arange(lp * 8, lp * 8 + 8))
     assert (k8r == k8[5]).all() and (scr == scale[5]).all()
     assert ((k8 & 0x7F) != 0x7F).all()
+
+
+def test_pool_rows_match_pool_host():
+    """The batched pool builder gives paged_pool_host's pages, also when the
+    tables are renumbered to a local pool."""
+    cfg = gen.PagedCfg("t", requests=2, layers=3, n_pages=30, R=4, seed=8)
+    logical, phys, owner = gen.paged_tables(cfg)
+    k8, scale = gen.paged_pool_host(cfg, owner)
+    k8b, scb = gen.paged_pool_rows(cfg, logical, phys)
+    assert (k8b == k8).all() and (scb.view(np.uint32) == scale.view(np.uint32)).all()
+    qs = [3, 4]
+    local = np.arange(len(qs) * cfg.R, dtype=np.int32).reshape(len(qs), cfg.R)
+    table = np.zeros_like(phys)
+    table[qs] = local
+    k8l, scl = gen.paged_pool_rows(cfg, logical, table, queries=qs, n_pool=len(qs) * cfg.R)
+    assert (k8l == k8[phys[qs].reshape(-1)]).all() and (scl == scale[phys[qs].reshape(-1)]).all()

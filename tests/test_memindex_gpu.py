@@ -153,12 +153,10 @@ def _sampled_full_size(torch, dev, orc, cfg, n_samples, want_maxsig):
     assert cfg.hot_frac * 0.8 < frac < cfg.hot_frac + 0.9, frac
 
 
-def test_memindex_256k_full_size_sampled(torch_dev, orc):
-    torch, dev = torch_dev
-    _sampled_full_size(torch, dev, orc, gen.MEMINDEX_256K, 400, want_maxsig=False)
-
-
-@pytest.mark.parametrize("frac", [0.05, 0.12, 0.25])
+# The 256K workload and the 1M workload at 12% planted are compared in full
+# in test_full_configs_gpu.py; the 1M workload's other planted fractions are
+# sampled here.
+@pytest.mark.parametrize("frac", [0.05, 0.25])
 def test_memindex_1m_full_size_sampled(torch_dev, orc, frac):
     torch, dev = torch_dev
     cfg = gen.replace(gen.MEMINDEX_1M, hot_frac=frac)

@@ -121,6 +121,18 @@ def test_paged_bad_pages_are_flagged_and_skipped(torch_dev, orc):
     assert len(row0) == 5 * 64 and not any(i // 64 == logical[0, 2] for i in row0)
     row1 = [int(i) for i in idx[1] if i >= 0]
     assert len(row1) == 5 * 64 and len(set(row1)) == len(row1)
+    # the surviving rows equal the oracle's on the tables with the flagged
+    # entries removed: the out-of-range entry of row 0, and the later of the
+    # two entries of row 1 that repeat a logical page (the first one listed is
+    # kept); removed entries go last and n_res leaves them out
+    keep = {0: [0, 1, 3, 4, 5], 1: [0, 1, 2, 3, 5]}
+    n_res = np.full(cfg.Q, 6, dtype=np.int32)
+    for r, cols in keep.items():
+        order = cols + [c for c in range(6) if c not in cols]
+        phys[r], logical[r] = phys[r, order], logical[r, order]
+        n_res[r] = len(cols)
+    phys[0, 5] = 0  # the removed entry is past n_res; any in-range value
+    check_rows(orc, q, w, k8, scale, phys, logical, idx, sc, 512, n_res=n_res)
 
 
 def test_paged_scale_signs(torch_dev, orc):
@@ -135,31 +147,7 @@ def test_paged_scale_signs(torch_dev, orc):
     check_rows(orc, q, w, k8, scale, phys, logical, idx, sc, 200)
 
 
-@pytest.mark.parametrize("cfg", [gen.PAGED_512K, gen.PAGED_1M], ids=lambda c: c.name)
-def test_paged_full_size_sampled(torch_dev, orc, cfg):
-    """Full-size pool filled on the device; sampled queries recomputed by the
-    oracle from host-regenerated keys of their resident pages."""
-    torch, dev = torch_dev
-    logical, phys, owner = gen.paged_tables(cfg)
-    q, w = gen.paged_qw(cfg)
-    own_d = torch.from_numpy(owner).to(dev)
-    k8d = torch.empty((cfg.P, cfg.page, cfg.d), dtype=torch.uint8, device=dev)
-    scd = torch.empty((cfg.P, cfg.page), dtype=torch.float32, device=dev)
-    gen.paged_pool_device(cfg, own_d.data_ptr(), k8d.data_ptr(), scd.data_ptr())
-    idx, sc, status = run_paged(torch, dev, q, w, None, None, phys, logical, cfg.k, pool_dev=(k8d, scd))
-    assert status == 0
-    del k8d, scd
-    rng = np.random.default_rng(cfg.seed)
-    for qi in rng.choice(cfg.Q, size=6, replace=False):
-        a, b = qi // cfg.layers, qi % cfg.layers
-        k8s = np.empty((cfg.R, cfg.page, cfg.d), np.uint8)
-        scs = np.empty((cfg.R, cfg.page), np.float32)
-        for j in range(cfg.R):
-            lp = int(logical[qi, j])
-            k8s[j], scs[j] = gen.paged_chunk_rows(cfg, a, b, np.arange(lp * 64, lp * 64 + 64))
-        sub_phys = np.arange(cfg.R, dtype=np.int32)[None, :]
-        check_rows(orc, q[qi:qi + 1], w[qi:qi + 1], k8s, scs, sub_phys, logical[qi:qi + 1], idx[qi:qi + 1],
-                   sc[qi:qi + 1], cfg.k)
+# The 512K and 1M paged workloads are compared in full in test_full_configs_gpu.py.
 
 
 def test_paged_full_history_whole_rows(torch_dev, orc):
@@ -200,3 +188,22 @@ def test_paged_full_history_1m_sampled(torch_dev, orc):
         # logical page j sits in local pool page j
         check_rows(orc, q[qi:qi + 1], w[qi:qi + 1], k8s, scs, logical[qi:qi + 1], logical[qi:qi + 1],
                    idx[qi:qi + 1], sc[qi:qi + 1], cfg.k)
+
+
+def test_check_device_status_reports_bounds(torch_dev, orc):
+    """fm_check_device_status turns the flagged status word into
+    FM_ERR_DEVICE_BOUNDS once, and clears it."""
+    import sparse_attention_kv_c4_gb300 as fm
+    torch, dev = torch_dev
+    cfg, q, w, k8, scale, phys, logical = small_case(19, R=4)
+    fm.fm_check_device_status()  # a clean word to start from
+    phys = phys.copy()
+    phys[2, 1] = -3
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    idx = torch.empty((cfg.Q, 64), dtype=torch.int32, device=dev)
+    ws = torch.empty(fm.fm_native_topk_paged_workspace(cfg.Q, cfg.R), dtype=torch.uint8, device=dev)
+    fm.fm_native_topk_paged(t(q.view(np.int16)), t(w), t(k8), t(scale), t(phys), t(logical), 64, idx, workspace=ws)
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_check_device_status()
+    assert e.value.status == fm.FM_ERR_DEVICE_BOUNDS and "out of range" in str(e.value)
+    fm.fm_check_device_status()  # cleared
