@@ -440,6 +440,23 @@ def paged_pool_rows(cfg: PagedCfg, logical: np.ndarray, phys: np.ndarray, querie
     return k8, scale
 
 
+def paged_pool_rows_bf16(cfg: PagedCfg, logical: np.ndarray, phys: np.ndarray, queries=None, n_pool=None):
+    """A pool of bf16 keys for the listed queries' tables (the same cold-key
+    recipe, N(0, 1/128), rounded to bf16 instead of quantised to E4M3):
+    kbf [n_pool, page, d] bf16 bits; pages no listed query names stay zero."""
+    queries = range(cfg.Q) if queries is None else queries
+    n_pool = cfg.P if n_pool is None else n_pool
+    kbf = np.zeros((n_pool, cfg.page, cfg.d), dtype=np.uint16)
+    off = np.arange(cfg.page, dtype=np.int64)
+    for qi in queries:
+        a, b = int(qi) // cfg.layers, int(qi) % cfg.layers
+        s = np.ascontiguousarray((logical[qi].astype(np.int64)[:, None] * cfg.page + off[None, :]).reshape(-1))
+        rows = np.empty((len(s), cfg.d), dtype=np.uint16)
+        host_lib().gen_k_bf16_rows(cfg.seed, a, b, _p(s, i64p), len(s), cfg.d, 0, None, _p(rows, u16p))
+        kbf[phys[qi]] = rows.reshape(-1, cfg.page, cfg.d)
+    return kbf
+
+
 def paged_chunk_rows(cfg: PagedCfg, a: int, b: int, s_list):
     """E4M3 codes [n,d] and scales [n] of chunks s_list of stream (request a, layer b)."""
     s = np.ascontiguousarray(np.asarray(s_list, dtype=np.int64))
@@ -482,5 +499,5 @@ __all__ = [
     "BASE_SEED", "MemIndexCfg", "PagedCfg", "PrefillCfg", "TINY", "MEMINDEX_256K", "MEMINDEX_1M",
     "PAGED_512K", "PAGED_1M", "PAGED_FULL_1M", "RETRIEVER_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
     "memindex_keys_device", "planted", "pack_compressed_k", "query_chain_inputs", "paged_tables", "paged_qw", "paged_pool_host",
-    "paged_chunk_rows", "paged_pool_rows", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
+    "paged_chunk_rows", "paged_pool_rows", "paged_pool_rows_bf16", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
 ]

@@ -73,6 +73,12 @@ typedef enum {
                              /* gave up (fm_check_device_status; FM_DEVERR_TIMEOUT)        */
 } fm_status;
 
+/* Key element types of a paged key pool (fm_native_topk_paged's key_dtype). */
+typedef enum {
+  FM_DTYPE_BF16 = 1,     /* bf16 keys, no scale                                        */
+  FM_DTYPE_FP8_E4M3 = 2  /* E4M3 codes with one fp32 dequant scale per chunk           */
+} fm_dtype;
+
 /* Bits of the device status word (fm_device_status). */
 #define FM_PAGED_MAX_R 4096       /* page-table entries per query of the paged calls     */
 #define FM_DEVERR_PAGE_RANGE 0x1u  /* page_phys outside [0, P): that page was skipped     */
@@ -286,19 +292,24 @@ fm_status fm_page_recall(const uint32_t* mask, int B, int64_t S, int64_t sink, i
  * "Page-recall" 64-chunk pages, "compressed_k format"; [V4] sec. 3 CSA-1/2).
  *
  * Query qi scores the chunks of its first n_res[qi] page-table entries:
- *     y = sum_h w[qi,h] * ReLU( scale[p,o] * sum_j q[qi,h,j] * e4m3(k_pool[p,o,j]) )
+ *     y = sum_h w[qi,h] * ReLU( scale[p,o] * sum_j q[qi,h,j] * e4m3(k_pool[p,o,j]) )   (E4M3 pool)
+ *     y = sum_h w[qi,h] * ReLU( sum_j q[qi,h,j] * k_pool[p,o,j] )                      (bf16 pool)
  * for pool page p = page_phys[qi,r] and offset o < 64; the chunk's id is
  * page_logical[qi,r] * 64 + o.  Chunks outside the listed pages are not
  * candidates (equivalent to Mode A's -inf).  The result does not depend on the
  * order of a query's page-table entries.
  *
- *   q            [Q, n_h, d] bf16;  w [Q, n_h] fp32 (fused weights)
- *   k_pool       [P, 64, d] E4M3 codes, 16-byte aligned
- *   k_scale      [P, 64] fp32 per-chunk dequant scale
+ *   q            [Q, n_h, d] bf16, 16-byte aligned;  w [Q, n_h] fp32 (fused weights)
+ *   k_pool       [P, 64, d], 16-byte aligned: E4M3 codes (key_dtype
+ *                FM_DTYPE_FP8_E4M3, the compressed_k keys) or bf16 keys
+ *                (FM_DTYPE_BF16)
+ *   key_dtype    FM_DTYPE_FP8_E4M3 or FM_DTYPE_BF16
+ *   k_scale      [P, 64] fp32 per-chunk dequant scale (E4M3); NULL for bf16
  *   page_phys    [Q, R] int32 pool page; entries outside [0, P) are skipped and
  *                flagged FM_DEVERR_PAGE_RANGE
  *   page_logical [Q, R] int32 logical page id in [0, 2^25); distinct within
- *                a query (a repeat is flagged FM_DEVERR_DUP_PAGE)
+ *                a query (a repeat is flagged FM_DEVERR_DUP_PAGE and skipped:
+ *                the entry listed first is kept)
  *   n_res        [Q] int32 entries used per query (clamped to [0, R]), or NULL = R
  *   1 <= R <= FM_PAGED_MAX_R (4096 pages = 262144 chunks: the whole history
  *   of a 1M-token request, so the call also serves the full-history native
@@ -307,10 +318,11 @@ fm_status fm_page_recall(const uint32_t* mask, int B, int64_t S, int64_t sink, i
  *   workspace    >= fm_native_topk_paged_workspace(Q, R) bytes, 256-byte aligned
  */
 size_t fm_native_topk_paged_workspace(int Q, int R);
-fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
-                               int64_t P, const int32_t* page_phys, const int32_t* page_logical,
-                               const int32_t* n_res, int Q, int R, int n_h, int d, int k, int32_t* idx_out,
-                               float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream);
+fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const void* k_pool, int key_dtype,
+                               const float* k_scale, int64_t P, const int32_t* page_phys,
+                               const int32_t* page_logical, const int32_t* n_res, int Q, int R, int n_h, int d,
+                               int k, int32_t* idx_out, float* score_out, void* workspace, size_t workspace_bytes,
+                               fm_stream_t stream);
 
 /*
  * fm_native_topk_paged with the Level-2 resident mask and the fused remap
@@ -338,8 +350,8 @@ fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t*
  * workspace size); FM_ERR_INVALID_ARG also for a bad id_mode / mask_ld /
  * mask_group.
  */
-fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
-                                  int64_t P, const int32_t* page_phys, const int32_t* page_logical,
+fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const void* k_pool, int key_dtype,
+                                  const float* k_scale, int64_t P, const int32_t* page_phys, const int32_t* page_logical,
                                   const int32_t* n_res, int Q, int R, int n_h, int d, int k,
                                   const uint32_t* res_mask, int64_t mask_ld, int mask_group, int id_mode,
                                   int32_t* idx_out, float* score_out, void* workspace, size_t workspace_bytes,
@@ -354,8 +366,9 @@ fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const uint8
  * or fragment that pool), a decode loop that must not stall on the implicit
  * device synchronisation cudaMalloc/cudaFree may perform, or a plugin host that
  * gives its kernels no allocator.  It computes exactly what
- * fm_native_topk_paged computes, with the same arguments minus the workspace,
- * and calls no allocating routine.
+ * fm_native_topk_paged computes for an E4M3 pool (key_dtype
+ * FM_DTYPE_FP8_E4M3), with the same arguments minus key_dtype and the
+ * workspace, and calls no allocating routine.
  *
  * Its scratch is a fixed FM_NOALLOC_SCRATCH_BYTES array inside the library's
  * device image: every GPU that loads the library holds it until the process

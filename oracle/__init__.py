@@ -85,6 +85,8 @@ class Oracle:
                                        I32, i32p, f64p, f64p]
         lib.orc_paged_topk_ex.argtypes = [u16p, f32p, u8p, f32p, i32p, i32p, i32p, I64, I64, I32, I32, I32, I32,
                                           u32p, I64, I32, I32, i32p, f64p, f64p]
+        lib.orc_paged_topk_bf16_ex.argtypes = [u16p, f32p, u16p, i32p, i32p, i32p, I64, I64, I32, I32, I32, I32,
+                                               u32p, I64, I32, I32, i32p, f64p, f64p]
         lib.orc_causal_limit.argtypes = [I64, I64, I32]
         lib.orc_causal_limit.restype = I64
         lib.orc_prefill_topk.argtypes = [u16p, f32p, i64p, u16p, I64, I64, I32, I32, I32, I32, i32p, f64p]
@@ -238,6 +240,25 @@ class Oracle:
         self.lib.orc_paged_topk_ex(_p(q, u16p), _p(w, f32p), _p(k8, u8p), _p(scale, f32p), _p(page_phys, i32p),
                                    _p(page_logical, i32p), _p(nr, i32p), Q, R, n_h, d, page, k, _p(m, u32p),
                                    mask_ld, mask_group, id_mode, _p(idx, i32p), _p(sc, f64p), _p(lg, f64p))
+        return (idx, sc, lg) if want_logits else (idx, sc)
+
+    def paged_topk_bf16(self, q, w, kbf, page_phys, page_logical, n_res=None, k: int = 512,
+                        want_logits: bool = False, res_mask=None, mask_group: int = 1, id_mode: int = 0):
+        """paged_topk over a pool of bf16 keys kbf [P, page, d] (bf16 bits, no scale)."""
+        q = _c(q, np.uint16); w = _c(w, np.float32); kbf = _c(kbf, np.uint16)
+        page_phys = _c(page_phys, np.int32); page_logical = _c(page_logical, np.int32)
+        Q, n_h, d = q.shape
+        R = page_phys.shape[1]
+        page = kbf.shape[1]
+        nr = _c(n_res, np.int32) if n_res is not None else None
+        idx = np.empty((Q, k), dtype=np.int32)
+        sc = np.empty((Q, k), dtype=np.float64)
+        lg = np.empty((Q, R * page), dtype=np.float64) if want_logits else None
+        m = _c(np.atleast_2d(res_mask), np.uint32) if res_mask is not None else None
+        mask_ld = m.shape[1] if m is not None else 0
+        self.lib.orc_paged_topk_bf16_ex(_p(q, u16p), _p(w, f32p), _p(kbf, u16p), _p(page_phys, i32p),
+                                        _p(page_logical, i32p), _p(nr, i32p), Q, R, n_h, d, page, k, _p(m, u32p),
+                                        mask_ld, mask_group, id_mode, _p(idx, i32p), _p(sc, f64p), _p(lg, f64p))
         return (idx, sc, lg) if want_logits else (idx, sc)
 
     def causal_limit(self, pos: int, S: int, ratio: int = 4) -> int:

@@ -284,11 +284,13 @@ ORC_API int orc_topk(const int64_t* ids, const double* x, int64_t n, int k, int3
  * the logical chunk ids.
  * logit_out (optional) is [Q][R*page_size] in page-table order: the score of
  * every listed chunk, NaN for slots past n_res. */
-ORC_API void orc_paged_topk_ex(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
-                               const int32_t* page_phys, const int32_t* page_logical, const int32_t* n_res,
-                               int64_t Q, int64_t R, int n_h, int d, int page_size, int k, const uint32_t* res_mask,
-                               int64_t mask_ld, int mask_group, int id_mode, int32_t* idx_out, double* score_out,
-                               double* logit_out) {
+/* The pool holds either E4M3 codes with a per-chunk scale (k8, scale) or bf16
+ * keys (kbf, no scale); exactly one of k8 / kbf is given. */
+static void orc_paged_topk_any(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
+                               const uint16_t* kbf, const int32_t* page_phys, const int32_t* page_logical,
+                               const int32_t* n_res, int64_t Q, int64_t R, int n_h, int d, int page_size, int k,
+                               const uint32_t* res_mask, int64_t mask_ld, int mask_group, int id_mode,
+                               int32_t* idx_out, double* score_out, double* logit_out) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t qi = 0; qi < Q; ++qi) {
     int64_t nr = n_res ? n_res[qi] : R;
@@ -302,8 +304,9 @@ ORC_API void orc_paged_topk_ex(const uint16_t* q, const float* w, const uint8_t*
       int64_t lp = page_logical[qi * R + j];
       for (int o = 0; o < page_size; ++o) {
         int64_t row = p * page_size + o;
-        double x = orc_score_fp8(q + (size_t)qi * n_h * d, w + (size_t)qi * n_h, k8 + (size_t)row * d,
-                                 scale[row], n_h, d);
+        double x = kbf ? orc_score_bf16(q + (size_t)qi * n_h * d, w + (size_t)qi * n_h, kbf + (size_t)row * d, n_h, d)
+                       : orc_score_fp8(q + (size_t)qi * n_h * d, w + (size_t)qi * n_h, k8 + (size_t)row * d,
+                                       scale[row], n_h, d);
         if (logit_out) logit_out[(size_t)qi * R * page_size + j * page_size + o] = x;
         int64_t chunk = lp * page_size + o;
         if (mrow) {
@@ -331,6 +334,27 @@ ORC_API void orc_paged_topk_ex(const uint16_t* q, const float* w, const uint8_t*
       }
     free(c);
   }
+}
+
+ORC_API void orc_paged_topk_ex(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,
+                               const int32_t* page_phys, const int32_t* page_logical, const int32_t* n_res,
+                               int64_t Q, int64_t R, int n_h, int d, int page_size, int k, const uint32_t* res_mask,
+                               int64_t mask_ld, int mask_group, int id_mode, int32_t* idx_out, double* score_out,
+                               double* logit_out) {
+  orc_paged_topk_any(q, w, k8, scale, NULL, page_phys, page_logical, n_res, Q, R, n_h, d, page_size, k, res_mask,
+                     mask_ld, mask_group, id_mode, idx_out, score_out, logit_out);
+}
+
+/* The same over a pool of bf16 keys kbf [P][page_size][d] (no scale): the
+ * native score with the keys as the Memory Indexer reads them ([V4] sec. 3
+ * CSA-1 over paged keys; bf16 is the pages' uncompressed key type). */
+ORC_API void orc_paged_topk_bf16_ex(const uint16_t* q, const float* w, const uint16_t* kbf,
+                                    const int32_t* page_phys, const int32_t* page_logical, const int32_t* n_res,
+                                    int64_t Q, int64_t R, int n_h, int d, int page_size, int k,
+                                    const uint32_t* res_mask, int64_t mask_ld, int mask_group, int id_mode,
+                                    int32_t* idx_out, double* score_out, double* logit_out) {
+  orc_paged_topk_any(q, w, NULL, NULL, kbf, page_phys, page_logical, n_res, Q, R, n_h, d, page_size, k, res_mask,
+                     mask_ld, mask_group, id_mode, idx_out, score_out, logit_out);
 }
 
 ORC_API void orc_paged_topk(const uint16_t* q, const float* w, const uint8_t* k8, const float* scale,

@@ -28,6 +28,7 @@ LIB_PATH = os.path.join(HERE, "libfm_index.so")
 FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_CUDA = 0, 1, 2, 3
 FM_ERR_DEVICE_BOUNDS, FM_ERR_WORKSPACE, FM_ERR_DEVICE_TIMEOUT = 4, 5, 6
 FM_DEVERR_PAGE_RANGE, FM_DEVERR_TIMEOUT, FM_DEVERR_DUP_PAGE = 0x1, 0x2, 0x4
+FM_DTYPE_BF16, FM_DTYPE_FP8_E4M3 = 1, 2  # key element types of a paged pool
 FM_NOALLOC_SCRATCH_BYTES = 16 << 20  # the no-allocation paged top-k's built-in scratch (fm_index.h)
 
 _VP, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -65,11 +66,11 @@ def lib() -> ctypes.CDLL:
         if hasattr(L, "fm_native_topk_paged_workspace"):
             L.fm_native_topk_paged_workspace.argtypes = [_I32, _I32]
             L.fm_native_topk_paged_workspace.restype = _SZ
-            L.fm_native_topk_paged.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
-                                               _I32, _VP, _VP, _VP, _SZ, _VP]
+            L.fm_native_topk_paged.argtypes = [_VP, _VP, _VP, _I32, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32,
+                                               _I32, _I32, _VP, _VP, _VP, _SZ, _VP]
         if hasattr(L, "fm_native_topk_paged_ex"):
-            L.fm_native_topk_paged_ex.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
-                                                  _I32, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _SZ, _VP]
+            L.fm_native_topk_paged_ex.argtypes = [_VP, _VP, _VP, _I32, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32,
+                                                  _I32, _I32, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _SZ, _VP]
         if hasattr(L, "fm_native_topk_paged_noalloc"):
             L.fm_native_topk_paged_noalloc.argtypes = [_VP, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _I32, _I32, _I32,
                                                        _I32, _I32, _VP, _VP, _VP]
@@ -277,16 +278,29 @@ def fm_native_topk_paged_workspace(Q: int, R: int) -> int:
     return lib().fm_native_topk_paged_workspace(Q, R)
 
 
+def _key_dtype(k_pool) -> int:
+    """The pool's key type from its tensor dtype: uint8 holds E4M3 codes;
+    int16 / bfloat16 hold bf16 keys."""
+    import torch
+    if k_pool.dtype == torch.uint8:
+        return FM_DTYPE_FP8_E4M3
+    if k_pool.dtype in (torch.int16, torch.bfloat16):
+        return FM_DTYPE_BF16
+    raise ValueError(f"k_pool dtype {k_pool.dtype}: uint8 (E4M3 codes) or int16/bfloat16 (bf16 keys)")
+
+
 def fm_native_topk_paged(q, w, k_pool, k_scale, page_phys, page_logical, k: int, idx_out, score_out=None,
                          n_res=None, workspace=None, stream=None) -> None:
-    """q [Q,64,128] bf16, w [Q,64] fp32, k_pool [P,64,128] uint8 E4M3 codes,
-    k_scale [P,64] fp32, page_phys/page_logical [Q,R] int32, n_res [Q] int32
-    or None, idx_out [Q,k] int32, score_out [Q,k] fp32 or None."""
+    """q [Q,64,128] bf16, w [Q,64] fp32, k_pool [P,64,128]: uint8 E4M3 codes
+    with k_scale [P,64] fp32, or int16/bfloat16 bf16 keys with k_scale None;
+    page_phys/page_logical [Q,R] int32, n_res [Q] int32 or None, idx_out
+    [Q,k] int32, score_out [Q,k] fp32 or None."""
     Q, n_h, d = q.shape
     R = page_phys.shape[1]
     P = k_pool.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().fm_native_topk_paged(_ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), P, _ptr(page_phys),
+    _check(lib().fm_native_topk_paged(_ptr(q), _ptr(w), _ptr(k_pool), _key_dtype(k_pool), _ptr(k_scale), P,
+                                      _ptr(page_phys),
                                       _ptr(page_logical), _ptr(n_res), Q, R, n_h, d, k, _ptr(idx_out),
                                       _ptr(score_out), _ptr(workspace), ws_bytes, _stream(stream)))
 
@@ -302,7 +316,8 @@ def fm_native_topk_paged_ex(q, w, k_pool, k_scale, page_phys, page_logical, k: i
     P = k_pool.shape[0]
     mask_ld = 0 if res_mask is None else res_mask.shape[1]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().fm_native_topk_paged_ex(_ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), P, _ptr(page_phys),
+    _check(lib().fm_native_topk_paged_ex(_ptr(q), _ptr(w), _ptr(k_pool), _key_dtype(k_pool), _ptr(k_scale), P,
+                                         _ptr(page_phys),
                                          _ptr(page_logical), _ptr(n_res), Q, R, n_h, d, k, _ptr(res_mask), mask_ld,
                                          mask_group, id_mode, _ptr(idx_out), _ptr(score_out), _ptr(workspace),
                                          ws_bytes, _stream(stream)))

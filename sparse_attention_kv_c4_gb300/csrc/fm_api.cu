@@ -186,7 +186,7 @@ FM_API size_t fm_native_topk_paged_workspace(int Q, int R) {
   return paged_workspace_bytes(Q, R);
 }
 
-FM_API fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const uint8_t* k_pool,
+FM_API fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, const void* k_pool, int key_dtype,
                                          const float* k_scale, int64_t P, const int32_t* page_phys,
                                          const int32_t* page_logical, const int32_t* n_res, int Q, int R, int n_h,
                                          int d, int k, const uint32_t* res_mask, int64_t mask_ld, int mask_group,
@@ -200,11 +200,17 @@ FM_API fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, cons
   if (id_mode != 0 && id_mode != 1)
     return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: id_mode=%d (0 = chunk ids, 1 = reserve cells)",
                      id_mode);
+  if (key_dtype != FM_DTYPE_FP8_E4M3 && key_dtype != FM_DTYPE_BF16)
+    return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: key_dtype=%d (FM_DTYPE_FP8_E4M3 or FM_DTYPE_BF16)",
+                     key_dtype);
+  if (key_dtype == FM_DTYPE_BF16 && k_scale != nullptr)
+    return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: a bf16 key pool takes no k_scale (pass NULL)");
   if (res_mask != nullptr && (mask_ld < 1 || mask_group < 1 || !aligned(res_mask, 4)))
     return set_error(FM_ERR_INVALID_ARG,
                      "fm_native_topk_paged: resident mask needs mask_ld >= 1, mask_group >= 1, 4-byte alignment");
   if (Q == 0) return FM_OK;
-  if (!q || !w || !page_phys || !page_logical || !idx_out || (P > 0 && (!k_pool || !k_scale)))
+  if (!q || !w || !page_phys || !page_logical || !idx_out ||
+      (P > 0 && (!k_pool || (key_dtype == FM_DTYPE_FP8_E4M3 && !k_scale))))
     return set_error(FM_ERR_INVALID_ARG, "fm_native_topk_paged: required pointer is NULL");
   if (!aligned(q, 16) || !aligned(w, 16) || (k_pool && !aligned(k_pool, 16)) || (k_scale && !aligned(k_scale, 16)) ||
       !aligned(page_phys, 4) || !aligned(page_logical, 4) || (n_res && !aligned(n_res, 4)) ||
@@ -223,6 +229,7 @@ FM_API fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, cons
   a.q = q;
   a.w = w;
   a.k_pool = k_pool;
+  a.key_dtype = key_dtype;
   a.k_scale = k_scale;
   a.P = P;
   a.page_phys = page_phys;
@@ -241,12 +248,13 @@ FM_API fm_status fm_native_topk_paged_ex(const uint16_t* q, const float* w, cons
   return launch_paged(a, sms, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
-FM_API fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const uint8_t* k_pool, const float* k_scale,
-                                      int64_t P, const int32_t* page_phys, const int32_t* page_logical,
-                                      const int32_t* n_res, int Q, int R, int n_h, int d, int k, int32_t* idx_out,
-                                      float* score_out, void* workspace, size_t workspace_bytes, fm_stream_t stream) {
-  return fm_native_topk_paged_ex(q, w, k_pool, k_scale, P, page_phys, page_logical, n_res, Q, R, n_h, d, k, nullptr,
-                                 0, 1, 0, idx_out, score_out, workspace, workspace_bytes, stream);
+FM_API fm_status fm_native_topk_paged(const uint16_t* q, const float* w, const void* k_pool, int key_dtype,
+                                      const float* k_scale, int64_t P, const int32_t* page_phys,
+                                      const int32_t* page_logical, const int32_t* n_res, int Q, int R, int n_h, int d,
+                                      int k, int32_t* idx_out, float* score_out, void* workspace,
+                                      size_t workspace_bytes, fm_stream_t stream) {
+  return fm_native_topk_paged_ex(q, w, k_pool, key_dtype, k_scale, P, page_phys, page_logical, n_res, Q, R, n_h, d, k,
+                                 nullptr, 0, 1, 0, idx_out, score_out, workspace, workspace_bytes, stream);
 }
 
 FM_API size_t fm_index_prefill_workspace(int T, int64_t S) {

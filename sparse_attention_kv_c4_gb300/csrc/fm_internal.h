@@ -56,7 +56,8 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
 struct PagedArgs {
   const uint16_t* q;
   const float* w;
-  const uint8_t* k_pool;
+  const void* k_pool;        // E4M3 codes [P, 64, 128] or bf16 keys [P, 64, 128]
+  int key_dtype;             // FM_DTYPE_FP8_E4M3 or FM_DTYPE_BF16
   const float* k_scale;
   int64_t P;
   const int32_t* page_phys;

@@ -85,6 +85,7 @@ FM_API fm_status fm_native_topk_paged_noalloc(const uint16_t* q, const float* w,
   a.q = q;
   a.w = w;
   a.k_pool = k_pool;
+  a.key_dtype = FM_DTYPE_FP8_E4M3;
   a.k_scale = k_scale;
   a.P = P;
   a.page_phys = page_phys;

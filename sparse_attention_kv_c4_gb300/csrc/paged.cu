@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threa
                       int32_t* __restrict__ s_logical, int32_t* __restrict__ s_phys,
                       int32_t* __restrict__ nres_eff, int32_t* __restrict__ n_valid,
                       unsigned long long* __restrict__ pmask, int32_t* __restrict__ pprefix,
-                      uint8_t* __restrict__ qsplit, float* __restrict__ wq, unsigned int* __restrict__ status) {
+                      uint8_t* __restrict__ qsplit, float* __restrict__ wq, unsigned int* __restrict__ status,
+                      bool split) {
   __shared__ unsigned long long keys[kMaxR];
   __shared__ uint32_t warp_tot[THREADS / 32];
   const int qi = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threa
   float wraw[kHeadsPerWarp];
 #pragma unroll
   for (int i = 0; i < kHeadsPerWarp; ++i) {
-    qraw[i] = load_head_slice(q + (int64_t)qi * kHeads * kDim, warp + i * kWarps);
+    if (split) qraw[i] = load_head_slice(q + (int64_t)qi * kHeads * kDim, warp + i * kWarps);
     wraw[i] = __ldg(w + (int64_t)qi * kHeads + warp + i * kWarps);
   }
   int nr = R;
@@ -226,13 +227,17 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threa
       n_valid[qi] = (int32_t)run;
     }
   }
-  // q split: q_h = 2^e_h (t1 + t2), 2^e_h folded into w
+  // q split (E4M3 pool): q_h = 2^e_h (t1 + t2), 2^e_h folded into w; a bf16
+  // pool takes q as it is and w unchanged
   uint8_t* t1 = qsplit + (int64_t)qi * 2 * kHeads * kDim;
 #pragma unroll
   for (int i = 0; i < kHeadsPerWarp; ++i) {
     const int h = warp + i * kWarps;
-    split_head(qraw[i], wraw[i], t1 + (int64_t)h * kDim, t1 + (int64_t)(kHeads + h) * kDim,
-               wq + (int64_t)qi * kHeads + h);
+    if (split)
+      split_head(qraw[i], wraw[i], t1 + (int64_t)h * kDim, t1 + (int64_t)(kHeads + h) * kDim,
+                 wq + (int64_t)qi * kHeads + h);
+    else if (lane == 0)
+      wq[(int64_t)qi * kHeads + h] = wraw[i];
   }
 }
 
@@ -258,15 +263,22 @@ struct ScoreParams {
 // kMasked: write only the resident chunks of each page, compacted (the
 // Level-2 resident mask); a separate instantiation so that the unmasked
 // kernel's code is unchanged by it.
-template <bool kMasked>
+// kBf16: the pool holds bf16 keys (no scale).  A stage is then two 16 KB
+// K-halves of the 128-chunk tile (elements 0-63 and 64-127 of every key, one
+// SWIZZLE_128B box of 64 rows per page and half), q is the caller's bf16
+// query in two 8 KB K-halves, and each tile is eight tcgen05.mma kind::f16
+// M128 N64 K16 into the head accumulator; the epilogue is the E4M3 one with
+// the scale fixed at 1.
+template <bool kMasked, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_score_kernel(const __grid_constant__ CUtensorMap tmap_pool, const __grid_constant__ CUtensorMap tmap_q,
                        const ScoreParams p) {
+  constexpr int kStageBytes = kBf16 ? 2 * kTileBytes : kTileBytes;  // key bytes per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_smem = smem;                       // 16 KB
-  uint8_t* a_smem = smem + kQBytes;             // stages x 16 KB
-  float* scale_smem = reinterpret_cast<float*>(a_smem + p.stages * kTileBytes);            // stages x 128
+  uint8_t* a_smem = smem + kQBytes;             // stages x kStageBytes
+  float* scale_smem = reinterpret_cast<float*>(a_smem + p.stages * kStageBytes);          // stages x 128 (E4M3)
 
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[kAccBufs], bar_tempty[kAccBufs], bar_qfull, bar_qempty, bar_drain;
@@ -336,7 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (ok) {
             mbar_arrive_expect_tx(&bar_qfull, (uint32_t)kQBytes);
-            tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * 2 * kHeads));
+            if constexpr (kBf16) {  // the two K-halves of the query's 64 head rows
+              tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * kHeads));
+              tma_load_2d(q_smem + kQBytes / 2, &tmap_q, &bar_qfull, 64, (int32_t)(qi * kHeads));
+            } else {
+              tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * 2 * kHeads));
+            }
             q_issued = (q_issued + 1) & 1;
           }
         }
@@ -345,6 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nb = p.tiles_per_q - tile;
       if ((int64_t)nb > t_end - t) nb = (int)(t_end - t);
       if (nb > kBatch) nb = kBatch;
+      // A batch never holds two uses of one stage: each lane's parity wait
+      // on its stage's empty barrier is exact only if the stage's previous
+      // use was issued (and its wait passed) in an earlier batch.  (With four
+      // stages of bf16 tiles, lanes i and i + 4 of an eight-tile batch would
+      // wait for consecutive uses of the same stage at once, and the later
+      // wait could pass on the phase two uses back.)
+      if (nb > stages) nb = stages;
       const int my_tile = tile + lane;
       const bool valid = lane < nb && 2 * my_tile < nres;
       const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
@@ -355,15 +379,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         } else {
           const int npg = nres - 2 * my_tile >= 2 ? 2 : 1;
-          mbar_arrive_expect_tx(&bar_full[stage], (uint32_t)(npg * (kPageBytes + kPage * 4)));
+          mbar_arrive_expect_tx(&bar_full[stage],
+                                (uint32_t)(npg * (kBf16 ? 2 * kPageBytes : kPageBytes + kPage * 4)));
           for (int h = 0; h < npg; ++h) {
             // the sorted page table is in the workspace (L2-resident): one
             // load per page, issued by all lanes of the batch in parallel
             const int32_t ph = __ldg(p.s_phys + qi * p.R + 2 * my_tile + h);
-            tma_load_2d_hint(a_smem + stage * kTileBytes + h * kPageBytes, &tmap_pool, &bar_full[stage], 0,
-                             ph * kPage, stream_policy);
-            bulk_load_hint(scale_smem + stage * kM + h * kPage, p.k_scale + (int64_t)ph * kPage, kPage * 4,
-                           &bar_full[stage], stream_policy);
+            uint8_t* dst = a_smem + stage * kStageBytes + h * kPageBytes;
+            if constexpr (kBf16) {  // rows h*64.. of both K-halves
+              tma_load_2d_hint(dst, &tmap_pool, &bar_full[stage], 0, ph * kPage, stream_policy);
+              tma_load_2d_hint(dst + kTileBytes, &tmap_pool, &bar_full[stage], 64, ph * kPage, stream_policy);
+            } else {
+              tma_load_2d_hint(dst, &tmap_pool, &bar_full[stage], 0, ph * kPage, stream_policy);
+              bulk_load_hint(scale_smem + stage * kM + h * kPage, p.k_scale + (int64_t)ph * kPage, kPage * 4,
+                             &bar_full[stage], stream_policy);
+            }
           }
           issued_ph[stage] = (int)phase;
         }
@@ -390,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulator m, so the issuers' barrier waits and commits overlap each
       // other's MMAs.
       const uint32_t me = (uint32_t)(warp - 1);
-      const uint32_t idesc = idesc_e4m3_f32(kM, kHeads);
+      const uint32_t idesc = kBf16 ? idesc_bf16_f32(kM, kHeads) : idesc_e4m3_f32(kM, kHeads);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, q_phase = 0, seq = 0;
       int64_t cur_q = -1;
       int nres = 0;
@@ -421,15 +451,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kAccCols;
-          // descriptor start-address field counts 16-byte units; the t2 rows
-          // start 8 KB (eight 1 KB swizzle atoms) after the t1 rows
-          const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
-          constexpr uint64_t kT2 = (kHeads * kDim) >> 4;
+          // descriptor start-address field counts 16-byte units
+          const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kStageBytes >> 4));
+          if constexpr (kBf16) {
+            // K steps of 16 elements (32 bytes): four in each K-half; the
+            // halves are 16 KB (keys) and 8 KB (query) apart
 #pragma unroll
-          for (int k = 0; k < kDim / 32; ++k)
-            umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc0 + 2 * k, idesc, k != 0 ? 1u : 0u);
+            for (int k = 0; k < 8; ++k)
+              umma_bf16_ss(d_tmem, a_desc + (k >> 2) * (kTileBytes >> 4) + (k & 3) * 2,
+                           b_desc0 + (k >> 2) * ((kQBytes / 2) >> 4) + (k & 3) * 2, idesc, k != 0 ? 1u : 0u);
+          } else {
+            // the t2 rows start 8 KB (eight 1 KB swizzle atoms) after the t1 rows
+            constexpr uint64_t kT2 = (kHeads * kDim) >> 4;
 #pragma unroll
-          for (int k = 0; k < kDim / 32; ++k) umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc0 + kT2 + 2 * k, idesc, 1u);
+            for (int k = 0; k < kDim / 32; ++k)
+              umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc0 + 2 * k, idesc, k != 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < kDim / 32; ++k)
+              umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc0 + kT2 + 2 * k, idesc, 1u);
+          }
           umma_commit(&bar_tfull[acc]);  // also frees the stage: its epilogue releases it
         }
         if (++stage == (uint32_t)stages) {
@@ -483,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the stage's scales landed with its full barrier (already complete)
         if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
         tc_fence_after();
-        const float sc = valid ? scale_smem[stage * kM + row] : 0.f;
+        const float sc = valid ? (kBf16 ? 1.f : scale_smem[stage * kM + row]) : 0.f;
         mbar_arrive(&bar_empty[stage]);
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kAccCols;
         const float4* wl = reinterpret_cast<const float4*>(w_mine);
@@ -597,36 +637,53 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   // but only two such CTAs fit an SM: when the queries exceed one wave of
   // them, 256 threads (five per SM) finish the batch sooner.
   const bool wide = a.R > 1024 && a.Q <= 2 * num_sms;
+  const bool bf16 = a.key_dtype == FM_DTYPE_BF16;
   auto prep = wide ? paged_prep_kernel<1024> : paged_prep_kernel<kPrepThreads>;
   prep<<<a.Q, wide ? 1024 : kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
                                                       Rpow2, a.res_mask, a.mask_ld, a.mask_group, ws.s_logical,
                                                       ws.s_phys, ws.nres_eff, ws.n_valid, ws.pmask, ws.pprefix,
-                                                      ws.qsplit, ws.wq, status);
+                                                      ws.qsplit, ws.wq, status, !bf16);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged prep: launch: %s", cudaGetErrorString(e));
 
   CUtensorMap tmap_pool, tmap_q;
-  {
-    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.P * kPage};
-    const uint64_t strides[1] = {(uint64_t)kDim};
-    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)kPage};
-    fm_status st = make_tmap(&tmap_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.k_pool, dims, strides, box,
+  if (bf16) {
+    // pool rows of 128 bf16 (256 bytes); boxes of 64 elements x 64 rows, one
+    // per page and K-half; the caller's q [Q*64, 128] bf16 the same way
+    const uint64_t strides[1] = {(uint64_t)kDim * 2};
+    const uint32_t box[2] = {64u, (uint32_t)kPage};
+    const uint64_t pdims[2] = {(uint64_t)kDim, (uint64_t)a.P * kPage};
+    fm_status st = make_tmap(&tmap_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k_pool, pdims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != FM_OK) return st;
-  }
-  {
-    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.Q * 2 * kHeads};
-    const uint64_t strides[1] = {(uint64_t)kDim};
-    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)(2 * kHeads)};
-    fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws.qsplit, dims, strides, box,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t qdims[2] = {(uint64_t)kDim, (uint64_t)a.Q * kHeads};
+    const uint32_t qbox[2] = {64u, (uint32_t)kHeads};
+    st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, qdims, strides, qbox,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != FM_OK) return st;
+  } else {
+    {
+      const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.P * kPage};
+      const uint64_t strides[1] = {(uint64_t)kDim};
+      const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)kPage};
+      fm_status st = make_tmap(&tmap_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.k_pool, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != FM_OK) return st;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.Q * 2 * kHeads};
+      const uint64_t strides[1] = {(uint64_t)kDim};
+      const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)(2 * kHeads)};
+      fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws.qsplit, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != FM_OK) return st;
+    }
   }
   const int tiles_per_q = (a.R + 1) / 2;
   const int64_t total = (int64_t)a.Q * tiles_per_q;
   const int smem_cap = 227 * 1024 - 6 * 1024;  // less the kernel's static shared memory
   const int fixed = 1024 + kQBytes;
-  const int per_stage = kTileBytes + kM * 4;
+  const int per_stage = bf16 ? 2 * kTileBytes : kTileBytes + kM * 4;
   int stages = (smem_cap - fixed) / per_stage;
   if (stages > kMaxStages) stages = kMaxStages;
   // Tile i uses stage i % stages and is consumed by issuer / epilogue group
@@ -652,7 +709,8 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   p.tiles_per_q = tiles_per_q;
   p.R = a.R;
   p.stages = stages;
-  auto* score_kernel = a.res_mask != nullptr ? paged_score_kernel<true> : paged_score_kernel<false>;
+  auto* score_kernel = a.res_mask != nullptr ? (bf16 ? paged_score_kernel<true, true> : paged_score_kernel<true, false>)
+                                             : (bf16 ? paged_score_kernel<false, true> : paged_score_kernel<false, false>);
   e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const int grid = (int)(total < num_sms ? total : num_sms);

@@ -310,6 +310,56 @@ def pin_paged_mode_a(orc):
             assert list(idx[qi]) == want, qi
 
 
+def pin_paged_bf16_pool_mode_a(orc):
+    """A pool of bf16 keys: the paged top-k equals the brute-force top-k over
+    a dense copy of the listed pages' keys scored by the Memory Indexer's
+    logits (orc_memindex_logits, pinned on its own), with the chunks of
+    unlisted pages excluded; n_res, a resident mask and the remap follow the
+    E4M3 pool's rules."""
+    rng = np.random.default_rng(31)
+    Q, R, n_pages, page, n_h, d = 3, 5, 9, 4, 3, 8
+    P = Q * R + 2
+    q = f32_to_bf16_bits(rng.standard_normal((Q, n_h, d)).astype(np.float32))
+    w = rng.standard_normal((Q, n_h)).astype(np.float32)
+    kbf = f32_to_bf16_bits(rng.standard_normal((P, page, d)).astype(np.float32))
+    phys = rng.permutation(P)[: Q * R].reshape(Q, R).astype(np.int32)
+    logical = np.stack([rng.permutation(n_pages)[:R] for _ in range(Q)]).astype(np.int32)
+    n_res = np.array([5, 2, 0], dtype=np.int32)
+    for k in (6, 40):
+        idx, sc, lg = orc.paged_topk_bf16(q, w, kbf, phys, logical, n_res=n_res, k=k, want_logits=True)
+        for qi in range(Q):
+            dense = np.zeros((1, 1, n_pages * page, d), np.uint16)
+            for j in range(n_res[qi]):
+                dense[0, 0, logical[qi, j] * page:(logical[qi, j] + 1) * page] = kbf[phys[qi, j]]
+            x = orc.memindex_logits(q[qi][None, None], w[qi][None, None], dense)[0, 0]
+            listed = [int(lp) * page + o for lp in sorted(logical[qi, :n_res[qi]].tolist()) for o in range(page)]
+            want = expected_topk(listed, [x[i] for i in listed], k)
+            assert list(idx[qi]) == want, qi
+            got = [float(v) for v, i in zip(sc[qi], idx[qi]) if i >= 0]
+            assert got == [float(x[i]) for i in idx[qi] if i >= 0]
+            for j in range(n_res[qi]):  # logits in table order
+                assert np.array_equal(lg[qi, j * page:(j + 1) * page],
+                                      x[logical[qi, j] * page:(logical[qi, j] + 1) * page])
+    # a resident mask and the remap: the same selection rules as the E4M3 pool
+    mask = np.packbits(rng.random((Q, 64)) < 0.5, axis=-1, bitorder="little").view("<u4").reshape(Q, 2)
+    for id_mode in (0, 1):
+        idx, _ = orc.paged_topk_bf16(q, w, kbf, phys, logical, k=40, res_mask=mask, id_mode=id_mode)
+        for qi in range(Q):
+            dense = np.zeros((1, 1, n_pages * page, d), np.uint16)
+            for j in range(R):
+                dense[0, 0, logical[qi, j] * page:(logical[qi, j] + 1) * page] = kbf[phys[qi, j]]
+            x = orc.memindex_logits(q[qi][None, None], w[qi][None, None], dense)[0, 0]
+            bits = np.unpackbits(mask[qi].view(np.uint8), bitorder="little")
+            cand = [int(lp) * page + o for lp in sorted(logical[qi].tolist()) for o in range(page)
+                    if bits[int(lp) * page + o]]
+            want = expected_topk(cand, [x[i] for i in cand], 40)
+            if id_mode == 1:
+                cell = {int(logical[qi, j]) * page + o: int(phys[qi, j]) * page + o for j in range(R)
+                        for o in range(page)}
+                want = [cell[i] if i >= 0 else -1 for i in want]  # in the order of the logical ids
+            assert list(idx[qi]) == want, (qi, id_mode)
+
+
 def pin_paged_resident_mask_and_remap(orc):
     """Level 2 inside the resident set ([RM] Level 2; [FM] sec. 6 Mode A):
     with a chunk-level resident mask (shared by groups of queries, ragged mask

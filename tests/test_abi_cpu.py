@@ -196,3 +196,18 @@ def test_python_constants_match_header():
 
 def test_check_device_status_is_exported(lib):
     assert hasattr(lib, "fm_check_device_status")
+
+
+def test_paged_rejects_bad_key_dtype_on_host(lib):
+    import sparse_attention_kv_c4_gb300 as fm
+    fm.lib()  # sets argtypes
+    f = lib.fm_native_topk_paged
+    fake = 4096  # never dereferenced: validation fails first
+
+    def call(dtype, scale, ws=fake, wsb=1 << 30):
+        return f(fake, fake, fake, dtype, scale, 8, fake, fake, None, 2, 3, 64, 128, 512, fake, None, ws, wsb, None)
+    assert call(0, fake) == fm.FM_ERR_INVALID_ARG and "key_dtype" in fm.fm_last_error()
+    assert call(3, fake) == fm.FM_ERR_INVALID_ARG
+    assert call(fm.FM_DTYPE_BF16, fake) == fm.FM_ERR_INVALID_ARG and "k_scale" in fm.fm_last_error()
+    assert call(fm.FM_DTYPE_FP8_E4M3, None) == fm.FM_ERR_INVALID_ARG  # an E4M3 pool needs its scales
+    assert call(fm.FM_DTYPE_BF16, None, ws=None) == fm.FM_ERR_WORKSPACE

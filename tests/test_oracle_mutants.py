@@ -56,6 +56,7 @@ MUTANTS = {
                                       "(int32_t)(page_phys[qi * R + j] * page_size)"),
     "paged_mask_past_row": ("uint32_t bits = word < mask_ld ? mrow[word] : 0u;",
                             "uint32_t bits = word < mask_ld ? mrow[word] : ~0u;"),
+    "paged_bf16_pool_row_shifted": ("kbf + (size_t)row * d", "kbf + (size_t)(row ^ 1) * d"),
     "paged_nres_ignored": ("int64_t nr = n_res ? n_res[qi] : R;", "int64_t nr = R;"),
     "causal_inclusive": ("int64_t lim = pos / ratio;", "int64_t lim = pos / ratio + 1;"),
     "causal_token_not_chunk": ("int64_t lim = pos / ratio;", "int64_t lim = pos;"),
