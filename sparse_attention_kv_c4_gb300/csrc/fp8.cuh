@@ -29,10 +29,17 @@ FM_DEV float e4m3_value(uint32_t code) {
   return __half2float(__half(h));
 }
 
+// 2^n as an fp32 built from its exponent field (-126 <= n <= 127).
+FM_DEV float pow2f(int n) { return __int_as_float((n + 127) << 23); }
+
 // One head of the query split.  `raw` holds the lane's four bf16 elements
 // 4l .. 4l+3 of the head (the low half of raw.x is element 4l); r1 / r2 are
 // the head's t1 / t2 rows (128 bytes each); wq_h receives w_h * 2^e_h.  All
 // lanes of the warp call it.
+// Scaling by 2^-e_h is a multiply by that power of two built from its
+// exponent field: an exact power of two, so the product is x 2^-e_h rounded
+// once, as ldexpf gives it, whenever 2^-e_h and 2^e_h are normal floats
+// (max|q_h| >= 2^-118).  Heads below that take ldexpf.
 FM_DEV void split_head(uint2 raw, float w_h, uint8_t* __restrict__ r1, uint8_t* __restrict__ r2,
                        float* __restrict__ wq_h) {
   const int lane = threadIdx.x & 31;
@@ -42,13 +49,22 @@ FM_DEV void split_head(uint2 raw, float w_h, uint8_t* __restrict__ r1, uint8_t* 
   for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(v[j]));
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   int e = 0;
+  bool pow2 = true;  // warp-uniform: amax is the warp's maximum
   if (amax > 0.f && isfinite(amax)) {
-    e = ilogbf(amax) - 8;
-    if (ldexpf(amax, -e) > 448.f) e += 1;
+    const int be = (int)(__float_as_uint(amax) >> 23);  // biased exponent (amax > 0)
+    if (be >= 9) {                                      // e and e + 1 within [-126, 126]
+      e = be - 127 - 8;
+      if (amax * pow2f(-e) > 448.f) e += 1;
+    } else {
+      pow2 = false;
+      e = ilogbf(amax) - 8;
+      if (ldexpf(amax, -e) > 448.f) e += 1;
+    }
   }
+  const float down = pow2 ? pow2f(-e) : 0.f;
   uint32_t c1w = 0, c2w = 0;
   for (int j = 0; j < 4; ++j) {
-    const float s = ldexpf(v[j], -e);
+    const float s = pow2 ? v[j] * down : ldexpf(v[j], -e);
     const uint32_t c1 = e4m3_rne(s);
     const float r = s - e4m3_value(c1);
     c1w |= c1 << (8 * j);
@@ -56,7 +72,7 @@ FM_DEV void split_head(uint2 raw, float w_h, uint8_t* __restrict__ r1, uint8_t* 
   }
   reinterpret_cast<uint32_t*>(r1)[lane] = c1w;
   reinterpret_cast<uint32_t*>(r2)[lane] = c2w;
-  if (lane == 0) *wq_h = ldexpf(w_h, e);
+  if (lane == 0) *wq_h = pow2 ? w_h * pow2f(e) : ldexpf(w_h, e);
 }
 
 // The lane's slice of head h of a query block (16-byte aligned rows of 128

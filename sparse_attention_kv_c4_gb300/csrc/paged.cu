@@ -96,11 +96,19 @@ __device__ __forceinline__ void st_f32_hint(float* addr, float v, uint64_t polic
 // 1. prep: sort pages, validate, split q
 // --------------------------------------------------------------------------
 
-// THREADS: 256, or 1024 for tables longer than 1024 entries when the queries
+// THREADS: 256; 1024 for tables longer than 1024 entries when the queries
 // fit one wave of such CTAs (the bitonic sort's passes then take four
-// elements per thread instead of sixteen).
+// elements per thread instead of sixteen); 128 for tables of at most 256
+// entries when the queries exceed one wave of 256-thread CTAs (ten such CTAs
+// share an SM: 1520 queries per wave, so a 512K-context batch of 1260
+// queries runs in one wave; each thread still has one compare-exchange per
+// sorting stage).  The keys live in dynamic shared memory sized to the
+// table (Rpow2 entries).
 template <int THREADS>
-__global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threads: 760 queries per wave
+constexpr int prep_ctas_per_sm() { return THREADS <= 128 ? 10 : (THREADS <= 256 ? 5 : 1); }
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, prep_ctas_per_sm<THREADS>())
     paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                       const int32_t* __restrict__ page_phys, const int32_t* __restrict__ page_logical,
                       const int32_t* __restrict__ n_res, int R, int64_t P, int Rpow2,
@@ -110,16 +118,18 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threa
                       unsigned long long* __restrict__ pmask, int32_t* __restrict__ pprefix,
                       uint8_t* __restrict__ qsplit, float* __restrict__ wq, unsigned int* __restrict__ status,
                       bool split) {
-  __shared__ unsigned long long keys[kMaxR];
+  extern __shared__ unsigned long long keys[];  // [Rpow2]
   __shared__ uint32_t warp_tot[THREADS / 32];
   const int qi = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the query and head weights are loaded first, so that their latency
-  // overlaps the page-table sort (warp i splits heads i, i + THREADS/32, ...)
+  // overlaps the page-table sort (warp i splits heads i, i + THREADS/32, ...;
+  // at most eight heads' loads in flight per warp, the rest after the sort)
   constexpr int kWarps = THREADS / 32, kHeadsPerWarp = kHeads / kWarps;
-  uint2 qraw[kHeadsPerWarp];
-  float wraw[kHeadsPerWarp];
+  constexpr int kEarly = kHeadsPerWarp < 8 ? kHeadsPerWarp : 8;
+  uint2 qraw[kEarly];
+  float wraw[kEarly];
 #pragma unroll
-  for (int i = 0; i < kHeadsPerWarp; ++i) {
+  for (int i = 0; i < kEarly; ++i) {
     if (split) qraw[i] = load_head_slice(q + (int64_t)qi * kHeads * kDim, warp + i * kWarps);
     wraw[i] = __ldg(w + (int64_t)qi * kHeads + warp + i * kWarps);
   }
@@ -231,13 +241,23 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 256 ? 5 : 1)  // 256 threa
   // pool takes q as it is and w unchanged
   uint8_t* t1 = qsplit + (int64_t)qi * 2 * kHeads * kDim;
 #pragma unroll
-  for (int i = 0; i < kHeadsPerWarp; ++i) {
-    const int h = warp + i * kWarps;
-    if (split)
-      split_head(qraw[i], wraw[i], t1 + (int64_t)h * kDim, t1 + (int64_t)(kHeads + h) * kDim,
-                 wq + (int64_t)qi * kHeads + h);
-    else if (lane == 0)
-      wq[(int64_t)qi * kHeads + h] = wraw[i];
+  for (int i0 = 0; i0 < kHeadsPerWarp; i0 += kEarly) {
+    if (i0 > 0) {
+#pragma unroll
+      for (int i = 0; i < kEarly; ++i) {
+        if (split) qraw[i] = load_head_slice(q + (int64_t)qi * kHeads * kDim, warp + (i0 + i) * kWarps);
+        wraw[i] = __ldg(w + (int64_t)qi * kHeads + warp + (i0 + i) * kWarps);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kEarly; ++i) {
+      const int h = warp + (i0 + i) * kWarps;
+      if (split)
+        split_head(qraw[i], wraw[i], t1 + (int64_t)h * kDim, t1 + (int64_t)(kHeads + h) * kDim,
+                   wq + (int64_t)qi * kHeads + h);
+      else if (lane == 0)
+        wq[(int64_t)qi * kHeads + h] = wraw[i];
+    }
   }
 }
 
@@ -338,26 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t t = t_begin;
     __syncwarp();
     while (t < t_end) {
+      // A new query's q is loaded after its first batch of key copies has
+      // been issued: the copies wait only for stages the old query's
+      // epilogues free, while the q slot waits until every issuer is done
+      // with the old q, so issuing them first keeps the ring filling across
+      // the query boundary instead of draining it.
+      bool load_q = false;
       if (qi != cur_q) {
         nres = p.nres_eff[qi];
         cur_q = qi;
-        if (nres > 0 && lane == 0) {
-          if (q_issued >= 0) {
-            if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) ok = false;
-            q_phase ^= 1;
-          }
-          if (ok) {
-            mbar_arrive_expect_tx(&bar_qfull, (uint32_t)kQBytes);
-            if constexpr (kBf16) {  // the two K-halves of the query's 64 head rows
-              tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * kHeads));
-              tma_load_2d(q_smem + kQBytes / 2, &tmap_q, &bar_qfull, 64, (int32_t)(qi * kHeads));
-            } else {
-              tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * 2 * kHeads));
-            }
-            q_issued = (q_issued + 1) & 1;
-          }
-        }
-        if (__any_sync(0xffffffffu, !ok)) break;
+        load_q = nres > 0;
       }
       int nb = p.tiles_per_q - tile;
       if ((int64_t)nb > t_end - t) nb = (int)(t_end - t);
@@ -399,6 +409,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       seq += (uint32_t)__popc(vmask);
+      if (load_q && lane == 0 && ok) {
+        if (q_issued >= 0) {  // every issuer has committed its last MMA on the old q
+          if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) ok = false;
+          q_phase ^= 1;
+        }
+        if (ok) {
+          mbar_arrive_expect_tx(&bar_qfull, (uint32_t)kQBytes);
+          if constexpr (kBf16) {  // the two K-halves of the query's 64 head rows
+            tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * kHeads));
+            tma_load_2d(q_smem + kQBytes / 2, &tmap_q, &bar_qfull, 64, (int32_t)(qi * kHeads));
+          } else {
+            tma_load_2d(q_smem, &tmap_q, &bar_qfull, 0, (int32_t)(qi * 2 * kHeads));
+          }
+          q_issued = (q_issued + 1) & 1;
+        }
+      }
       if (__any_sync(0xffffffffu, !ok)) break;
       t += nb;
       tile += nb;
@@ -638,8 +664,12 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   // them, 256 threads (five per SM) finish the batch sooner.
   const bool wide = a.R > 1024 && a.Q <= 2 * num_sms;
   const bool bf16 = a.key_dtype == FM_DTYPE_BF16;
-  auto prep = wide ? paged_prep_kernel<1024> : paged_prep_kernel<kPrepThreads>;
-  prep<<<a.Q, wide ? 1024 : kPrepThreads, 0, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
+  // Tables of at most 256 entries: 128-thread CTAs when the queries exceed
+  // one wave of 256-thread CTAs.
+  const bool narrow = !wide && Rpow2 <= 256 && a.Q > prep_ctas_per_sm<kPrepThreads>() * num_sms;
+  auto prep = wide ? paged_prep_kernel<1024> : (narrow ? paged_prep_kernel<128> : paged_prep_kernel<kPrepThreads>);
+  const int prep_threads = wide ? 1024 : (narrow ? 128 : kPrepThreads);
+  prep<<<a.Q, prep_threads, (size_t)Rpow2 * 8, stream>>>(a.q, a.w, a.page_phys, a.page_logical, a.n_res, a.R, a.P,
                                                       Rpow2, a.res_mask, a.mask_ld, a.mask_group, ws.s_logical,
                                                       ws.s_phys, ws.nres_eff, ws.n_valid, ws.pmask, ws.pprefix,
                                                       ws.qsplit, ws.wq, status, !bf16);

@@ -87,6 +87,45 @@ __global__ void __launch_bounds__(kTopkThreads, kShort ? 5 : 4)
 }
 
 
+// Rows of at most kTopkTinyN scores with k <= 512 (a 512K-context decode
+// batch: 1260 queries x 192 pages = 12288 chunks each): 128 threads, a
+// 1536-entry candidate list, a 1024-score sample and a bitmap for 16384 ids
+// (24 KB of shared memory), so nine CTAs share an SM and a 1260-query batch
+// runs in one wave rather than two.  The sample aims at 1024 candidates; a
+// row where it misses is re-aimed once (block_topk) before the exact path.
+constexpr int kTopkTinyThreads = 128;
+constexpr int kTopkTinyN = 16384;
+constexpr int kTopkTinyK = 512;
+constexpr int kTopkTinyCap = 1536;
+constexpr int kTopkTinyRuns = 16;
+using TinySmem = TopkFastSmem<kTopkTinyThreads, kTopkTinyCap, kTopkTinyRuns, kTopkTinyN>;
+
+template <int kMap>
+__global__ void __launch_bounds__(kTopkTinyThreads, 9)
+    topk_rows_tiny_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid, int n,
+                          int k, const int32_t* __restrict__ page_ids, int64_t page_ld,
+                          const int32_t* __restrict__ page_prefix, const unsigned long long* __restrict__ page_mask,
+                          int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  extern __shared__ uint8_t topk_smem_raw[];
+  TinySmem& sm = *reinterpret_cast<TinySmem*>(topk_smem_raw);
+  const int64_t r = blockIdx.x;
+  const int nr = row_len(n_valid, r, n);
+  const float* row = scores + r * ld;
+  int32_t* io = idx_out + r * k;
+  float* so = score_out != nullptr ? score_out + r * k : nullptr;
+  if constexpr (kMap == 2) {
+    const MaskedPageMap map{page_ids + r * page_ld, page_prefix + r * (page_ld + 1), page_mask + r * page_ld,
+                            (int)page_ld};
+    block_topk<kTopkTinyThreads, kTopkTinyCap, MaskedPageMap, kTopkTinyRuns, kTopkTinyN>(row, nr, k, map, io, so, sm);
+  } else if constexpr (kMap == 1) {
+    block_topk<kTopkTinyThreads, kTopkTinyCap, PageMap, kTopkTinyRuns, kTopkTinyN>(
+        row, nr, k, PageMap{page_ids + r * page_ld}, io, so, sm);
+  } else {
+    block_topk<kTopkTinyThreads, kTopkTinyCap, IdentityMap, kTopkTinyRuns, kTopkTinyN>(row, nr, k, IdentityMap{}, io,
+                                                                                        so, sm);
+  }
+}
+
 }  // namespace
 
 size_t topk_workspace_bytes(int rows, int n) {
@@ -100,6 +139,21 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
                            const unsigned long long* page_mask, int32_t* idx_out, float* score_out,
                            cudaStream_t stream) {
   if (rows == 0) return FM_OK;
+  if (n <= kTopkTinyN && k <= kTopkTinyK && rows > 5 * 152) {
+    // more rows than one wave of 256-thread CTAs (five per SM on GB300's 152
+    // SMs): the 128-thread kernel runs nine per SM
+    auto* kernel = page_mask != nullptr ? topk_rows_tiny_kernel<2>
+                                        : (page_ids != nullptr ? topk_rows_tiny_kernel<1> : topk_rows_tiny_kernel<0>);
+    const int smem = (int)sizeof(TinySmem);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    kernel<<<rows, kTopkTinyThreads, smem, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, page_prefix,
+                                                     page_mask, idx_out, score_out);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: launch: %s", cudaGetErrorString(e));
+    return FM_OK;
+  }
   const bool short_rows = n <= kTopkShortN;
   const int smem = short_rows ? (int)sizeof(TopkFastSmem<kTopkThreads, kTopkCapShort>)
                               : (int)sizeof(TopkFastSmem<kTopkThreads, kTopkCap>);

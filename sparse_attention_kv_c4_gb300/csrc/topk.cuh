@@ -197,15 +197,17 @@ struct SelectSmem {
   uint32_t digit[2], above[2], in_digit[2];
 };
 
-template <int THREADS, int CAP = kTopkCap>
+// RUNS: sampled runs of 64 scores; BITMAP_N: rows up to this length emit ids
+// through a bitmap (a CTA instantiated for shorter rows only needs that much).
+template <int THREADS, int CAP = kTopkCap, int RUNS = kTopkRuns, int BITMAP_N = kTopkBitmapN>
 struct TopkFastSmem {
   unsigned long long cand[CAP];
   unsigned long long cmax;
   union {
-    unsigned long long sample[kTopkSample];
-    uint32_t sample32[2 * kTopkSample];  // rows longer than kTopkBitmapN: twice the sample, keys only
+    unsigned long long sample[RUNS * 64];
+    uint32_t sample32[2 * RUNS * 64];  // rows longer than BITMAP_N: twice the sample, keys only
     unsigned long long sel[1024];
-    uint32_t bitmap[kTopkBitmapN / 32];
+    uint32_t bitmap[BITMAP_N / 32];
   } u;
   uint32_t tpre[THREADS];
   uint32_t count;
@@ -310,9 +312,12 @@ FM_DEV T block_select(const T* a, int n, int r, T lo, T hi, uint32_t loose, Sele
   return prefix;
 }
 
-template <int THREADS, int CAP, typename IdxMap>
+template <int THREADS, int CAP, typename IdxMap, int RUNS = kTopkRuns, int BITMAP_N = kTopkBitmapN>
 FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
-                       float* __restrict__ score_out, TopkFastSmem<THREADS, CAP>& sm) {
+                       float* __restrict__ score_out, TopkFastSmem<THREADS, CAP, RUNS, BITMAP_N>& sm) {
+  constexpr int kTopkRuns = RUNS;  // this instantiation's sample and bitmap sizes
+  constexpr int kTopkSample = RUNS * 64;
+  constexpr int kTopkBitmapN = BITMAP_N;
   const int tid = threadIdx.x;
   const int kk = n < k ? n : k;
   if (kk == 0) {
@@ -323,9 +328,18 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
     return;
   }
   // ---- 1. threshold from a sample --------------------------------------------
+  // A sample that misjudges the row (fewer than min(k, n) candidates reach
+  // theta, or more than the list holds) is re-aimed once: the survivor count
+  // c observed at sample rank r gives the rank r * want / c, and the sample and
+  // the filter pass run again (the row is in L2 by then).  Only a second miss
+  // takes the exact global-memory path, whose four radix passes and ordered
+  // output pass over the row cost a multiple of the fast path.
+  const long long want = 3 * kk < 2 * CAP / 3 ? 3 * kk : 2 * CAP / 3;  // expected candidates
+  long long r_aim = -1;  // sample rank of theta (-1: from `want`)
   unsigned long long theta = 0ull;
+  for (int attempt = 0;; ++attempt) {
+  theta = 0ull;
   if (n > CAP) {
-    const long long want = 3 * kk < 2 * CAP / 3 ? 3 * kk : 2 * CAP / 3;  // expected candidates
     if (n <= kTopkBitmapN) {
       for (int i = tid; i < kTopkSample; i += THREADS) {
         const int run = i >> 6, off = i & 63;
@@ -333,9 +347,10 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
         sm.u.sample[i] = ((unsigned long long)float_key(__ldg(row + j)) << 32) | (uint32_t)(~(uint32_t)j);
       }
       __syncthreads();
-      int r = (int)((want * kTopkSample) / (long long)n);
+      long long r = r_aim >= 0 ? r_aim : (want * kTopkSample) / (long long)n;
       r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
-      theta = block_select<THREADS>(sm.u.sample, kTopkSample, r, 0ull, ~0ull, 4u, sm.sel);
+      r_aim = r;
+      theta = block_select<THREADS>(sm.u.sample, kTopkSample, (int)r, 0ull, ~0ull, 4u, sm.sel);
     } else {
       // Long rows (a whole 1M-token history is 262144 scores): with 2048
       // samples only ~12 would lie above the threshold and about one row in
@@ -349,9 +364,11 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
         sm.u.sample32[i] = float_key(__ldg(row + j));
       }
       __syncthreads();
-      int r = (int)((want * 2 * kTopkSample) / (long long)n);
+      long long r = r_aim >= 0 ? r_aim : (want * 2 * kTopkSample) / (long long)n;
       r = r < 1 ? 1 : (r > 2 * kTopkSample ? 2 * kTopkSample : r);
-      theta = (unsigned long long)block_select<THREADS>(sm.u.sample32, 2 * kTopkSample, r, 0u, ~0u, 4u, sm.sel) << 32;
+      r_aim = r;
+      theta = (unsigned long long)block_select<THREADS>(sm.u.sample32, 2 * kTopkSample, (int)r, 0u, ~0u, 4u, sm.sel)
+              << 32;
     }
   }
   // the sample is dead from here: its space becomes the (cleared) bitmap
@@ -461,12 +478,20 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   }
   if (lane == 0 && tmax != 0ull) atomicMax(&sm.cmax, tmax);
   __syncthreads();
-  const int cnt = (int)sm.count;
-  if (sm.overflow || cnt < kk) {
-    __syncthreads();
+  const int survivors = (int)sm.count;  // every survivor, also those past the list
+  if (!sm.overflow && survivors >= kk) break;
+  __syncthreads();
+  // a miss: re-aim the sample rank once (n > CAP here: a row that fits the
+  // list takes every score and cannot miss), else the exact path
+  long long r_next = r_aim * want / (survivors > 0 ? survivors : 1);
+  r_next = r_next < 1 ? 1 : r_next;
+  if (attempt > 0 || n <= CAP || r_next == r_aim) {
     block_topk_radix<THREADS>(row, n, k, idx_map, idx_out, score_out, sm.radix);
     return;
   }
+  r_aim = r_next;
+  }  // attempts
+  const int cnt = (int)sm.count;
   // ---- 3. exact select among the candidates -------------------------------------
   // every candidate lies in [theta, cmax]
   const unsigned long long T = block_select<THREADS>(sm.cand, cnt, kk, theta, sm.cmax, 0u, sm.sel);
