@@ -142,16 +142,17 @@ __global__ void __launch_bounds__(THREADS, prep_ctas_per_sm<THREADS>())
     keys[i] = i < nr ? (((unsigned long long)(uint32_t)page_logical[(int64_t)qi * R + i] << 32) | (uint32_t)i)
                      : ~0ull;
   __syncthreads();
+  // bitonic sort, ascending: each stage's Rpow2 / 2 compare-exchange pairs
+  // are indexed directly (pair t joins element lo = 2j (t / j) + t % j with
+  // lo + j), so no thread idles on the upper element of a pair
   for (int k2 = 2; k2 <= Rpow2; k2 <<= 1)
     for (int j = k2 >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < Rpow2; i += THREADS) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = keys[i], b = keys[ixj];
-          if ((a > b) == ((i & k2) == 0)) {
-            keys[i] = b;
-            keys[ixj] = a;
-          }
+      for (int t = tid; t < Rpow2 / 2; t += THREADS) {
+        const int lo = ((t & ~(j - 1)) << 1) | (t & (j - 1)), hi = lo + j;  // j is a power of two
+        const unsigned long long a = keys[lo], b = keys[hi];
+        if ((a > b) == ((lo & k2) == 0)) {
+          keys[lo] = b;
+          keys[hi] = a;
         }
       }
       __syncthreads();
