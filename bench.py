@@ -521,6 +521,17 @@ def run_ours(args):
         print(json.dumps({"profile_case": True, "only": args.only, "ms_per_step": ms,
                           "device_status": fm.fm_device_status(reset=True)}), flush=True)
         return
+    if args.only == "recall":  # page recall alone: the 1M recall workload's masks (30 x 262144 chunks, KMAX 384)
+        import gen
+        rc = gen.RECALL_1M
+        mask = torch.from_numpy(gen.recall_mask(rc).view(np.int32)).to(dev)
+        pages = torch.empty((rc.B, rc.kmax), dtype=torch.int32, device=dev)
+        n_out = torch.empty((rc.B,), dtype=torch.int32, device=dev)
+        ms = time_call(torch, lambda: fm.fm_page_recall(mask, rc.S, rc.kmax, pages, None, n_out),
+                       max(1, args.steps), args.warmup)
+        print(json.dumps({"profile_case": True, "only": args.only, "ms_per_step": ms,
+                          "device_status": fm.fm_device_status(reset=True)}), flush=True)
+        return
     if args.only in ("memindex_fp8", "paged_full", "retriever", "query_chain"):
         v = {"memindex_fp8": Fp8MemIndex, "paged_full": FullHistoryPaged, "retriever": RetrieverMemIndex,
              "query_chain": QueryChain}[args.only](torch, dev, fm, small=args.small)
@@ -1121,7 +1132,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the variant rows timed after the step")
     ap.add_argument("--only", choices=["memindex", "paged", "prefill", "memindex_fp8", "paged_full", "retriever",
-                                       "query_chain", "prefill_scores"], default=None,
+                                       "query_chain", "prefill_scores", "recall"], default=None,
                     help="profiling case: run one phase only")
     ap.add_argument("--small", action="store_true", help="profiling case: reduced sizes for ncu captures")
     args = ap.parse_args()
