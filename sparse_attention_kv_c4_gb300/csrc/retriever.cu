@@ -19,25 +19,31 @@
 //           SWIZZLE_128B TMA); per layer-tile one bulk copy of its 128 packed
 //           rows (16,896 contiguous bytes) into the stage ring of the pair
 //           (below) that takes the tile.
-//   warps 3-10  two epilogue groups of four warps (one per TMEM lane
-//           quadrant).  A group first unpacks a layer-tile: thread = chunk
-//           row reads its 33 words from shared memory (a 33-word row stride
-//           spreads a warp over all 32 banks), keeps the scale and writes
-//           the 128 key bytes into TMEM (tcgen05.st, lane = row): the MMA's
-//           A operand, with no shared-memory re-layout.  A negative scale
-//           becomes positive with every key sign bit flipped (the same
-//           dequantised key), so the scoring needs only ReLU(sc d) = sc ReLU(d).  It then reads the
-//           previous layer-tile's n_h dots and computes y = sum_h w_h 2^e_h
-//           ReLU(scale (t1 + t2).k), the per-layer logits, the ensemble,
-//           the mask word (ballot) and the ensembled score.
+//   warps 11-14  the unpack group (one warp per TMEM lane quadrant): for
+//           every layer-tile, thread = chunk row reads its 33 words from
+//           shared memory (a 33-word row stride spreads a warp over all 32
+//           banks) and writes the 128 key bytes into the owning pair's TMEM A
+//           slot (tcgen05.st, lane = row): the MMA's A operand, with no
+//           shared-memory re-layout; the scale goes to a shared-memory scale
+//           ring of the pair.  A negative scale becomes positive with every
+//           key sign bit flipped (the same dequantised key), so the scoring
+//           needs only ReLU(sc d) = sc ReLU(d).
+//   warps 3-10  two scoring groups of four warps (one per TMEM lane
+//           quadrant): a group reads its layer-tile's n_h dots and scales and
+//           computes y = sum_h w_h 2^e_h ReLU(scale (t1 + t2).k), the
+//           per-layer logits, the ensemble, the mask word (ballot) and the
+//           ensembled score.  (With the unpack in the same warps, the
+//           shared-memory reads and TMEM stores sat on the scoring's
+//           critical path.)
 //   warps 1-2  UMMA issuers: per layer-tile 8 x tcgen05.mma kind::f8f6f4
 //           M=128 N=n_h K=32 with A from TMEM, four K steps against the
 //           query's t1 rows and four against its t2 rows into one
 //           accumulator (the query split of fp8.cuh).
-// Issuer m and group m form pair m: the pair takes the CTA's tiles with
-// local index = m (mod 2) and owns its stage ring, two TMEM A slots and
-// its accumulators (256 TMEM columns), so every ring has a single filler and
-// a single reader and each parity wait is exact.
+// Issuer m and scoring group m form pair m: the pair takes the CTA's tiles
+// with local index = m (mod 2) and owns its stage ring, two TMEM A slots,
+// four scale slots and its accumulators (256 TMEM columns).  Every ring has
+// a single filler and a single reader (the producer / the unpack group / the
+// issuer / the scoring group), so each parity wait is exact.
 #include <math.h>
 
 #include "fm_common.cuh"
@@ -58,7 +64,9 @@ constexpr int kMaxL = 4;
 constexpr int kPairs = 2;
 constexpr int kMmaWarps = kPairs;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
-constexpr int kThreads = kFirstEpiWarp * 32 + kPairs * 128;
+constexpr int kFirstUnpackWarp = kFirstEpiWarp + kPairs * 4;  // four unpack warps, one per TMEM lane quadrant
+constexpr int kThreads = (kFirstUnpackWarp + 4) * 32;
+constexpr int kSSlots = 4;                 // scale slots per pair (shared memory), handed from unpack to scoring
 constexpr int kASlots = 2;                 // TMEM A slots per pair
 constexpr int kACols = kDim / 4;           // 32 columns: 128 E4M3 bytes per lane
 constexpr int kPairCols = 256;             // TMEM columns per pair
@@ -134,7 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_full[kPairs * kMaxRing], bar_empty[kPairs * kMaxRing];
   __shared__ __align__(8) uint64_t bar_afull[kPairs * kASlots], bar_aempty[kPairs * kASlots];
   __shared__ __align__(8) uint64_t bar_tfull[kPairs * kMaxDAccs], bar_tempty[kPairs * kMaxDAccs];
+  __shared__ __align__(8) uint64_t bar_sfull[kPairs * kSSlots], bar_sempty[kPairs * kSSlots];
   __shared__ __align__(8) uint64_t bar_qfull, bar_qempty, bar_drain;
+  __shared__ float scale_ring[kPairs * kSSlots][kM];  // each chunk's (non-negative) scale, per layer-tile
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   // one copy of the current request's head weights per epilogue warp, so a
@@ -158,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kPairs * C::kDAccs; ++i) {
       mbar_init(&bar_tfull[i], 1);
       mbar_init(&bar_tempty[i], 128);
+    }
+    for (int i = 0; i < kPairs * kSSlots; ++i) {
+      mbar_init(&bar_sfull[i], 128);   // the unpack group wrote the slot's scales
+      mbar_init(&bar_sempty[i], 128);  // the scoring group read them
     }
     mbar_init(&bar_qfull, 1);
     mbar_init(&bar_qempty, kMmaWarps);
@@ -288,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bar_drain);  // every MMA issued above has finished before TMEM is freed
       mbar_wait_drain(&bar_drain, 0);
     }
-  } else {
-    // -------------------------------- epilogue ----------------------------------
+  } else if (warp < kFirstUnpackWarp) {
+    // ------------------------------ scoring groups ------------------------------
     const int group = (warp - kFirstEpiWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp can access
     const int row = quad * 32 + lane;
@@ -299,53 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t span = t_end - t_begin;
     const int64_t n_lt = (span > group ? (span - group + kPairs - 1) / kPairs : 0) * L;  // the pair's layer-tiles
 
-    // unpack one layer-tile (the loader cursor's) into the pair's next A slot
-    Cursor lc;
-    lc.init(t_begin + group, p.tiles_per_b);
-    uint32_t lstage = 0, lphase = 0, aslot = 0, a_phase = 0;
-    float sc_next = 0.f;
-    auto load = [&]() -> bool {
-      const uint32_t stage = group * ring + lstage;
-      if (!mbar_wait(&bar_full[stage], lphase, &abort_flag, p.status)) return false;
-      const bool valid = (int64_t)lc.tile * kM + row < p.S;  // rows past S hold stale bytes
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(k_smem + stage * kTileBytes) + row * kRowWords;
-      uint32_t kw[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) kw[i] = valid ? src[i] : 0u;
-      float sc = valid ? __uint_as_float(src[32]) : 0.f;
-      if (sc < 0.f) {  // scale * e4m3(k) == (-scale) * e4m3(-k): flip every sign bit, keep the scale positive
-        sc = -sc;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) kw[i] ^= 0x80808080u;
-      }
-      sc_next = sc;
-      mbar_arrive(&bar_empty[stage]);
-      if (++lstage == (uint32_t)ring) {
-        lstage = 0;
-        lphase ^= 1u;
-      }
-      const int ai = group * kASlots + (int)aslot;
-      if (!mbar_wait(&bar_aempty[ai], a_phase ^ 1u, &abort_flag, p.status)) return false;
-      tc_fence_after();
-      tmem_st32(lane_base + aslot * kACols, kw);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_afull[ai]);
-      if (++aslot == (uint32_t)kASlots) {
-        aslot = 0;
-        a_phase ^= 1u;
-      }
-      lc.next(L, p.tiles_per_b);
-      return true;
-    };
-
-    // score one layer-tile (the compute cursor's) and, at its last layer, the chunk
+    // score one layer-tile (the cursor's) and, at its last layer, the chunk
     Cursor cc;
     cc.init(t_begin + group, p.tiles_per_b);
-    uint32_t dacc = 0, d_phase = 0;
+    uint32_t dacc = 0, d_phase = 0, sslot = 0, s_phase = 0;
     int64_t w_b = -1;
     float acc_m = -INFINITY, acc_sum = 0.f;
-    auto compute = [&](float sc) -> bool {
+    auto compute = [&]() -> bool {
       const int64_t b = cc.b;
       const int l = cc.l;
       if (b != w_b) {  // a new request: its weights into this warp's copy
@@ -353,6 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = lane; i < L * NH; i += 32) w_mine[i] = __ldg(p.wq + b * L * NH + i);
         __syncwarp();
         w_b = b;
+      }
+      // the chunk's scale, from the unpack group (>= 0: a negative scale's
+      // sign went into the key bytes)
+      const int si = group * kSSlots + (int)sslot;
+      if (!mbar_wait(&bar_sfull[si], s_phase, &abort_flag, p.status)) return false;
+      const float sc = scale_ring[si][row];
+      mbar_arrive(&bar_sempty[si]);
+      if (++sslot == (uint32_t)kSSlots) {
+        sslot = 0;
+        s_phase ^= 1u;
       }
       const int di = group * C::kDAccs + (int)dacc;
       if (!mbar_wait(&bar_tfull[di], d_phase, &abort_flag, p.status)) return false;
@@ -369,9 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar_tempty[di]);  // the dots are in registers: the MMA may reuse the accumulator
         }
-        // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w
-        // the scale is >= 0 (the unpack moved its sign into the key), so
-        // ReLU(sc d) = sc ReLU(d): one multiply per chunk
+        // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w, and
+        // ReLU(sc d) = sc ReLU(d) for sc >= 0: one multiply per chunk
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
         for (int h = 0; h < 32; h += 4) {
@@ -416,18 +399,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       cc.next(L, p.tiles_per_b);
       return true;
     };
-
-    // the unpack of layer-tile j + 1 runs ahead of the scoring of j, so the
-    // pair's MMAs for j + 1 overlap this group's arithmetic for j
-    if (n_lt > 0 && load()) {
-      for (int64_t j = 0; j < n_lt; ++j) {
-        const float sc = sc_next;
-        if (j + 1 < n_lt && !load()) break;
-        if (!compute(sc)) break;
+    for (int64_t j = 0; j < n_lt; ++j)
+      if (!compute()) break;
+  } else {
+    // ------------------------------ unpack group --------------------------------
+    // Every layer-tile of the CTA, in order (tile i belongs to pair i % 2):
+    // thread = chunk row reads its 33 words from the pair's stage (a 33-word
+    // row stride spreads a warp over all 32 banks), frees the stage, moves a
+    // negative scale's sign into the key bytes, writes the 128 key bytes into
+    // the pair's next TMEM A slot (tcgen05.st, lane = row) and the scale into
+    // the pair's next scale slot.  Doing this in warps of its own takes the
+    // row unpack off the scoring warps' critical path.
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    // each pair's ring positions, in registers (a runtime-indexed array of
+    // them would live in local memory)
+    struct Ring {
+      uint32_t lstage, lphase, aslot, a_phase, sslot, s_phase;
+    };
+    Ring r0 = {}, r1 = {};
+    // one layer-tile of pair m
+    auto unpack = [&](Ring& c, const int m, const bool valid) -> bool {
+      const uint32_t stage = m * ring + c.lstage;
+      if (!mbar_wait(&bar_full[stage], c.lphase, &abort_flag, p.status)) return false;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(k_smem + stage * kTileBytes) + row * kRowWords;
+      uint32_t kw[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) kw[i] = valid ? src[i] : 0u;
+      float sc = valid ? __uint_as_float(src[32]) : 0.f;
+      mbar_arrive(&bar_empty[stage]);
+      if (++c.lstage == (uint32_t)ring) {
+        c.lstage = 0;
+        c.lphase ^= 1u;
       }
+      if (sc < 0.f) {  // scale * e4m3(k) == (-scale) * e4m3(-k): flip every sign bit, keep the scale positive
+        sc = -sc;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) kw[i] ^= 0x80808080u;
+      }
+      const int ai = m * kASlots + (int)c.aslot;
+      if (!mbar_wait(&bar_aempty[ai], c.a_phase ^ 1u, &abort_flag, p.status)) return false;
+      tc_fence_after();
+      tmem_st32(tmem_base + lane_off + (uint32_t)(m * kPairCols) + c.aslot * kACols, kw);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_afull[ai]);
+      if (++c.aslot == (uint32_t)kASlots) {
+        c.aslot = 0;
+        c.a_phase ^= 1u;
+      }
+      const int si = m * kSSlots + (int)c.sslot;
+      if (!mbar_wait(&bar_sempty[si], c.s_phase ^ 1u, &abort_flag, p.status)) return false;
+      scale_ring[si][row] = sc;
+      mbar_arrive(&bar_sfull[si]);
+      if (++c.sslot == (uint32_t)kSSlots) {
+        c.sslot = 0;
+        c.s_phase ^= 1u;
+      }
+      return true;
+    };
+    int tile = (int)(t_begin % p.tiles_per_b) - 1;
+    bool ok = true;
+    for (int64_t t = t_begin; t < t_end && ok; ++t) {
+      if (++tile == p.tiles_per_b) tile = 0;
+      const bool valid = (int64_t)tile * kM + row < p.S;  // rows past S hold stale bytes
+      const bool pair1 = ((t - t_begin) & 1) != 0;
+      for (int l = 0; l < L && ok; ++l) ok = pair1 ? unpack(r1, 1, valid) : unpack(r0, 0, valid);
     }
   }
-
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -478,7 +518,9 @@ fm_status launch_retriever(const RetrieverArgs& a, int num_sms, unsigned int* st
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != FM_OK) return st;
   }
-  const int smem_cap = 227 * 1024 - (int)sizeof(float) * kPairs * 4 * kMaxL * NH - 2048;  // less static
+  // less the static shared memory: head weights, the scale ring, barriers
+  const int smem_cap = 227 * 1024 - (int)sizeof(float) * kPairs * 4 * kMaxL * NH -
+                       (int)sizeof(float) * kPairs * kSSlots * kM - 2048;
   const int fixed = 1024 + a.L * C::kQLayerBytes;
   int ring = (smem_cap - fixed) / (kPairs * kTileBytes);
   if (ring > kMaxRing) ring = kMaxRing;
