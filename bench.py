@@ -697,7 +697,7 @@ def run_ours(args):
         del sets, host_in, host_out
         variants = {}
         for name, cls, reps in (("tiny", TinyConfig, 50), ("memindex_256k", MemIndex256K, 10),
-                                ("paged_512k", Paged512K, 10)):
+                                ("paged_512k", Paged512K, 10), ("paged_bf16_1m", PagedBf16, 10)):
             v = cls(torch, dev, fm)
             variants[name] = v.measure(reps, 3, pk)
             del v
@@ -876,6 +876,46 @@ class Paged512K:
                 "queries_per_s": c.Q / (ms / 1e3), "bound": "hbm", "achieved": round(ach, 2), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "algorithmic_bytes": nbytes, "launches": 3,
                 "reps": reps, "workload": f"paged top-{c.k} 512K: {c.Q} queries x {c.R} pages, E4M3 + fp32 scale"}
+
+
+class PagedBf16:
+    """The native paged top-512 over a pool of bf16 keys (key_dtype
+    FM_DTYPE_BF16, no scale) at the 1M decode workload's sizes: 630 queries x
+    384 resident pages, 4.0 GB of keys per call (twice the E4M3 pool's
+    bytes)."""
+
+    def __init__(self, torch, dev, fm):
+        import gen
+        self.torch, self.fm, self.cfg = torch, fm, gen.PAGED_1M
+        c = self.cfg
+        logical, phys, owner = gen.paged_tables(c)
+        q, w = gen.paged_qw(c)
+        self.q = torch.from_numpy(q.view(np.int16)).to(dev)
+        self.w = torch.from_numpy(w).to(dev)
+        own_d = torch.from_numpy(owner).to(dev)
+        self.kbf = torch.empty((c.P, c.page, c.d), dtype=torch.int16, device=dev)
+        gen.paged_pool_bf16_device(c, own_d.data_ptr(), self.kbf.data_ptr())
+        del own_d
+        self.phys = torch.from_numpy(phys).to(dev)
+        self.logical = torch.from_numpy(logical).to(dev)
+        self.idx = torch.empty((c.Q, c.k), dtype=torch.int32, device=dev)
+        self.score = torch.empty((c.Q, c.k), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(fm.fm_native_topk_paged_workspace(c.Q, c.R), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def call(self):
+        self.fm.fm_native_topk_paged(self.q, self.w, self.kbf, None, self.phys, self.logical, self.cfg.k, self.idx,
+                                     self.score, workspace=self.ws)
+
+    def measure(self, reps, warmup, pk):
+        c = self.cfg
+        ms = time_call(self.torch, self.call, reps, warmup)
+        nbytes = c.P * c.page * c.d * 2 + c.Q * c.R * 8 + c.Q * c.k * 8
+        ach = nbytes / (ms / 1e3) / 1e9
+        return {"ms": round(ms, 4), "chunk_scores_per_s": c.chunk_scores / (ms / 1e3),
+                "queries_per_s": c.Q / (ms / 1e3), "bound": "hbm", "achieved": round(ach, 2), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "algorithmic_bytes": nbytes, "launches": 3,
+                "reps": reps, "workload": f"paged top-{c.k} over bf16 keys: {c.Q} queries x {c.R} pages"}
 
 
 class Fp8MemIndex:

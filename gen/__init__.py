@@ -89,7 +89,9 @@ def cuda_lib():
         lib.gen_cuda_fill_k_bf16.argtypes = [U64, I64, I64, I64, I32, U32, VP, VP, I64, I64, VP]
         lib.gen_cuda_fill_k_fp8_pool.argtypes = [U64, I64, I32, I32, U32, VP, VP, I64, I64, VP, VP, VP]
         lib.gen_cuda_fill_q_bf16.argtypes = [U64, I64, I64, I32, I32, VP, VP]
-        for f in (lib.gen_cuda_fill_k_bf16, lib.gen_cuda_fill_k_fp8_pool, lib.gen_cuda_fill_q_bf16):
+        lib.gen_cuda_fill_k_bf16_pool.argtypes = [U64, I64, I32, I32, VP, VP, VP]
+        for f in (lib.gen_cuda_fill_k_bf16, lib.gen_cuda_fill_k_fp8_pool, lib.gen_cuda_fill_q_bf16,
+                  lib.gen_cuda_fill_k_bf16_pool):
             f.restype = ctypes.c_int
         _cuda = lib
     return _cuda
@@ -475,6 +477,14 @@ def paged_pool_device(cfg: PagedCfg, owner_dev_ptr: int, k8_ptr: int, scale_ptr:
         raise RuntimeError(f"gen_cuda_fill_k_fp8_pool failed: cuda error {rc}")
 
 
+def paged_pool_bf16_device(cfg: PagedCfg, owner_dev_ptr: int, kbf_ptr: int, stream: int = 0) -> None:
+    """A bf16 key pool [P, page, d] on the device with the values of
+    paged_pool_rows_bf16 (owner_dev_ptr: paged_tables' owner on the device)."""
+    rc = cuda_lib().gen_cuda_fill_k_bf16_pool(cfg.seed, cfg.P, cfg.d, cfg.page, owner_dev_ptr, kbf_ptr, stream)
+    if rc != 0:
+        raise RuntimeError(f"gen_cuda_fill_k_bf16_pool failed: cuda error {rc}")
+
+
 # --------------------------------------------------------------------------
 # Prefill inputs
 # --------------------------------------------------------------------------
@@ -499,5 +509,5 @@ __all__ = [
     "BASE_SEED", "MemIndexCfg", "PagedCfg", "PrefillCfg", "TINY", "MEMINDEX_256K", "MEMINDEX_1M",
     "PAGED_512K", "PAGED_1M", "PAGED_FULL_1M", "RETRIEVER_1M", "PREFILL", "memindex_qw", "memindex_keys_host", "memindex_key_rows",
     "memindex_keys_device", "planted", "pack_compressed_k", "query_chain_inputs", "paged_tables", "paged_qw", "paged_pool_host",
-    "paged_chunk_rows", "paged_pool_rows", "paged_pool_rows_bf16", "paged_pool_device", "prefill_host", "w_pattern", "thr32", "replace",
+    "paged_chunk_rows", "paged_pool_rows", "paged_pool_rows_bf16", "paged_pool_device", "paged_pool_bf16_device", "prefill_host", "w_pattern", "thr32", "replace",
 ]

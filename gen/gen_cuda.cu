@@ -59,6 +59,22 @@ __global__ void gen_k_fp8_pool_kernel(uint64_t seed, int64_t P, int32_t d, int32
   }
 }
 
+// bf16 keys of a pool: one warp per chunk of a physical page, owner[p] =
+// (a, b, logical page); cold keys only (the paged recipe plants nothing).
+__global__ void gen_k_bf16_pool_kernel(uint64_t seed, int64_t P, int32_t d, int32_t page_size,
+                                       const int32_t* __restrict__ owner, uint16_t* __restrict__ out) {
+  int64_t rows = P * page_size;
+  int lane = threadIdx.x % 32;
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; row < rows;
+       row += (int64_t)gridDim.x * (blockDim.x / 32)) {
+    int64_t p = row / page_size;
+    int64_t o = row % page_size;
+    int64_t a = owner[3 * p + 0], b = owner[3 * p + 1], lp = owner[3 * p + 2];
+    int64_t s = lp * page_size + o;
+    for (int32_t x = lane; x < d; x += 32) out[row * d + x] = gen_bf16_rne(gen_k_f32(seed, a, b, s, x, d, 0, 0.0f));
+  }
+}
+
 __global__ void gen_q_bf16_kernel(uint64_t seed, int64_t A, int64_t Bc, int32_t n_h, int32_t d,
                                   uint16_t* __restrict__ out) {
   int64_t n = A * Bc * n_h * d;
@@ -93,6 +109,12 @@ GEN_API int gen_cuda_fill_k_fp8_pool(uint64_t seed, int64_t P, int32_t d, int32_
   if (d > 256) return (int)cudaErrorInvalidValue;
   gen_k_fp8_pool_kernel<<<gen_grid(P * page_size, 8), 256, 0, stream>>>(
       seed, P, d, page_size, thr32, owner_dev, hot_dev, hot_stride_a, hot_stride_b, k8_dev, scale_dev);
+  return (int)cudaGetLastError();
+}
+
+GEN_API int gen_cuda_fill_k_bf16_pool(uint64_t seed, int64_t P, int32_t d, int32_t page_size,
+                                      const int32_t* owner_dev, uint16_t* out_dev, cudaStream_t stream) {
+  gen_k_bf16_pool_kernel<<<gen_grid(P * page_size, 8), 256, 0, stream>>>(seed, P, d, page_size, owner_dev, out_dev);
   return (int)cudaGetLastError();
 }
 

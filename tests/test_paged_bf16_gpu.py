@@ -137,3 +137,17 @@ def test_bf16_pool_takes_no_scale(torch_dev):
     with pytest.raises(fm.FmError) as e:
         fm.fm_native_topk_paged(q, w, pool, scale, table, table, 8, idx, workspace=ws)
     assert e.value.status == fm.FM_ERR_INVALID_ARG
+
+
+def test_bf16_pool_device_fill_matches_host(torch_dev):
+    """The generator's device fill of a bf16 pool (used by the benchmark row)
+    gives the host builder's values bit for bit."""
+    torch, dev = torch_dev
+    cfg = gen.PagedCfg("t", requests=2, layers=3, n_pages=50, R=6, seed=361)
+    logical, phys, owner = gen.paged_tables(cfg)
+    host = gen.paged_pool_rows_bf16(cfg, logical, phys)
+    own_d = torch.from_numpy(owner).to(dev)
+    kd = torch.empty((cfg.P, cfg.page, cfg.d), dtype=torch.int16, device=dev)
+    gen.paged_pool_bf16_device(cfg, own_d.data_ptr(), kd.data_ptr())
+    torch.cuda.synchronize()
+    assert (kd.cpu().numpy().view(np.uint16) == host).all()
