@@ -199,11 +199,6 @@ FM_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
-// 32 lanes x 2 consecutive 32-bit columns: thread i gets lane (base + i).
-FM_DEV void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr) : "memory");
-}
-
 // 32 lanes x 32 consecutive 32-bit columns store: thread i writes lane (base + i).
 FM_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
