@@ -328,5 +328,5 @@ FM_API fm_status fm_index_prefill_scores(const uint16_t* q, const float* w, cons
   a.T = T;
   a.S = S;
   a.ratio = ratio;
-  return launch_prefill_scores(a, logits_out, true, sms, status, reinterpret_cast<cudaStream_t>(stream));
+  return launch_prefill_scores(a, logits_out, nullptr, true, sms, status, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -52,6 +52,13 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
                            const int32_t* page_ids, int64_t page_ld, const int32_t* page_prefix,
                            const unsigned long long* page_mask, int32_t* idx_out, float* score_out,
                            cudaStream_t stream);
+// The same select (candidate i has id i) for rows that come with segment
+// maxima: segmax[r*seg_ld + g] is, for the scores 32g .. 32g+31 of row r below
+// its n_valid, the largest of their bit patterns read as signed integers.  Rows
+// with at least 2k segments read only the segments that can hold a top-k score.
+fm_status launch_topk_rows_segmax(const float* scores, int64_t ld, const int32_t* n_valid, const int32_t* segmax,
+                                  int64_t seg_ld, int rows, int n, int k, int32_t* idx_out, float* score_out,
+                                  cudaStream_t stream);
 
 struct PagedArgs {
   const uint16_t* q;
@@ -88,9 +95,10 @@ struct PrefillArgs {
 };
 size_t prefill_workspace_bytes(int T, int64_t S);
 fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
-// The dense scores Y [T, S] alone into `logits` (row stride S); with
-// fill_masked, -inf wherever s >= the token's causal limit.
-fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, bool fill_masked, int num_sms,
+// The dense scores Y [T, S] into `logits` (row stride S) for s below each
+// token's causal limit; with fill_masked, -inf at every other s.  With segmax
+// ([T, ceil(S / 32)]), also each token's segment maxima (launch_topk_rows_segmax).
+fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, int32_t* segmax, bool fill_masked, int num_sms,
                                 unsigned int* status, cudaStream_t stream);
 fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cudaStream_t stream);
 

@@ -52,6 +52,8 @@ struct Params {
   const float* w;
   const int64_t* pos;
   float* logits;
+  int32_t* segmax;  // [T, seg_ld] segment maxima for the top-k, or null
+  int64_t seg_ld;
   unsigned int* status;
   int64_t S;
   int64_t total_items;
@@ -235,58 +237,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = (warp - kFirstEpiWarp) >> 2;  // token of the block handled by this warp
     const int row = quad * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
-    int64_t cur_qb = -1, lim = 0;
-    int64_t qb = t_begin / p.tiles_per_qb;
-    int ct = (int)(t_begin % p.tiles_per_qb) - 1;
-    for (int64_t it = t_begin; it < t_end; ++it) {
-      if (++ct == p.tiles_per_qb) {
-        ct = 0;
-        ++qb;
-      }
-      if (qb != cur_qb) {
-        cur_qb = qb;
-        lim = block_limit(p, qb);
-        // the warp's token weights stay in shared memory for the whole block
-        const int64_t tw = qb * kTok + j;
-        const float* wsrc = p.w + (tw < p.T ? tw : 0) * kHeads;
-        __syncwarp();
-        w_smem[warp - kFirstEpiWarp][lane] = __ldg(wsrc + lane);
-        w_smem[warp - kFirstEpiWarp][lane + 32] = __ldg(wsrc + lane + 32);
-        __syncwarp();
-      }
-      if ((int64_t)ct * kM >= lim) continue;
-      const int64_t t = qb * kTok + j;
-      const int64_t s = (int64_t)ct * kM + row;
-      if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHeads;
-      // both halves of the row in flight at once, one wait, then the
-      // accumulator is released before the arithmetic
-      uint32_t r0[32], r1[32];
-      tmem_ld32(taddr, r0);
-      tmem_ld32(taddr + 32, r1);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_tempty[acc]);
-      const float4* w4 = reinterpret_cast<const float4*>(w_smem[warp - kFirstEpiWarp]);
-      float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, x4 = 0.f, x5 = 0.f, x6 = 0.f, x7 = 0.f;
+    bool aborted = false;
+    // The same tile sequence as the producer and the issuers, walked one query
+    // block at a time: an int32 loop over the block's tiles in this CTA's
+    // range that lie below the block's causal limit (the skipped ones advance
+    // no barrier), with the token's causal limit and its rows of logits and
+    // segment entries set once per block.
+    for (int64_t it = t_begin; it < t_end && !aborted;) {
+      const int64_t qb = it / p.tiles_per_qb;
+      const int ct0 = (int)(it - qb * p.tiles_per_qb);
+      const int ct_end = (t_end - it < (int64_t)(p.tiles_per_qb - ct0)) ? ct0 + (int)(t_end - it) : p.tiles_per_qb;
+      it += ct_end - ct0;
+      const int64_t lim = block_limit(p, qb);
+      const int ct_live = (int)((lim + kM - 1) / kM);  // tiles with ct * kM < lim
+      const int ct_stop = ct_end < ct_live ? ct_end : ct_live;
+      // the warp's token weights stay in shared memory for the whole block
+      const int64_t tw = qb * kTok + j;
+      const bool live = tw < p.T;
+      const int lim_t = live ? (int)causal_limit(__ldg(p.pos + tw), p.S, p.ratio) : 0;  // S < 2^31
+      float* const lrow = p.logits + (live ? tw : 0) * p.S + row;
+      int32_t* const srow = p.segmax != nullptr ? p.segmax + (live ? tw : 0) * p.seg_ld + quad : nullptr;
+      const float* wsrc = p.w + (live ? tw : 0) * kHeads;
+      __syncwarp();
+      w_smem[warp - kFirstEpiWarp][lane] = __ldg(wsrc + lane);
+      w_smem[warp - kFirstEpiWarp][lane + 32] = __ldg(wsrc + lane + 32);
+      __syncwarp();
+      for (int ct = ct0; ct < ct_stop; ++ct) {
+        if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHeads;
+        // both halves of the row in flight at once, one wait, then the
+        // accumulator is released before the arithmetic
+        uint32_t r0[32], r1[32];
+        tmem_ld32(taddr, r0);
+        tmem_ld32(taddr + 32, r1);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_tempty[acc]);
+        const float4* w4 = reinterpret_cast<const float4*>(w_smem[warp - kFirstEpiWarp]);
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, x4 = 0.f, x5 = 0.f, x6 = 0.f, x7 = 0.f;
 #pragma unroll
-      for (int h4 = 0; h4 < 8; ++h4) {
-        const float4 a = w4[h4];
-        const float4 c = w4[8 + h4];
-        x0 = fmaf(a.x, fmaxf(__uint_as_float(r0[4 * h4]), 0.f), x0);
-        x1 = fmaf(a.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), x1);
-        x2 = fmaf(a.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), x2);
-        x3 = fmaf(a.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), x3);
-        x4 = fmaf(c.x, fmaxf(__uint_as_float(r1[4 * h4]), 0.f), x4);
-        x5 = fmaf(c.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), x5);
-        x6 = fmaf(c.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), x6);
-        x7 = fmaf(c.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), x7);
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 a = w4[h4];
+          const float4 c = w4[8 + h4];
+          x0 = fmaf(a.x, fmaxf(__uint_as_float(r0[4 * h4]), 0.f), x0);
+          x1 = fmaf(a.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), x1);
+          x2 = fmaf(a.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), x2);
+          x3 = fmaf(a.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), x3);
+          x4 = fmaf(c.x, fmaxf(__uint_as_float(r1[4 * h4]), 0.f), x4);
+          x5 = fmaf(c.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), x5);
+          x6 = fmaf(c.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), x6);
+          x7 = fmaf(c.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), x7);
+        }
+        const float y = ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
+        // only the token's own candidates (s below its causal limit) are written
+        const bool valid = ct * kM + row < lim_t;
+        if (valid) lrow[ct * kM] = y;
+        if (srow != nullptr) {
+          // the warp's 32 scores are one segment: its entry is the largest bit
+          // pattern read as a signed integer (the largest score when any is
+          // >= +0; see topk.cuh, block_topk_segmax, for how the select reads
+          // it).  Lane 0's score is the segment's first, so its `valid` says
+          // whether the segment starts below the limit.
+          const int m = __reduce_max_sync(0xffffffffu, valid ? __float_as_int(y) : INT_MIN);
+          if (lane == 0 && valid) srow[ct * 4] = m;
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
       }
-      const float y = ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
-      if (t < p.T && s < p.S) p.logits[t * p.S + s] = y;
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
     }
   }
 
@@ -312,12 +333,16 @@ __global__ void causal_fill_kernel(const int64_t* __restrict__ pos, int64_t S, i
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int64_t seg_count(int64_t S) { return (S + 31) / 32; }
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int T, int64_t S) { return align256((size_t)T * S * 4) + align256((size_t)T * 4); }
+// logits [T, S], the causal limits [T], the segment maxima [T, ceil(S / 32)]
+size_t prefill_workspace_bytes(int T, int64_t S) {
+  return align256((size_t)T * S * 4) + align256((size_t)T * 4) + align256((size_t)T * seg_count(S) * 4);
+}
 
-fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, bool fill_masked, int num_sms,
+fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, int32_t* segmax, bool fill_masked, int num_sms,
                                 unsigned int* status, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   if (a.T > 0 && a.S > 0) {
@@ -355,6 +380,8 @@ fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, bool fill_m
     p.w = a.w;
     p.pos = a.pos;
     p.logits = logits;
+    p.segmax = segmax;
+    p.seg_ld = seg_count(a.S);
     p.status = status;
     p.S = a.S;
     p.total_items = total;
@@ -380,14 +407,17 @@ fm_status launch_prefill_scores(const PrefillArgs& a, float* logits, bool fill_m
 fm_status launch_prefill(const PrefillArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
   if (a.T == 0) return FM_OK;
   float* logits = static_cast<float*>(a.workspace);
-  int32_t* n_valid = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + align256((size_t)a.T * a.S * 4));
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const size_t logits_bytes = align256((size_t)a.T * a.S * 4);
+  int32_t* n_valid = reinterpret_cast<int32_t*>(ws + logits_bytes);
+  int32_t* segmax = reinterpret_cast<int32_t*>(ws + logits_bytes + align256((size_t)a.T * 4));
   causal_limits_kernel<<<(a.T + 255) / 256, 256, 0, stream>>>(a.pos, a.T, a.S, a.ratio, n_valid);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "prefill limits: launch: %s", cudaGetErrorString(e));
-  fm_status st = launch_prefill_scores(a, logits, false, num_sms, status, stream);
+  fm_status st = launch_prefill_scores(a, logits, segmax, false, num_sms, status, stream);
   if (st != FM_OK) return st;
-  return launch_topk_rows(logits, a.S, n_valid, a.T, (int)a.S, a.k, nullptr, 0, nullptr, nullptr, a.idx_out,
-                          a.score_out, stream);
+  return launch_topk_rows_segmax(logits, a.S, n_valid, segmax, seg_count(a.S), a.T, (int)a.S, a.k, a.idx_out,
+                                 a.score_out, stream);
 }
 
 }  // namespace fm

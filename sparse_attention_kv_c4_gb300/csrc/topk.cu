@@ -126,6 +126,25 @@ __global__ void __launch_bounds__(kTopkTinyThreads, 9)
   }
 }
 
+// Prefill rows with segment entries (block_topk_segmax): read the entries,
+// then only the segments that can hold a top-k score.  Same shared memory and
+// occupancy as the short-row kernel (five CTAs per SM), whose select it falls
+// back on for a row it cannot prune.
+constexpr int kSegMaxN = kTopkBitmapN;  // rows of at most this many scores
+using SegSmem = TopkFastSmem<kTopkThreads, kTopkCapShort>;
+
+__global__ void __launch_bounds__(kTopkThreads, 5)
+    topk_rows_segmax_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
+                            const int32_t* __restrict__ segmax, int64_t seg_ld, int n, int k,
+                            int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  extern __shared__ uint8_t topk_smem_raw[];
+  SegSmem& sm = *reinterpret_cast<SegSmem*>(topk_smem_raw);
+  const int64_t r = blockIdx.x;
+  const int nr = row_len(n_valid, r, n);
+  block_topk_segmax<kTopkThreads, kTopkCapShort>(scores + r * ld, nr, k, segmax + r * seg_ld, ld % 4 == 0,
+                                                 IdentityMap{}, idx_out + r * k,
+                                                 score_out != nullptr ? score_out + r * k : nullptr, sm);
+}
 }  // namespace
 
 size_t topk_workspace_bytes(int rows, int n) {
@@ -175,6 +194,27 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
                                                idx_out, score_out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: launch: %s", cudaGetErrorString(e));
+  return FM_OK;
+}
+
+fm_status launch_topk_rows_segmax(const float* scores, int64_t ld, const int32_t* n_valid, const int32_t* segmax,
+                                  int64_t seg_ld, int rows, int n, int k, int32_t* idx_out, float* score_out,
+                                  cudaStream_t stream) {
+  if (rows == 0) return FM_OK;
+  // rows too short to prune (fewer than 2k segments) or longer than the
+  // short-row kernel takes: the plain select
+  if ((n + 31) / 32 < 2 * k || n > kSegMaxN)
+    return launch_topk_rows(scores, ld, n_valid, rows, n, k, nullptr, 0, nullptr, nullptr, idx_out, score_out,
+                            stream);
+  const int smem = (int)sizeof(SegSmem);
+  cudaError_t e = cudaFuncSetAttribute(topk_rows_segmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(topk_rows_segmax_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk segmax: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  topk_rows_segmax_kernel<<<rows, kTopkThreads, smem, stream>>>(scores, ld, n_valid, segmax, seg_ld, n, k, idx_out,
+                                                                score_out);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk segmax: launch: %s", cudaGetErrorString(e));
   return FM_OK;
 }
 

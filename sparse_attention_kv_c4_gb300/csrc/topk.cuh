@@ -212,6 +212,7 @@ struct TopkFastSmem {
   uint32_t tpre[THREADS];
   uint32_t count;
   int overflow;
+  uint32_t klo, khi, nlist;  // block_topk_segmax: range of the segment keys, list length
   SelectSmem<THREADS> sel;
   TopkSmem<THREADS> radix;
 };
@@ -310,6 +311,80 @@ FM_DEV T block_select(const T* a, int n, int r, T lo, T hi, uint32_t loose, Sele
     if (shift == 0 || in_digit == need || in_digit <= loose) break;
   }
   return prefix;
+}
+
+// Steps 3 and 4 of the select, shared by block_topk and block_topk_segmax:
+// the exact kk-th largest composite T among the cnt candidates in sm.cand
+// (every one of them in [theta, sm.cmax]), then every candidate >= T written
+// in index order, and -1 / -inf in positions kk .. k-1.  Rows of at most
+// BITMAP_N scores emit through sm.u.bitmap, whose first (n + 31) / 32 words
+// the caller has cleared.  All threads call it.
+template <int THREADS, int CAP, typename IdxMap, int RUNS, int BITMAP_N>
+FM_DEV void block_topk_emit(TopkFastSmem<THREADS, CAP, RUNS, BITMAP_N>& sm, int cnt, unsigned long long theta, int n,
+                            int kk, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
+                            float* __restrict__ score_out) {
+  constexpr int kTopkBitmapN = BITMAP_N;
+  const int tid = threadIdx.x;
+  // ---- 3. exact select among the candidates -------------------------------------
+  // every candidate lies in [theta, cmax]
+  const unsigned long long T = block_select<THREADS>(sm.cand, cnt, kk, theta, sm.cmax, 0u, sm.sel);
+  // ---- 4. emit in index order -------------------------------------------------
+  if (n <= kTopkBitmapN) {
+    const int words = (n + 31) >> 5;
+    for (int i = tid; i < cnt; i += THREADS) {
+      const unsigned long long c = sm.cand[i];
+      if (c >= T) {
+        const uint32_t idx = ~(uint32_t)c;
+        atomicOr(&sm.u.bitmap[idx >> 5], 1u << (idx & 31));
+      }
+    }
+    __syncthreads();
+    const int per = (words + THREADS - 1) / THREADS;  // consecutive words per thread
+    const int w0 = tid * per;
+    uint32_t mine = 0;
+    for (int j = 0; j < per; ++j)
+      if (w0 + j < words) mine += (uint32_t)__popc(sm.u.bitmap[w0 + j]);
+    uint32_t tot;
+    sm.tpre[tid] = block_excl_scan<THREADS>(mine, sm.radix.warp_tot, &tot);
+    __syncthreads();
+    for (int i = tid; i < cnt; i += THREADS) {
+      const unsigned long long c = sm.cand[i];
+      if (c >= T) {
+        const uint32_t idx = ~(uint32_t)c;
+        const int w = (int)(idx >> 5), owner = w / per;
+        uint32_t pos = sm.tpre[owner] + (uint32_t)__popc(sm.u.bitmap[w] & ((1u << (idx & 31)) - 1u));
+        for (int w2 = owner * per; w2 < w; ++w2) pos += (uint32_t)__popc(sm.u.bitmap[w2]);
+        idx_out[pos] = idx_map((int)idx);
+        if (score_out) score_out[pos] = key_float((uint32_t)(c >> 32));
+      }
+    }
+  } else {
+    if (tid == 0) sm.count = 0;
+    __syncthreads();
+    for (int i = tid; i < cnt; i += THREADS) {
+      const unsigned long long c = sm.cand[i];
+      if (c >= T) {
+        // re-key by index: ascending index == descending ~index
+        const uint32_t slot = atomicAdd(&sm.count, 1u);
+        sm.u.sel[slot] = ((unsigned long long)(uint32_t)c << 32) | (c >> 32);
+      }
+    }
+    __syncthreads();
+    const int K2 = next_pow2(kk);
+    for (int i = kk + tid; i < K2; i += THREADS) sm.u.sel[i] = 0ull;
+    __syncthreads();
+    bitonic_desc<THREADS>(sm.u.sel, K2);
+    for (int p = tid; p < kk; p += THREADS) {
+      const unsigned long long c = sm.u.sel[p];
+      const int i = (int)(~(uint32_t)(c >> 32));
+      idx_out[p] = idx_map(i);
+      if (score_out) score_out[p] = key_float((uint32_t)c);
+    }
+  }
+  for (int p = kk + tid; p < k; p += THREADS) {
+    idx_out[p] = -1;
+    if (score_out) score_out[p] = -INFINITY;
+  }
 }
 
 template <int THREADS, int CAP, typename IdxMap, int RUNS = kTopkRuns, int BITMAP_N = kTopkBitmapN>
@@ -491,67 +566,227 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   }
   r_aim = r_next;
   }  // attempts
-  const int cnt = (int)sm.count;
-  // ---- 3. exact select among the candidates -------------------------------------
-  // every candidate lies in [theta, cmax]
-  const unsigned long long T = block_select<THREADS>(sm.cand, cnt, kk, theta, sm.cmax, 0u, sm.sel);
-  // ---- 4. emit in index order -------------------------------------------------
-  if (n <= kTopkBitmapN) {
-    const int words = (n + 31) >> 5;
-    for (int i = tid; i < cnt; i += THREADS) {
-      const unsigned long long c = sm.cand[i];
-      if (c >= T) {
-        const uint32_t idx = ~(uint32_t)c;
-        atomicOr(&sm.u.bitmap[idx >> 5], 1u << (idx & 31));
-      }
+  block_topk_emit(sm, (int)sm.count, theta, n, kk, k, idx_map, idx_out, score_out);
+}
+
+// A segment entry e -- of the 32 scores 32g .. 32g+31 of a row that lie below
+// its length, the largest bit pattern read as a signed integer (what the
+// prefill score kernel writes) -- gives two keys:
+//  - seg_floor_key: the key of one of those scores.  Unless e is a NaN it is
+//    one of their bit patterns; a NaN gives 0, below every score's key.
+//  - seg_ceil_key: a key no smaller than any of theirs.  With e >= 0 (not
+//    NaN), no pattern with the sign bit clear exceeds e, so e is the largest
+//    score and every negative score, -0 and NaN (which float_key ranks as
+//    -inf) keys lower.  With e < 0 every score has its sign bit set, so none
+//    keys above +0.  A NaN entry bounds nothing: ~0.
+FM_DEV uint32_t seg_floor_key(int32_t e) {
+  const float f = __int_as_float(e);
+  return f != f ? 0u : float_key(f);
+}
+FM_DEV uint32_t seg_ceil_key(int32_t e) {
+  const float f = __int_as_float(e);
+  if (f != f) return ~0u;
+  return float_key(e < 0 ? 0.0f : f);
+}
+
+// Exact top-k of a row of n scores that comes with its segment entries
+// segmax[0 .. ceil(n/32)) (above): same output as block_topk.
+//   1. tau = the kk-th largest floor key over the segments.  kk distinct
+//      segments each hold a score keyed >= tau, so the kk-th largest score
+//      keys >= tau: no score below tau can be selected.
+//   2. Every score keyed >= tau lies in a segment whose ceiling key is
+//      >= tau; those segments are listed (for kk = 512 of 2048 segments,
+//      about a quarter of the row).
+//   3. One pass over the listed segments keeps every score keyed >= tau as a
+//      candidate (for independent scores, ~1.15 kk of them).
+//   4. The exact select and the emission of block_topk among the candidates
+//      (ties resolve to the lower index as there: all tied scores are in).
+// Rows with fewer than 2 kk segments, more segments than the sample space
+// holds, or more candidates than the list, take block_topk on the whole row.
+template <int THREADS, int CAP, typename IdxMap, int RUNS = kTopkRuns, int BITMAP_N = kTopkBitmapN>
+FM_DEV void block_topk_segmax(const float* __restrict__ row, int n, int k, const int32_t* __restrict__ segmax,
+                              bool ld4, IdxMap idx_map, int32_t* __restrict__ idx_out, float* __restrict__ score_out,
+                              TopkFastSmem<THREADS, CAP, RUNS, BITMAP_N>& sm) {
+  constexpr int kSegCap = 2 * RUNS * 64;   // entries of sm.u.sample32
+  constexpr int kPer = kSegCap / THREADS;  // segment entries per thread
+  constexpr int kU = 16;                   // segments in flight per warp
+  constexpr int kWarps = THREADS / 32;
+  static_assert(kPer <= 32 && kPer * THREADS == kSegCap, "segment entries per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kk = n < k ? n : k;
+  const int nseg = (n + 31) >> 5;
+  if (kk == 0 || nseg < 2 * kk || nseg > kSegCap || n > BITMAP_N) {
+    block_topk<THREADS, CAP, IdxMap, RUNS, BITMAP_N>(row, n, k, idx_map, idx_out, score_out, sm);
+    return;
+  }
+  // ---- 1. tau -------------------------------------------------------------------
+  // thread t holds the entries of segments t, t + THREADS, ...
+  uint32_t* keys = sm.u.sample32;
+  if (tid == 0) {
+    sm.klo = ~0u;
+    sm.khi = 0u;
+    sm.nlist = 0u;
+  }
+  int32_t e[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int g = tid + j * THREADS;
+    e[j] = g < nseg ? __ldg(segmax + g) : 0;
+  }
+  uint32_t lo = ~0u, hi = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int g = tid + j * THREADS;
+    if (g < nseg) {
+      const uint32_t f = seg_floor_key(e[j]);
+      keys[g] = f;
+      lo = f < lo ? f : lo;
+      hi = f > hi ? f : hi;
     }
-    __syncthreads();
-    const int per = (words + THREADS - 1) / THREADS;  // consecutive words per thread
-    const int w0 = tid * per;
-    uint32_t mine = 0;
-    for (int j = 0; j < per; ++j)
-      if (w0 + j < words) mine += (uint32_t)__popc(sm.u.bitmap[w0 + j]);
-    uint32_t tot;
-    sm.tpre[tid] = block_excl_scan<THREADS>(mine, sm.radix.warp_tot, &tot);
-    __syncthreads();
-    for (int i = tid; i < cnt; i += THREADS) {
-      const unsigned long long c = sm.cand[i];
-      if (c >= T) {
-        const uint32_t idx = ~(uint32_t)c;
-        const int w = (int)(idx >> 5), owner = w / per;
-        uint32_t pos = sm.tpre[owner] + (uint32_t)__popc(sm.u.bitmap[w] & ((1u << (idx & 31)) - 1u));
-        for (int w2 = owner * per; w2 < w; ++w2) pos += (uint32_t)__popc(sm.u.bitmap[w2]);
-        idx_out[pos] = idx_map((int)idx);
-        if (score_out) score_out[pos] = key_float((uint32_t)(c >> 32));
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  __syncthreads();  // klo / khi / nlist initialised
+  if (lane == 0) {
+    atomicMin(&sm.klo, lo);
+    atomicMax(&sm.khi, hi);
+  }
+  __syncthreads();
+  // loose: a tau a little below the exact kk-th key is still a bound (a few
+  // more segments listed); the select skips the bits that every key shares
+  const uint32_t tau = block_select<THREADS>(keys, nseg, kk, sm.klo, sm.khi, 64u, sm.sel);
+  // ---- 2. the listed segments (in no particular order: ids leave in index
+  // order through the bitmap) ---------------------------------------------------
+  const bool vec = ld4 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  uint32_t flags = 0;  // bit j: segment tid + j * THREADS is listed
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int g = tid + j * THREADS;
+    if (g < nseg && seg_ceil_key(e[j]) >= tau) flags |= 1u << j;
+  }
+  {
+    // one warp scan and one shared-memory atomic per warp place the entries;
+    // no thread reads keys[] once the select has returned
+    const uint32_t c = (uint32_t)__popc(flags);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t base = 0;
+    if (lane == 31 && total > 0u) base = atomicAdd(&sm.nlist, total);
+    uint32_t pos = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+    while (flags) {
+      const int j = __ffs(flags) - 1;
+      flags &= flags - 1u;
+      const int g = tid + j * THREADS;
+      keys[pos++] = (uint32_t)g;
+    }
+  }
+  if (tid == 0) {
+    sm.count = 0;
+    sm.overflow = 0;
+    sm.cmax = 0ull;
+  }
+  __syncthreads();
+  // ---- 3. candidates: every score of a listed segment keyed >= tau --------------
+  // A score keys >= tau exactly when it is >= tau's float (-0 == +0 as their
+  // keys); with tau at or below the key of -inf (where NaN ranks) the keys are
+  // compared instead.  With ld4 (the row's allocated length a multiple of 4)
+  // and the row on a 16-byte boundary, four segments are read per float4 load
+  // (eight lanes each), else one per scalar load.
+  const int m = (int)sm.nlist;
+  const bool take_all = tau <= 0x007FFFFFu;
+  const float tau_f = take_all ? -INFINITY : key_float(tau);
+  unsigned long long tmax = 0ull;
+  auto passes = [&](float x, int i) -> bool {
+    return i < n && (take_all ? float_key(x) >= tau : x >= tau_f);
+  };
+  // `c` list slots for this lane (most lanes have none: one shared-memory
+  // atomic each for the rest beats a warp scan's chain of shuffles)
+  auto reserve = [&](uint32_t c) -> uint32_t { return c ? atomicAdd(&sm.count, c) : 0u; };
+  auto store = [&](uint32_t slot, float x, int i) {
+    const unsigned long long cv = ((unsigned long long)float_key(x) << 32) | (uint32_t)(~(uint32_t)i);
+    if (slot < (uint32_t)CAP) {
+      sm.cand[slot] = cv;
+      tmax = cv > tmax ? cv : tmax;
+    } else {
+      sm.overflow = 1;
+    }
+  };
+  if (vec) {
+    // a float4 starting at a multiple of 4 below n stays inside the row
+    constexpr int kLoads = kU / 4;
+    const int sub = lane >> 3, part = (lane & 7) * 4;
+    for (int j0 = warp * kU; j0 < m; j0 += kWarps * kU) {  // warp-uniform trip count
+      float4 v[kLoads];
+      int base[kLoads];
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int j = j0 + 4 * u + sub;
+        base[u] = j < m ? (int)keys[j] * 32 + part : n;
+        v[u] = base[u] < n ? __ldg(reinterpret_cast<const float4*>(row + base[u]))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      uint32_t mask = 0;  // bit 4u + e: element e of v[u] is a candidate
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u)
+        mask |= ((uint32_t)passes(v[u].x, base[u]) | ((uint32_t)passes(v[u].y, base[u] + 1) << 1) |
+                 ((uint32_t)passes(v[u].z, base[u] + 2) << 2) | ((uint32_t)passes(v[u].w, base[u] + 3) << 3))
+                << (4 * u);
+      // candidates are rare (~4% of the listed scores): each lane walks its
+      // own, re-reading the score (a cache hit) rather than indexing v[] at run
+      // time, which would put v in local memory
+      uint32_t slot = reserve((uint32_t)__popc(mask));
+      while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const int i = (int)keys[j0 + 4 * (b >> 2) + sub] * 32 + part + (b & 3);
+        store(slot++, __ldg(row + i), i);
       }
     }
   } else {
-    if (tid == 0) sm.count = 0;
-    __syncthreads();
-    for (int i = tid; i < cnt; i += THREADS) {
-      const unsigned long long c = sm.cand[i];
-      if (c >= T) {
-        // re-key by index: ascending index == descending ~index
-        const uint32_t slot = atomicAdd(&sm.count, 1u);
-        sm.u.sel[slot] = ((unsigned long long)(uint32_t)c << 32) | (c >> 32);
+    for (int j0 = warp * kU; j0 < m; j0 += kWarps * kU) {  // warp-uniform trip count
+      float v[kU];
+      int idx[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = j0 + u;
+        idx[u] = j < m ? (int)keys[j] * 32 + lane : n;
+        v[u] = idx[u] < n ? __ldg(row + idx[u]) : 0.f;
+      }
+      uint32_t mask = 0;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) mask |= (uint32_t)passes(v[u], idx[u]) << u;
+      uint32_t slot = reserve((uint32_t)__popc(mask));
+      while (mask) {
+        const int u = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const int i = (int)keys[j0 + u] * 32 + lane;
+        store(slot++, __ldg(row + i), i);
       }
     }
-    __syncthreads();
-    const int K2 = next_pow2(kk);
-    for (int i = kk + tid; i < K2; i += THREADS) sm.u.sel[i] = 0ull;
-    __syncthreads();
-    bitonic_desc<THREADS>(sm.u.sel, K2);
-    for (int p = tid; p < kk; p += THREADS) {
-      const unsigned long long c = sm.u.sel[p];
-      const int i = (int)(~(uint32_t)(c >> 32));
-      idx_out[p] = idx_map(i);
-      if (score_out) score_out[p] = key_float((uint32_t)c);
-    }
   }
-  for (int p = kk + tid; p < k; p += THREADS) {
-    idx_out[p] = -1;
-    if (score_out) score_out[p] = -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, tmax, o);
+    tmax = y > tmax ? y : tmax;
   }
+  if (lane == 0 && tmax != 0ull) atomicMax(&sm.cmax, tmax);
+  __syncthreads();
+  const int cnt = (int)sm.count;
+  if (sm.overflow || cnt < kk) {  // cnt >= kk always holds (step 1); overflow: a row of clustered maxima
+    __syncthreads();
+    block_topk<THREADS, CAP, IdxMap, RUNS, BITMAP_N>(row, n, k, idx_map, idx_out, score_out, sm);
+    return;
+  }
+  // ---- 4. the list is dead: its space becomes the (cleared) bitmap ---------------
+  const int words = (n + 31) >> 5;
+  for (int i = tid; i < words; i += THREADS) sm.u.bitmap[i] = 0u;
+  __syncthreads();
+  block_topk_emit(sm, cnt, (unsigned long long)tau << 32, n, kk, k, idx_map, idx_out, score_out);
 }
 
 }  // namespace fm
