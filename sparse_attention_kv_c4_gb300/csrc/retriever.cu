@@ -107,29 +107,6 @@ __global__ void __launch_bounds__(kPrepThreads)
   split_query(q + bl * NH * kDim, w + bl * NH, NH, kPrepThreads, t1, t1 + NH * kDim, wq + bl * NH);
 }
 
-// Position of a pair's j-th layer-tile: tile t = t_begin + pair + 2i of
-// request b, tile index `tile` within it, layer l (j = i*L + l).
-struct Cursor {
-  int64_t t, b;
-  int tile, l;
-  FM_DEV void init(int64_t t0, int tiles_per_b) {
-    t = t0;
-    b = t0 / tiles_per_b;
-    tile = (int)(t0 % tiles_per_b);
-    l = 0;
-  }
-  FM_DEV void next(int L, int tiles_per_b) {
-    if (++l < L) return;
-    l = 0;
-    t += kPairs;
-    tile += kPairs;
-    while (tile >= tiles_per_b) {
-      tile -= tiles_per_b;
-      ++b;
-    }
-  }
-};
-
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     retriever_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
@@ -311,96 +288,103 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t words = (p.S + 31) / 32;
     float* w_mine = w_smem[warp - kFirstEpiWarp];
     const int64_t span = t_end - t_begin;
-    const int64_t n_lt = (span > group ? (span - group + kPairs - 1) / kPairs : 0) * L;  // the pair's layer-tiles
+    const int64_t n_tiles = span > group ? (span - group + kPairs - 1) / kPairs : 0;  // the pair's tiles
 
-    // score one layer-tile (the cursor's) and, at its last layer, the chunk
-    Cursor cc;
-    cc.init(t_begin + group, p.tiles_per_b);
+    // The pair's tiles t_begin + group + 2i in order, each scored layer by
+    // layer: the request, the tile's rows and output pointers are set once per
+    // tile, so a layer-tile carries little besides its own waits and dots.
+    int64_t b = (t_begin + group) / p.tiles_per_b;
+    int tile = (int)((t_begin + group) % p.tiles_per_b);
     uint32_t dacc = 0, d_phase = 0, sslot = 0, s_phase = 0;
     int64_t w_b = -1;
-    float acc_m = -INFINITY, acc_sum = 0.f;
-    auto compute = [&]() -> bool {
-      const int64_t b = cc.b;
-      const int l = cc.l;
+    bool ok = true;
+    for (int64_t i = 0; i < n_tiles && ok; ++i) {
       if (b != w_b) {  // a new request: its weights into this warp's copy
         __syncwarp();
-        for (int i = lane; i < L * NH; i += 32) w_mine[i] = __ldg(p.wq + b * L * NH + i);
+        for (int k = lane; k < L * NH; k += 32) w_mine[k] = __ldg(p.wq + b * L * NH + k);
         __syncwarp();
         w_b = b;
       }
-      // the chunk's scale, from the unpack group (>= 0: a negative scale's
-      // sign went into the key bytes)
-      const int si = group * kSSlots + (int)sslot;
-      if (!mbar_wait(&bar_sfull[si], s_phase, &abort_flag, p.status)) return false;
-      const float sc = scale_ring[si][row];
-      mbar_arrive(&bar_sempty[si]);
-      if (++sslot == (uint32_t)kSSlots) {
-        sslot = 0;
-        s_phase ^= 1u;
-      }
-      const int di = group * C::kDAccs + (int)dacc;
-      if (!mbar_wait(&bar_tfull[di], d_phase, &abort_flag, p.status)) return false;
-      tc_fence_after();
-      const uint32_t taddr = lane_base + kASlots * kACols + dacc * NH;
-      const float4* wl = reinterpret_cast<const float4*>(w_mine + l * NH);
-      float y = 0.f;
-#pragma unroll
-      for (int c = 0; c < NH / 32; ++c) {  // 32 heads at a time
-        uint32_t r[32];
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
-        if (c == NH / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(&bar_tempty[di]);  // the dots are in registers: the MMA may reuse the accumulator
-        }
-        // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w, and
-        // ReLU(sc d) = sc ReLU(d) for sc >= 0: one multiply per chunk
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 wv = wl[c * 8 + h / 4];
-          x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
-          x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
-          x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
-          x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
-        }
-        y += sc * ((x0 + x1) + (x2 + x3));
-      }
-      if (++dacc == (uint32_t)C::kDAccs) {
-        dacc = 0;
-        d_phase ^= 1u;
-      }
-      const int64_t s = (int64_t)cc.tile * kM + row;
+      const int64_t s = (int64_t)tile * kM + row;
       const bool valid = s < p.S;
-      if (p.logits != nullptr && valid) p.logits[(b * L + l) * p.S + s] = y;
-      if (l == 0) {
-        acc_m = -INFINITY;
-        acc_sum = 0.f;
-      }
-      if (p.mode == 0)
-        acc_m = fmaxf(acc_m, y);
-      else
-        acc_sum += 1.0f / (1.0f + expf(-y));
-      if (l == L - 1) {  // the ensemble over the tile's layers
-        float e;
-        bool res;
-        if (p.mode == 0) {  // max of sigmoids = sigmoid of the max: compare the logit
-          e = 1.0f / (1.0f + expf(-acc_m));
-          res = valid && acc_m >= p.thr_logit;
-        } else {
-          e = acc_sum / (float)L;
-          res = valid && e >= p.thr;
+      float* const lg = p.logits != nullptr ? p.logits + b * L * p.S + s : nullptr;
+      float acc_m = -INFINITY, acc_sum = 0.f;
+      for (int l = 0; l < L; ++l) {
+        // the chunk's scale, from the unpack group (>= 0: a negative scale's
+        // sign went into the key bytes)
+        const int si = group * kSSlots + (int)sslot;
+        if (!mbar_wait(&bar_sfull[si], s_phase, &abort_flag, p.status)) {
+          ok = false;
+          break;
         }
-        const uint32_t bits = __ballot_sync(0xffffffffu, res);
-        const int64_t word = (int64_t)cc.tile * (kM / 32) + quad;
-        if (lane == 0 && word < words) p.mask[b * words + word] = bits;
-        if (p.ens != nullptr && valid) p.ens[b * p.S + s] = e;
+        const float sc = scale_ring[si][row];
+        mbar_arrive(&bar_sempty[si]);
+        if (++sslot == (uint32_t)kSSlots) {
+          sslot = 0;
+          s_phase ^= 1u;
+        }
+        const int di = group * C::kDAccs + (int)dacc;
+        if (!mbar_wait(&bar_tfull[di], d_phase, &abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = lane_base + kASlots * kACols + dacc * NH;
+        const float4* wl = reinterpret_cast<const float4*>(w_mine + l * NH);
+        float y = 0.f;
+#pragma unroll
+        for (int c = 0; c < NH / 32; ++c) {  // 32 heads at a time
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_ld_wait();
+          if (c == NH / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bar_tempty[di]);  // the dots are in registers: the MMA may reuse the accumulator
+          }
+          // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w, and
+          // ReLU(sc d) = sc ReLU(d) for sc >= 0: one multiply per chunk
+          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 wv = wl[c * 8 + h / 4];
+            x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
+            x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
+            x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
+            x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
+          }
+          y += sc * ((x0 + x1) + (x2 + x3));
+        }
+        if (++dacc == (uint32_t)C::kDAccs) {
+          dacc = 0;
+          d_phase ^= 1u;
+        }
+        if (lg != nullptr && valid) lg[l * p.S] = y;
+        if (p.mode == 0)
+          acc_m = fmaxf(acc_m, y);
+        else
+          acc_sum += 1.0f / (1.0f + expf(-y));
       }
-      cc.next(L, p.tiles_per_b);
-      return true;
-    };
-    for (int64_t j = 0; j < n_lt; ++j)
-      if (!compute()) break;
+      if (!ok) break;
+      // the ensemble over the tile's layers
+      float e;
+      bool res;
+      if (p.mode == 0) {  // max of sigmoids = sigmoid of the max: compare the logit
+        e = 1.0f / (1.0f + expf(-acc_m));
+        res = valid && acc_m >= p.thr_logit;
+      } else {
+        e = acc_sum / (float)L;
+        res = valid && e >= p.thr;
+      }
+      const uint32_t bits = __ballot_sync(0xffffffffu, res);
+      const int64_t word = (int64_t)tile * (kM / 32) + quad;
+      if (lane == 0 && word < words) p.mask[b * words + word] = bits;
+      if (p.ens != nullptr && valid) p.ens[b * p.S + s] = e;
+      tile += kPairs;
+      while (tile >= p.tiles_per_b) {
+        tile -= p.tiles_per_b;
+        ++b;
+      }
+    }
   } else {
     // ------------------------------ unpack group --------------------------------
     // Every layer-tile of the CTA, in order (tile i belongs to pair i % 2):
