@@ -2,10 +2,11 @@
 segments of 32 chunks below the causal limit), against the oracle: the pruned
 path itself, each of its fallbacks (too few segments, more segments than the
 select holds, a candidate list that overflows on clustered scores), rows of
-negative scores and rows of exact ties."""
+negative scores, rows of exact ties and rows with NaN and infinite scores."""
 import numpy as np
 import pytest
 
+import parity
 from test_prefill_gpu import check, run_prefill, small
 
 pytestmark = pytest.mark.gpu
@@ -82,3 +83,45 @@ def test_segmax_exact_ties(torch_dev, orc):
     check(orc, q, w, pos, K, idx, sc, k)
     assert (idx == np.arange(k, dtype=np.int32)[None, :]).all()
     assert (sc == 0).all()
+
+
+def test_segmax_nonfinite_scores(torch_dev, orc):
+    """Three chunk keys with +inf in one element.  Their dots are ±inf, so
+    with mixed-sign head weights (tokens 0-2) their score is NaN in every row
+    (ranked as -inf: never selected while finite scores remain), and with
+    non-negative weights (tokens 3-5) +inf (selected first).  The segments
+    holding them carry NaN / +inf entries through the pruned select.  Token 6
+    has a NaN head weight, so every score of its row is NaN: all of them tie
+    at -inf and the lowest chunk ids are selected."""
+    torch, dev = torch_dev
+    T, S, k = 7, 20000, 64
+    q, w, pos, K = small(T, S, seed=123)
+    K = K.copy()
+    special = [5, 4100, 13377]
+    K[special, 0] = 0x7F80  # bf16 +inf
+    w = w.copy()
+    w[3:6] = np.abs(w[3:6])
+    w[6, 0] = np.nan
+    idx, sc = run_prefill(torch, dev, q, w, pos, K, k)
+    ref_idx, _ = orc.prefill_topk(q, w, pos, K, k=k)
+    assert (ref_idx[6] == np.arange(k)).all() and (idx[6] == np.arange(k)).all()
+    assert np.all(~(sc[6] > -np.inf))  # NaN scores rank as -inf
+    for t in range(6):
+        x = {int(i): orc.score_bf16(q[t], w[t], K[int(i)]) for i in set(idx[t]) | set(ref_idx[t]) if i >= 0}
+        if t < 3:
+            assert all(np.isnan(orc.score_bf16(q[t], w[t], K[s])) for s in special)
+            assert not set(special) & set(int(i) for i in idx[t])
+        else:
+            assert all(np.isposinf(orc.score_bf16(q[t], w[t], K[s])) for s in special)
+            assert set(special) <= set(int(i) for i in idx[t])
+        got, ref = set(int(i) for i in idx[t]), set(int(i) for i in ref_idx[t])
+        assert list(idx[t]) == sorted(got) and len(got) == k
+        finite_ref = [x[i] for i in ref if np.isfinite(x[i])]
+        kth = min(finite_ref)
+        for i in got ^ ref:  # only near-ties at the k-th score may differ
+            assert np.isfinite(x[i]) and abs(x[i] - kth) <= parity.tol(kth), (t, i, x[i], kth)
+        for j, i in enumerate(idx[t]):
+            if np.isfinite(x[int(i)]):
+                parity.assert_logits_close([sc[t, j]], [x[int(i)]], what="top-k scores")
+            else:
+                assert sc[t, j] == x[int(i)]
