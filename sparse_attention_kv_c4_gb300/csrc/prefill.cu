@@ -262,13 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       w_smem[warp - kFirstEpiWarp][lane] = __ldg(wsrc + lane);
       w_smem[warp - kFirstEpiWarp][lane + 32] = __ldg(wsrc + lane + 32);
       __syncwarp();
-      for (int ct = ct0; ct < ct_stop; ++ct) {
-        if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) {
-          aborted = true;
-          break;
-        }
+      // tiles in pairs, so the accumulator index (and with it the barrier and
+      // TMEM addresses) is a constant in each copy of the body
+      auto tile_body = [&](const int ct, const uint32_t ai, const uint32_t ph) -> bool {
+        if (!mbar_wait(&bar_tfull[ai], ph, &abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHeads;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + ai * kN + j * kHeads;
         // both halves of the row in flight at once, one wait, then the
         // accumulator is released before the arithmetic
         uint32_t r0[32], r1[32];
@@ -276,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(taddr + 32, r1);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&bar_tempty[acc]);
+        mbar_arrive(&bar_tempty[ai]);
         const float4* w4 = reinterpret_cast<const float4*>(w_smem[warp - kFirstEpiWarp]);
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, x4 = 0.f, x5 = 0.f, x6 = 0.f, x7 = 0.f;
 #pragma unroll
@@ -305,8 +304,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = __reduce_max_sync(0xffffffffu, valid ? __float_as_int(y) : INT_MIN);
           if (lane == 0 && valid) srow[ct * 4] = m;
         }
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        return true;
+      };
+      int ct = ct0;
+      if (acc == 1u && ct < ct_stop) {  // the second tile of a pair begun in an earlier block
+        if (!tile_body(ct, 1u, acc_phase)) {
+          aborted = true;
+          break;
+        }
+        ++ct;
+        acc = 0u;
+        acc_phase ^= 1u;
+      }
+      for (; ct + 1 < ct_stop; ct += 2) {
+        if (!tile_body(ct, 0u, acc_phase) || !tile_body(ct + 1, 1u, acc_phase)) {
+          aborted = true;
+          break;
+        }
+        acc_phase ^= 1u;
+      }
+      if (!aborted && ct < ct_stop) {
+        if (!tile_body(ct, 0u, acc_phase))
+          aborted = true;
+        else
+          acc = 1u;
       }
     }
   }
