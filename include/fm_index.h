@@ -164,7 +164,7 @@ fm_status fm_memindex_score_mask_fp8(const uint16_t* q, const float* w, const ui
  *   ens_out       [B, S] fp32 e[b,s], or NULL
  *   logits_out    [B, L, S] fp32 x, or NULL
  *   workspace     >= fm_retriever_workspace(B, L, n_h) bytes, 256-byte aligned
- *                 (the split query and weights: 32.5 KB per (request, layer)
+ *                 (the split query and weights: 36.5 KB per (request, layer)
  *                 at 128 heads)
  * Errors: FM_ERR_INVALID_ARG for n_h not 64/128, d != 128, L outside 1..4,
  * S % 4 != 0, a bad ensemble, threshold, pointer or stride; FM_ERR_WORKSPACE

@@ -60,7 +60,6 @@ constexpr int kDim = 128;                  // E4M3 key bytes per chunk
 constexpr int kRowBytes = kDim + 4;        // packed compressed_k row
 constexpr int kRowWords = kRowBytes / 4;   // 33
 constexpr int kTileBytes = kM * kRowBytes;  // 16,896 bytes per layer-tile
-constexpr int kMaxL = 4;
 constexpr int kPairs = 2;
 constexpr int kMmaWarps = kPairs;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
@@ -75,11 +74,28 @@ constexpr int kMaxRing = 6;                // key stages per pair
 constexpr int kMaxDAccs = 3;
 constexpr int kPrepThreads = 256;
 
-template <int NH>
+// kLin: the linear half of the ReLU on the tensor core.  With ReLU(d) =
+// (d + |d|) / 2 a chunk's score is sc/2 (q_w . k + sum_h w'_h |d_h|), where
+// q_w = sum_h w_h q_h; q_w is split into four E4M3 terms (two per power of
+// two), one row of each term block of B, so the MMA leaves q_w . k in two more
+// accumulator columns and the epilogue has one FFMA (|d| folded in) per head.
+template <int NH, bool kLin>
 struct Cfg {
-  static constexpr int kDAccs = (kPairCols - kASlots * kACols) / NH;  // 1 for 128 heads, 3 for 64
-  static constexpr int kQLayerBytes = 2 * NH * kDim;                  // t1 and t2 rows of one layer
+  static constexpr int kBRows = NH + (kLin ? 16 : 0);                  // B rows per term block: the MMA's N
+  static constexpr int kQTermBytes = kBRows * kDim;                   // the t1 block, then the t2 block
+  static constexpr int kQLayerBytes = 2 * kQTermBytes;
+  static constexpr int kDAccs = (kPairCols - kASlots * kACols) / kBRows;  // 1 for 128 heads, 3 for 64
+  static constexpr int kWStride = NH + (kLin ? 4 : 0);  // floats per (request, layer) of wq: w', then 2^e1, 2^e2
+  static constexpr int kMaxL = kLin ? 3 : 4;             // layers the launch takes (the launcher picks kLin by L)
 };
+
+// Two consecutive 32-bit TMEM columns: thread i gets lane (base + i).
+FM_DEV void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(taddr)
+               : "memory");
+}
 
 struct Params {
   const uint8_t* ck;         // packed rows
@@ -98,19 +114,72 @@ struct Params {
   float thr, thr_logit;
 };
 
-template <int NH>
+template <int NH, bool kLin>
 __global__ void __launch_bounds__(kPrepThreads)
     retriever_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w, uint8_t* __restrict__ qsplit,
                           float* __restrict__ wq) {
+  using C = Cfg<NH, kLin>;
   const int64_t bl = blockIdx.x;
-  uint8_t* t1 = qsplit + bl * Cfg<NH>::kQLayerBytes;
-  split_query(q + bl * NH * kDim, w + bl * NH, NH, kPrepThreads, t1, t1 + NH * kDim, wq + bl * NH);
+  uint8_t* t1 = qsplit + bl * C::kQLayerBytes;
+  uint8_t* t2 = t1 + C::kQTermBytes;
+  float* wl = wq + bl * C::kWStride;
+  split_query(q + bl * NH * kDim, w + bl * NH, NH, kPrepThreads, t1, t2, wl);
+  if constexpr (kLin) {
+    // q_w[j] = sum_h w_h q_h[j] (fp32, heads in order); with 2^e1 putting
+    // max|q_w| in (224, 448]: u1 = RNE(q_w 2^-e1), u2 = RNE(rest), then the
+    // rest after those two times 2^8 the same way (u3, u4), so q_w =
+    // 2^e1 (u1 + u2) + 2^(e1-8) (u3 + u4) to within 2^-18 of max|q_w|.
+    // Rows NH (u1 | u2) and NH+1 (u3 | u4) of the t1 | t2 blocks, zeros in
+    // rows NH+2 .. NH+15.
+    __shared__ float red[kPrepThreads / 32];
+    const int j = threadIdx.x;
+    float qw = 0.f;
+    if (j < kDim) {
+      const uint16_t* qb = q + bl * NH * kDim + j;
+      for (int h = 0; h < NH; ++h)
+        qw = fmaf(__ldg(w + bl * NH + h), __uint_as_float((uint32_t)__ldg(qb + (int64_t)h * kDim) << 16), qw);
+    }
+    float m = fabsf(qw);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((j & 31) == 0) red[j >> 5] = m;
+    __syncthreads();
+    float amax = 0.f;
+    for (int i = 0; i < kPrepThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    int e = 0;
+    if (amax > 0.f && isfinite(amax)) {
+      e = ilogbf(amax) - 8;
+      if (ldexpf(amax, -e) > 448.f) e += 1;
+    }
+    if (j < kDim) {
+      const float s1 = ldexpf(qw, -e);
+      const uint32_t u1 = e4m3_rne(s1);
+      const float r1 = s1 - e4m3_value(u1);
+      const uint32_t u2 = e4m3_rne(r1);
+      const float s2 = (r1 - e4m3_value(u2)) * 256.f;
+      const uint32_t u3 = e4m3_rne(s2);
+      const uint32_t u4 = e4m3_rne(s2 - e4m3_value(u3));
+      t1[NH * kDim + j] = (uint8_t)u1;
+      t2[NH * kDim + j] = (uint8_t)u2;
+      t1[(NH + 1) * kDim + j] = (uint8_t)u3;
+      t2[(NH + 1) * kDim + j] = (uint8_t)u4;
+    }
+    for (int i = threadIdx.x; i < 14 * kDim; i += kPrepThreads) {
+      t1[(NH + 2) * kDim + i] = 0;
+      t2[(NH + 2) * kDim + i] = 0;
+    }
+    if (threadIdx.x == 0) {
+      wl[NH] = ldexpf(1.f, e);
+      wl[NH + 1] = ldexpf(1.f, e - 8);
+      wl[NH + 2] = 0.f;
+      wl[NH + 3] = 0.f;
+    }
+  }
 }
 
-template <int NH>
+template <int NH, bool kLin>
 __global__ void __launch_bounds__(kThreads, 1)
     retriever_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
-  using C = Cfg<NH>;
+  using C = Cfg<NH, kLin>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_smem = smem;
@@ -124,9 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float scale_ring[kPairs * kSSlots][kM];  // each chunk's (non-negative) scale, per layer-tile
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  // one copy of the current request's head weights per epilogue warp, so a
-  // warp refreshes its own copy with __syncwarp alone
-  __shared__ __align__(16) float w_smem[kPairs * 4][kMaxL * NH];
+  // one copy of the current request's weights per scoring warp, so a warp
+  // refreshes its own copy with __syncwarp alone (a static array: copies in
+  // dynamic shared memory measured 2.6% slower)
+  __shared__ __align__(16) float w_smem[kPairs * 4][C::kMaxL * C::kWStride];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int L = p.L, ring = p.ring;
@@ -188,8 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             q_phase ^= 1;
           }
           mbar_arrive_expect_tx(&bar_qfull, (uint32_t)(L * C::kQLayerBytes));
-          for (int l = 0; l < L; ++l)
-            tma_load_2d(q_smem + l * C::kQLayerBytes, &tmap_q, &bar_qfull, 0, (int32_t)((b * L + l) * 2 * NH));
+          for (int l = 0; l < L; ++l)  // the layer's t1 block, then its t2 block (one box of kBRows rows each)
+            for (int tb = 0; tb < 2; ++tb)
+              tma_load_2d(q_smem + l * C::kQLayerBytes + tb * C::kQTermBytes, &tmap_q, &bar_qfull, 0,
+                          (int32_t)(((b * L + l) * 2 + tb) * C::kBRows));
           q_issued = (q_issued + 1) & 1;
           cur_b = b;
         }
@@ -223,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ------------------------------ UMMA issuers ------------------------------
       const int me = warp - 1;
-      const uint32_t idesc = idesc_e4m3_f32(kM, NH);
+      const uint32_t idesc = idesc_e4m3_f32(kM, C::kBRows);
       uint32_t aslot = 0, a_phase = 0, dacc = 0, d_phase = 0, q_phase = 0;
       int64_t cur_b = -1;
       bool ok = true;
@@ -253,12 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_tmem = pair_base + aslot * kACols;
-          const uint32_t d_tmem = pair_base + kASlots * kACols + dacc * NH;
-          // B: the layer's t1 rows, then its t2 rows NH * 128 bytes later
+          const uint32_t d_tmem = pair_base + kASlots * kACols + dacc * C::kBRows;
+          // B: the layer's t1 block, then its t2 block kQTermBytes later
           // (descriptor addresses count 16-byte units); A: 8 TMEM columns
           // (32 E4M3 values per lane) per K step
           const uint64_t b_desc = b_desc0 + (uint64_t)(l * (C::kQLayerBytes >> 4));
-          constexpr uint64_t kT2 = (uint64_t)(NH * kDim) >> 4;
+          constexpr uint64_t kT2 = (uint64_t)C::kQTermBytes >> 4;
 #pragma unroll
           for (int k = 0; k < kDim / 32; ++k)
             umma_e4m3_ts(d_tmem, a_tmem + 8 * k, b_desc + 2 * k, idesc, k != 0 ? 1u : 0u);
@@ -301,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t i = 0; i < n_tiles && ok; ++i) {
       if (b != w_b) {  // a new request: its weights into this warp's copy
         __syncwarp();
-        for (int k = lane; k < L * NH; k += 32) w_mine[k] = __ldg(p.wq + b * L * NH + k);
+        for (int k = lane; k < L * C::kWStride; k += 32) w_mine[k] = __ldg(p.wq + b * L * C::kWStride + k);
         __syncwarp();
         w_b = b;
       }
@@ -329,13 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = lane_base + kASlots * kACols + dacc * NH;
-        const float4* wl = reinterpret_cast<const float4*>(w_mine + l * NH);
+        const uint32_t taddr = lane_base + kASlots * kACols + dacc * C::kBRows;
+        const float4* wl = reinterpret_cast<const float4*>(w_mine + l * C::kWStride);
         float y = 0.f;
+        uint32_t lin[2] = {0u, 0u};
+        const float scc = kLin ? 0.5f * sc : sc;  // each chunk's partial sum times the scale as it lands
 #pragma unroll
         for (int c = 0; c < NH / 32; ++c) {  // 32 heads at a time
           uint32_t r[32];
           tmem_ld32(taddr + c * 32, r);
+          if (kLin && c == 0) tmem_ld2(taddr + NH, lin);  // q_w . k in two powers of two
           tmem_ld_wait();
           if (c == NH / 32 - 1) {
             tc_fence_before();
@@ -347,12 +422,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 wv = wl[c * 8 + h / 4];
-            x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
-            x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
-            x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
-            x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
+            if constexpr (kLin) {  // w |d| (the absolute value folds into the FFMA)
+              x0 = fmaf(wv.x, fabsf(__uint_as_float(r[h])), x0);
+              x1 = fmaf(wv.y, fabsf(__uint_as_float(r[h + 1])), x1);
+              x2 = fmaf(wv.z, fabsf(__uint_as_float(r[h + 2])), x2);
+              x3 = fmaf(wv.w, fabsf(__uint_as_float(r[h + 3])), x3);
+            } else {
+              x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
+              x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
+              x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
+              x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
+            }
           }
-          y += sc * ((x0 + x1) + (x2 + x3));
+          y = fmaf(scc, (x0 + x1) + (x2 + x3), y);
+        }
+        if constexpr (kLin) {
+          const float* we = w_mine + l * C::kWStride + NH;  // 2^e1, 2^e2
+          y = fmaf(scc, fmaf(we[0], __uint_as_float(lin[0]), we[1] * __uint_as_float(lin[1])), y);
         }
         if (++dacc == (uint32_t)C::kDAccs) {
           dacc = 0;
@@ -462,8 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The split query [B*L][2 term blocks][rows][128] and the weights
+// [B*L][stride]; at 128 heads sized for the linear half's wider layout (16
+// more rows per term block, 4 more weights), which either launch fits in.
 size_t retriever_ws_bytes(int B, int L, int n_h) {
-  return align256((size_t)B * L * 2 * n_h * kDim) + align256((size_t)B * L * n_h * 4);
+  const int rows = n_h == 128 ? n_h + 16 : n_h, stride = n_h == 128 ? n_h + 4 : n_h;
+  return align256((size_t)B * L * 2 * rows * kDim) + align256((size_t)B * L * stride * 4);
 }
 
 struct RetrieverArgs {
@@ -480,36 +570,44 @@ struct RetrieverArgs {
   void* workspace;
 };
 
-template <int NH>
-fm_status launch_retriever(const RetrieverArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
-  using C = Cfg<NH>;
+// Key stages per pair that fit beside L layers of the split query (less the
+// static shared memory: the weight copies, the scale ring, the barriers); 0
+// for more layers than the configuration takes.
+template <int NH, bool kLin>
+int retriever_ring(int L) {
+  using C = Cfg<NH, kLin>;
+  if (L > C::kMaxL) return 0;
+  const int smem_cap = 227 * 1024 - (int)sizeof(float) * kPairs * 4 * C::kMaxL * C::kWStride -
+                       (int)sizeof(float) * kPairs * kSSlots * kM - 2048;
+  const int ring = (smem_cap - 1024 - L * C::kQLayerBytes) / (kPairs * kTileBytes);
+  return ring > kMaxRing ? kMaxRing : ring;
+}
+
+template <int NH, bool kLin>
+fm_status launch_retriever_cfg(const RetrieverArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
+  using C = Cfg<NH, kLin>;
   const int tiles_per_b = (int)((a.S + kM - 1) / kM);
   const int64_t total = (int64_t)a.B * tiles_per_b;
   if (total == 0) return FM_OK;
   uint8_t* qsplit = static_cast<uint8_t*>(a.workspace);
   float* wq = reinterpret_cast<float*>(qsplit + align256((size_t)a.B * a.L * C::kQLayerBytes));
-  retriever_prep_kernel<NH><<<a.B * a.L, kPrepThreads, 0, stream>>>(a.q, a.w, qsplit, wq);
+  retriever_prep_kernel<NH, kLin><<<a.B * a.L, kPrepThreads, 0, stream>>>(a.q, a.w, qsplit, wq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever prep: launch: %s", cudaGetErrorString(e));
 
   CUtensorMap tmap_q;
   {
-    // split query: rows (B*L*2*n_h) x 128 B, one box of 2*n_h rows per layer
-    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.B * a.L * 2 * NH};
+    // split query: rows (B*L*2*kBRows) x 128 B, one box per term block
+    const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.B * a.L * 2 * C::kBRows};
     const uint64_t strides[1] = {(uint64_t)kDim};
-    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)(2 * NH)};
+    const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)C::kBRows};
     fm_status st = make_tmap(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, qsplit, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != FM_OK) return st;
   }
-  // less the static shared memory: head weights, the scale ring, barriers
-  const int smem_cap = 227 * 1024 - (int)sizeof(float) * kPairs * 4 * kMaxL * NH -
-                       (int)sizeof(float) * kPairs * kSSlots * kM - 2048;
-  const int fixed = 1024 + a.L * C::kQLayerBytes;
-  int ring = (smem_cap - fixed) / (kPairs * kTileBytes);
-  if (ring > kMaxRing) ring = kMaxRing;
+  const int ring = retriever_ring<NH, kLin>(a.L);
   if (ring < 2) return set_error(FM_ERR_UNSUPPORTED, "retriever: %d key stages per pair are too few", ring);
-  const int smem = fixed + kPairs * ring * kTileBytes;
+  const int smem = 1024 + a.L * C::kQLayerBytes + kPairs * ring * kTileBytes;
 
   Params p;
   p.ck = a.ck;
@@ -528,13 +626,23 @@ fm_status launch_retriever(const RetrieverArgs& a, int num_sms, unsigned int* st
   p.mode = a.mode;
   p.thr = a.thr;
   p.thr_logit = logf(a.thr / (1.0f - a.thr));
-  e = cudaFuncSetAttribute(retriever_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(retriever_kernel<NH, kLin>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const int grid = (int)(total < num_sms ? total : num_sms);
-  retriever_kernel<NH><<<grid, kThreads, smem, stream>>>(tmap_q, p);
+  retriever_kernel<NH, kLin><<<grid, kThreads, smem, stream>>>(tmap_q, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever: launch: %s", cudaGetErrorString(e));
   return FM_OK;
+}
+
+// The linear half on the tensor core wherever it still leaves three key
+// stages per pair (128 heads, up to three layers); else the ReLU in the
+// epilogue (two stages cost 7% at three layers).
+template <int NH>
+fm_status launch_retriever(const RetrieverArgs& a, int num_sms, unsigned int* status, cudaStream_t stream) {
+  if constexpr (NH == 128)
+    if (retriever_ring<NH, true>(a.L) >= 3) return launch_retriever_cfg<NH, true>(a, num_sms, status, stream);
+  return launch_retriever_cfg<NH, false>(a, num_sms, status, stream);
 }
 
 }  // namespace
