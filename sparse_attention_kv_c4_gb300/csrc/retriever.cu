@@ -89,6 +89,16 @@ struct Cfg {
   static constexpr int kMaxL = kLin ? 3 : 4;             // layers the launch takes (the launcher picks kLin by L)
 };
 
+// Programmatic dependent launch between the prep kernel and the scoring
+// kernel: the prep lets the scoring kernel start at once, whose producer sends
+// its first key copies (inputs of the call, which no kernel of the call
+// writes) before griddepcontrol.wait; every read of the prep's output (the
+// split query, the weights) comes after a wait.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Two consecutive 32-bit TMEM columns: thread i gets lane (base + i).
 FM_DEV void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
@@ -119,6 +129,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     retriever_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w, uint8_t* __restrict__ qsplit,
                           float* __restrict__ wq) {
   using C = Cfg<NH, kLin>;
+  grid_dep_launch_dependents();
   const int64_t bl = blockIdx.x;
   uint8_t* t1 = qsplit + bl * C::kQLayerBytes;
   uint8_t* t2 = t1 + C::kQTermBytes;
@@ -252,17 +263,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile = 0;
           ++b;
         }
+        // the request's split query: t1 block, then t2 block (one box of
+        // kBRows rows each) per layer
+        auto load_q = [&](int64_t rb) {
+          mbar_arrive_expect_tx(&bar_qfull, (uint32_t)(L * C::kQLayerBytes));
+          for (int l = 0; l < L; ++l)
+            for (int tb = 0; tb < 2; ++tb)
+              tma_load_2d(q_smem + l * C::kQLayerBytes + tb * C::kQTermBytes, &tmap_q, &bar_qfull, 0,
+                          (int32_t)(((rb * L + l) * 2 + tb) * C::kBRows));
+          q_issued = (q_issued + 1) & 1;
+        };
+        bool q_after_keys = false;  // the first request: its key copies go out before the wait for the prep
         if (b != cur_b) {
           if (cur_b >= 0) {
             if (!mbar_wait(&bar_qempty, q_phase, &abort_flag, p.status)) break;
             q_phase ^= 1;
+            load_q(b);
+          } else {
+            q_after_keys = true;
           }
-          mbar_arrive_expect_tx(&bar_qfull, (uint32_t)(L * C::kQLayerBytes));
-          for (int l = 0; l < L; ++l)  // the layer's t1 block, then its t2 block (one box of kBRows rows each)
-            for (int tb = 0; tb < 2; ++tb)
-              tma_load_2d(q_smem + l * C::kQLayerBytes + tb * C::kQTermBytes, &tmap_q, &bar_qfull, 0,
-                          (int32_t)(((b * L + l) * 2 + tb) * C::kBRows));
-          q_issued = (q_issued + 1) & 1;
           cur_b = b;
         }
         const int m = (int)((t - t_begin) % kPairs);
@@ -283,6 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             rstage[m] = 0;
             rphase[m] ^= 1u;
           }
+        }
+        if (q_after_keys && ok) {
+          grid_dep_wait();
+          load_q(b);
         }
       }
       if (abort_flag) {  // let copies already in flight land before the CTA exits
@@ -370,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t dacc = 0, d_phase = 0, sslot = 0, s_phase = 0;
     int64_t w_b = -1;
     bool ok = true;
+    grid_dep_wait();  // the weights come from the prep kernel
     for (int64_t i = 0; i < n_tiles && ok; ++i) {
       if (b != w_b) {  // a new request: its weights into this warp's copy
         __syncwarp();
@@ -629,8 +653,17 @@ fm_status launch_retriever_cfg(const RetrieverArgs& a, int num_sms, unsigned int
   e = cudaFuncSetAttribute(retriever_kernel<NH, kLin>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const int grid = (int)(total < num_sms ? total : num_sms);
-  retriever_kernel<NH, kLin><<<grid, kThreads, smem, stream>>>(tmap_q, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, retriever_kernel<NH, kLin>, tmap_q, p);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "retriever: launch: %s", cudaGetErrorString(e));
   return FM_OK;
 }
