@@ -523,32 +523,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp refreshes its own copy with __syncwarp alone
     __shared__ __align__(16) float w_smem[kEpiGroups * 4][kHeads];
     float* w_mine = w_smem[warp - kFirstEpiWarp];
-    uint32_t acc = 0, acc_phase = 0, stage = 0, phase = 0, seq = 0;
-    int64_t cur_q = -1;
-    int nres = 0;
-    int64_t qi = t_begin / p.tiles_per_q;
-    int tile = (int)(t_begin % p.tiles_per_q) - 1;
+    // Group g takes the CTA's live tiles (those with 2 tile < n_res) with
+    // sequence number g, g + 4, ..., so its accumulator is g, and its stage
+    // and the two phases step by four tiles each time (the stage count is a
+    // multiple of four).  It walks each query's own tiles with an int32 loop;
+    // the weights and the query's live range are set once per query.
+    const uint32_t acc = (uint32_t)group;
+    uint32_t acc_phase = 0, stage = (uint32_t)group, phase = 0;
+    uint32_t seq_base = 0;  // live tiles of the CTA before the current query's
+    bool aborted = false;
     const uint64_t keep_policy = l2_policy_evict_last();
-    for (int64_t t = t_begin; t < t_end; ++t) {
-      if (++tile == p.tiles_per_q) {
-        tile = 0;
-        ++qi;
-      }
-      if (qi != cur_q) {
-        nres = p.nres_eff[qi];
-        cur_q = qi;
-        __syncwarp();
-        for (int i = lane; i < kHeads; i += 32) w_mine[i] = __ldg(p.wq + qi * kHeads + i);
-        __syncwarp();
-      }
-      if (2 * tile >= nres) continue;
-      const bool mine = (seq++ % kEpiGroups) == (uint32_t)group;
-      if (mine) {
+    for (int64_t it = t_begin; it < t_end && !aborted;) {
+      const int64_t qi = it / p.tiles_per_q;
+      const int tile0 = (int)(it - qi * p.tiles_per_q);
+      const int tile_end = (t_end - it < (int64_t)(p.tiles_per_q - tile0)) ? tile0 + (int)(t_end - it) : p.tiles_per_q;
+      it += tile_end - tile0;
+      const int nres = p.nres_eff[qi];
+      const int live_end = tile_end < (nres + 1) / 2 ? tile_end : (nres + 1) / 2;
+      const int live = live_end > tile0 ? live_end - tile0 : 0;
+      if (live == 0) continue;
+      __syncwarp();
+      for (int i = lane; i < kHeads; i += 32) w_mine[i] = __ldg(p.wq + qi * kHeads + i);
+      __syncwarp();
+      for (int k = (int)(((uint32_t)group - seq_base) & (kEpiGroups - 1)); k < live; k += kEpiGroups) {
+        const int tile = tile0 + k;
         const int j = 2 * tile + (row >> 6);
         const bool valid = j < nres;
-        if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status)) break;
-        // the stage's scales landed with its full barrier (already complete)
-        if (!mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) break;
+        if (!mbar_wait(&bar_tfull[acc], acc_phase, &abort_flag, p.status) ||
+            // the stage's scales landed with its full barrier (already complete)
+            !mbar_wait(&bar_full[stage], phase, &abort_flag, p.status)) {
+          aborted = true;
+          break;
+        }
         tc_fence_after();
         const float sc = valid ? (kBf16 ? 1.f : scale_smem[stage * kM + row]) : 0.f;
         mbar_arrive(&bar_empty[stage]);
@@ -593,21 +599,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned long long m = __ldg(p.pmask + qi * p.R + j);
             const int o = row & (kPage - 1);
             if ((m >> o) & 1ull)
-              st_f32_hint(p.scores + qi * ld + __ldg(p.pprefix + qi * (p.R + 1) + j) + __popcll(m & ((1ull << o) - 1ull)),
-                          y, keep_policy);
+              st_f32_hint(
+                  p.scores + qi * ld + __ldg(p.pprefix + qi * (p.R + 1) + j) + __popcll(m & ((1ull << o) - 1ull)), y,
+                  keep_policy);
           }
         } else {
           if (valid) st_f32_hint(p.scores + qi * ld + (int64_t)tile * kM + row, y, keep_policy);
         }
-      }
-      if (++acc == (uint32_t)kAccBufs) {
-        acc = 0;
         acc_phase ^= 1u;
+        stage += kEpiGroups;
+        if (stage >= (uint32_t)stages) {
+          stage -= (uint32_t)stages;
+          phase ^= 1u;
+        }
       }
-      if (++stage == (uint32_t)stages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      seq_base += (uint32_t)live;
     }
   }
 
