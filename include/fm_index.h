@@ -32,7 +32,9 @@
  *     the library never frees or retains them.  Layouts are dense row-major in
  *     the order of the bracketed shape, except where a stride is passed.
  *   - bf16 tensors are passed as uint16_t bit patterns; E4M3 keys as uint8_t
- *     codes (OCP FP8 E4M3: bias 7, max 448, S.1111.111 = NaN).
+ *     codes (OCP FP8 E4M3: bias 7, max 448, S.1111.111 = NaN).  Key codes must
+ *     be finite: a chunk whose key holds the NaN code gets an unspecified
+ *     logit (quantised keys never hold it).
  *   - Calls are asynchronous on `stream` (0 = legacy default stream).  The
  *     host validates every argument before the first launch; on a non-OK
  *     return nothing was enqueued (FM_ERR_CUDA: a launch failed; earlier
@@ -133,7 +135,7 @@ fm_status fm_memindex_score_mask(const uint16_t* q, const float* w, const uint16
  *               16-byte aligned)
  *   k_scale     fp32, (b,l,s) at k_scale[b*scale_stride_b + l*scale_stride_l + s]
  *   workspace   >= fm_memindex_fp8_workspace(B, L) bytes, 256-byte aligned
- *               (the split query: 16.25 KB per (request, layer))
+ *               (the split query and its weights: 20.3 KB per (request, layer))
  * Other arguments, outputs and errors as fm_memindex_score_mask;
  * FM_ERR_WORKSPACE for a missing or short workspace.
  */

@@ -15,28 +15,31 @@
 // so the dots run on the tensor cores in E4M3 (kind::f8f6f4) to stay
 // HBM-bound:
 //   prep    one CTA per (request, layer): q split into two E4M3 terms per head
-//           (fp8.cuh), 2^e_h folded into w.
-//   warp 0  TMA producer: the request's split q (L x 16 KB) once per request,
+//           (fp8.cuh), 2^e_h folded into w; the weighted query sum q_w in
+//           four E4M3 terms in two more rows (the ReLU's linear half, below).
+//   warp 0  TMA producer: the request's split q (L x 20 KB) once per request,
 //           then per layer a key tile [128 chunks x 128 B] (SWIZZLE_128B)
 //           into the stage ring of the pair (below) that takes the tile.
 //   warps 1-2  UMMA issuers: per layer-tile 8 x tcgen05.mma M=128 (chunks)
-//           x N=64 (heads) x K=32: four K steps against the t1 rows, then
-//           four against the t2 rows into the same accumulator, so TMEM holds
-//           (t1 + t2).k directly.  One issuing thread alone cannot keep up
-//           with the key stream (each MMA costs it tens of cycles), so two
-//           issue in parallel.
+//           x N=80 (64 heads, the q_w rows, zeros) x K=32: four K steps
+//           against the t1 block, then four against the t2 block into the
+//           same accumulator, so TMEM holds (t1 + t2).k directly.  One issuing
+//           thread alone cannot keep up with the key stream (each MMA costs it
+//           tens of cycles), so two issue in parallel.
 //   warps 3-10  epilogue, two groups of four warps (one warp per SM
 //           sub-partition would leave every latency exposed).  Issuer m and
 //           group m form pair m: the pair takes the CTA's tiles with local
-//           index = m (mod 2) and owns four of the eight 64-column
+//           index = m (mod 2) and owns three of the six 80-column
 //           accumulators.  Thread = chunk row; its chunk's scales are fetched
 //           with cp.async two of its pair's tiles ahead into a shared-memory
 //           ring (a load from HBM per layer-tile would stall the warp for its
-//           full latency), the head weights come from a per-warp shared copy,
-//           then y = sum_h w_h 2^e_h ReLU(scale (t1 + t2).k) from the 64
-//           accumulated dots, the running max over the tile's layers, the
-//           ballot of the mask word, max-sigmoid (and per-layer logits when
-//           asked).
+//           full latency), the head weights come from a per-warp shared copy.
+//           With ReLU(d) = (d + |d|) / 2 a chunk's logit is
+//           (sc q_w.k + |sc| sum_h w'_h |d_h|) / 2, w'_h = w_h 2^e_h and
+//           d_h = (t1 + t2).k: one FFMA per head (the absolute value folds
+//           into it), q_w.k from two accumulator columns.  Then the running
+//           max over the tile's layers, the ballot of the mask word,
+//           max-sigmoid (and per-layer logits when asked).
 #include <math.h>
 
 #include "fm_common.cuh"
@@ -49,13 +52,19 @@ namespace fm {
 namespace {
 
 constexpr int kM = 128;                      // chunks per tile (UMMA M)
-constexpr int kHeads = 64;                   // UMMA N: t1.k + t2.k accumulate in one column per head
-constexpr int kQRows = 2 * kHeads;           // t1 rows 0..63, t2 rows 64..127 of the split query
+constexpr int kHeads = 64;                   // t1.k + t2.k accumulate in one column per head
+// The split query of a layer: a t1 block and a t2 block of kQTermRows rows
+// each (the 64 heads, then the weighted query sum's terms and zeros: the
+// ReLU's linear half on the tensor core, below); kQTermRows is the MMA's N.
+constexpr int kQTermRows = kHeads + 16;
+constexpr int kQRows = 2 * kQTermRows;
 constexpr int kDim = 128;                    // E4M3 bytes per key (UMMA K, 4 steps of 32)
 constexpr int kMaxL = 4;
 constexpr int kTileBytes = kM * kDim;        // 16 KB of keys per layer-tile
-constexpr int kQLayerBytes = kQRows * kDim;  // 16 KB of split query per layer
-constexpr int kAccBufs = 8;                  // 64-column accumulators
+constexpr int kQTermBytes = kQTermRows * kDim;  // 10 KB
+constexpr int kQLayerBytes = kQRows * kDim;  // 20 KB of split query per layer
+constexpr int kWStride = kHeads + 4;         // floats per (request, layer) of wq: w', then 2^e1, 2^e2
+constexpr int kAccBufs = 6;                  // accumulators of kQTermRows columns (480 of 512)
 constexpr int kMaxStages = 12;
 // Issuer m and epilogue group m form pair m: the pair takes the CTA's tiles
 // with local index i = m (mod kPairs) and owns accumulators
@@ -70,7 +79,7 @@ constexpr int kRingAccs = kAccBufs / kPairs;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreads = kFirstEpiWarp * 32 + kEpiGroups * 128;
 constexpr int kPrepThreads = 256;
-constexpr uint32_t kTmemCols = kAccBufs * kHeads;  // 512
+constexpr uint32_t kTmemCols = 512;          // kAccBufs x kQTermRows, as a power of two
 constexpr int kScDepth = 2;                  // a group's tiles of scales in flight ahead of it
 constexpr int kScSlots = kScDepth + 1;
 constexpr int kScRingBytes = kEpiGroups * kScSlots * kMaxL * kM * 4;  // 12 KB
@@ -87,7 +96,7 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 struct Params {
-  const float* wq;            // [B*L, 64] head weights with 2^e_h folded in
+  const float* wq;            // [B*L, kWStride]: head weights with 2^e_h folded in, then q_w's two scales
   const float* k_scale;
   int64_t sstride_b, sstride_l;
   uint32_t* mask;
@@ -107,8 +116,64 @@ __global__ void __launch_bounds__(kPrepThreads)
                              uint8_t* __restrict__ qsplit, float* __restrict__ wq) {
   const int64_t bl = blockIdx.x;
   uint8_t* t1 = qsplit + bl * kQLayerBytes;
-  split_query(q + bl * kHeads * kDim, w + bl * kHeads, kHeads, kPrepThreads, t1, t1 + kHeads * kDim,
-              wq + bl * kHeads);
+  uint8_t* t2 = t1 + kQTermBytes;
+  float* wl = wq + bl * kWStride;
+  split_query(q + bl * kHeads * kDim, w + bl * kHeads, kHeads, kPrepThreads, t1, t2, wl);
+  // The ReLU's linear half: with ReLU(d) = (d + |d|) / 2 a chunk's logit is
+  // (sc q_w.k + |sc| sum_h w'_h |d_h|) / 2, where q_w = sum_h w_h q_h.  q_w
+  // (fp32, heads in order) goes into four E4M3 terms: with 2^e1 putting
+  // max|q_w| in (224, 448], u1 = RNE(q_w 2^-e1), u2 = RNE(rest), then the
+  // rest times 2^8 the same way (u3, u4), within 2^-18 of max|q_w|.  Rows
+  // 64 (u1 | u2) and 65 (u3 | u4) of the t1 | t2 blocks, zeros in 66 .. 79.
+  __shared__ float red[kPrepThreads / 32];
+  const int j = threadIdx.x;
+  float qw = 0.f;
+  if (j < kDim) {
+    const uint16_t* qb = q + bl * kHeads * kDim + j;
+    for (int h = 0; h < kHeads; ++h)
+      qw = fmaf(__ldg(w + bl * kHeads + h), __uint_as_float((uint32_t)__ldg(qb + h * kDim) << 16), qw);
+  }
+  float m = fabsf(qw);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((j & 31) == 0) red[j >> 5] = m;
+  __syncthreads();
+  float amax = 0.f;
+  for (int i = 0; i < kPrepThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+  int e = 0;
+  if (amax > 0.f && isfinite(amax)) {
+    e = ilogbf(amax) - 8;
+    if (ldexpf(amax, -e) > 448.f) e += 1;
+  }
+  if (j < kDim) {
+    const float s1 = ldexpf(qw, -e);
+    const uint32_t u1 = e4m3_rne(s1);
+    const float r1 = s1 - e4m3_value(u1);
+    const uint32_t u2 = e4m3_rne(r1);
+    const float s2 = (r1 - e4m3_value(u2)) * 256.f;
+    const uint32_t u3 = e4m3_rne(s2);
+    t1[kHeads * kDim + j] = (uint8_t)u1;
+    t2[kHeads * kDim + j] = (uint8_t)u2;
+    t1[(kHeads + 1) * kDim + j] = (uint8_t)u3;
+    t2[(kHeads + 1) * kDim + j] = (uint8_t)e4m3_rne(s2 - e4m3_value(u3));
+  }
+  for (int i = threadIdx.x; i < 14 * kDim; i += kPrepThreads) {
+    t1[(kHeads + 2) * kDim + i] = 0;
+    t2[(kHeads + 2) * kDim + i] = 0;
+  }
+  if (threadIdx.x == 0) {
+    wl[kHeads] = ldexpf(1.f, e);
+    wl[kHeads + 1] = ldexpf(1.f, e - 8);
+    wl[kHeads + 2] = 0.f;
+    wl[kHeads + 3] = 0.f;
+  }
+}
+
+// Two consecutive 32-bit TMEM columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(taddr)
+               : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -126,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   // one copy of the current request's head weights per epilogue warp, so a
   // warp refreshes its own copy with __syncwarp alone
-  __shared__ __align__(16) float w_smem[kEpiGroups * 4][kMaxL * kHeads];
+  __shared__ __align__(16) float w_smem[kEpiGroups * 4][kMaxL * kWStride];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int L = p.L, ring = p.stages;  // key stages per pair; pair m owns [m * ring, (m + 1) * ring)
@@ -222,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // stage ring, so one issuer's barrier waits and commits overlap the
       // other's MMAs.
       const int me = warp - 1;
-      const uint32_t idesc = idesc_e4m3_f32(kM, kHeads);
+      const uint32_t idesc = idesc_e4m3_f32(kM, kQTermRows);
       uint32_t rstage = 0, phase = 0, racc = 0, acc_phase = 0, q_phase = 0;
       int64_t cur_b = -1;
       bool ok = true;
@@ -252,13 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + acc * kHeads;
+          const uint32_t d_tmem = tmem_base + acc * kQTermRows;
           // descriptor start-address field counts 16-byte units; K steps of
           // 32 bytes advance it by 2 inside the 128-byte swizzle atom
           const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kTileBytes >> 4));
           const uint64_t b_desc = b_desc0 + (uint64_t)(l * (kQLayerBytes >> 4));
-          // the t2 rows start 8 KB (eight 1 KB swizzle atoms) after the t1 rows
-          constexpr uint64_t kT2 = (kHeads * kDim) >> 4;
+          // the t2 block starts 10 KB (ten 1 KB swizzle atoms) after the t1 block
+          constexpr uint64_t kT2 = kQTermBytes >> 4;
 #pragma unroll
           for (int k = 0; k < kDim / 32; ++k)
             umma_e4m3_ss(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k != 0 ? 1u : 0u);
@@ -327,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((int)((t - t_begin) % kPairs) != group) continue;  // the other pair's tile
       if (b != w_b) {  // a new request: its weights into this warp's copy
         __syncwarp();
-        for (int i = lane; i < L * kHeads; i += 32) w_mine[i] = __ldg(p.wq + b * L * kHeads + i);
+        for (int i = lane; i < L * kWStride; i += 32) w_mine[i] = __ldg(p.wq + b * L * kWStride + i);
         __syncwarp();
         w_b = b;
       }
@@ -346,11 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kHeads;
-        uint32_t r0[32], r1[32];
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kQTermRows;
+        uint32_t r0[32], r1[32], lin[2];
         tmem_ld32(taddr, r0);
         tmem_ld32(taddr + 32, r1);
-        const float4* wl = reinterpret_cast<const float4*>(w_mine + l * kHeads);
+        tmem_ld2(taddr + kHeads, lin);  // q_w . k in two powers of two
+        const float* wlayer = w_mine + l * kWStride;
+        const float4* wl = reinterpret_cast<const float4*>(wlayer);
         float wr[kHeads];
 #pragma unroll
         for (int i = 0; i < kHeads / 4; ++i) {
@@ -360,44 +427,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           wr[4 * i + 2] = v.z;
           wr[4 * i + 3] = v.w;
         }
+        const float e1 = wlayer[kHeads], e2 = wlayer[kHeads + 1];
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&bar_tempty[acc]);  // the dots are in registers: the MMA may reuse the accumulator
-        // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, y;
-        if (sc > 0.f) {  // ReLU(sc d) = sc ReLU(d): one multiply per chunk
+        // q_h . k = 2^e_h (t1 + t2) . k with 2^e_h folded into w', and
+        // ReLU(sc d) = (sc d + |sc| |d|) / 2 for either sign of sc: here
+        // sum_h w'_h |d_h| (the absolute value folds into the FFMA), then the
+        // linear half sc q_w.k
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            x0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), x0);
-            x1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), x1);
-            x2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(r0[h + 2]), 0.f), x2);
-            x3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(r0[h + 3]), 0.f), x3);
-          }
-#pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            x0 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), x0);
-            x1 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), x1);
-            x2 = fmaf(wr[34 + h], fmaxf(__uint_as_float(r1[h + 2]), 0.f), x2);
-            x3 = fmaf(wr[35 + h], fmaxf(__uint_as_float(r1[h + 3]), 0.f), x3);
-          }
-          y = sc * ((x0 + x1) + (x2 + x3));
-        } else {
-#pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            x0 = fmaf(wr[h], fmaxf(sc * __uint_as_float(r0[h]), 0.f), x0);
-            x1 = fmaf(wr[h + 1], fmaxf(sc * __uint_as_float(r0[h + 1]), 0.f), x1);
-            x2 = fmaf(wr[h + 2], fmaxf(sc * __uint_as_float(r0[h + 2]), 0.f), x2);
-            x3 = fmaf(wr[h + 3], fmaxf(sc * __uint_as_float(r0[h + 3]), 0.f), x3);
-          }
-#pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            x0 = fmaf(wr[32 + h], fmaxf(sc * __uint_as_float(r1[h]), 0.f), x0);
-            x1 = fmaf(wr[33 + h], fmaxf(sc * __uint_as_float(r1[h + 1]), 0.f), x1);
-            x2 = fmaf(wr[34 + h], fmaxf(sc * __uint_as_float(r1[h + 2]), 0.f), x2);
-            x3 = fmaf(wr[35 + h], fmaxf(sc * __uint_as_float(r1[h + 3]), 0.f), x3);
-          }
-          y = (x0 + x1) + (x2 + x3);
+        for (int h = 0; h < 32; h += 4) {
+          x0 = fmaf(wr[h], fabsf(__uint_as_float(r0[h])), x0);
+          x1 = fmaf(wr[h + 1], fabsf(__uint_as_float(r0[h + 1])), x1);
+          x2 = fmaf(wr[h + 2], fabsf(__uint_as_float(r0[h + 2])), x2);
+          x3 = fmaf(wr[h + 3], fabsf(__uint_as_float(r0[h + 3])), x3);
         }
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          x0 = fmaf(wr[32 + h], fabsf(__uint_as_float(r1[h])), x0);
+          x1 = fmaf(wr[33 + h], fabsf(__uint_as_float(r1[h + 1])), x1);
+          x2 = fmaf(wr[34 + h], fabsf(__uint_as_float(r1[h + 2])), x2);
+          x3 = fmaf(wr[35 + h], fabsf(__uint_as_float(r1[h + 3])), x3);
+        }
+        const float qwk = fmaf(e1, __uint_as_float(lin[0]), e2 * __uint_as_float(lin[1]));
+        const float y = 0.5f * fmaf(sc, qwk, fabsf(sc) * ((x0 + x1) + (x2 + x3)));
         if (p.logits != nullptr && valid) p.logits[(b * L + l) * p.S + s] = y;
         m = fmaxf(m, y);
         if (++racc == (uint32_t)kRingAccs) {
@@ -427,7 +481,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 size_t memindex_fp8_workspace_bytes(int B, int L) {
-  return align256((size_t)B * L * kQLayerBytes) + align256((size_t)B * L * kHeads * 4);
+  return align256((size_t)B * L * kQLayerBytes) + align256((size_t)B * L * kWStride * 4);
 }
 
 namespace {
@@ -468,7 +522,7 @@ fm_status launch_memindex_fp8(const Fp8Args& a, int num_sms, unsigned int* statu
     if (st != FM_OK) return st;
   }
   {
-    // split query: rows (B*L*128) x 128 B, one box of 128 rows per layer
+    // split query: rows (B*L*kQRows) x 128 B, one box of kQRows rows per layer
     const uint64_t dims[2] = {(uint64_t)kDim, (uint64_t)a.B * a.L * kQRows};
     const uint64_t strides[1] = {(uint64_t)kDim};
     const uint32_t box[2] = {(uint32_t)kDim, (uint32_t)kQRows};
