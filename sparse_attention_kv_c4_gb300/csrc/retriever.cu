@@ -77,8 +77,9 @@ constexpr int kPrepThreads = 256;
 // kLin: the linear half of the ReLU on the tensor core.  With ReLU(d) =
 // (d + |d|) / 2 a chunk's score is sc/2 (q_w . k + sum_h w'_h |d_h|), where
 // q_w = sum_h w_h q_h; q_w is split into four E4M3 terms (two per power of
-// two), one row of each term block of B, so the MMA leaves q_w . k in two more
-// accumulator columns and the epilogue has one FFMA (|d| folded in) per head.
+// two) in four more rows of the t1 block of B, so the t1 MMAs (N = NH + 16)
+// leave the four terms' dots in four more accumulator columns, the t2 MMAs
+// keep N = NH, and the epilogue has one FFMA (|d| folded in) per head.
 template <int NH, bool kLin>
 struct Cfg {
   static constexpr int kBRows = NH + (kLin ? 16 : 0);                  // B rows per term block: the MMA's N
@@ -99,10 +100,10 @@ __device__ __forceinline__ void grid_dep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Two consecutive 32-bit TMEM columns: thread i gets lane (base + i).
-FM_DEV void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
+// Four consecutive 32-bit TMEM columns: thread i gets lane (base + i).
+FM_DEV void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr)
                : "memory");
 }
@@ -140,8 +141,8 @@ __global__ void __launch_bounds__(kPrepThreads)
     // max|q_w| in (224, 448]: u1 = RNE(q_w 2^-e1), u2 = RNE(rest), then the
     // rest after those two times 2^8 the same way (u3, u4), so q_w =
     // 2^e1 (u1 + u2) + 2^(e1-8) (u3 + u4) to within 2^-18 of max|q_w|.
-    // Rows NH (u1 | u2) and NH+1 (u3 | u4) of the t1 | t2 blocks, zeros in
-    // rows NH+2 .. NH+15.
+    // Rows NH .. NH+3 of the t1 block hold u1, u2, u3, u4, zeros in rows
+    // NH+4 .. NH+15 (and in the t2 block's rows NH .., which no MMA reads).
     __shared__ float red[kPrepThreads / 32];
     const int j = threadIdx.x;
     float qw = 0.f;
@@ -170,14 +171,12 @@ __global__ void __launch_bounds__(kPrepThreads)
       const uint32_t u3 = e4m3_rne(s2);
       const uint32_t u4 = e4m3_rne(s2 - e4m3_value(u3));
       t1[NH * kDim + j] = (uint8_t)u1;
-      t2[NH * kDim + j] = (uint8_t)u2;
-      t1[(NH + 1) * kDim + j] = (uint8_t)u3;
-      t2[(NH + 1) * kDim + j] = (uint8_t)u4;
+      t1[(NH + 1) * kDim + j] = (uint8_t)u2;
+      t1[(NH + 2) * kDim + j] = (uint8_t)u3;
+      t1[(NH + 3) * kDim + j] = (uint8_t)u4;
     }
-    for (int i = threadIdx.x; i < 14 * kDim; i += kPrepThreads) {
-      t1[(NH + 2) * kDim + i] = 0;
-      t2[(NH + 2) * kDim + i] = 0;
-    }
+    for (int i = threadIdx.x; i < 12 * kDim; i += kPrepThreads) t1[(NH + 4) * kDim + i] = 0;
+    for (int i = threadIdx.x; i < 16 * kDim; i += kPrepThreads) t2[NH * kDim + i] = 0;
     if (threadIdx.x == 0) {
       wl[NH] = ldexpf(1.f, e);
       wl[NH + 1] = ldexpf(1.f, e - 8);
@@ -318,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ------------------------------ UMMA issuers ------------------------------
       const int me = warp - 1;
-      const uint32_t idesc = idesc_e4m3_f32(kM, C::kBRows);
+      const uint32_t idesc = idesc_e4m3_f32(kM, C::kBRows), idesc2 = idesc_e4m3_f32(kM, NH);
       uint32_t aslot = 0, a_phase = 0, dacc = 0, d_phase = 0, q_phase = 0;
       int64_t cur_b = -1;
       bool ok = true;
@@ -358,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kDim / 32; ++k)
             umma_e4m3_ts(d_tmem, a_tmem + 8 * k, b_desc + 2 * k, idesc, k != 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < kDim / 32; ++k) umma_e4m3_ts(d_tmem, a_tmem + 8 * k, b_desc + kT2 + 2 * k, idesc, 1u);
+          for (int k = 0; k < kDim / 32; ++k) umma_e4m3_ts(d_tmem, a_tmem + 8 * k, b_desc + kT2 + 2 * k, idesc2, 1u);
           umma_commit(&bar_aempty[ai]);
           umma_commit(&bar_tfull[di]);
           if (++aslot == (uint32_t)kASlots) {
@@ -428,18 +427,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t taddr = lane_base + kASlots * kACols + dacc * C::kBRows;
         const float4* wl = reinterpret_cast<const float4*>(w_mine + l * C::kWStride);
         float y = 0.f;
-        uint32_t lin[2] = {0u, 0u};
+        uint32_t lin[4] = {0u, 0u, 0u, 0u};
         const float scc = kLin ? 0.5f * sc : sc;  // each chunk's partial sum times the scale as it lands
+        // 32 heads at a time, double-buffered: the load of chunk c + 1 is in
+        // flight while chunk c is summed, so the accumulator is released one
+        // load latency earlier
+        uint32_t r[2][32];
+        tmem_ld32(taddr, r[0]);
+        if constexpr (kLin) tmem_ld4(taddr + NH, lin);  // q_w . k as four terms' dots
 #pragma unroll
-        for (int c = 0; c < NH / 32; ++c) {  // 32 heads at a time
-          uint32_t r[32];
-          tmem_ld32(taddr + c * 32, r);
-          if (kLin && c == 0) tmem_ld2(taddr + NH, lin);  // q_w . k in two powers of two
+        for (int c = 0; c < NH / 32; ++c) {
           tmem_ld_wait();
-          if (c == NH / 32 - 1) {
+          if (c + 1 < NH / 32) {
+            tmem_ld32(taddr + (c + 1) * 32, r[(c + 1) & 1]);
+          } else {
             tc_fence_before();
             mbar_arrive(&bar_tempty[di]);  // the dots are in registers: the MMA may reuse the accumulator
           }
+          const uint32_t* rc = r[c & 1];
           // q_h . k = 2^e_h (t1 + t2) . k; 2^e_h is folded into w, and
           // ReLU(sc d) = sc ReLU(d) for sc >= 0: one multiply per chunk
           float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
@@ -447,22 +452,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 32; h += 4) {
             const float4 wv = wl[c * 8 + h / 4];
             if constexpr (kLin) {  // w |d| (the absolute value folds into the FFMA)
-              x0 = fmaf(wv.x, fabsf(__uint_as_float(r[h])), x0);
-              x1 = fmaf(wv.y, fabsf(__uint_as_float(r[h + 1])), x1);
-              x2 = fmaf(wv.z, fabsf(__uint_as_float(r[h + 2])), x2);
-              x3 = fmaf(wv.w, fabsf(__uint_as_float(r[h + 3])), x3);
+              x0 = fmaf(wv.x, fabsf(__uint_as_float(rc[h])), x0);
+              x1 = fmaf(wv.y, fabsf(__uint_as_float(rc[h + 1])), x1);
+              x2 = fmaf(wv.z, fabsf(__uint_as_float(rc[h + 2])), x2);
+              x3 = fmaf(wv.w, fabsf(__uint_as_float(rc[h + 3])), x3);
             } else {
-              x0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), x0);
-              x1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), x1);
-              x2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), x2);
-              x3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), x3);
+              x0 = fmaf(wv.x, fmaxf(__uint_as_float(rc[h]), 0.f), x0);
+              x1 = fmaf(wv.y, fmaxf(__uint_as_float(rc[h + 1]), 0.f), x1);
+              x2 = fmaf(wv.z, fmaxf(__uint_as_float(rc[h + 2]), 0.f), x2);
+              x3 = fmaf(wv.w, fmaxf(__uint_as_float(rc[h + 3]), 0.f), x3);
             }
           }
           y = fmaf(scc, (x0 + x1) + (x2 + x3), y);
         }
         if constexpr (kLin) {
           const float* we = w_mine + l * C::kWStride + NH;  // 2^e1, 2^e2
-          y = fmaf(scc, fmaf(we[0], __uint_as_float(lin[0]), we[1] * __uint_as_float(lin[1])), y);
+          const float hi = __uint_as_float(lin[0]) + __uint_as_float(lin[1]);
+          const float lo = __uint_as_float(lin[2]) + __uint_as_float(lin[3]);
+          y = fmaf(scc, fmaf(we[0], hi, we[1] * lo), y);
         }
         if (++dacc == (uint32_t)C::kDAccs) {
           dacc = 0;
