@@ -165,19 +165,20 @@ namespace fm {
 //  1. Sample 32 evenly spaced runs of 64 consecutive scores (coalesced) and
 //     take theta = about the r-th largest sample composite, r chosen so that
 //     about 3 min(k, n) candidates (at most 2/3 of the list) are expected at or
-//     above it (equal scores are thresholded by index, so ties cannot flood
-//     the list).
+//     above it.
 //  2. One vectorised pass compares each score with theta's score as a plain
-//     fp32 compare; only scores that reach it (a few percent) build their
-//     composite and are appended, when composite >= theta, to a shared-memory
-//     list (one shared-memory atomic per appended candidate); the largest
-//     appended composite is tracked too.
+//     fp32 compare; the scores that reach it (a few percent, ties with
+//     theta's score included) are appended with their composites to a
+//     shared-memory list (one shared-memory atomic per warp and pass); the
+//     largest appended composite is tracked too.
 //  3. If the list holds at least min(k, n) entries and did not overflow, the
-//     true top-k is inside it (the k-th largest composite is >= theta): a
-//     block-wide radix select over the composites, starting at the first bit
-//     where theta and the largest candidate differ, finds the min(k, n)-th
-//     largest T.  Otherwise the exact global-memory radix path
-//     (block_topk_radix) runs.
+//     true top-k is inside it (the k-th largest composite is >= the lowest
+//     composite with theta's key): a block-wide radix select over the
+//     composites, starting at the first bit where that bound and the largest
+//     candidate differ, finds the min(k, n)-th largest T.  A list that
+//     overflows (rows flooded by ties at the threshold) or falls short takes
+//     one re-aimed sample, then the exact global-memory radix path
+//     (block_topk_radix).
 //  4. The selected indices are marked in a bitmap; one block-wide prefix sum
 //     over the bitmap words gives each thread's word range its first output
 //     slot, and each selected candidate computes its own slot (rank by index)
@@ -416,11 +417,21 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   theta = 0ull;
   if (n > CAP) {
     if (n <= kTopkBitmapN) {
-      for (int i = tid; i < kTopkSample; i += THREADS) {
-        const int run = i >> 6, off = i & 63;
-        const int j = (int)(((long long)run * (n - 64)) / (kTopkRuns - 1)) + off;
-        sm.u.sample[i] = ((unsigned long long)float_key(__ldg(row + j)) << 32) | (uint32_t)(~(uint32_t)j);
+      // every thread's samples are loaded before any is stored, so their
+      // loads overlap (run * (n - 64) < 2^31 for these rows)
+      constexpr int kPerT = kTopkSample / THREADS;
+      static_assert(kPerT * THREADS == kTopkSample, "sample entries per thread");
+      float sv[kPerT];
+      int sj[kPerT];
+#pragma unroll
+      for (int t = 0; t < kPerT; ++t) {
+        const int i = tid + t * THREADS, run = i >> 6, off = i & 63;
+        sj[t] = run * (n - 64) / (kTopkRuns - 1) + off;
+        sv[t] = __ldg(row + sj[t]);
       }
+#pragma unroll
+      for (int t = 0; t < kPerT; ++t)
+        sm.u.sample[tid + t * THREADS] = ((unsigned long long)float_key(sv[t]) << 32) | (uint32_t)(~(uint32_t)sj[t]);
       __syncthreads();
       long long r = r_aim >= 0 ? r_aim : (want * kTopkSample) / (long long)n;
       r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
@@ -458,36 +469,24 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   }
   __syncthreads();
   // ---- 2. filter pass ---------------------------------------------------------
-  // A score can only pass if score >= theta's score (as floats: -0 compares
-  // equal to +0 like its key); the composite then decides ties by index.  A
-  // threshold at -inf (rows dominated by -inf/NaN) cannot be tested as a float
-  // because NaN ranks as -inf: then every score goes to the composite test.
+  // Every score keyed at or above theta's score key survives: the threshold
+  // drops from theta to the lowest composite with that key, so all scores
+  // tied with theta's are kept.  The list then holds every composite at or
+  // above that bound; with at least min(k, n) of them (checked below) the
+  // top min(k, n) of the row are all among them, so the select is exact.
+  // A key test is a plain fp32 compare (-0 == +0 like their keys, NaN below
+  // every threshold); a threshold at or below the key of -inf (rows
+  // dominated by -inf/NaN, where NaN ranks as -inf) takes every score.
   const uint32_t theta_key = (uint32_t)(theta >> 32);
-  const bool take_all = theta == 0ull || theta_key <= 0x007FFFFFu;
+  const bool take_all = theta_key <= 0x007FFFFFu;
   const float theta_f = take_all ? -INFINITY : key_float(theta_key);
-  // A score survives if its composite reaches theta: a score above theta's
-  // score always does; one equal to it only if the index breaks the tie (rare,
-  // so the composite is built only then).  Under take_all every score takes
-  // the composite test (NaN ranks as -inf).  Each warp counts its survivors,
-  // reserves their slots with one shared-memory atomic and then writes them.
   const int lane = tid & 31;
   auto composite_of = [](float v, int i) -> unsigned long long {
     return ((unsigned long long)float_key(v) << 32) | (uint32_t)(~(uint32_t)i);
   };
-  auto passes = [&](float v, int i) -> bool {
-    if (take_all || v == theta_f) return composite_of(v, i) >= theta;
-    return v > theta_f;
-  };
-  // 4-bit survivor mask of one float4 (the common case tests floats only)
-  auto mask4 = [&](const float4& v, int i) -> uint32_t {
-    const bool any_eq = v.x == theta_f || v.y == theta_f || v.z == theta_f || v.w == theta_f;
-    if (!take_all && !any_eq)
-      return (uint32_t)(v.x > theta_f) | ((uint32_t)(v.y > theta_f) << 1) | ((uint32_t)(v.z > theta_f) << 2) |
-             ((uint32_t)(v.w > theta_f) << 3);
-    return (uint32_t)passes(v.x, i) | ((uint32_t)passes(v.y, i + 1) << 1) | ((uint32_t)passes(v.z, i + 2) << 2) |
-           ((uint32_t)passes(v.w, i + 3) << 3);
-  };
-  auto reserve = [&](uint32_t mine) -> uint32_t {  // all lanes of the warp call it
+  // Each warp counts its survivors and reserves their slots with one
+  // shared-memory atomic (all lanes call it).
+  auto reserve = [&](uint32_t mine) -> uint32_t {
     uint32_t incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -515,34 +514,35 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   constexpr int kVec = 8;  // float4 loads in flight per thread
   for (int i40 = 0; i40 < n4; i40 += THREADS * kVec) {  // same trip count in every thread
     float4 v[kVec];
-    uint32_t mask = 0;  // bit 4u + j: element j of v[u] survives
 #pragma unroll
     for (int u = 0; u < kVec; ++u) {
       const int i4 = i40 + u * THREADS + tid;
       v[u] = i4 < n4 ? __ldg(row4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
+    uint32_t mask = 0;  // bit 4u + e: element e of v[u] survives
 #pragma unroll
     for (int u = 0; u < kVec; ++u) {
-      const int i4 = i40 + u * THREADS + tid;
-      if (i4 < n4) mask |= mask4(v[u], 4 * i4) << (4 * u);
+      const float4 x = v[u];
+      const uint32_t m4 = take_all ? 15u
+                                   : (uint32_t)(x.x >= theta_f) | ((uint32_t)(x.y >= theta_f) << 1) |
+                                         ((uint32_t)(x.z >= theta_f) << 2) | ((uint32_t)(x.w >= theta_f) << 3);
+      if (i40 + u * THREADS + tid < n4) mask |= m4 << (4 * u);
     }
     uint32_t slot = reserve((uint32_t)__popc(mask));
-#pragma unroll
-    for (int u = 0; u < kVec; ++u) {
-      uint32_t sub = (mask >> (4 * u)) & 15u;
-      const int i = 4 * (i40 + u * THREADS + tid);
-      while (sub) {
-        const int j = __ffs(sub) - 1;
-        sub &= sub - 1u;
-        const float x = j == 0 ? v[u].x : (j == 1 ? v[u].y : (j == 2 ? v[u].z : v[u].w));
-        store(slot++, x, i + j);
-      }
+    // survivors are few (~6% of a row): each lane walks its own, re-reading
+    // the score (a cache hit) rather than indexing v[] at run time, which
+    // would put v in local memory
+    while (mask) {
+      const int b = __ffs(mask) - 1;
+      mask &= mask - 1u;
+      const int i = 4 * (i40 + (b >> 2) * THREADS + tid) + (b & 3);
+      store(slot++, __ldg(row + i), i);
     }
   }
   for (int i0 = 4 * n4; i0 < n; i0 += THREADS) {  // scalar rest (all of an unaligned row)
     const int i = i0 + tid;
     const float v = i < n ? __ldg(row + i) : -INFINITY;
-    const bool p = i < n && passes(v, i);
+    const bool p = i < n && (take_all || v >= theta_f);
     const uint32_t slot = reserve((uint32_t)p);
     if (p) store(slot, v, i);
   }
@@ -566,7 +566,8 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   }
   r_aim = r_next;
   }  // attempts
-  block_topk_emit(sm, (int)sm.count, theta, n, kk, k, idx_map, idx_out, score_out);
+  block_topk_emit(sm, (int)sm.count, (unsigned long long)(uint32_t)(theta >> 32) << 32, n, kk, k, idx_map, idx_out,
+                  score_out);
 }
 
 // A segment entry e -- of the 32 scores 32g .. 32g+31 of a row that lie below
