@@ -164,8 +164,9 @@ namespace fm {
 //  which orders (score desc, index asc).
 //  1. Sample 32 evenly spaced runs of 64 consecutive scores (coalesced) and
 //     take theta = about the r-th largest sample composite, r chosen so that
-//     about 3 min(k, n) candidates (at most 2/3 of the list) are expected at or
-//     above it.
+//     about 2 min(k, n) candidates (3 min(k, n) for rows long enough that r
+//     would fall below 64; at most 2/3 of the list) are expected at or above
+//     it.
 //  2. One vectorised pass compares each score with theta's score as a plain
 //     fp32 compare; the scores that reach it (a few percent, ties with
 //     theta's score included) are appended with their composites to a
@@ -410,7 +411,11 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   // the filter pass run again (the row is in L2 by then).  Only a second miss
   // takes the exact global-memory path, whose four radix passes and ordered
   // output pass over the row cost a multiple of the fast path.
-  const long long want = 3 * kk < 2 * CAP / 3 ? 3 * kk : 2 * CAP / 3;  // expected candidates
+  // expected candidates: 2 min(k, n) where the sample rank of theta is at
+  // least 64 (the survivor count then stays within about half of its aim at
+  // four standard deviations), else 3 min(k, n); at most 2/3 of the list
+  const long long aim = 2LL * kk * kTopkSample >= 64LL * n ? 2LL * kk : 3LL * kk;
+  const long long want = aim < 2 * CAP / 3 ? aim : 2 * CAP / 3;
   long long r_aim = -1;  // sample rank of theta (-1: from `want`)
   unsigned long long theta = 0ull;
   for (int attempt = 0;; ++attempt) {
