@@ -88,6 +88,15 @@ __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint3
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Programmatic dependent launch: the prep kernel lets the scorer launch
+// once every prep CTA has started; the scorer sets up its barriers, TMEM and
+// tensor-map prefetches, then waits for the prep grid's completion (and its
+// memory) before any role reads the prep's output.  The top-k launched after
+// the scorer waits the same way.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void st_f32_hint(float* addr, float v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy) : "memory");
 }
@@ -107,6 +116,49 @@ __device__ __forceinline__ void st_f32_hint(float* addr, float v, uint64_t polic
 template <int THREADS>
 constexpr int prep_ctas_per_sm() { return THREADS <= 128 ? 10 : (THREADS <= 256 ? 5 : 1); }
 
+// Ascending bitonic sort of keys[0 .. 2 THREADS) with thread t holding
+// elements 2t and 2t+1 in registers: a compare-exchange at distance j joins
+// them inside the thread (j = 1), with lane t ^ j/2 of the same warp through
+// shuffles (j <= 32), or through shared memory (j >= 64), so only the
+// stages at distance 64 and more (six of 45 for 512 keys) pay block
+// barriers.  The lower element of a pair keeps the minimum where the block
+// of k2 elements it sits in is ascending.  Ends with keys[] sorted.
+template <int THREADS>
+__device__ __forceinline__ void bitonic_sort_pairs(unsigned long long* keys) {
+  constexpr int N = 2 * THREADS;
+  const int e0 = 2 * (int)threadIdx.x;
+  unsigned long long v0 = keys[e0], v1 = keys[e0 + 1];
+  for (int k2 = 2; k2 <= N; k2 <<= 1) {
+    const bool asc = (e0 & k2) == 0;
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      if (j == 1) {
+        const unsigned long long lo = v0 < v1 ? v0 : v1, hi = v0 < v1 ? v1 : v0;
+        v0 = asc ? lo : hi;
+        v1 = asc ? hi : lo;
+        continue;
+      }
+      unsigned long long p0, p1;
+      if (j <= 32) {
+        p0 = __shfl_xor_sync(0xffffffffu, v0, j >> 1);
+        p1 = __shfl_xor_sync(0xffffffffu, v1, j >> 1);
+      } else {
+        keys[e0] = v0;
+        keys[e0 + 1] = v1;
+        __syncthreads();
+        p0 = keys[e0 ^ j];
+        p1 = keys[(e0 + 1) ^ j];
+        __syncthreads();
+      }
+      const bool keep_min = ((e0 & j) == 0) == asc;  // both elements share bit j (j >= 2)
+      v0 = keep_min ? (v0 < p0 ? v0 : p0) : (v0 < p0 ? p0 : v0);
+      v1 = keep_min ? (v1 < p1 ? v1 : p1) : (v1 < p1 ? p1 : v1);
+    }
+  }
+  keys[e0] = v0;
+  keys[e0 + 1] = v1;
+  __syncthreads();
+}
+
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, prep_ctas_per_sm<THREADS>())
     paged_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
@@ -120,6 +172,7 @@ __global__ void __launch_bounds__(THREADS, prep_ctas_per_sm<THREADS>())
                       bool split) {
   extern __shared__ unsigned long long keys[];  // [Rpow2]
   __shared__ uint32_t warp_tot[THREADS / 32];
+  grid_dep_launch_dependents();
   const int qi = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the query and head weights are loaded first, so that their latency
   // overlaps the page-table sort (warp i splits heads i, i + THREADS/32, ...;
@@ -142,21 +195,26 @@ __global__ void __launch_bounds__(THREADS, prep_ctas_per_sm<THREADS>())
     keys[i] = i < nr ? (((unsigned long long)(uint32_t)page_logical[(int64_t)qi * R + i] << 32) | (uint32_t)i)
                      : ~0ull;
   __syncthreads();
-  // bitonic sort, ascending: each stage's Rpow2 / 2 compare-exchange pairs
-  // are indexed directly (pair t joins element lo = 2j (t / j) + t % j with
-  // lo + j), so no thread idles on the upper element of a pair
-  for (int k2 = 2; k2 <= Rpow2; k2 <<= 1)
-    for (int j = k2 >> 1; j > 0; j >>= 1) {
-      for (int t = tid; t < Rpow2 / 2; t += THREADS) {
-        const int lo = ((t & ~(j - 1)) << 1) | (t & (j - 1)), hi = lo + j;  // j is a power of two
-        const unsigned long long a = keys[lo], b = keys[hi];
-        if ((a > b) == ((lo & k2) == 0)) {
-          keys[lo] = b;
-          keys[hi] = a;
+  // bitonic sort, ascending: with two keys per thread in registers where the
+  // table fits that exactly, else each stage's Rpow2 / 2 compare-exchange
+  // pairs indexed directly in shared memory (pair t joins element lo =
+  // 2j (t / j) + t % j with lo + j, so no thread idles on the upper element)
+  if (Rpow2 == 2 * THREADS) {
+    bitonic_sort_pairs<THREADS>(keys);
+  } else {
+    for (int k2 = 2; k2 <= Rpow2; k2 <<= 1)
+      for (int j = k2 >> 1; j > 0; j >>= 1) {
+        for (int t = tid; t < Rpow2 / 2; t += THREADS) {
+          const int lo = ((t & ~(j - 1)) << 1) | (t & (j - 1)), hi = lo + j;  // j is a power of two
+          const unsigned long long a = keys[lo], b = keys[hi];
+          if ((a > b) == ((lo & k2) == 0)) {
+            keys[lo] = b;
+            keys[hi] = a;
+          }
         }
+        __syncthreads();
       }
-      __syncthreads();
-    }
+  }
   uint32_t base = 0;
   for (int i0 = 0; i0 < Rpow2; i0 += THREADS) {
     const int i = i0 + tid;
@@ -338,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_wait();  // the page tables, split query and weights come from the prep kernel
   const uint32_t tmem_base = tmem_slot;
 
   if (warp == 0) {
@@ -617,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  grid_dep_launch_dependents();  // the top-k may launch; it waits for this grid's completion
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -751,8 +811,18 @@ fm_status launch_paged(const PagedArgs& a, int num_sms, unsigned int* status, cu
   e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const int grid = (int)(total < num_sms ? total : num_sms);
-  score_kernel<<<grid, kThreads, smem, stream>>>(tmap_pool, tmap_q, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, score_kernel, tmap_pool, tmap_q, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "paged score: launch: %s", cudaGetErrorString(e));
 
   // ids: logical chunk ids, or reserve cells (the fused remap)

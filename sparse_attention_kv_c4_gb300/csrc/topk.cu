@@ -10,6 +10,26 @@ namespace {
 
 constexpr int kTopkThreads = 256;
 
+// Programmatic dependent launch: a top-k kernel may start while the kernel
+// before it on the stream (the scorer that wrote its rows) finishes; every
+// thread waits for that kernel's completion, and its memory, before reading.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, int grid, int block, int smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 struct IdentityMap {
   FM_DEV int32_t operator()(int i) const { return i; }
 };
@@ -67,6 +87,7 @@ __global__ void __launch_bounds__(kTopkThreads, kShort ? 5 : 4)
                      const unsigned long long* __restrict__ page_mask, int32_t* __restrict__ idx_out,
                      float* __restrict__ score_out) {
   constexpr int kCap = kShort ? kTopkCapShort : kTopkCap;
+  grid_dep_wait();
   extern __shared__ uint8_t topk_smem_raw[];
   TopkFastSmem<kTopkThreads, kCap>& sm = *reinterpret_cast<TopkFastSmem<kTopkThreads, kCap>*>(topk_smem_raw);
   const int64_t r = blockIdx.x;
@@ -106,6 +127,7 @@ __global__ void __launch_bounds__(kTopkTinyThreads, 9)
                           int k, const int32_t* __restrict__ page_ids, int64_t page_ld,
                           const int32_t* __restrict__ page_prefix, const unsigned long long* __restrict__ page_mask,
                           int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  grid_dep_wait();
   extern __shared__ uint8_t topk_smem_raw[];
   TinySmem& sm = *reinterpret_cast<TinySmem*>(topk_smem_raw);
   const int64_t r = blockIdx.x;
@@ -137,6 +159,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5)
     topk_rows_segmax_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
                             const int32_t* __restrict__ segmax, int64_t seg_ld, int n, int k,
                             int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  grid_dep_wait();
   extern __shared__ uint8_t topk_smem_raw[];
   SegSmem& sm = *reinterpret_cast<SegSmem*>(topk_smem_raw);
   const int64_t r = blockIdx.x;
@@ -167,9 +190,9 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kernel<<<rows, kTopkTinyThreads, smem, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, page_prefix,
-                                                     page_mask, idx_out, score_out);
-    e = cudaGetLastError();
+    e = launch_pdl(kernel, rows, kTopkTinyThreads, smem, stream, scores, ld, n_valid, n, k, page_ids, page_ld,
+                   page_prefix, page_mask, idx_out, score_out);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: launch: %s", cudaGetErrorString(e));
     return FM_OK;
   }
@@ -190,9 +213,9 @@ fm_status launch_topk_rows(const float* scores, int64_t ld, const int32_t* n_val
   // allows (four or five CTAs) is not cut by a smaller L1 split
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: carveout: %s", cudaGetErrorString(e));
-  kernel<<<rows, kTopkThreads, smem, stream>>>(scores, ld, n_valid, n, k, page_ids, page_ld, page_prefix, page_mask,
-                                               idx_out, score_out);
-  e = cudaGetLastError();
+  e = launch_pdl(kernel, rows, kTopkThreads, smem, stream, scores, ld, n_valid, n, k, page_ids, page_ld, page_prefix,
+                 page_mask, idx_out, score_out);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk: launch: %s", cudaGetErrorString(e));
   return FM_OK;
 }
@@ -211,9 +234,9 @@ fm_status launch_topk_rows_segmax(const float* scores, int64_t ld, const int32_t
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(topk_rows_segmax_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk segmax: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  topk_rows_segmax_kernel<<<rows, kTopkThreads, smem, stream>>>(scores, ld, n_valid, segmax, seg_ld, n, k, idx_out,
-                                                                score_out);
-  e = cudaGetLastError();
+  e = launch_pdl(topk_rows_segmax_kernel, rows, kTopkThreads, smem, stream, scores, ld, n_valid, segmax, seg_ld, n, k,
+                 idx_out, score_out);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(FM_ERR_CUDA, "topk segmax: launch: %s", cudaGetErrorString(e));
   return FM_OK;
 }
