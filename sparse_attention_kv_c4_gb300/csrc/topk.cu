@@ -36,6 +36,7 @@ struct IdentityMap {
 
 // Candidate i of a paged row is chunk page_ids[i / 64] * 64 + i % 64.
 struct PageMap {
+  static constexpr bool kPageIds = true;  // the emit may stage ids[] in shared memory
   const int32_t* ids;
   FM_DEV int32_t operator()(int i) const { return __ldg(ids + (i >> 6)) * 64 + (i & 63); }
 };

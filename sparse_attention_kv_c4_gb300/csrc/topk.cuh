@@ -321,6 +321,19 @@ FM_DEV T block_select(const T* a, int n, int r, T lo, T hi, uint32_t loose, Sele
 // in index order, and -1 / -inf in positions kk .. k-1.  Rows of at most
 // BITMAP_N scores emit through sm.u.bitmap, whose first (n + 31) / 32 words
 // the caller has cleared.  All threads call it.
+// An id map that reads page ids (candidate i -> ids[i / 64] * 64 + i % 64)
+// declares kPageIds; the emit then stages the row's page ids in shared memory
+// (past the bitmap words it uses) before the select, so the ids it writes
+// cost no global load on the way out.
+template <typename M, typename = void>
+struct has_page_ids {
+  static constexpr bool value = false;
+};
+template <typename M>
+struct has_page_ids<M, decltype((void)M::kPageIds)> {
+  static constexpr bool value = M::kPageIds;
+};
+
 template <int THREADS, int CAP, typename IdxMap, int RUNS, int BITMAP_N>
 FM_DEV void block_topk_emit(TopkFastSmem<THREADS, CAP, RUNS, BITMAP_N>& sm, int cnt, unsigned long long theta, int n,
                             int kk, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
@@ -328,11 +341,20 @@ FM_DEV void block_topk_emit(TopkFastSmem<THREADS, CAP, RUNS, BITMAP_N>& sm, int 
   constexpr int kTopkBitmapN = BITMAP_N;
   const int tid = threadIdx.x;
   // ---- 3. exact select among the candidates -------------------------------------
-  // every candidate lies in [theta, cmax]
+  const int words = (n + 31) >> 5;
+  const int npages = (n + 63) >> 6;
+  uint32_t* staged = sm.u.bitmap + words;  // page ids past the bitmap words in use
+  bool use_staged = false;
+  if constexpr (has_page_ids<IdxMap>::value) {
+    use_staged = n <= kTopkBitmapN && words + npages <= kTopkBitmapN / 32;
+    if (use_staged)
+      for (int i = tid; i < npages; i += THREADS) staged[i] = (uint32_t)__ldg(idx_map.ids + i);
+  }
+  // every candidate lies in [theta, cmax] (the select's barriers also publish
+  // the staged ids)
   const unsigned long long T = block_select<THREADS>(sm.cand, cnt, kk, theta, sm.cmax, 0u, sm.sel);
   // ---- 4. emit in index order -------------------------------------------------
   if (n <= kTopkBitmapN) {
-    const int words = (n + 31) >> 5;
     for (int i = tid; i < cnt; i += THREADS) {
       const unsigned long long c = sm.cand[i];
       if (c >= T) {
@@ -356,7 +378,7 @@ FM_DEV void block_topk_emit(TopkFastSmem<THREADS, CAP, RUNS, BITMAP_N>& sm, int 
         const int w = (int)(idx >> 5), owner = w / per;
         uint32_t pos = sm.tpre[owner] + (uint32_t)__popc(sm.u.bitmap[w] & ((1u << (idx & 31)) - 1u));
         for (int w2 = owner * per; w2 < w; ++w2) pos += (uint32_t)__popc(sm.u.bitmap[w2]);
-        idx_out[pos] = idx_map((int)idx);
+        idx_out[pos] = use_staged ? (int32_t)staged[idx >> 6] * 64 + (int32_t)(idx & 63) : idx_map((int)idx);
         if (score_out) score_out[pos] = key_float((uint32_t)(c >> 32));
       }
     }
@@ -423,25 +445,25 @@ FM_DEV void block_topk(const float* __restrict__ row, int n, int k, IdxMap idx_m
   if (n > CAP) {
     if (n <= kTopkBitmapN) {
       // every thread's samples are loaded before any is stored, so their
-      // loads overlap (run * (n - 64) < 2^31 for these rows)
+      // loads overlap (run * (n - 64) < 2^31 for these rows).  The filter
+      // thresholds at theta's score key, so the sample is kept as 32-bit
+      // keys and theta's index part is zero.
       constexpr int kPerT = kTopkSample / THREADS;
       static_assert(kPerT * THREADS == kTopkSample, "sample entries per thread");
       float sv[kPerT];
-      int sj[kPerT];
 #pragma unroll
       for (int t = 0; t < kPerT; ++t) {
         const int i = tid + t * THREADS, run = i >> 6, off = i & 63;
-        sj[t] = run * (n - 64) / (kTopkRuns - 1) + off;
-        sv[t] = __ldg(row + sj[t]);
+        sv[t] = __ldg(row + run * (n - 64) / (kTopkRuns - 1) + off);
       }
 #pragma unroll
-      for (int t = 0; t < kPerT; ++t)
-        sm.u.sample[tid + t * THREADS] = ((unsigned long long)float_key(sv[t]) << 32) | (uint32_t)(~(uint32_t)sj[t]);
+      for (int t = 0; t < kPerT; ++t) sm.u.sample32[tid + t * THREADS] = float_key(sv[t]);
       __syncthreads();
       long long r = r_aim >= 0 ? r_aim : (want * kTopkSample) / (long long)n;
       r = r < 1 ? 1 : (r > kTopkSample ? kTopkSample : r);
       r_aim = r;
-      theta = block_select<THREADS>(sm.u.sample, kTopkSample, (int)r, 0ull, ~0ull, 4u, sm.sel);
+      theta = (unsigned long long)block_select<THREADS>(sm.u.sample32, kTopkSample, (int)r, 0u, ~0u, 4u, sm.sel)
+              << 32;
     } else {
       // Long rows (a whole 1M-token history is 262144 scores): with 2048
       // samples only ~12 would lie above the threshold and about one row in
