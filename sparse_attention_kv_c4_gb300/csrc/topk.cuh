@@ -163,7 +163,7 @@ namespace fm {
 //  Every candidate is ranked by its unique composite key (key << 32 | ~index),
 //  which orders (score desc, index asc).
 //  1. Sample 32 evenly spaced runs of 64 consecutive scores (coalesced) and
-//     take theta = about the r-th largest sample composite, r chosen so that
+//     take theta = about the r-th largest sampled score key, r chosen so that
 //     about 2 min(k, n) candidates (3 min(k, n) for rows long enough that r
 //     would fall below 64; at most 2/3 of the list) are expected at or above
 //     it.
@@ -315,12 +315,6 @@ FM_DEV T block_select(const T* a, int n, int r, T lo, T hi, uint32_t loose, Sele
   return prefix;
 }
 
-// Steps 3 and 4 of the select, shared by block_topk and block_topk_segmax:
-// the exact kk-th largest composite T among the cnt candidates in sm.cand
-// (every one of them in [theta, sm.cmax]), then every candidate >= T written
-// in index order, and -1 / -inf in positions kk .. k-1.  Rows of at most
-// BITMAP_N scores emit through sm.u.bitmap, whose first (n + 31) / 32 words
-// the caller has cleared.  All threads call it.
 // An id map that reads page ids (candidate i -> ids[i / 64] * 64 + i % 64)
 // declares kPageIds; the emit then stages the row's page ids in shared memory
 // (past the bitmap words it uses) before the select, so the ids it writes
@@ -334,6 +328,12 @@ struct has_page_ids<M, decltype((void)M::kPageIds)> {
   static constexpr bool value = M::kPageIds;
 };
 
+// Steps 3 and 4 of the select, shared by block_topk and block_topk_segmax:
+// the exact kk-th largest composite T among the cnt candidates in sm.cand
+// (every one of them in [theta, sm.cmax]), then every candidate >= T written
+// in index order, and -1 / -inf in positions kk .. k-1.  Rows of at most
+// BITMAP_N scores emit through sm.u.bitmap, whose first (n + 31) / 32 words
+// the caller has cleared.  All threads call it.
 template <int THREADS, int CAP, typename IdxMap, int RUNS, int BITMAP_N>
 FM_DEV void block_topk_emit(TopkFastSmem<THREADS, CAP, RUNS, BITMAP_N>& sm, int cnt, unsigned long long theta, int n,
                             int kk, int k, IdxMap idx_map, int32_t* __restrict__ idx_out,
