@@ -152,6 +152,22 @@ def test_paged_workspace_accepts_a_whole_1m_history(lib):
     assert lib.fm_native_topk_paged_workspace(1, 0) == 0
 
 
+def test_memindex_fp8_workspace_contract(lib):
+    """The fp8 Memory Indexer's workspace holds, per (request, layer), the
+    split query's two 80-row E4M3 term blocks (64 heads, then the weighted
+    query sum's four terms and zeros) and 68 floats of weights: at least
+    20,752 bytes each; L outside 1..4 or a negative B sizes nothing."""
+    lib.fm_memindex_fp8_workspace.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.fm_memindex_fp8_workspace.restype = ctypes.c_size_t
+    per = 2 * 80 * 128 + 68 * 4
+    for B, L in ((1, 1), (4, 3), (30, 3), (2, 4)):
+        ws = lib.fm_memindex_fp8_workspace(B, L)
+        assert ws >= B * L * per and ws % 256 == 0, (B, L, ws)
+    assert lib.fm_memindex_fp8_workspace(1, 0) == 0 and lib.fm_memindex_fp8_workspace(1, 5) == 0
+    assert lib.fm_memindex_fp8_workspace(-1, 3) == 0
+    assert lib.fm_memindex_fp8_workspace(0, 3) == 0
+
+
 def test_retriever_workspace_and_host_checks(lib):
     """Workspace sizing is host arithmetic; bad arguments are rejected before
     any device work (no GPU needed)."""
